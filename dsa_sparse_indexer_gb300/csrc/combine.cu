@@ -1,0 +1,121 @@
+// LSE combine of the shards' partial attention outputs.
+//
+// PR #46076 report, "[Attention][DSA] support dcp for FLASHINFER_MLA_SPARSE",
+// section 实现拆解 item 5 and section 评论区精华 (LSE base normalisation: the
+// sparse MLA kernel reports a base-2 LSE, the DCP reducer needs base e);
+// PR #52046 report, "DSV3.2 PCP sharding", section 关键源码片段
+// (`dcp_manager.combine` of attn_out by lse).
+//
+// Per (row, head): lambda_s = lse2_s ln 2, M = max lambda_s,
+// w_s = exp(lambda_s - M), out = sum w_s O_s / sum w_s, lse = M + ln sum w_s.
+// Since exp((lse2_s - max lse2) ln 2) = 2^(lse2_s - max lse2) exactly, the
+// weights are taken with exp2 on the base-2 values and only the final LSE is
+// converted; that is the same quantity with one rounding fewer per weight.
+//
+// One warp per (row, head); each lane streams 8 bf16 (16 bytes) per shard per
+// 256-wide slice of D; shards whose LSE is -inf are not read.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kCombThreads = 256;
+constexpr int kCombWarps = kCombThreads / 32;
+constexpr float kLn2 = 0.693147180559945309417f;
+
+__device__ __forceinline__ void accum8(float* acc, uint4 v, float w) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q] = fmaf(w, __uint_as_float(u[q] << 16), acc[2 * q]);
+    acc[2 * q + 1] = fmaf(w, __uint_as_float(u[q] & 0xffff0000u), acc[2 * q + 1]);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kCombThreads)
+    lse_combine_kernel(const uint16_t* __restrict__ part, const float* __restrict__ lse2,
+                       int S, int rows, int H, int D, uint16_t* __restrict__ out,
+                       float* __restrict__ lse_out) {
+  const int64_t rh = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5);
+  const int64_t RH = (int64_t)rows * H;
+  if (rh >= RH) return;
+  const int lane = threadIdx.x & 31;
+
+  const float a0 = lane < S ? __ldg(lse2 + lane * RH + rh) : -INFINITY;
+  const float a1 = lane + 32 < S ? __ldg(lse2 + (lane + 32) * RH + rh) : -INFINITY;
+  float M = fmaxf(a0, a1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+  uint16_t* dst = out + rh * D;
+  if (M == -INFINITY) {  // no shard holds anything
+    for (int d = lane * 8; d < D; d += 256)
+      *reinterpret_cast<uint4*>(dst + d) = make_uint4(0u, 0u, 0u, 0u);
+    if (lse_out && lane == 0) lse_out[rh] = -INFINITY;
+    return;
+  }
+  const float w0 = a0 == -INFINITY ? 0.f : exp2f(a0 - M);
+  const float w1 = a1 == -INFINITY ? 0.f : exp2f(a1 - M);
+  float wsum = w0 + w1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(kFull, wsum, o);
+  const float inv = 1.f / wsum;
+
+  for (int d = lane * 8; d < D; d += 256) {
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 4) {
+      uint4 v[4];
+      float w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int s = s0 + u;
+        const float ws = __shfl_sync(kFull, s < 32 ? w0 : w1, s & 31);
+        w[u] = s < S ? ws : 0.f;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (w[u] != 0.f)
+          v[u] = __ldg(reinterpret_cast<const uint4*>(part + ((int64_t)s * RH + rh) * D + d));
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (w[u] != 0.f) accum8(acc, v[u], w[u]);
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(dst + d) = o;
+  }
+  if (lse_out && lane == 0) lse_out[rh] = (M + log2f(wsum)) * kLn2;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" dsa_status dsa_lse_combine(const uint16_t* partial_out, const float* lse2, int S,
+                                      int rows, int H, int D, uint16_t* out, float* lse_out,
+                                      cudaStream_t stream) {
+  if (!partial_out || !lse2 || !out || rows < 0 || H < 1 || D < 8 || (D & 7) ||
+      !aligned16(partial_out) || !aligned16(out))
+    return DSA_ERR_INVALID_ARG;
+  if (S < 1 || S > DSA_MAX_SHARDS) return DSA_ERR_UNSUPPORTED;
+  if (rows == 0) return DSA_OK;
+  const int64_t warps = (int64_t)rows * H;
+  const int64_t blocks = (warps + kCombWarps - 1) / kCombWarps;
+  if (blocks > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  lse_combine_kernel<<<(unsigned)blocks, kCombThreads, 0, stream>>>(partial_out, lse2, S, rows, H,
+                                                                    D, out, lse_out);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}

@@ -1,0 +1,156 @@
+// Device helpers shared by the DCP sparse-indexer kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// Order-preserving keys.
+//
+// score_key maps an fp32 score to a uint32 whose unsigned order is the score
+// order (NaN excluded); -0.0 is folded into +0.0 so the two tie.  Ties on the
+// score are broken toward the smaller global token id, so a candidate's full
+// rank key is (score_key << 32) | ~id: larger key = better candidate.  A valid
+// score never maps below 0x007FFFFF (the key of -inf), so the 64-bit key 0 is
+// free to mean "padding".
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// ---------------------------------------------------------------------------
+// Interleaved DCP sharding, closed forms of the ownership rule
+// owner(t) = (t / I) mod S (PR #46076 report, "[Attention][DSA] support dcp for
+// FLASHINFER_MLA_SPARSE", section 关键源码片段, `_dcp_localize_decode_seq_lens`).
+// A shard keeps its tokens in increasing global order.
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int64_t owner_of(int64_t t, int S, int I) {
+  return (t / I) % S;
+}
+__host__ __device__ __forceinline__ int64_t local_slot_of(int64_t t, int S, int I) {
+  return (t / ((int64_t)I * S)) * I + t % I;
+}
+__host__ __device__ __forceinline__ int64_t global_of(int s, int64_t l, int S, int I) {
+  return (l / I) * ((int64_t)I * S) + (int64_t)s * I + l % I;
+}
+// Tokens of the global prefix [0, L) that shard s holds.
+__host__ __device__ __forceinline__ int64_t local_len(int64_t L, int s, int S, int I) {
+  const int64_t round = (int64_t)I * S;
+  int64_t rem = L % round - (int64_t)s * I;
+  rem = rem < 0 ? 0 : (rem > I ? I : rem);
+  return (L / round) * I + rem;
+}
+
+__device__ __forceinline__ void raise_flag(uint32_t* flags, uint32_t bit) {
+  if (flags) atomicOr(flags, bit);
+}
+
+// ---------------------------------------------------------------------------
+// Bulk async copies (TMA, non-tensor form) global -> shared, completed on an
+// mbarrier.  Both addresses 16-byte aligned, size a multiple of 16.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+// Make mbarrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait for phase `parity` of an mbarrier.  Returns false (and the
+// caller raises DSA_FLAG_TIMEOUT) after `limit` polls; each poll may suspend
+// the thread for a hardware-chosen interval, so the bound is generous.
+constexpr uint32_t kWaitPolls = 1u << 22;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i > 64) __nanosleep(64);
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// Block-wide exclusive prefix sum of one int per thread.  `scratch` holds at
+// least blockDim.x/32 + 1 ints.  Returns the exclusive prefix; *total gets the
+// sum over the block.  Contains two __syncthreads().
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? scratch[lane] : 0;
+    int incl = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane < nwarps) scratch[lane] = incl - w;
+    if (lane == 31) scratch[32] = incl;
+  }
+  __syncthreads();
+  *total = scratch[32];
+  return scratch[warp] + x - v;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+}  // namespace dsa

@@ -1,0 +1,151 @@
+"""Torch-facing binding of the C ABI: argument checks and marshalling only.
+
+Every function here validates dtype / device / contiguity, passes raw device
+pointers and the current CUDA stream to libdsa.so, and returns the output
+tensors.  No step of the path is computed in Python and there is no CPU path:
+CPU tensors are rejected.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+__all__ = ["shard_topk", "pack_candidates", "shard_topk_pack", "merge_topk_stable",
+           "convert_index_compact", "lse_combine", "new_error_flags", "SUPPORTED_K"]
+
+SUPPORTED_K = (512, 1024, 2048)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, dim: int | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dims, got {t.dim()}")
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def new_error_flags(device) -> torch.Tensor:
+    """A zeroed device word for the kernels' DSA_FLAG_* bits."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def shard_topk(logits, row_ends, K: int, I: int, row_starts=None, out=None, err_flags=None):
+    """Local top-K of every shard.  logits [S, rows, ld] fp32 -> [S, rows, K] int32."""
+    _need(logits, "logits", torch.float32, 3)
+    S, rows, ld = logits.shape
+    _need(row_ends, "row_ends", torch.int32, 1)
+    if row_starts is not None:
+        _need(row_starts, "row_starts", torch.int32, 1)
+    if out is None:
+        out = torch.empty((S, rows, K), dtype=torch.int32, device=logits.device)
+    _need(out, "out", torch.int32, 3)
+    _lib.call("dsa_shard_topk", _ptr(logits), ld, rows, S, I, K, _ptr(row_starts),
+              _ptr(row_ends), _ptr(out), _ptr(err_flags), _stream(logits))
+    return out
+
+
+def pack_candidates(logits, local_idx, I: int, out=None, err_flags=None):
+    """(score, global id) candidates: -> [rows, S*K, 2] fp32 (id lane = int32 bits)."""
+    _need(logits, "logits", torch.float32, 3)
+    _need(local_idx, "local_idx", torch.int32, 3)
+    S, rows, ld = logits.shape
+    K = local_idx.shape[2]
+    if out is None:
+        out = torch.empty((rows, S * K, 2), dtype=torch.float32, device=logits.device)
+    _need(out, "out", torch.float32, 3)
+    _lib.call("dsa_pack_candidates", _ptr(logits), ld, _ptr(local_idx), rows, S, I, K,
+              _ptr(out), _ptr(err_flags), _stream(logits))
+    return out
+
+
+def shard_topk_pack(logits, row_ends, K: int, I: int, row_starts=None, local_idx=None,
+                    cand=None, want_local_idx: bool = True, err_flags=None):
+    """Fused shard top-K + pack.  Returns (local_idx or None, cand)."""
+    _need(logits, "logits", torch.float32, 3)
+    S, rows, ld = logits.shape
+    _need(row_ends, "row_ends", torch.int32, 1)
+    if row_starts is not None:
+        _need(row_starts, "row_starts", torch.int32, 1)
+    if local_idx is None and want_local_idx:
+        local_idx = torch.empty((S, rows, K), dtype=torch.int32, device=logits.device)
+    if cand is None:
+        cand = torch.empty((rows, S * K, 2), dtype=torch.float32, device=logits.device)
+    _need(cand, "cand", torch.float32, 3)
+    if local_idx is not None:
+        _need(local_idx, "local_idx", torch.int32, 3)
+    _lib.call("dsa_shard_topk_pack", _ptr(logits), ld, rows, S, I, K, _ptr(row_starts),
+              _ptr(row_ends), _ptr(local_idx), _ptr(cand), _ptr(err_flags), _stream(logits))
+    return local_idx, cand
+
+
+def merge_topk_stable(cand, K: int, ids=None, scores=None, want_scores: bool = False,
+                      err_flags=None):
+    """Stable global top-K of [rows, C, 2] candidates -> ids [rows, K] (, scores)."""
+    _need(cand, "cand", torch.float32, 3)
+    rows, C, _two = cand.shape
+    if ids is None:
+        ids = torch.empty((rows, K), dtype=torch.int32, device=cand.device)
+    _need(ids, "ids", torch.int32, 2)
+    if scores is None and want_scores:
+        scores = torch.empty((rows, K), dtype=torch.float32, device=cand.device)
+    if scores is not None:
+        _need(scores, "scores", torch.float32, 2)
+    _lib.call("dsa_merge_topk_stable", _ptr(cand), rows, C, K, _ptr(ids), _ptr(scores),
+              _ptr(err_flags), _stream(cand))
+    return (ids, scores) if (want_scores or scores is not None) else ids
+
+
+def convert_index_compact(ids, block_table, block_size: int, I: int, row_to_req=None,
+                          slots=None, counts=None, want_counts: bool = True, err_flags=None):
+    """Merged ids [rows, K] -> per-shard slots [S, rows, K] (, counts [S, rows])."""
+    _need(ids, "ids", torch.int32, 2)
+    _need(block_table, "block_table", torch.int32, 3)
+    rows, K = ids.shape
+    S, reqs, max_blocks = block_table.shape
+    if row_to_req is not None:
+        _need(row_to_req, "row_to_req", torch.int32, 1)
+    if slots is None:
+        slots = torch.empty((S, rows, K), dtype=torch.int32, device=ids.device)
+    _need(slots, "slots", torch.int32, 3)
+    if counts is None and want_counts:
+        counts = torch.empty((S, rows), dtype=torch.int32, device=ids.device)
+    if counts is not None:
+        _need(counts, "counts", torch.int32, 2)
+    _lib.call("dsa_convert_index_compact", _ptr(ids), rows, K, S, I, _ptr(block_table), reqs,
+              max_blocks, block_size, _ptr(row_to_req), _ptr(slots), _ptr(counts),
+              _ptr(err_flags), _stream(ids))
+    return slots, counts
+
+
+def lse_combine(partial_out, lse2, out=None, lse_out=None, want_lse: bool = True):
+    """partial_out [S, rows, H, D] bf16, lse2 [S, rows, H] fp32 (base 2)
+    -> out [rows, H, D] bf16 (, lse [rows, H] fp32 base e)."""
+    _need(partial_out, "partial_out", torch.bfloat16, 4)
+    _need(lse2, "lse2", torch.float32, 3)
+    S, rows, H, D = partial_out.shape
+    if tuple(lse2.shape) != (S, rows, H):
+        raise ValueError("lse2 must be [S, rows, H]")
+    if out is None:
+        out = torch.empty((rows, H, D), dtype=torch.bfloat16, device=partial_out.device)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((rows, H), dtype=torch.float32, device=partial_out.device)
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32, 2)
+    _lib.call("dsa_lse_combine", _ptr(partial_out), _ptr(lse2), S, rows, H, D, _ptr(out),
+              _ptr(lse_out), _stream(partial_out))
+    return out, lse_out

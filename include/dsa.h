@@ -1,0 +1,201 @@
+/*
+ * dsa.h - C ABI of the DCP sparse-indexer hot path for GB300 (sm_103a).
+ *
+ * The path, in the order a DCP decode step runs it (PR #46076 report,
+ * "[Attention][DSA] support dcp for FLASHINFER_MLA_SPARSE", section 关键源码片段,
+ * `_merge_dcp_topk_global`):
+ *
+ *   dsa_shard_topk        every shard's local top-K of fp32 indexer logits
+ *   dsa_pack_candidates   (score, global id) pairs, written straight into each
+ *                         shard's slice of one [rows, S*K, 2] buffer (the
+ *                         all_gather of the pages, with no copy)
+ *   dsa_merge_topk_stable stable global top-K of the S*K candidates
+ *   dsa_convert_index_compact  global ids -> each shard's paged KV slots,
+ *                         valid slots compacted to the front
+ *   dsa_lse_combine       LSE-weighted combine of the shards' partial
+ *                         attention outputs, base-2 LSE converted to base e
+ *
+ * plus dsa_shard_topk_pack, the first two steps fused in one kernel.
+ *
+ * Sharding (PR #46076 report, section 关键源码片段, comment in
+ * `_dcp_localize_decode_seq_lens`): global token t lives on shard
+ * owner(t) = (t / I) mod S; a shard keeps its tokens in increasing global
+ * order, so t is its local slot loc(t) = (t / (I*S))*I + t mod I, and local
+ * slot l of shard s is global token (l / I)*(I*S) + s*I + l mod I.  A global
+ * range [start, end) is, on shard s, the local range [n_s(start), n_s(end)),
+ * n_s(L) = (L / (I*S))*I + clamp(L mod (I*S) - s*I, 0, I).
+ *
+ * Ranking everywhere: score descending, ties to the smaller global token id
+ * (the "stable" of the pages' selector; -0.0 and +0.0 are the same score).
+ * Scores must not be NaN; results for NaN inputs are unspecified.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller; the library
+ *     allocates nothing, keeps no state between calls and frees nothing.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream) and
+ *     enqueues one kernel; results are ready when the stream reaches it.
+ *   - Arguments are checked on the host before anything is enqueued.  A bad
+ *     argument returns DSA_ERR_INVALID_ARG or DSA_ERR_UNSUPPORTED and touches
+ *     nothing.  rows == 0 returns DSA_OK and enqueues nothing.
+ *   - DSA_ERR_CUDA means the launch itself failed (cudaGetLastError).
+ *   - Problems only visible on the device set bits of `*err_flags` (a caller
+ *     owned device word, may be NULL) with atomicOr; kernels never trap.
+ *   - Row-major layouts; int32 indices; -1 marks padding.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment */
+  DSA_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels support */
+  DSA_ERR_CUDA = 3           /* a CUDA launch error */
+} dsa_status;
+
+/* Bits set in *err_flags by the kernels. */
+enum {
+  DSA_FLAG_BOUNDS = 1u,      /* a row range or block-table column was out of range */
+  DSA_FLAG_TIMEOUT = 2u      /* a bounded wait on an async copy ran out */
+};
+
+/* Supported top-K sizes: the pages' set, PR #46076 report, section 关键源码片段,
+ * `_assert_cutedsl_dcp_merge_supported` (index_topk in 512/1024/2048). */
+#define DSA_MAX_SHARDS 64
+
+/* Human-readable name of a status code (static string). */
+const char* dsa_status_string(dsa_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int dsa_version(void);
+
+/*
+ * dsa_shard_topk - every shard's local top-K.
+ * PR #46076 report, section 关键源码片段, `_merge_dcp_topk_global` docstring:
+ * "topk_indices are top-K positions in this rank's local KV shard".
+ *
+ *   logits      [S][rows][ld] fp32: shard s, row r, local slot l at
+ *               logits[(s*rows + r)*ld + l].  16-byte aligned; ld % 4 == 0.
+ *   row_starts  [rows] int32 global start of each row (NULL = all 0)
+ *   row_ends    [rows] int32 global end (exclusive) of each row
+ *   local_idx   [S][rows][K] int32 out: the K best local slots of
+ *               [n_s(start), n_s(end)), ascending; -1 after the first
+ *               min(K, n_s(end) - n_s(start)).  Absolute local slots.
+ *   err_flags   DSA_FLAG_BOUNDS if a local range ends past ld (the range is
+ *               clipped to ld) or starts after it ends (treated as empty).
+ * Errors: S not in [1, 64], I < 1, K not in {512, 1024, 2048} -> UNSUPPORTED;
+ *         null pointers, rows < 0, ld < 4, ld % 4, misaligned logits -> INVALID_ARG.
+ */
+dsa_status dsa_shard_topk(const float* logits, int64_t ld, int rows, int S, int I,
+                          int K, const int32_t* row_starts, const int32_t* row_ends,
+                          int32_t* local_idx, uint32_t* err_flags, cudaStream_t stream);
+
+/*
+ * dsa_pack_candidates - (score, global id) candidates of every shard's top-K.
+ * PR #46076 report, section 实现拆解 item 1 (`pack_dcp_topk_candidates_cutedsl`)
+ * and section 关键源码片段 (packed = [batch, topk, 2] fp32, then all_gather
+ * along dim 1).
+ *
+ *   logits, ld  as dsa_shard_topk
+ *   local_idx   [S][rows][K] int32 local slots (-1 = padding), as written by
+ *               dsa_shard_topk
+ *   cand        [rows][S*K][2] fp32 out.  cand[r][s*K + j] = (logits[s][r][l],
+ *               global id of local slot l on shard s) for l = local_idx[s][r][j];
+ *               element 1 holds the int32 id's BIT PATTERN (read it back as
+ *               int32).  Padding -> (-inf, -1).  16-byte aligned.
+ *   err_flags   DSA_FLAG_BOUNDS if a local index is >= ld (written as padding).
+ */
+dsa_status dsa_pack_candidates(const float* logits, int64_t ld, const int32_t* local_idx,
+                               int rows, int S, int I, int K, float* cand,
+                               uint32_t* err_flags, cudaStream_t stream);
+
+/*
+ * dsa_shard_topk_pack - dsa_shard_topk and dsa_pack_candidates in one kernel:
+ * the winning logits are packed while still in shared memory, so the pack
+ * step's gather from the logits is not repeated.  Same arguments and results;
+ * local_idx may be NULL when only the candidates are wanted.
+ */
+dsa_status dsa_shard_topk_pack(const float* logits, int64_t ld, int rows, int S, int I,
+                               int K, const int32_t* row_starts, const int32_t* row_ends,
+                               int32_t* local_idx, float* cand, uint32_t* err_flags,
+                               cudaStream_t stream);
+
+/*
+ * dsa_merge_topk_stable - the global top-K of each row's C gathered candidates.
+ * PR #46076 report, section 实现拆解 item 1
+ * (`stable_topk_from_gathered_candidates_cutedsl`) and the
+ * `_merge_dcp_topk_global` docstring: topk_indices are overwritten with global
+ * token ids, -1 for padding.
+ *
+ *   cand        [rows][C][2] fp32 candidates as written by the pack; a
+ *               candidate whose id is < 0 is padding and never selected.
+ *               16-byte aligned; C % 4 == 0; C >= K.
+ *   ids         [rows][K] int32 out: the K best valid candidates' ids, best
+ *               first; -1 after the valid ones.
+ *   scores      [rows][K] fp32 out, may be NULL: their scores (-inf after the
+ *               valid ones; a -0.0 score may come back as +0.0).
+ *   err_flags   DSA_FLAG_TIMEOUT if staging the row in shared memory stalled.
+ * Candidate ids within a row must be distinct (the pack guarantees it).
+ */
+dsa_status dsa_merge_topk_stable(const float* cand, int rows, int C, int K,
+                                 int32_t* ids, float* scores, uint32_t* err_flags,
+                                 cudaStream_t stream);
+
+/*
+ * dsa_convert_index_compact - merged global ids -> per-shard physical KV slots.
+ * PR #46076 report, section 实现拆解 item 4 (`_convert_req_index_to_global_index_kernel`
+ * with DCP_SIZE/DCP_RANK/DCP_INTERLEAVE and the COMPACT_TO_FRONT branch) and
+ * PR #40996 report, "DCP supports hybrid attention", section 关键源码片段
+ * (rank-local block tables of cdiv(max_len, block_size * cp) columns).
+ *
+ *   ids         [rows][K] int32 merged ids (-1 = padding)
+ *   block_table [S][reqs][max_blocks] int32 physical block numbers per shard
+ *   row_to_req  [rows] int32 request of each row (NULL: row r is request r)
+ *   slots       [S][rows][K] int32 out: for shard s, the ids it holds, in the
+ *               merged order, mapped to block_table[s][req][l / block_size] *
+ *               block_size + l % block_size (l = local slot), packed at the
+ *               front; -1 after them.  The order is deterministic.
+ *   counts      [S][rows] int32 out, may be NULL: number of slots written.
+ *   err_flags   DSA_FLAG_BOUNDS if a column is >= max_blocks, a table entry is
+ *               negative, a slot does not fit in int32, or a row's request is
+ *               outside [0, reqs); such an entry is written as -1 in its place.
+ */
+dsa_status dsa_convert_index_compact(const int32_t* ids, int rows, int K, int S, int I,
+                                     const int32_t* block_table, int reqs, int max_blocks,
+                                     int block_size, const int32_t* row_to_req,
+                                     int32_t* slots, int32_t* counts, uint32_t* err_flags,
+                                     cudaStream_t stream);
+
+/*
+ * dsa_lse_combine - merge the shards' partial attention outputs by their LSE.
+ * PR #46076 report, section 实现拆解 item 5 and section 评论区精华 (LSE base
+ * normalisation: the sparse MLA kernel's LSE is base 2, the DCP reducer wants
+ * base e); PR #52046 report, "DSV3.2 PCP sharding", section 关键源码片段
+ * (`dcp_manager.combine(attn_out, lse, ...)`).
+ *
+ * Per (row, head): lambda_s = lse2_s * ln 2, M = max_s lambda_s,
+ * w_s = exp(lambda_s - M), out = sum_s w_s O_s / sum_s w_s, lse = M + ln sum_s w_s.
+ * A shard with lse2 = -inf holds nothing and its output is not read; if every
+ * shard is -inf the result is out = 0, lse = -inf.
+ *
+ *   partial_out [S][rows][H][D] bf16 (raw uint16 bit patterns), 16-byte aligned
+ *   lse2        [S][rows][H] fp32 base-2 LSE
+ *   out         [rows][H][D] bf16 out (round to nearest even), 16-byte aligned
+ *   lse_out     [rows][H] fp32 out, base e; may be NULL
+ * Errors: D % 8 != 0, H < 1, D < 8 -> INVALID_ARG; S not in [1, 64] -> UNSUPPORTED.
+ */
+dsa_status dsa_lse_combine(const uint16_t* partial_out, const float* lse2, int S,
+                           int rows, int H, int D, uint16_t* out, float* lse_out,
+                           cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -59,9 +59,10 @@ def global_to_local(t, S: int, I: int):
 def local_to_global(s: int, slots, S: int, I: int) -> np.ndarray:
     """Global id of local slot(s) of shard s: the slot-th token shard s holds."""
     slots = np.asarray(slots, np.int64)
-    need = int(slots.max(initial=-1)) + 1
-    # Shard s holds at least `need` tokens within the first need*I*S tokens.
-    toks = owned_tokens(max(need, 1) * I * S, s, S, I)
+    need = max(int(slots.max(initial=-1)) + 1, 1)
+    # Every run of I*S consecutive tokens gives shard s exactly I of them, so the
+    # first ceil(need / I) runs hold at least `need` of its tokens.
+    toks = owned_tokens(-(-need // I) * I * S, s, S, I)
     return toks[slots]
 
 

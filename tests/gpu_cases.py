@@ -1,0 +1,121 @@
+"""Shared helpers for the GPU parity tests: build a workload's inputs, run the
+CUDA path through the binding, run the oracle on sampled rows, compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import workloads as W
+from oracle import combine as OC
+from oracle import dcp_layout as OL
+from oracle import indexer as OX
+from oracle import pipeline as OP
+
+
+def row_to_req_for(cfg) -> np.ndarray | None:
+    if cfg.reqs == cfg.rows:
+        return None
+    return np.zeros(cfg.rows, np.int32)          # prefill: every row is one request
+
+
+def make_case(name: str, fill=None, replica: int = 0) -> dict:
+    cfg = W.CONFIGS[name]
+    starts, ends = W.row_ranges(cfg, replica)
+    x = W.global_logits(cfg, replica)
+    local = OL.shard_rows(x, ends, cfg.S, cfg.I, cfg.ld, fill=fill)
+    return dict(cfg=cfg, x=x, local=local, starts=starts, ends=ends,
+                bt=W.block_tables(cfg, replica=replica), r2q=row_to_req_for(cfg))
+
+
+def dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def run_gpu(case: dict, fused: bool = True) -> dict:
+    """The launch sequence the benchmark times: fused shard top-K + pack, merge,
+    convert.  Also returns the error word."""
+    import dsa_sparse_indexer_gb300 as dsa
+    cfg = case["cfg"]
+    logits = dev(case["local"])
+    starts = dev(case["starts"])
+    ends = dev(case["ends"])
+    bt = dev(case["bt"])
+    r2q = None if case["r2q"] is None else dev(case["r2q"])
+    err = dsa.new_error_flags("cuda")
+    if fused:
+        local_idx, cand = dsa.shard_topk_pack(logits, ends, cfg.K, cfg.I, row_starts=starts,
+                                              err_flags=err)
+    else:
+        local_idx = dsa.shard_topk(logits, ends, cfg.K, cfg.I, row_starts=starts, err_flags=err)
+        cand = dsa.pack_candidates(logits, local_idx, cfg.I, err_flags=err)
+    ids, scores = dsa.merge_topk_stable(cand, cfg.K, want_scores=True, err_flags=err)
+    slots, counts = dsa.convert_index_compact(ids, bt, cfg.block_size, cfg.I, row_to_req=r2q,
+                                              err_flags=err)
+    torch.cuda.synchronize()
+    cand_np = cand.cpu().numpy()
+    return dict(local_idx=local_idx.cpu().numpy(), cand_scores=cand_np[..., 0],
+                cand_ids=cand_np[..., 1].view(np.int32), ids=ids.cpu().numpy(),
+                scores=scores.cpu().numpy(), slots=slots.cpu().numpy(),
+                counts=counts.cpu().numpy(), err=int(err.item()))
+
+
+def run_oracle(case: dict, rows) -> dict:
+    cfg = case["cfg"]
+    return OP.run_rows(case["local"], case["starts"], case["ends"], cfg.S, cfg.I, cfg.K,
+                       rows=rows, tables=case["bt"], row_to_req=case["r2q"],
+                       block_size=cfg.block_size)
+
+
+def bits(a) -> np.ndarray:
+    return np.ascontiguousarray(a, np.float32).view(np.uint32)
+
+
+def assert_indexer_parity(case: dict, got: dict, rows) -> None:
+    """Bit-exact comparison of every indexer output on the listed rows."""
+    cfg = case["cfg"]
+    want = run_oracle(case, rows)
+    rows = np.asarray(rows)
+    assert got["err"] == 0
+    np.testing.assert_array_equal(got["local_idx"][:, rows], want["local_idx"])
+    np.testing.assert_array_equal(bits(got["cand_scores"][rows]), bits(want["cand_scores"]))
+    np.testing.assert_array_equal(got["cand_ids"][rows], want["cand_ids"])
+    np.testing.assert_array_equal(got["ids"][rows], want["ids"])
+    # scores: value equality (-0.0 may come back as +0.0)
+    np.testing.assert_array_equal(got["scores"][rows], want["scores"])
+    np.testing.assert_array_equal(got["slots"][:, rows], want["slots"])
+    np.testing.assert_array_equal(got["counts"][:, rows], want["counts"])
+    # and the merged ids are the definition: top-K of the unsharded row
+    for j, r in enumerate(rows):
+        ref_ids, _ = OX.global_topk(case["x"][r], int(case["starts"][r]), int(case["ends"][r]),
+                                    cfg.K)
+        np.testing.assert_array_equal(got["ids"][r], ref_ids)
+    return want
+
+
+def bf16_ulp(ref: np.ndarray) -> np.ndarray:
+    a = np.maximum(np.abs(ref), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def combine_tolerance(ref: np.ndarray) -> np.ndarray:
+    """bf16 output vs the oracle's unrounded fp64: 1e-2 absolute, widened to half
+    a bf16 ulp (+ fp32 accumulation slack) where a bf16 ulp exceeds it."""
+    return np.maximum(1e-2, 0.5 * bf16_ulp(ref) + 1e-5 * np.maximum(1.0, np.abs(ref)))
+
+
+def assert_combine_parity(out_bf16: torch.Tensor, lse: torch.Tensor, part_bits: np.ndarray,
+                          lse2: np.ndarray, rows) -> None:
+    rows = np.asarray(rows)
+    ref_out, ref_lse = OC.lse_combine(OC.bf16_to_f64(part_bits[:, rows]), lse2[:, rows])
+    got = out_bf16.float().cpu().numpy()[rows].astype(np.float64)
+    tol = combine_tolerance(ref_out)
+    bad = np.abs(got - ref_out) > tol
+    assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], ref_out[bad][:5])
+    got_lse = lse.cpu().numpy()[rows].astype(np.float64)
+    inf = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(got_lse), inf)
+    d = np.abs(got_lse[~inf] - ref_lse[~inf])
+    assert np.all(d <= 1e-5 * np.maximum(1.0, np.abs(ref_lse[~inf]))), d.max()

@@ -203,7 +203,8 @@ def combine_inputs(cfg: Config, empty: np.ndarray | None = None, replica: int = 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 to bf16 (round to nearest, ties to even); returns uint16 bits.
     Inputs are finite."""
-    b = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
-    rounded = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    b = np.ascontiguousarray(x, np.float32).view(np.uint32)
+    # finite inputs: the largest sum, 0xFF7FFFFF + 0x8000, still fits in uint32
+    rounded = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return rounded.astype(np.uint16)
 
