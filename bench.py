@@ -46,9 +46,16 @@ import workloads as W  # noqa: E402
 WORKLOAD = "decode"
 METRIC = "merged top-K rows/s"
 REPLICAS = 8                 # rotating input sets: 8 x ~52 MB > 2 x L2 (126 MB)
-KERNELS = ("shard_topk_pack", "merge_topk_stable", "convert_index_compact", "lse_combine")
-KERNEL_SOURCES = {"shard_topk_pack": "shard_topk.cu", "merge_topk_stable": "merge.cu",
-                  "convert_index_compact": "convert.cu", "lse_combine": "combine.cu"}
+PATHS = {
+    # one kernel for steps a1-a4 (a cluster of S CTAs per row), then the combine
+    "fused": ("indexer_fused", "lse_combine"),
+    # one kernel per step (a1+a2 fused), then the combine
+    "steps": ("shard_topk_pack", "merge_topk_stable", "convert_index_compact", "lse_combine"),
+}
+KERNEL_SOURCES = {"shard_topk_pack": ("shard_topk.cu", "local_topk.cuh"),
+                  "merge_topk_stable": ("merge.cu",), "convert_index_compact": ("convert.cu",),
+                  "indexer_fused": ("fused.cu", "local_topk.cuh"),
+                  "lse_combine": ("combine.cu",)}
 
 
 # ---------------------------------------------------------------------------
@@ -110,10 +117,13 @@ def algorithmic_bytes(cfg, ends: np.ndarray) -> dict:
         written, per row.
     """
     S, K, R, H, D = cfg.S, cfg.K, cfg.rows, cfg.H, cfg.D
+    logits = 4 * ends.astype(np.int64).sum()
     return {
-        "shard_topk_pack": int(4 * ends.astype(np.int64).sum() + R * 8 * S * K),
+        "shard_topk_pack": int(logits + R * 8 * S * K),
         "merge_topk_stable": int(R * (8 * S * K + 4 * K)),
         "convert_index_compact": int(R * (4 * K + 4 * K + 4 * S * K + 4 * S)),
+        # logits once, one table word per merged id, ids + slots + counts written
+        "indexer_fused": int(logits + R * (4 * K + 4 * K + 4 * S * K + 4 * S)),
         "lse_combine": int(R * (S * H * D * 2 + S * H * 4 + H * D * 2 + H * 4)),
     }
 
@@ -208,7 +218,7 @@ def measured_peak() -> tuple[float, str]:
 def kernel_source_hash(kernel: str) -> str:
     csrc = os.path.join(ROOT, "dsa_sparse_indexer_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (KERNEL_SOURCES[kernel], "common.cuh", "select.cuh"):
+    for f in KERNEL_SOURCES[kernel] + ("common.cuh", "select.cuh"):
         p = os.path.join(csrc, f)
         if os.path.exists(p):
             h.update(open(p, "rb").read())
@@ -301,14 +311,13 @@ def run_reference(args, world, rank):
     return 0
 
 
-def config_block(cfg) -> dict:
+def config_block(cfg, path: str = "fused") -> dict:
     return {"workload": "decode batch: 64 rows, S=4, I=1, K=2048, seq_len U[8192, 65536], "
                         "N(0,1) fp32 logits, block_size 64 permuted per shard, combine "
                         "[4, 64, 128, 512] bf16 with base-2 LSE U[-5, 20]",
             "rows": cfg.rows, "S": cfg.S, "I": cfg.I, "K": cfg.K, "block_size": cfg.block_size,
             "H": cfg.H, "D": cfg.D,
-            "path": "shard_topk_pack -> merge_topk_stable -> convert_index_compact -> "
-                    "lse_combine (C ABI, one stream)",
+            "path": " -> ".join(PATHS[path]) + " (C ABI, one stream)",
             "l2": f"{REPLICAS} rotating input sets (> 2x L2); no flush",
             "parallelism": "replicas (rows independent, no collective)"}
 
@@ -324,6 +333,8 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=sorted(PATHS), default="fused",
+                    help="fused: one cluster kernel for steps a1-a4; steps: one kernel per step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -364,18 +375,27 @@ def main(argv=None) -> int:
     P = lambda t: t.data_ptr()
     ld = cfg.ld
 
+    KERNELS = PATHS[args.path]
     calls = []
     for st in sets:
-        calls.append((
-            (lib.dsa_shard_topk_pack, (P(st["logits"]), ld, R, S, cfg.I, K, P(st["starts"]),
-                                       P(st["ends"]), None, P(cand), P(err), sp)),
-            (lib.dsa_merge_topk_stable, (P(cand), R, S * K, K, P(ids), None, P(err), sp)),
-            (lib.dsa_convert_index_compact, (P(ids), R, K, S, cfg.I, P(st["bt"]), cfg.reqs,
-                                             cfg.max_blocks, cfg.block_size, None, P(slots),
-                                             P(counts), P(err), sp)),
-            (lib.dsa_lse_combine, (P(st["part"]), P(st["lse2"]), S, R, H, D, P(out), P(lse),
-                                   sp)),
-        ))
+        combine = (lib.dsa_lse_combine, (P(st["part"]), P(st["lse2"]), S, R, H, D, P(out),
+                                         P(lse), sp))
+        if args.path == "fused":
+            calls.append((
+                (lib.dsa_indexer_fused, (P(st["logits"]), ld, R, S, cfg.I, K, P(st["starts"]),
+                                         P(st["ends"]), P(st["bt"]), cfg.reqs, cfg.max_blocks,
+                                         cfg.block_size, None, P(ids), None, P(slots),
+                                         P(counts), None, None, P(err), sp)),
+                combine))
+        else:
+            calls.append((
+                (lib.dsa_shard_topk_pack, (P(st["logits"]), ld, R, S, cfg.I, K, P(st["starts"]),
+                                           P(st["ends"]), None, P(cand), P(err), sp)),
+                (lib.dsa_merge_topk_stable, (P(cand), R, S * K, K, P(ids), None, P(err), sp)),
+                (lib.dsa_convert_index_compact, (P(ids), R, K, S, cfg.I, P(st["bt"]), cfg.reqs,
+                                                 cfg.max_blocks, cfg.block_size, None,
+                                                 P(slots), P(counts), P(err), sp)),
+                combine))
 
     def launch(fn, a):
         status = fn(*a)
@@ -513,7 +533,7 @@ def main(argv=None) -> int:
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": config_block(cfg),
+        "data": "synthetic", "config": config_block(cfg, args.path),
         "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
         "hbm_frac_step": step_bytes / (ms_per_step / 1e3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,

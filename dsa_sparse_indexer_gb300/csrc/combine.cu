@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(kCombThreads)
     if (lse_out && lane == 0) lse_out[rh] = -INFINITY;
     return;
   }
+  // The slice loop below is warp-uniform (the shuffles need every lane); a
+  // lane past the end of D only skips its loads and its store.
   const float w0 = a0 == -INFINITY ? 0.f : exp2f(a0 - M);
   const float w1 = a1 == -INFINITY ? 0.f : exp2f(a1 - M);
   float wsum = w0 + w1;
@@ -67,7 +69,9 @@ __global__ void __launch_bounds__(kCombThreads)
   for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(kFull, wsum, o);
   const float inv = 1.f / wsum;
 
-  for (int d = lane * 8; d < D; d += 256) {
+  for (int d0 = 0; d0 < D; d0 += 256) {
+    const int d = d0 + lane * 8;
+    const bool in = d < D;
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
@@ -80,7 +84,7 @@ __global__ void __launch_bounds__(kCombThreads)
         const float ws = __shfl_sync(kFull, s < 32 ? w0 : w1, s & 31);
         w[u] = s < S ? ws : 0.f;
         v[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (w[u] != 0.f)
+        if (in && w[u] != 0.f)
           v[u] = __ldg(reinterpret_cast<const uint4*>(part + ((int64_t)s * RH + rh) * D + d));
       }
 #pragma unroll
@@ -92,7 +96,7 @@ __global__ void __launch_bounds__(kCombThreads)
     o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
     o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
     o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4*>(dst + d) = o;
+    if (in) *reinterpret_cast<uint4*>(dst + d) = o;
   }
   if (lse_out && lane == 0) lse_out[rh] = (M + log2f(wsum)) * kLn2;
 }
@@ -107,11 +111,11 @@ using namespace dsa;
 extern "C" dsa_status dsa_lse_combine(const uint16_t* partial_out, const float* lse2, int S,
                                       int rows, int H, int D, uint16_t* out, float* lse_out,
                                       cudaStream_t stream) {
-  if (!partial_out || !lse2 || !out || rows < 0 || H < 1 || D < 8 || (D & 7) ||
-      !aligned16(partial_out) || !aligned16(out))
-    return DSA_ERR_INVALID_ARG;
+  if (rows < 0 || H < 1 || D < 8 || (D & 7)) return DSA_ERR_INVALID_ARG;
   if (S < 1 || S > DSA_MAX_SHARDS) return DSA_ERR_UNSUPPORTED;
   if (rows == 0) return DSA_OK;
+  if (!partial_out || !lse2 || !out || !aligned16(partial_out) || !aligned16(out))
+    return DSA_ERR_INVALID_ARG;
   const int64_t warps = (int64_t)rows * H;
   const int64_t blocks = (warps + kCombWarps - 1) / kCombWarps;
   if (blocks > INT32_MAX) return DSA_ERR_UNSUPPORTED;

@@ -66,24 +66,30 @@ __global__ void __launch_bounds__(kConvThreads)
   }
   __syncthreads();
 
+  // Issue every block-table load of this warp before the dependent compaction.
   bool bad = !req_ok;
+  int slot_c[kMaxChunks];
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    slot_c[c] = -1;
+    if (c < nch && own_c[c] >= 0) {
+      const int id = id_c[c], o = own_c[c];
+      const int64_t l = local_slot_of(id, S, I);
+      const int64_t col = l / bs;
+      if (req_ok && col < max_blocks) {
+        const int blk = __ldg(bt + ((int64_t)o * reqs + req) * max_blocks + col);
+        const int64_t v = (int64_t)blk * bs + l % bs;
+        if (blk >= 0 && v <= (int64_t)INT32_MAX) slot_c[c] = (int)v;
+        else bad = true;
+      } else {
+        bad = true;
+      }
+    }
+  }
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     if (c < nch) {
-      const int id = id_c[c], o = own_c[c];
-      int slot = -1;
-      if (o >= 0) {
-        const int64_t l = local_slot_of(id, S, I);
-        const int64_t col = l / bs;
-        if (req_ok && col < max_blocks) {
-          const int blk = bt[((int64_t)o * reqs + req) * max_blocks + col];
-          const int64_t v = (int64_t)blk * bs + l % bs;
-          if (blk >= 0 && v <= (int64_t)INT32_MAX) slot = (int)v;
-          else bad = true;
-        } else {
-          bad = true;
-        }
-      }
+      const int o = own_c[c], slot = slot_c[c];
       const unsigned peers = __match_any_sync(kFull, o);
       if (o >= 0) slots[((int64_t)o * rows + r) * K + cnt[warp][o] + __popc(peers & lt)] = slot;
       __syncwarp();
@@ -113,12 +119,11 @@ extern "C" dsa_status dsa_convert_index_compact(const int32_t* ids, int rows, in
                                                 const int32_t* row_to_req, int32_t* slots,
                                                 int32_t* counts, uint32_t* err_flags,
                                                 cudaStream_t stream) {
-  if (!ids || !block_table || !slots || rows < 0 || reqs < 1 || max_blocks < 1 ||
-      block_size < 1)
-    return DSA_ERR_INVALID_ARG;
+  if (rows < 0 || reqs < 1 || max_blocks < 1 || block_size < 1) return DSA_ERR_INVALID_ARG;
   if (S < 1 || S > DSA_MAX_SHARDS || I < 1) return DSA_ERR_UNSUPPORTED;
   if (K != 512 && K != 1024 && K != 2048) return DSA_ERR_UNSUPPORTED;
   if (rows == 0) return DSA_OK;
+  if (!ids || !block_table || !slots) return DSA_ERR_INVALID_ARG;
   convert_kernel<<<rows, kConvThreads, 0, stream>>>(ids, rows, K, S, I, block_table, reqs,
                                                     max_blocks, block_size, row_to_req, slots,
                                                     counts, err_flags);

@@ -183,10 +183,11 @@ using namespace dsa;
 extern "C" dsa_status dsa_merge_topk_stable(const float* cand, int rows, int C, int K,
                                             int32_t* ids, float* scores, uint32_t* err_flags,
                                             cudaStream_t stream) {
-  if (!cand || !ids || rows < 0 || C < 0 || !aligned16(cand)) return DSA_ERR_INVALID_ARG;
+  if (rows < 0 || C < 0) return DSA_ERR_INVALID_ARG;
   if (K != 512 && K != 1024 && K != 2048) return DSA_ERR_UNSUPPORTED;
   if (C < K || (C & 3)) return DSA_ERR_INVALID_ARG;
   if (rows == 0) return DSA_OK;
+  if (!cand || !ids || !aligned16(cand)) return DSA_ERR_INVALID_ARG;
   const int stage_cap = kStageCapCand;
   const size_t smem = merge_stage_offset() + (size_t)min(C, stage_cap) * sizeof(float2);
   if (cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -12,7 +12,8 @@ import torch
 from . import _lib
 
 __all__ = ["shard_topk", "pack_candidates", "shard_topk_pack", "merge_topk_stable",
-           "convert_index_compact", "lse_combine", "new_error_flags", "SUPPORTED_K"]
+           "convert_index_compact", "indexer_fused", "lse_combine", "new_error_flags",
+           "SUPPORTED_K"]
 
 SUPPORTED_K = (512, 1024, 2048)
 
@@ -129,6 +130,47 @@ def convert_index_compact(ids, block_table, block_size: int, I: int, row_to_req=
               max_blocks, block_size, _ptr(row_to_req), _ptr(slots), _ptr(counts),
               _ptr(err_flags), _stream(ids))
     return slots, counts
+
+
+def indexer_fused(logits, row_ends, K: int, I: int, block_table, block_size: int,
+                  row_starts=None, row_to_req=None, ids=None, slots=None, counts=None,
+                  want_scores: bool = False, want_local_idx: bool = False,
+                  want_cand: bool = False, err_flags=None) -> dict:
+    """Shard top-K, pack, merge and convert in one kernel (S <= 8).
+
+    Returns a dict with ids [rows, K], slots [S, rows, K], counts [S, rows] and,
+    when asked for, scores, local_idx and cand."""
+    _need(logits, "logits", torch.float32, 3)
+    S, rows, ld = logits.shape
+    _need(row_ends, "row_ends", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 3)
+    if block_table.shape[0] != S:
+        raise ValueError("block_table must be [S, reqs, max_blocks]")
+    _, reqs, max_blocks = block_table.shape
+    for name, t in (("row_starts", row_starts), ("row_to_req", row_to_req)):
+        if t is not None:
+            _need(t, name, torch.int32, 1)
+    dv = logits.device
+    out = {
+        "ids": ids if ids is not None else torch.empty((rows, K), dtype=torch.int32, device=dv),
+        "slots": slots if slots is not None else
+        torch.empty((S, rows, K), dtype=torch.int32, device=dv),
+        "counts": counts if counts is not None else
+        torch.empty((S, rows), dtype=torch.int32, device=dv),
+        "scores": torch.empty((rows, K), dtype=torch.float32, device=dv) if want_scores else None,
+        "local_idx": torch.empty((S, rows, K), dtype=torch.int32, device=dv)
+        if want_local_idx else None,
+        "cand": torch.empty((rows, S * K, 2), dtype=torch.float32, device=dv)
+        if want_cand else None,
+    }
+    _need(out["ids"], "ids", torch.int32, 2)
+    _need(out["slots"], "slots", torch.int32, 3)
+    _need(out["counts"], "counts", torch.int32, 2)
+    _lib.call("dsa_indexer_fused", _ptr(logits), ld, rows, S, I, K, _ptr(row_starts),
+              _ptr(row_ends), _ptr(block_table), reqs, max_blocks, block_size, _ptr(row_to_req),
+              _ptr(out["ids"]), _ptr(out["scores"]), _ptr(out["slots"]), _ptr(out["counts"]),
+              _ptr(out["local_idx"]), _ptr(out["cand"]), _ptr(err_flags), _stream(logits))
+    return out
 
 
 def lse_combine(partial_out, lse2, out=None, lse_out=None, want_lse: bool = True):

@@ -15,7 +15,9 @@
  *   dsa_lse_combine       LSE-weighted combine of the shards' partial
  *                         attention outputs, base-2 LSE converted to base e
  *
- * plus dsa_shard_topk_pack, the first two steps fused in one kernel.
+ * plus dsa_shard_topk_pack (the first two steps in one kernel) and
+ * dsa_indexer_fused (the first four steps in one kernel per row, a thread-block
+ * cluster of S CTAs exchanging candidates through distributed shared memory).
  *
  * Sharding (PR #46076 report, section 关键源码片段, comment in
  * `_dcp_localize_decode_seq_lens`): global token t lives on shard
@@ -36,7 +38,8 @@
  *     enqueues one kernel; results are ready when the stream reaches it.
  *   - Arguments are checked on the host before anything is enqueued.  A bad
  *     argument returns DSA_ERR_INVALID_ARG or DSA_ERR_UNSUPPORTED and touches
- *     nothing.  rows == 0 returns DSA_OK and enqueues nothing.
+ *     nothing.  rows == 0 returns DSA_OK and enqueues nothing once the scalar
+ *     arguments pass (array pointers are then not checked and may be NULL).
  *   - DSA_ERR_CUDA means the launch itself failed (cudaGetLastError).
  *   - Problems only visible on the device set bits of `*err_flags` (a caller
  *     owned device word, may be NULL) with atomicOr; kernels never trap.
@@ -171,6 +174,39 @@ dsa_status dsa_convert_index_compact(const int32_t* ids, int rows, int K, int S,
                                      int block_size, const int32_t* row_to_req,
                                      int32_t* slots, int32_t* counts, uint32_t* err_flags,
                                      cudaStream_t stream);
+
+/*
+ * dsa_indexer_fused - dsa_shard_topk, dsa_pack_candidates, dsa_merge_topk_stable
+ * and dsa_convert_index_compact for each row in one kernel, with the same
+ * results.  PR #46076 report, section 关键源码片段 (`_merge_dcp_topk_global`:
+ * local top-K on every rank, candidate all_gather, stable selector) and section
+ * 实现拆解 items 1, 2 and 4.
+ *
+ * Each row is handled by a thread-block cluster of S CTAs, one per shard; the
+ * candidates a shard selects stay in its shared memory and the all_gather of
+ * the pages becomes distributed-shared-memory reads inside the cluster, so
+ * neither candidates nor merged ids make a round trip through HBM.
+ *
+ *   logits, ld, rows, S, I, K, row_starts, row_ends   as dsa_shard_topk
+ *   block_table, reqs, max_blocks, block_size, row_to_req
+ *                    as dsa_convert_index_compact
+ *   ids      [rows][K] int32 out, as dsa_merge_topk_stable
+ *   scores   [rows][K] fp32 out, may be NULL, as dsa_merge_topk_stable
+ *   slots    [S][rows][K] int32 out, counts [S][rows] int32 out (may be NULL),
+ *            as dsa_convert_index_compact
+ *   local_idx [S][rows][K] int32 out, may be NULL, as dsa_shard_topk
+ *   cand     [rows][S*K][2] fp32 out, may be NULL, as dsa_pack_candidates
+ *   err_flags as the single-step calls.
+ * Errors: as the single-step calls; S > 8 (the portable cluster size) returns
+ * DSA_ERR_UNSUPPORTED (use the single-step calls).
+ */
+dsa_status dsa_indexer_fused(const float* logits, int64_t ld, int rows, int S, int I, int K,
+                             const int32_t* row_starts, const int32_t* row_ends,
+                             const int32_t* block_table, int reqs, int max_blocks,
+                             int block_size, const int32_t* row_to_req, int32_t* ids,
+                             float* scores, int32_t* slots, int32_t* counts,
+                             int32_t* local_idx, float* cand, uint32_t* err_flags,
+                             cudaStream_t stream);
 
 /*
  * dsa_lse_combine - merge the shards' partial attention outputs by their LSE.

@@ -101,6 +101,33 @@ def test_convert_argument_checks(lib):
     assert call(K=64) == UNSUPPORTED
 
 
+def test_fused_argument_checks(lib):
+    f = lib.dsa_indexer_fused
+
+    def call(logits=P, ld=1024, rows=4, S=4, I=1, K=512, ends=P, bt=P, reqs=4, mb=8, bs=64,
+             ids=P, slots=P, cand=NULL):
+        return f(logits, ld, rows, S, I, K, NULL, ends, bt, reqs, mb, bs, NULL, ids, NULL, slots,
+                 NULL, NULL, cand, NULL, NULL)
+    assert call(rows=0, logits=NULL, ends=NULL, bt=NULL, ids=NULL, slots=NULL) == OK
+    assert call(logits=NULL) == INVALID
+    assert call(ends=NULL) == INVALID
+    assert call(bt=NULL) == INVALID
+    assert call(ids=NULL) == INVALID
+    assert call(slots=NULL) == INVALID
+    assert call(cand=P + 8) == INVALID
+    assert call(ld=1023) == INVALID
+    assert call(bs=0) == INVALID
+    assert call(S=9) == UNSUPPORTED        # above the portable cluster size
+    assert call(S=0) == UNSUPPORTED
+    assert call(K=4096) == UNSUPPORTED
+
+
+def test_zero_rows_accepts_null_arrays(lib):
+    assert lib.dsa_shard_topk(NULL, 64, 0, 2, 1, 512, NULL, NULL, NULL, NULL, NULL) == OK
+    assert lib.dsa_merge_topk_stable(NULL, 0, 1024, 512, NULL, NULL, NULL, NULL) == OK
+    assert lib.dsa_lse_combine(NULL, NULL, 2, 0, 4, 64, NULL, NULL, NULL) == OK
+
+
 def test_combine_argument_checks(lib):
     f = lib.dsa_lse_combine
     assert f(P, P, 4, 0, 8, 64, P, NULL, NULL) == OK

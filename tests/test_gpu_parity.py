@@ -57,6 +57,17 @@ def test_merge_alone_on_oracle_candidates():
     np.testing.assert_array_equal(scores.cpu().numpy(), want["scores"])
 
 
+@pytest.mark.parametrize("name,nsample", [("tiny", 4), ("decode", 64), ("long_decode", 128),
+                                          ("prefill", 40), ("ragged", 256)])
+def test_fused_cluster_kernel_parity_full_size(name, nsample):
+    case = G.make_case(name)
+    got = G.run_gpu_fused(case)
+    G.assert_indexer_parity(case, got, sample_rows(case["cfg"], nsample))
+    lean = G.run_gpu_fused(case, with_intermediates=False)   # the benchmark's call
+    for k in ("ids", "slots", "counts"):
+        np.testing.assert_array_equal(lean[k], got[k])
+
+
 def test_reads_stay_inside_each_rows_range():
     """+inf canaries at every slot past a row's end must never be selected."""
     case = G.make_case("ragged", fill=np.inf)
@@ -92,6 +103,7 @@ def test_small_shapes_ties_and_tails(K, S, I):
     for fused in (True, False):
         got = G.run_gpu(case, fused=fused)
         G.assert_indexer_parity(case, got, np.arange(rows))
+    G.assert_indexer_parity(case, G.run_gpu_fused(case), np.arange(rows))
 
 
 def test_rows_longer_than_the_shared_memory_stage():
@@ -112,6 +124,23 @@ def test_rows_longer_than_the_shared_memory_stage():
                 r2q=None)
     got = G.run_gpu(case)
     G.assert_indexer_parity(case, got, np.arange(rows))
+
+
+def test_fused_rows_longer_than_the_shared_memory_stage():
+    rng = np.random.default_rng(12)
+    rows, S, I, K = 3, 8, 2, 1024
+    ld = 52000
+    Lmax = S * ld
+    x = (np.rint(rng.standard_normal((rows, Lmax)) * 16) / 16).astype(np.float32)
+    ends = np.array([Lmax, Lmax - 999, 3000], np.int32)
+    cfg = W.Config("adhoc", 9, rows=rows, S=S, I=I, K=K, block_size=32, max_len=Lmax, ld=ld,
+                   reqs=rows, max_blocks=(ld + 31) // 32)
+    local = OL.shard_rows(x, ends, S, I, ld)
+    bt = np.stack([rng.permutation(rows * cfg.max_blocks).astype(np.int32).reshape(rows, -1)
+                   for _ in range(S)])
+    case = dict(cfg=cfg, x=x, local=local, starts=np.zeros(rows, np.int32), ends=ends, bt=bt,
+                r2q=None)
+    G.assert_indexer_parity(case, G.run_gpu_fused(case), np.arange(rows))
 
 
 def test_out_of_range_ends_and_tables_set_the_bounds_flag():
@@ -142,6 +171,9 @@ def test_zero_rows_is_a_no_op():
     logits = torch.zeros(2, 0, 64, device="cuda")
     out = dsa.shard_topk(logits, torch.zeros(0, dtype=torch.int32, device="cuda"), 512, 1)
     assert out.shape == (2, 0, 512)
+    o = dsa.indexer_fused(logits, torch.zeros(0, dtype=torch.int32, device="cuda"), 512, 1,
+                          torch.zeros(2, 1, 4, dtype=torch.int32, device="cuda"), 64)
+    assert o["ids"].shape == (0, 512)
 
 
 def _combine_case(name, rows=None):
