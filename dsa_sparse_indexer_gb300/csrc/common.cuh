@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "dsa.h"
+#include "fastdiv.h"
 
 namespace dsa {
 
@@ -52,6 +53,30 @@ __host__ __device__ __forceinline__ int64_t local_len(int64_t L, int s, int S, i
   rem = rem < 0 ? 0 : (rem > I ? I : rem);
   return (L / round) * I + rem;
 }
+
+// The same maps on 32-bit ids (< 2^31) with the divisions by I, I*S and S
+// precomputed on the host (fastdiv.h).
+struct ShardMath {
+  int S, I;
+  FastDiv fI, fIS, fS;
+  ShardMath() : S(1), I(1) {}
+  ShardMath(int S_, int I_) : S(S_), I(I_), fI(I_), fIS((uint32_t)(I_ * S_)), fS(S_) {}
+
+  __device__ __forceinline__ int owner(uint32_t t) const {
+    const uint32_t q = fdiv(t, fI);
+    return (int)(q - fdiv(q, fS) * (uint32_t)S);
+  }
+  __device__ __forceinline__ uint32_t local_slot(uint32_t t) const {
+    uint32_t r;
+    fdivmod(t, fI, &r);
+    return fdiv(t, fIS) * (uint32_t)I + r;
+  }
+  __device__ __forceinline__ uint32_t global_id(int s, uint32_t l) const {
+    uint32_t r;
+    const uint32_t q = fdivmod(l, fI, &r);
+    return q * fIS.d + (uint32_t)s * (uint32_t)I + r;
+  }
+};
 
 __device__ __forceinline__ void raise_flag(uint32_t* flags, uint32_t bit) {
   if (flags) atomicOr(flags, bit);

@@ -6,36 +6,48 @@
 // (score, global_id) candidates, all_gather, stable selector) and section
 // 实现拆解 items 1, 2 and 4 (pack, merge, convert with compaction).
 //
-// The cluster holds S CTAs, CTA rank s playing DCP rank s.  Each CTA stages its
-// shard's local range in shared memory (bulk async copies) and selects its K
-// local candidates as in the per-shard kernel, keeping them in shared memory as
-// 64-bit rank keys (score_key << 32 | ~global_id).  The pages' all_gather of
-// candidates becomes reads of the other CTAs' shared memory (DSMEM): the
-// cluster runs a radix select over all S*K candidates with per-CTA histograms
-// summed across the cluster, each CTA sorts the global winners it holds (a
-// bitonic sort in shared memory), and a winner's global rank is its rank among
-// its own CTA's winners plus, for every other CTA, the number of that CTA's
-// winners ranked above it (binary search in a local copy of their sorted
-// lists).  A shard's winners in rank order are exactly its compacted slots, so
-// each CTA maps them through its own block table and writes them directly.
+// The cluster holds S CTAs, CTA rank s playing DCP rank s.
+//  1. Each CTA selects its shard's K local candidates: the local range is held
+//     in registers as score keys (reg_topk.cuh; longer ranges are staged in
+//     shared memory, local_topk.cuh), and the winners are kept in shared memory
+//     as 64-bit rank keys (score_key << 32 | ~global_id), in slot order.
+//  2. The pages' all_gather becomes reads of the other CTAs' shared memory
+//     (DSMEM): a radix select over all S*K candidates whose per-CTA histograms
+//     are summed across the cluster (double-buffered, one cluster barrier per
+//     digit) decides which candidates are global winners.
+//  3. Each CTA sorts the winners it holds (bitonic network over registers,
+//     warp shuffles and shared memory).  A shard's winners in rank order are
+//     exactly its compacted slots, so each CTA maps them through its own block
+//     table and writes them.
+//  4. A winner's global rank is its position among its CTA's winners plus, for
+//     every other CTA, the number of that CTA's winners ranked above it
+//     (binary search in a local copy of their sorted lists); it writes its id
+//     at that rank.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "local_topk.cuh"
+#include "reg_topk.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace dsa {
 namespace {
 
-constexpr int kFusedThreads = 512;
+constexpr int kNT = 512;
+constexpr int kVec = 8;                      // 32 keys per thread: local ranges up to 16384
 constexpr int kMaxK = 2048;
+constexpr int kCandPerThread = kMaxK / kNT;  // 4
 constexpr int kMaxCluster = 8;
+using RT = RegTopk<kNT, kVec>;
+using ull = unsigned long long;
 
 struct FusedSmem {
-  LocalTopkSmem loc;
-  uint32_t chist[2048];             // this CTA's share of a cluster-wide histogram
-  unsigned long long cand[kMaxK];   // local candidates as rank keys, slot order
+  LocalTopkSmem loc;                 // select scratch (also the staged path's barriers)
+  RegEmitSmem<kNT, kVec> es;
+  uint32_t chist[2][2048];           // cluster-visible histograms, double-buffered
+  ull cand[kMaxK];                   // this shard's candidates, slot order
+  ull win[kMaxK];                    // this shard's global winners, best first
   int scan[64];
   int wr[kMaxCluster], off[kMaxCluster];
   int m, w, total, tied, nwin, bin, above, count;
@@ -45,62 +57,89 @@ __host__ __device__ constexpr size_t fused_dyn_offset() {
   return (sizeof(FusedSmem) + 127) & ~size_t(127);
 }
 
-__device__ __forceinline__ unsigned long long rank_key(float v, int gid) {
-  return ((unsigned long long)score_key(v) << 32) | (unsigned long long)(~(uint32_t)gid);
+__device__ __forceinline__ ull rank_key(uint32_t k, uint32_t gid) {
+  return ((ull)k << 32) | (ull)(~gid);
 }
 
-// Cluster-wide version of radix_select (select.cuh): the need-th largest key
-// among all CTAs' elements i in [0, m) with key_at(i, &k) true; every CTA of
-// the cluster computes the same result.  Two cluster barriers per digit.
-template <typename KeyAt>
-__device__ SelectResult cluster_select(cg::cluster_group& cluster, int nranks, int m, int need,
-                                       KeyAt key_at, FusedSmem& sm) {
-  constexpr int NT = kFusedThreads;
+// One digit of the cluster-wide select over `h` (NB bins, PER per thread):
+// histogram this CTA's keys, then sum every CTA's histogram for this thread's
+// bins and find the bin holding the need-th key (highest bins first).
+template <int NB, int PER, typename Visit>
+__device__ __forceinline__ void cluster_digit(cg::cluster_group& cluster, int nranks, int need,
+                                              uint32_t prefix, uint32_t mask, int shift,
+                                              Visit visit, uint32_t* h, FusedSmem& sm) {
+  static_assert(NB == PER * kNT, "bins per thread");
   const int tid = threadIdx.x;
+  for (int b = tid; b < NB; b += kNT) h[b] = 0u;
+  __syncthreads();
+  visit([&](uint32_t k) {
+    if ((k & mask) == prefix) atomicAdd(&h[(k >> shift) & (NB - 1)], 1u);
+  });
+  cluster.sync();
+  const int g = NB - PER * (tid + 1);   // this thread's bins g .. g+PER-1
+  int c[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) c[j] = 0;
+  for (int rk = 0; rk < nranks; ++rk) {
+    const uint32_t* rh = cluster.map_shared_rank(h, rk);
+    if constexpr (PER == 4) {
+      const uint4 q = *reinterpret_cast<const uint4*>(rh + g);
+      c[0] += (int)q.w; c[1] += (int)q.z; c[2] += (int)q.y; c[3] += (int)q.x;
+    } else {
+      const uint2 q = *reinterpret_cast<const uint2*>(rh + g);
+      c[0] += (int)q.y; c[1] += (int)q.x;
+    }
+  }
+  int local = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) local += c[j];
+  int total;
+  int running = block_exclusive_scan(local, sm.scan, &total);
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    if (running < need && running + c[j] >= need) {
+      sm.bin = g + PER - 1 - j;
+      sm.above = running;
+      sm.count = c[j];
+    }
+    running += c[j];
+  }
+  __syncthreads();
+}
+
+// Cluster-wide radix select: the need-th largest key over every CTA's keys
+// (visit(f) calls f(k) for each key the calling thread holds).  Every CTA
+// computes the same result.  `phase` counts histogram uses across calls: the
+// buffer written in a pass was last read remotely two passes earlier, before
+// the cluster barrier of the previous pass, so one barrier per digit suffices.
+template <typename Visit>
+__device__ SelectResult cluster_select(cg::cluster_group& cluster, int nranks, int need,
+                                       Visit visit, FusedSmem& sm, int& phase) {
   uint32_t prefix = 0, mask = 0;
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int nb = pass == 2 ? 1024 : 2048;
-    const int per = nb / NT;
-    for (int b = tid; b < nb; b += NT) sm.chist[b] = 0u;
-    __syncthreads();
-    for (int i = tid; i < m; i += NT) {
-      uint32_t k;
-      if (key_at(i, k) && (k & mask) == prefix) atomicAdd(&sm.chist[(k >> shift) & (nb - 1)], 1u);
+    uint32_t* h = sm.chist[phase & 1];
+    ++phase;
+    int shift;
+    if (pass < 2) {
+      shift = pass == 0 ? 21 : 10;
+      cluster_digit<2048, 4>(cluster, nranks, need, prefix, mask, shift, visit, h, sm);
+    } else {
+      shift = 0;
+      cluster_digit<1024, 2>(cluster, nranks, need, prefix, mask, shift, visit, h, sm);
     }
-    cluster.sync();
-    int c[4] = {0, 0, 0, 0};
-    for (int rk = 0; rk < nranks; ++rk) {
-      const uint32_t* h = cluster.map_shared_rank(sm.chist, rk);
-      for (int j = 0; j < per; ++j) c[j] += (int)h[nb - 1 - (tid * per + j)];
-    }
-    int local = 0;
-    for (int j = 0; j < per; ++j) local += c[j];
-    int total;
-    int running = block_exclusive_scan(local, sm.scan, &total);
-    for (int j = 0; j < per; ++j) {
-      if (running < need && running + c[j] >= need) {
-        sm.bin = nb - 1 - (tid * per + j);
-        sm.above = running;
-        sm.count = c[j];
-      }
-      running += c[j];
-    }
-    __syncthreads();
+    const int nb = pass < 2 ? 2048 : 1024;
     const int b = sm.bin, above = sm.above, count = sm.count;
     need -= above;
     prefix |= (uint32_t)b << shift;
     mask |= (uint32_t)(nb - 1) << shift;
-    cluster.sync();  // every CTA is done reading chist before it is cleared again
     if (count == need) return SelectResult{prefix - 1u, 0};
   }
   return SelectResult{prefix, need};
 }
 
 // Entries of a descending list that rank above `key` (all keys distinct).
-__device__ __forceinline__ int count_above(const unsigned long long* list, int len,
-                                           unsigned long long key) {
+__device__ __forceinline__ int count_above(const ull* list, int len, ull key) {
   int lo = 0, hi = len;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
@@ -110,107 +149,300 @@ __device__ __forceinline__ int count_above(const unsigned long long* list, int l
   return lo;
 }
 
-__global__ void __launch_bounds__(kFusedThreads, 2)
-    fused_kernel(const float* __restrict__ logits, int64_t ld, int rows, int S, int I, int K,
-                 const int32_t* __restrict__ row_starts, const int32_t* __restrict__ row_ends,
-                 const int32_t* __restrict__ bt, int reqs, int max_blocks, int bs,
-                 const int32_t* __restrict__ row_to_req, int32_t* __restrict__ ids,
-                 float* __restrict__ scores, int32_t* __restrict__ slots,
-                 int32_t* __restrict__ counts, int32_t* __restrict__ local_idx,
-                 float* __restrict__ cand_out, uint32_t* flags, int stage_cap) {
-  constexpr int NT = kFusedThreads;
+// Descending bitonic sort of NT*E keys, thread t holding indices t*E .. t*E+E-1.
+// Partners closer than E are in the thread, closer than 32*E in the warp
+// (shuffles), farther ones go through `xchg` (NT*E entries of shared memory).
+template <int E>
+__device__ __forceinline__ void bitonic_desc(ull (&v)[E], ull* xchg) {
+  const int t = threadIdx.x;
+  constexpr int P = kNT * E;
+#pragma unroll 1
+  for (int k = 2; k <= P; k <<= 1) {
+#pragma unroll 1
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < E) {
+        // partners inside the thread; j is 1 or 2, spelled out so v stays in registers
+        if (j == 1) {
+#pragma unroll
+          for (int e = 0; e < E; e += 2) {
+            const bool desc = ((t * E + e) & k) == 0;
+            const ull a = v[e], b = v[e + 1];
+            if ((a < b) == desc) { v[e] = b; v[e + 1] = a; }
+          }
+        } else if constexpr (E == 4) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool desc = ((t * E + e) & k) == 0;
+            const ull a = v[e], b = v[e + 2];
+            if ((a < b) == desc) { v[e] = b; v[e + 2] = a; }
+          }
+        }
+      } else if (j < 32 * E) {
+        const int lm = j / E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = t * E + e;
+          const ull other = __shfl_xor_sync(kFull, v[e], lm);
+          const bool keep_max = ((i & j) == 0) == ((i & k) == 0);
+          v[e] = keep_max ? (v[e] > other ? v[e] : other) : (v[e] < other ? v[e] : other);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) xchg[t * E + e] = v[e];
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = t * E + e;
+          const ull other = xchg[i ^ j];
+          const bool keep_max = ((i & j) == 0) == ((i & k) == 0);
+          v[e] = keep_max ? (v[e] > other ? v[e] : other) : (v[e] < other ? v[e] : other);
+        }
+        __syncthreads();
+      }
+    }
+  }
+}
+
+struct FusedArgs {
+  const float* logits;
+  int64_t ld;
+  int rows, S, I, K;
+  const int32_t* row_starts;
+  const int32_t* row_ends;
+  const int32_t* bt;
+  int reqs, max_blocks, bs;
+  const int32_t* row_to_req;
+  int32_t* ids;
+  float* scores;
+  int32_t* slots;
+  int32_t* counts;
+  int32_t* local_idx;
+  float* cand_out;
+  uint32_t* flags;
+  int stage_cap;
+  ShardMath sh;
+  FastDiv fbs;
+};
+
+// Slots and global ranks for this CTA's E-per-thread sorted winners.
+template <int E>
+__device__ __forceinline__ void finish_winners(const FusedArgs& a, cg::cluster_group& cluster,
+                                               FusedSmem& sm, ull* others, int s, int r, int w,
+                                               int total) {
+  const int tid = threadIdx.x;
+  ull v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = tid * E + e;
+    v[e] = i < w ? sm.win[i] : 0ull;
+  }
+  __syncthreads();
+  bitonic_desc<E>(v, sm.win);
+#pragma unroll
+  for (int e = 0; e < E; ++e) sm.win[tid * E + e] = v[e];
+
+  // ---- slots: this shard's winners in rank order, through its block table --
+  const int req = a.row_to_req ? a.row_to_req[r] : r;
+  const bool req_ok = req >= 0 && req < a.reqs;
+  const int32_t* table = a.bt + ((int64_t)s * a.reqs + (req_ok ? req : 0)) * a.max_blocks;
+  int32_t* dst = a.slots + ((int64_t)s * a.rows + r) * a.K;
+  int blk[E];
+  uint32_t off[E];
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    blk[e] = -1;
+    off[e] = 0;
+    if (tid * E + e < w) {
+      const uint32_t l = a.sh.local_slot(~(uint32_t)v[e]);
+      const uint32_t col = fdivmod(l, a.fbs, &off[e]);
+      if (req_ok && col < (uint32_t)a.max_blocks) blk[e] = __ldg(table + col);
+      else bad = true;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = tid * E + e;
+    if (i < w) {
+      const int64_t slot = (int64_t)blk[e] * a.bs + off[e];
+      const bool ok = blk[e] >= 0 && slot <= (int64_t)INT32_MAX;
+      bad |= !ok;
+      dst[i] = ok ? (int32_t)slot : -1;
+    }
+  }
+  for (int i = w + tid; i < a.K; i += kNT) dst[i] = -1;
+  if (bad) raise_flag(a.flags, DSA_FLAG_BOUNDS);
+  if (tid == 0) {
+    if (a.counts) a.counts[(int64_t)s * a.rows + r] = w;
+    sm.w = w;
+  }
+  cluster.sync();  // every CTA's sorted winners are published
+
+  // ---- merged ids: rank = own position + other shards' winners above --------
+  if (tid < a.S) sm.wr[tid] = *cluster.map_shared_rank(&sm.w, tid);
+  __syncthreads();
+  if (tid == 0) {
+    int o = 0;
+    for (int rk = 0; rk < a.S; ++rk) {
+      sm.off[rk] = o;
+      if (rk != s) o += sm.wr[rk];
+    }
+  }
+  __syncthreads();
+  for (int rk = 0; rk < a.S; ++rk) {
+    if (rk == s) continue;
+    const ull* remote = cluster.map_shared_rank(sm.win, rk);
+    const int len = sm.wr[rk], o = sm.off[rk];
+    for (int j = tid; j < len; j += kNT)
+      if (o + j < kMaxK) others[o + j] = remote[j];
+  }
+  __syncthreads();
+  int32_t* out_ids = a.ids + (int64_t)r * a.K;
+  float* out_sc = a.scores ? a.scores + (int64_t)r * a.K : nullptr;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = tid * E + e;
+    if (i < w) {
+      int rank = i;
+      for (int rk = 0; rk < a.S; ++rk)
+        if (rk != s) rank += count_above(others + sm.off[rk], sm.wr[rk], v[e]);
+      if (rank < a.K) {
+        out_ids[rank] = (int32_t)~(uint32_t)v[e];
+        if (out_sc) out_sc[rank] = key_score((uint32_t)(v[e] >> 32));
+      }
+    }
+  }
+  if (s == 0) {
+    for (int j = min(total, a.K) + tid; j < a.K; j += kNT) {
+      out_ids[j] = -1;
+      if (out_sc) out_sc[j] = -INFINITY;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   FusedSmem& sm = *reinterpret_cast<FusedSmem*>(smem_raw);
-  unsigned char* dyn = smem_raw + fused_dyn_offset();
+  ull* others = reinterpret_cast<ull*>(smem_raw + fused_dyn_offset());
+  float* stage = reinterpret_cast<float*>(others + kMaxK);
   const int tid = threadIdx.x, lane = tid & 31;
   const int s = (int)cluster.block_rank();
-  const int r = blockIdx.x / S;
-  const float* row = logits + ((int64_t)s * rows + r) * ld;
+  const int r = blockIdx.x / a.S;
+  const int K = a.K;
+  const float* row = a.logits + ((int64_t)s * a.rows + r) * a.ld;
 
   // ---- this shard's local range ------------------------------------------
-  int64_t st = row_starts ? (int64_t)row_starts[r] : 0, en = row_ends[r];
+  int64_t st = a.row_starts ? (int64_t)a.row_starts[r] : 0, en = a.row_ends[r];
   bool bad = false;
   if (st < 0) { st = 0; bad = true; }
   if (en < st) { en = st; bad = true; }
-  int64_t lo = local_len(st, s, S, I), hi = local_len(en, s, S, I);
-  if (hi > ld) { hi = ld; bad = true; }
+  int64_t lo = local_len(st, s, a.S, a.I), hi = local_len(en, s, a.S, a.I);
+  if (hi > a.ld) { hi = a.ld; bad = true; }
   if (lo > hi) { lo = hi; bad = true; }
   const int n = (int)(hi - lo);
   if (tid == 0) {
-    if (bad) raise_flag(flags, DSA_FLAG_BOUNDS);
+    if (bad) raise_flag(a.flags, DSA_FLAG_BOUNDS);
     sm.m = min(n, K);
     sm.tied = 0;
     sm.nwin = 0;
   }
-  int32_t* out_idx = local_idx ? local_idx + ((int64_t)s * rows + r) * K : nullptr;
-  float2* out_cand = cand_out ? reinterpret_cast<float2*>(cand_out) + ((int64_t)r * S + s) * K
-                              : nullptr;
+  int32_t* out_idx = a.local_idx ? a.local_idx + ((int64_t)s * a.rows + r) * K : nullptr;
+  float2* out_cand = a.cand_out ? reinterpret_cast<float2*>(a.cand_out) + ((int64_t)r * a.S + s) * K
+                                : nullptr;
   __syncthreads();
 
   // ---- a1 + a2: local top-K, kept as rank keys -----------------------------
+  const int64_t base = lo & ~int64_t(3);
   if (n <= K) {
-    for (int j = tid; j < K; j += NT) {
+    for (int j = tid; j < K; j += kNT) {
       if (j < n) {
-        const int64_t l = lo + j;
+        const uint32_t l = (uint32_t)(lo + j);
         const float v = row[l];
-        const int gid = (int)global_of(s, l, S, I);
-        sm.cand[j] = rank_key(v, gid);
+        const uint32_t gid = a.sh.global_id(s, l);
+        sm.cand[j] = rank_key(score_key(v), gid);
         if (out_idx) out_idx[j] = (int32_t)l;
-        if (out_cand) out_cand[j] = make_float2(v, __int_as_float(gid));
+        if (out_cand) out_cand[j] = make_float2(v, __int_as_float((int)gid));
       } else {
         if (out_idx) out_idx[j] = -1;
         if (out_cand) out_cand[j] = make_float2(-INFINITY, __int_as_float(-1));
       }
     }
+  } else if (hi - base <= RT::kCap) {
+    uint32_t key[kVec][4];
+    load_keys<kNT, kVec>(row, lo, hi, key);
+    auto visit = [&](auto&& f) {
+#pragma unroll
+      for (int j = 0; j < kVec; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (key[j][c]) f(key[j][c]);
+    };
+    const SelectResult res = radix_select_visit<kNT>(K, visit, sm.loc.sel);
+    emit_winners<kNT, kVec>(key, res.thr, res.take_eq, sm.es, [&](int p, int e, uint32_t k) {
+      if (p >= K) return;
+      const uint32_t l = (uint32_t)(base + e);
+      const uint32_t gid = a.sh.global_id(s, l);
+      sm.cand[p] = rank_key(k, gid);
+      if (out_idx) out_idx[p] = (int32_t)l;
+      if (out_cand) out_cand[p] = make_float2(row[l], __int_as_float((int)gid));
+    });
   } else {
     bool ok;
-    const float* data = stage_local_range(row, lo, hi, reinterpret_cast<float*>(dyn), stage_cap,
-                                          sm.loc, flags, &ok);
-    local_topk_emit<NT>(data, n, K, sm.loc, [&](int p, int i, float v) {
-      const int64_t l = lo + i;
-      const int gid = (int)global_of(s, l, S, I);
-      sm.cand[p] = rank_key(v, gid);
+    const float* data = stage_local_range(row, lo, hi, stage, a.stage_cap, sm.loc, a.flags, &ok);
+    local_topk_emit<kNT>(data, n, K, sm.loc, [&](int p, int i, float v) {
+      const uint32_t l = (uint32_t)(lo + i);
+      const uint32_t gid = a.sh.global_id(s, l);
+      sm.cand[p] = rank_key(score_key(v), gid);
       if (out_idx) out_idx[p] = (int32_t)l;
-      if (out_cand) out_cand[p] = make_float2(v, __int_as_float(gid));
+      if (out_cand) out_cand[p] = make_float2(v, __int_as_float((int)gid));
     });
   }
   cluster.sync();  // every CTA's candidates are in place
 
-  // ---- a3: select the global winners across the cluster --------------------
+  // ---- a3: which candidates are global winners ------------------------------
   if (tid == 0) {
     int t = 0;
-    for (int rk = 0; rk < S; ++rk) t += *cluster.map_shared_rank(&sm.m, rk);
+    for (int rk = 0; rk < a.S; ++rk) t += *cluster.map_shared_rank(&sm.m, rk);
     sm.total = t;
   }
   __syncthreads();
   const int total = sm.total, m = sm.m;
+  ull ck[kCandPerThread];
+#pragma unroll
+  for (int q = 0; q < kCandPerThread; ++q) {
+    const int i = tid + q * kNT;
+    ck[q] = i < m ? sm.cand[i] : 0ull;    // 0: no candidate (valid keys are > 0)
+  }
   const bool all = total <= K;
   bool tie = false;
   uint32_t thr1 = 0, thr2 = 0;
+  int phase = 0;
   if (!all) {
-    auto key1 = [&](int i, uint32_t& k) {
-      k = (uint32_t)(sm.cand[i] >> 32);
-      return true;
+    auto visit1 = [&](auto&& f) {
+#pragma unroll
+      for (int q = 0; q < kCandPerThread; ++q)
+        if (ck[q]) f((uint32_t)(ck[q] >> 32));
     };
-    const SelectResult a = cluster_select(cluster, S, m, K, key1, sm);
-    thr1 = a.thr;
-    if (a.take_eq > 0) {
+    const SelectResult a1 = cluster_select(cluster, a.S, K, visit1, sm, phase);
+    thr1 = a1.thr;
+    if (a1.take_eq > 0) {
       int e = 0;
-      for (int i = tid; i < m; i += NT) e += (uint32_t)(sm.cand[i] >> 32) == thr1;
+#pragma unroll
+      for (int q = 0; q < kCandPerThread; ++q) e += ck[q] && (uint32_t)(ck[q] >> 32) == thr1;
       e = __reduce_add_sync(kFull, e);
       if (lane == 0 && e) atomicAdd(&sm.tied, e);
       cluster.sync();
       int tied = 0;
-      for (int rk = 0; rk < S; ++rk) tied += *cluster.map_shared_rank(&sm.tied, rk);
-      if (tied > a.take_eq) {
-        auto key2 = [&](int i, uint32_t& k) {
-          const unsigned long long c = sm.cand[i];
-          k = (uint32_t)c;  // ~global id: larger = smaller id
-          return (uint32_t)(c >> 32) == thr1;
+      for (int rk = 0; rk < a.S; ++rk) tied += *cluster.map_shared_rank(&sm.tied, rk);
+      if (tied > a1.take_eq) {
+        auto visit2 = [&](auto&& f) {
+#pragma unroll
+          for (int q = 0; q < kCandPerThread; ++q)
+            if (ck[q] && (uint32_t)(ck[q] >> 32) == thr1) f((uint32_t)ck[q]);
         };
-        const SelectResult b = cluster_select(cluster, S, m, a.take_eq, key2, sm);
-        thr2 = b.take_eq > 0 ? b.thr : b.thr + 1u;
+        const SelectResult b = cluster_select(cluster, a.S, a1.take_eq, visit2, sm, phase);
+        thr2 = b.take_eq > 0 ? b.thr : b.thr + 1u;   // ~id >= thr2: the smallest ids
         tie = true;
       } else {
         thr1 -= 1u;  // the whole tied group is in
@@ -218,110 +450,26 @@ __global__ void __launch_bounds__(kFusedThreads, 2)
     }
   }
 
-  // This CTA's winners, sorted best first (the staging area is free now).
-  unsigned long long* win = reinterpret_cast<unsigned long long*>(dyn);
-  unsigned long long* others = win + kMaxK;
-  for (int base = 0; base < m; base += NT) {
-    const int i = base + tid;
+  // This CTA's winners, gathered in any order.
+#pragma unroll
+  for (int q = 0; q < kCandPerThread; ++q) {
     bool wsel = false;
-    unsigned long long key = 0ull;
-    if (i < m) {
-      key = sm.cand[i];
-      const uint32_t k1 = (uint32_t)(key >> 32);
-      wsel = all || k1 > thr1 || (tie && k1 == thr1 && (uint32_t)key >= thr2);
+    if (ck[q]) {
+      const uint32_t k1 = (uint32_t)(ck[q] >> 32);
+      wsel = all || k1 > thr1 || (tie && k1 == thr1 && (uint32_t)ck[q] >= thr2);
     }
     const unsigned msk = __ballot_sync(kFull, wsel);
     int wbase = 0;
     if (lane == 0 && msk) wbase = atomicAdd(&sm.nwin, __popc(msk));
     wbase = __shfl_sync(kFull, wbase, 0);
     const int slot = wbase + __popc(msk & lanemask_lt());
-    if (wsel && slot < K) win[slot] = key;
+    if (wsel && slot < kMaxK) sm.win[slot] = ck[q];
   }
   __syncthreads();
   const int w = min(sm.nwin, K);
-  int P = 1;
-  while (P < w) P <<= 1;
-  for (int j = w + tid; j < P; j += NT) win[j] = 0ull;
-  __syncthreads();
-  for (int k = 2; k <= P; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int p = tid; p < (P >> 1); p += NT) {
-        const int i = 2 * p - (p & (j - 1));
-        const int ixj = i + j;
-        const bool desc = (i & k) == 0;
-        const unsigned long long a = win[i], b = win[ixj];
-        if ((a < b) == desc) { win[i] = b; win[ixj] = a; }
-      }
-      __syncthreads();
-    }
-  }
-
-  // ---- a4: this shard's winners in rank order are its compacted slots -------
-  const int req = row_to_req ? row_to_req[r] : r;
-  const bool req_ok = req >= 0 && req < reqs;
-  int32_t* dst = slots + ((int64_t)s * rows + r) * K;
-  bool slot_bad = false;
-  for (int i = tid; i < K; i += NT) {
-    int slot = -1;
-    if (i < w) {
-      const int gid = (int)~(uint32_t)win[i];
-      const int64_t l = local_slot_of(gid, S, I);
-      const int64_t col = l / bs;
-      if (req_ok && col < max_blocks) {
-        const int blk = bt[((int64_t)s * reqs + req) * max_blocks + col];
-        const int64_t v = (int64_t)blk * bs + l % bs;
-        if (blk >= 0 && v <= (int64_t)INT32_MAX) slot = (int)v;
-        else slot_bad = true;
-      } else {
-        slot_bad = true;
-      }
-    }
-    dst[i] = slot;
-  }
-  if (slot_bad || (!req_ok && w > 0)) raise_flag(flags, DSA_FLAG_BOUNDS);
-  if (tid == 0) {
-    if (counts) counts[(int64_t)s * rows + r] = w;
-    sm.w = w;
-  }
-  cluster.sync();  // every CTA's sorted winners are published
-
-  // ---- merged ids: rank = own position + winners of other shards above -------
-  if (tid < S) sm.wr[tid] = *cluster.map_shared_rank(&sm.w, tid);
-  __syncthreads();
-  if (tid == 0) {
-    int o = 0;
-    for (int rk = 0; rk < S; ++rk) {
-      sm.off[rk] = o;
-      if (rk != s) o += sm.wr[rk];
-    }
-  }
-  __syncthreads();
-  for (int rk = 0; rk < S; ++rk) {
-    if (rk == s) continue;
-    const unsigned long long* remote = cluster.map_shared_rank(win, rk);
-    const int len = sm.wr[rk], o = sm.off[rk];
-    for (int j = tid; j < len; j += NT)
-      if (o + j < kMaxK) others[o + j] = remote[j];
-  }
-  __syncthreads();
-  int32_t* out_ids = ids + (int64_t)r * K;
-  float* out_sc = scores ? scores + (int64_t)r * K : nullptr;
-  for (int i = tid; i < w; i += NT) {
-    const unsigned long long key = win[i];
-    int rank = i;
-    for (int rk = 0; rk < S; ++rk)
-      if (rk != s) rank += count_above(others + sm.off[rk], sm.wr[rk], key);
-    if (rank < K) {
-      out_ids[rank] = (int32_t)~(uint32_t)key;
-      if (out_sc) out_sc[rank] = key_score((uint32_t)(key >> 32));
-    }
-  }
-  if (s == 0) {
-    for (int j = min(total, K) + tid; j < K; j += NT) {
-      out_ids[j] = -1;
-      if (out_sc) out_sc[j] = -INFINITY;
-    }
-  }
+  if (w <= kNT) finish_winners<1>(a, cluster, sm, others, s, r, w, total);
+  else if (w <= 2 * kNT) finish_winners<2>(a, cluster, sm, others, s, r, w, total);
+  else finish_winners<4>(a, cluster, sm, others, s, r, w, total);
   cluster.sync();  // no CTA leaves while another still reads its shared memory
 }
 
@@ -343,22 +491,35 @@ extern "C" dsa_status dsa_indexer_fused(const float* logits, int64_t ld, int row
     return DSA_ERR_INVALID_ARG;
   if (S < 1 || S > kMaxCluster || I < 1) return DSA_ERR_UNSUPPORTED;
   if (K != 512 && K != 1024 && K != 2048) return DSA_ERR_UNSUPPORTED;
-  if (ld > (int64_t)INT32_MAX || (int64_t)rows * S > (int64_t)INT32_MAX)
+  if (ld > (int64_t)INT32_MAX || (int64_t)rows * S > (int64_t)INT32_MAX ||
+      (int64_t)I * S > (int64_t)INT32_MAX)
     return DSA_ERR_UNSUPPORTED;
   if (rows == 0) return DSA_OK;
   if (!logits || !row_ends || !block_table || !ids || !slots || !aligned16(logits))
     return DSA_ERR_INVALID_ARG;
   if (cand && !aligned16(cand)) return DSA_ERR_INVALID_ARG;
-  const int stage_cap = ld < kStageCapElems ? (int)ld : kStageCapElems;
-  size_t dyn = (size_t)stage_cap * sizeof(float);
-  if (dyn < 2 * kMaxK * sizeof(unsigned long long)) dyn = 2 * kMaxK * sizeof(unsigned long long);
-  const size_t smem = fused_dyn_offset() + dyn;
+  // Rows that fit the register path need no staging area; otherwise stage as
+  // much as the device's per-block shared memory allows (longer rows are read
+  // from global memory).
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  const size_t fixed = fused_dyn_offset() + kMaxK * sizeof(ull);
+  if ((size_t)optin < fixed) return DSA_ERR_UNSUPPORTED;
+  const int64_t room = (int64_t)(((size_t)optin - fixed) / sizeof(float)) & ~int64_t(3);
+  int stage_cap = 0;
+  if (ld > RT::kCap) stage_cap = (int)min(min(ld, room), (int64_t)kStageCapElems);
+  const size_t smem = fixed + (size_t)stage_cap * sizeof(float);
   if (cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return DSA_ERR_CUDA;
+  FusedArgs args{logits, ld, rows, S, I, K, row_starts, row_ends, block_table, reqs, max_blocks,
+                 block_size, row_to_req, ids, scores, slots, counts, local_idx, cand, err_flags,
+                 stage_cap, ShardMath(S, I), FastDiv((uint32_t)block_size)};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(rows * S));
-  cfg.blockDim = dim3(kFusedThreads);
+  cfg.blockDim = dim3(kNT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -368,9 +529,6 @@ extern "C" dsa_status dsa_indexer_fused(const float* logits, int64_t ld, int row
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel, logits, ld, rows, S, I, K,
-                                           row_starts, row_ends, block_table, reqs, max_blocks,
-                                           block_size, row_to_req, ids, scores, slots, counts,
-                                           local_idx, cand, err_flags, stage_cap);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel, args);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -20,13 +20,13 @@ struct SelectResult {
   int take_eq;
 };
 
-// Finds the `need`-th largest key among the elements i in [0, n) for which
-// key_at(i, &k) returns true.  Requires 1 <= need < (number of such elements).
-// Digits of 11, 11 and 10 bits, most significant first; stops early when the
-// bin holding the need-th element is taken whole.  NT threads, NT in
-// {256, 512, 1024}; every thread must call it.  Ends with __syncthreads().
-template <int NT, typename KeyAt>
-__device__ SelectResult radix_select(int n, int need, KeyAt key_at, SelectSmem& sm) {
+// Finds the `need`-th largest key among all threads' keys.  visit(f) must call
+// f(k) once for every key the calling thread holds.  Requires
+// 1 <= need < (number of keys).  Digits of 11, 11 and 10 bits, most
+// significant first; stops early when the bin holding the need-th key is
+// taken whole.  NT threads, NT in {256, 512, 1024}; every thread must call it.
+template <int NT, typename Visit>
+__device__ SelectResult radix_select_visit(int need, Visit visit, SelectSmem& sm) {
   static_assert(NT == 256 || NT == 512 || NT == 1024, "block size");
   const int tid = threadIdx.x;
   uint32_t prefix = 0, mask = 0;
@@ -36,10 +36,9 @@ __device__ SelectResult radix_select(int n, int need, KeyAt key_at, SelectSmem& 
     const int nb = pass == 2 ? 1024 : 2048;
     for (int b = tid; b < nb; b += NT) sm.hist[b] = 0u;
     __syncthreads();
-    for (int i = tid; i < n; i += NT) {
-      uint32_t k;
-      if (key_at(i, k) && (k & mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & (nb - 1)], 1u);
-    }
+    visit([&](uint32_t k) {
+      if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & (nb - 1)], 1u);
+    });
     __syncthreads();
     // Thread t owns bins nb-1-t*per ... (highest first); scan counts from the top.
     const int per = nb / NT;
@@ -66,6 +65,19 @@ __device__ SelectResult radix_select(int n, int need, KeyAt key_at, SelectSmem& 
     if (count == need) return SelectResult{prefix - 1u, 0};  // the whole bin is in
   }
   return SelectResult{prefix, need};
+}
+
+// The same over elements i in [0, n), strided over the block; key_at(i, &k)
+// returns whether element i takes part.
+template <int NT, typename KeyAt>
+__device__ SelectResult radix_select(int n, int need, KeyAt key_at, SelectSmem& sm) {
+  auto visit = [&](auto&& f) {
+    for (int i = threadIdx.x; i < n; i += NT) {
+      uint32_t k;
+      if (key_at(i, k)) f(k);
+    }
+  };
+  return radix_select_visit<NT>(need, visit, sm);
 }
 
 }  // namespace dsa

@@ -12,14 +12,22 @@
 // see local_topk.cuh.
 #include "common.cuh"
 #include "local_topk.cuh"
+#include "reg_topk.cuh"
 
 namespace dsa {
 namespace {
 
 constexpr int kTopkThreads = 512;
+constexpr int kVec = 8;   // register path: local ranges up to 16384 elements
+using RT = RegTopk<kTopkThreads, kVec>;
+
+struct TopkSmem {
+  LocalTopkSmem loc;
+  RegEmitSmem<kTopkThreads, kVec> es;
+};
 
 __host__ __device__ constexpr size_t topk_stage_offset() {
-  return (sizeof(LocalTopkSmem) + 127) & ~size_t(127);
+  return (sizeof(TopkSmem) + 127) & ~size_t(127);
 }
 
 __device__ __forceinline__ void write_pad(int32_t* out_idx, float2* out_cand, int j) {
@@ -32,9 +40,10 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
     shard_topk_kernel(const float* __restrict__ logits, int64_t ld, int rows, int S, int I,
                       int K, const int32_t* __restrict__ row_starts,
                       const int32_t* __restrict__ row_ends, int32_t* __restrict__ local_idx,
-                      float* __restrict__ cand, uint32_t* flags, int stage_cap) {
+                      float* __restrict__ cand, uint32_t* flags, int stage_cap,
+                      const ShardMath sh) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  LocalTopkSmem& sm = *reinterpret_cast<LocalTopkSmem*>(smem_raw);
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
   float* stage = reinterpret_cast<float*>(smem_raw + topk_stage_offset());
 
   const int tid = threadIdx.x;
@@ -68,13 +77,34 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
     return;
   }
 
+  const int64_t base = lo & ~int64_t(3);
+  if (hi - base <= RT::kCap) {
+    uint32_t key[kVec][4];
+    load_keys<kTopkThreads, kVec>(row, lo, hi, key);
+    auto visit = [&](auto&& f) {
+#pragma unroll
+      for (int j = 0; j < kVec; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (key[j][c]) f(key[j][c]);
+    };
+    const SelectResult res = radix_select_visit<kTopkThreads>(K, visit, sm.loc.sel);
+    emit_winners<kTopkThreads, kVec>(key, res.thr, res.take_eq, sm.es,
+                                     [&](int p, int e, uint32_t) {
+      if (p >= K) return;
+      const uint32_t l = (uint32_t)(base + e);
+      if (out_idx) out_idx[p] = (int32_t)l;
+      if (kPack) out_cand[p] = make_float2(row[l], __int_as_float((int)sh.global_id(s, l)));
+    });
+    return;
+  }
   bool ok;
-  const float* data = stage_local_range(row, lo, hi, stage, stage_cap, sm, flags, &ok);
+  const float* data = stage_local_range(row, lo, hi, stage, stage_cap, sm.loc, flags, &ok);
   if (!ok) return;
-  local_topk_emit<kTopkThreads>(data, n, K, sm, [&](int p, int i, float v) {
-    const int64_t l = lo + i;
+  local_topk_emit<kTopkThreads>(data, n, K, sm.loc, [&](int p, int i, float v) {
+    const uint32_t l = (uint32_t)(lo + i);
     if (out_idx) out_idx[p] = (int32_t)l;
-    if (kPack) out_cand[p] = make_float2(v, __int_as_float((int)global_of(s, l, S, I)));
+    if (kPack) out_cand[p] = make_float2(v, __int_as_float((int)sh.global_id(s, l)));
   });
 }
 
@@ -121,7 +151,8 @@ dsa_status check_common(const float* logits, int64_t ld, int rows, int S, int I,
   if (S < 1 || S > DSA_MAX_SHARDS || I < 1) return DSA_ERR_UNSUPPORTED;
   if (K != 512 && K != 1024 && K != 2048) return DSA_ERR_UNSUPPORTED;
   if (ld > (int64_t)INT32_MAX) return DSA_ERR_UNSUPPORTED;
-  if ((int64_t)rows * S > (int64_t)INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  if ((int64_t)rows * S > (int64_t)INT32_MAX || (int64_t)I * S > (int64_t)INT32_MAX)
+    return DSA_ERR_UNSUPPORTED;
   if (rows > 0 && (!logits || !aligned16(logits))) return DSA_ERR_INVALID_ARG;
   return DSA_OK;
 }
@@ -130,14 +161,16 @@ template <bool kPack>
 dsa_status launch_topk(const float* logits, int64_t ld, int rows, int S, int I, int K,
                        const int32_t* row_starts, const int32_t* row_ends, int32_t* local_idx,
                        float* cand, uint32_t* err_flags, cudaStream_t stream) {
-  const int stage_cap = ld < kStageCapElems ? (int)ld : kStageCapElems;
+  // Rows that fit the register path need no staging area.
+  const int stage_cap = ld <= RT::kCap ? 0 : (ld < kStageCapElems ? (int)ld : kStageCapElems);
   const size_t smem = topk_stage_offset() + (size_t)stage_cap * sizeof(float);
   auto kern = shard_topk_kernel<kPack>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return DSA_ERR_CUDA;
   kern<<<rows * S, kTopkThreads, smem, stream>>>(logits, ld, rows, S, I, K, row_starts, row_ends,
-                                                 local_idx, cand, err_flags, stage_cap);
+                                                 local_idx, cand, err_flags, stage_cap,
+                                                 ShardMath(S, I));
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

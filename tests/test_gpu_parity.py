@@ -106,15 +106,16 @@ def test_small_shapes_ties_and_tails(K, S, I):
     G.assert_indexer_parity(case, G.run_gpu_fused(case), np.arange(rows))
 
 
-def test_rows_longer_than_the_shared_memory_stage():
-    """Local rows above the staging capacity take the global-memory path, and a
-    merge over more candidates than fit in shared memory does too."""
+@pytest.mark.parametrize("ld", [24000, 60000])
+def test_rows_longer_than_the_register_path(ld):
+    """Local rows above the register capacity (16384) are staged in shared
+    memory (ld 24000) or, above the staging capacity, read from global memory
+    (ld 60000); with S=16 the merge's candidates exceed shared memory too."""
     rng = np.random.default_rng(11)
     rows, S, I, K = 3, 16, 1, 2048
-    Lmax = 16 * 60000
+    Lmax = 16 * ld
     x = rng.standard_normal((rows, Lmax)).astype(np.float32)
     ends = np.array([Lmax, Lmax - 1001, 5000], np.int32)
-    ld = 60000
     cfg = W.Config("adhoc", 9, rows=rows, S=S, I=I, K=K, block_size=64, max_len=Lmax, ld=ld,
                    reqs=rows, max_blocks=(ld + 63) // 64)
     local = OL.shard_rows(x, ends, S, I, ld)
@@ -126,10 +127,11 @@ def test_rows_longer_than_the_shared_memory_stage():
     G.assert_indexer_parity(case, got, np.arange(rows))
 
 
-def test_fused_rows_longer_than_the_shared_memory_stage():
+@pytest.mark.parametrize("ld", [30000, 52000])
+def test_fused_rows_longer_than_the_register_path(ld):
+    """The fused kernel's staged (ld 30000) and global-memory (ld 52000) paths."""
     rng = np.random.default_rng(12)
     rows, S, I, K = 3, 8, 2, 1024
-    ld = 52000
     Lmax = S * ld
     x = (np.rint(rng.standard_normal((rows, Lmax)) * 16) / 16).astype(np.float32)
     ends = np.array([Lmax, Lmax - 999, 3000], np.int32)
