@@ -10,11 +10,13 @@
 //  1. Each CTA selects its shard's K local candidates: the local range is held
 //     in registers as score keys (reg_topk.cuh; longer ranges are staged in
 //     shared memory, local_topk.cuh), and the winners are kept in shared memory
-//     as 64-bit rank keys (score_key << 32 | ~global_id), in slot order.
+//     as 64-bit rank keys (score_key << 32 | ~global_id).
 //  2. The pages' all_gather becomes reads of the other CTAs' shared memory
-//     (DSMEM): a radix select over all S*K candidates whose per-CTA histograms
-//     are summed across the cluster (double-buffered, one cluster barrier per
-//     digit) decides which candidates are global winners.
+//     (DSMEM).  The first digit of a radix select over all S*K candidates sums
+//     the CTAs' histograms across the cluster; every CTA then gathers the
+//     candidates of the threshold bin from all CTAs and finishes the select on
+//     its own (the same data, so the same answer everywhere).  Ties on the
+//     score are broken by a select on ~global_id: the smaller id wins.
 //  3. Each CTA sorts the winners it holds (bitonic network over registers,
 //     warp shuffles and shared memory).  A shard's winners in rank order are
 //     exactly its compacted slots, so each CTA maps them through its own block
@@ -24,6 +26,7 @@
 //     (binary search in a local copy of their sorted lists); it writes its id
 //     at that rank.
 #include <cooperative_groups.h>
+#include <cstddef>
 
 #include "common.cuh"
 #include "local_topk.cuh"
@@ -42,16 +45,23 @@ constexpr int kMaxCluster = 8;
 using RT = RegTopk<kNT, kVec>;
 using ull = unsigned long long;
 
+constexpr int kGatherCap = 2 * kMaxK;   // threshold-bin candidates gathered from the cluster
+
 struct FusedSmem {
   LocalTopkSmem loc;                 // select scratch (also the staged path's barriers)
   RegEmitSmem<kNT, kVec> es;
-  uint32_t chist[2][2048];           // cluster-visible histograms, double-buffered
-  ull cand[kMaxK];                   // this shard's candidates, slot order
-  ull win[kMaxK];                    // this shard's global winners, best first
+  alignas(16) uint32_t chist[2][2048];  // cluster-visible histograms, double-buffered
+                                        // (read four bins at a time: 16-byte aligned)
+  ull cand[kMaxK];                   // this shard's candidates; later its threshold-bin list
+  // Reused in turn: the local select's compacted list (as uint32), the
+  // gathered threshold-bin candidates, then win[kMaxK] + others[kMaxK].
+  ull scratch[kGatherCap];
   int scan[64];
   int wr[kMaxCluster], off[kMaxCluster];
-  int m, w, total, tied, nwin, bin, above, count;
+  int m, w, total, tied, nwin, ncl, bin, above, count;
 };
+
+static_assert(offsetof(FusedSmem, chist) % 16 == 0, "uint4 reads of the histograms");
 
 __host__ __device__ constexpr size_t fused_dyn_offset() {
   return (sizeof(FusedSmem) + 127) & ~size_t(127);
@@ -114,10 +124,10 @@ __device__ __forceinline__ void cluster_digit(cg::cluster_group& cluster, int nr
 // the cluster barrier of the previous pass, so one barrier per digit suffices.
 template <typename Visit>
 __device__ SelectResult cluster_select(cg::cluster_group& cluster, int nranks, int need,
-                                       Visit visit, FusedSmem& sm, int& phase) {
-  uint32_t prefix = 0, mask = 0;
+                                       Visit visit, FusedSmem& sm, int& phase, int pass0 = 0,
+                                       uint32_t prefix = 0, uint32_t mask = 0) {
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
+  for (int pass = pass0; pass < 3; ++pass) {
     uint32_t* h = sm.chist[phase & 1];
     ++phase;
     int shift;
@@ -227,19 +237,20 @@ struct FusedArgs {
 // Slots and global ranks for this CTA's E-per-thread sorted winners.
 template <int E>
 __device__ __forceinline__ void finish_winners(const FusedArgs& a, cg::cluster_group& cluster,
-                                               FusedSmem& sm, ull* others, int s, int r, int w,
-                                               int total) {
+                                               FusedSmem& sm, int s, int r, int w, int total) {
   const int tid = threadIdx.x;
+  ull* win = sm.scratch;
+  ull* others = sm.scratch + kMaxK;
   ull v[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int i = tid * E + e;
-    v[e] = i < w ? sm.win[i] : 0ull;
+    v[e] = i < w ? win[i] : 0ull;
   }
   __syncthreads();
-  bitonic_desc<E>(v, sm.win);
+  bitonic_desc<E>(v, win);
 #pragma unroll
-  for (int e = 0; e < E; ++e) sm.win[tid * E + e] = v[e];
+  for (int e = 0; e < E; ++e) win[tid * E + e] = v[e];
 
   // ---- slots: this shard's winners in rank order, through its block table --
   const int req = a.row_to_req ? a.row_to_req[r] : r;
@@ -291,7 +302,7 @@ __device__ __forceinline__ void finish_winners(const FusedArgs& a, cg::cluster_g
   __syncthreads();
   for (int rk = 0; rk < a.S; ++rk) {
     if (rk == s) continue;
-    const ull* remote = cluster.map_shared_rank(sm.win, rk);
+    const ull* remote = cluster.map_shared_rank(win, rk);
     const int len = sm.wr[rk], o = sm.off[rk];
     for (int j = tid; j < len; j += kNT)
       if (o + j < kMaxK) others[o + j] = remote[j];
@@ -324,8 +335,7 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(128) unsigned char smem_raw[];
   FusedSmem& sm = *reinterpret_cast<FusedSmem*>(smem_raw);
-  ull* others = reinterpret_cast<ull*>(smem_raw + fused_dyn_offset());
-  float* stage = reinterpret_cast<float*>(others + kMaxK);
+  float* stage = reinterpret_cast<float*>(smem_raw + fused_dyn_offset());
   const int tid = threadIdx.x, lane = tid & 31;
   const int s = (int)cluster.block_rank();
   const int r = blockIdx.x / a.S;
@@ -346,10 +356,13 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
     sm.m = min(n, K);
     sm.tied = 0;
     sm.nwin = 0;
+    sm.ncl = 0;
+    sm.es.nout = 0;
   }
   int32_t* out_idx = a.local_idx ? a.local_idx + ((int64_t)s * a.rows + r) * K : nullptr;
   float2* out_cand = a.cand_out ? reinterpret_cast<float2*>(a.cand_out) + ((int64_t)r * a.S + s) * K
                                 : nullptr;
+  const bool ordered = out_idx || out_cand;   // intermediates are written in slot order
   __syncthreads();
 
   // ---- a1 + a2: local top-K, kept as rank keys -----------------------------
@@ -371,22 +384,22 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
   } else if (hi - base <= RT::kCap) {
     uint32_t key[kVec][4];
     load_keys<kNT, kVec>(row, lo, hi, key);
-    auto visit = [&](auto&& f) {
-#pragma unroll
-      for (int j = 0; j < kVec; ++j)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (key[j][c]) f(key[j][c]);
-    };
-    const SelectResult res = radix_select_visit<kNT>(K, visit, sm.loc.sel);
-    emit_winners<kNT, kVec>(key, res.thr, res.take_eq, sm.es, [&](int p, int e, uint32_t k) {
+    int eq;
+    const SelectResult res = select_regs<kNT, kVec>(key, K, sm.loc.sel,
+                                                    reinterpret_cast<uint32_t*>(sm.scratch),
+                                                    sm.es, &eq);
+    auto put = [&](int p, int e, uint32_t k) {
       if (p >= K) return;
       const uint32_t l = (uint32_t)(base + e);
       const uint32_t gid = a.sh.global_id(s, l);
       sm.cand[p] = rank_key(k, gid);
       if (out_idx) out_idx[p] = (int32_t)l;
       if (out_cand) out_cand[p] = make_float2(row[l], __int_as_float((int)gid));
-    });
+    };
+    if (!ordered && (res.take_eq == 0 || res.take_eq == eq))
+      emit_unordered<kNT, kVec>(key, res.take_eq == 0 ? res.thr + 1u : res.thr, sm.es, put);
+    else
+      emit_winners<kNT, kVec>(key, res.thr, res.take_eq, sm.es, put);
   } else {
     bool ok;
     const float* data = stage_local_range(row, lo, hi, stage, a.stage_cap, sm.loc, a.flags, &ok);
@@ -424,33 +437,98 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
       for (int q = 0; q < kCandPerThread; ++q)
         if (ck[q]) f((uint32_t)(ck[q] >> 32));
     };
-    const SelectResult a1 = cluster_select(cluster, a.S, K, visit1, sm, phase);
-    thr1 = a1.thr;
-    if (a1.take_eq > 0) {
-      int e = 0;
+    // First digit across the cluster.
+    uint32_t* h = sm.chist[phase & 1];
+    ++phase;
+    cluster_digit<2048, 4>(cluster, a.S, K, 0u, 0u, 21, visit1, h, sm);
+    const uint32_t b1 = (uint32_t)sm.bin;
+    const int count1 = sm.count, need = K - sm.above;
+    const uint32_t prefix = b1 << 21, mask = 0x7ffu << 21;
+    if (count1 == need) {
+      thr1 = prefix - 1u;                              // the whole bin is in
+    } else if (count1 <= kGatherCap) {
+      // Publish this CTA's threshold-bin candidates (in place of its candidate
+      // list, which the registers now hold), then gather everyone's.
+      int mine = 0;
 #pragma unroll
-      for (int q = 0; q < kCandPerThread; ++q) e += ck[q] && (uint32_t)(ck[q] >> 32) == thr1;
-      e = __reduce_add_sync(kFull, e);
-      if (lane == 0 && e) atomicAdd(&sm.tied, e);
+      for (int q = 0; q < kCandPerThread; ++q)
+        mine += ck[q] && ((uint32_t)(ck[q] >> 32) & mask) == prefix;
+      const int incl = warp_inclusive_scan(mine);
+      int wb = 0;
+      if (lane == 31 && incl) wb = atomicAdd(&sm.ncl, incl);
+      int p = __shfl_sync(kFull, wb, 31) + incl - mine;
+#pragma unroll
+      for (int q = 0; q < kCandPerThread; ++q)
+        if (ck[q] && ((uint32_t)(ck[q] >> 32) & mask) == prefix) sm.cand[p++] = ck[q];
       cluster.sync();
-      int tied = 0;
-      for (int rk = 0; rk < a.S; ++rk) tied += *cluster.map_shared_rank(&sm.tied, rk);
-      if (tied > a1.take_eq) {
-        auto visit2 = [&](auto&& f) {
+      if (tid < a.S) sm.wr[tid] = *cluster.map_shared_rank(&sm.ncl, tid);
+      __syncthreads();
+      ull* g = sm.scratch;
+      int o = 0;
+      for (int rk = 0; rk < a.S; ++rk) {
+        const ull* remote = cluster.map_shared_rank(sm.cand, rk);
+        const int len = sm.wr[rk];
+        for (int j = tid; j < len; j += kNT)
+          if (o + j < kGatherCap) g[o + j] = remote[j];
+        o += len;
+      }
+      __syncthreads();
+      const int ng = min(o, kGatherCap);
+      auto visitg = [&](auto&& f) {
+        for (int i = tid; i < ng; i += kNT) f((uint32_t)(g[i] >> 32));
+      };
+      int eq;
+      const SelectResult a2 = radix_select_from<kNT>(1, prefix, mask, need, visitg, sm.loc.sel,
+                                                     &eq);
+      thr1 = a2.thr;
+      if (a2.take_eq > 0) {
+        if (eq > a2.take_eq) {
+          auto visit2 = [&](auto&& f) {
+            for (int i = tid; i < ng; i += kNT)
+              if ((uint32_t)(g[i] >> 32) == thr1) f((uint32_t)g[i]);
+          };
+          int eq2;
+          const SelectResult b = radix_select_from<kNT>(0, 0u, 0u, a2.take_eq, visit2, sm.loc.sel,
+                                                        &eq2);
+          thr2 = b.take_eq > 0 ? b.thr : b.thr + 1u;   // ~id >= thr2: the smallest ids
+          tie = true;
+        } else {
+          thr1 -= 1u;                                  // the whole tied group is in
+        }
+      }
+    } else {
+      // A huge threshold bin: finish the select digit by digit across the cluster.
+      const SelectResult a1 = cluster_select(cluster, a.S, need, visit1, sm, phase, 1, prefix,
+                                             mask);
+      thr1 = a1.thr;
+      if (a1.take_eq > 0) {
+        int e = 0;
 #pragma unroll
-          for (int q = 0; q < kCandPerThread; ++q)
-            if (ck[q] && (uint32_t)(ck[q] >> 32) == thr1) f((uint32_t)ck[q]);
-        };
-        const SelectResult b = cluster_select(cluster, a.S, a1.take_eq, visit2, sm, phase);
-        thr2 = b.take_eq > 0 ? b.thr : b.thr + 1u;   // ~id >= thr2: the smallest ids
-        tie = true;
-      } else {
-        thr1 -= 1u;  // the whole tied group is in
+        for (int q = 0; q < kCandPerThread; ++q) e += ck[q] && (uint32_t)(ck[q] >> 32) == thr1;
+        e = __reduce_add_sync(kFull, e);
+        if (lane == 0 && e) atomicAdd(&sm.tied, e);
+        cluster.sync();
+        int tied = 0;
+        for (int rk = 0; rk < a.S; ++rk) tied += *cluster.map_shared_rank(&sm.tied, rk);
+        if (tied > a1.take_eq) {
+          auto visit2 = [&](auto&& f) {
+#pragma unroll
+            for (int q = 0; q < kCandPerThread; ++q)
+              if (ck[q] && (uint32_t)(ck[q] >> 32) == thr1) f((uint32_t)ck[q]);
+          };
+          const SelectResult b = cluster_select(cluster, a.S, a1.take_eq, visit2, sm, phase);
+          thr2 = b.take_eq > 0 ? b.thr : b.thr + 1u;
+          tie = true;
+        } else {
+          thr1 -= 1u;
+        }
       }
     }
   }
+  __syncthreads();   // the gathered list in scratch is no longer read
 
   // This CTA's winners, gathered in any order.
+  ull* win = sm.scratch;
 #pragma unroll
   for (int q = 0; q < kCandPerThread; ++q) {
     bool wsel = false;
@@ -463,13 +541,13 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
     if (lane == 0 && msk) wbase = atomicAdd(&sm.nwin, __popc(msk));
     wbase = __shfl_sync(kFull, wbase, 0);
     const int slot = wbase + __popc(msk & lanemask_lt());
-    if (wsel && slot < kMaxK) sm.win[slot] = ck[q];
+    if (wsel && slot < kMaxK) win[slot] = ck[q];
   }
   __syncthreads();
   const int w = min(sm.nwin, K);
-  if (w <= kNT) finish_winners<1>(a, cluster, sm, others, s, r, w, total);
-  else if (w <= 2 * kNT) finish_winners<2>(a, cluster, sm, others, s, r, w, total);
-  else finish_winners<4>(a, cluster, sm, others, s, r, w, total);
+  if (w <= kNT) finish_winners<1>(a, cluster, sm, s, r, w, total);
+  else if (w <= 2 * kNT) finish_winners<2>(a, cluster, sm, s, r, w, total);
+  else finish_winners<4>(a, cluster, sm, s, r, w, total);
   cluster.sync();  // no CTA leaves while another still reads its shared memory
 }
 
@@ -505,7 +583,7 @@ extern "C" dsa_status dsa_indexer_fused(const float* logits, int64_t ld, int row
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return DSA_ERR_CUDA;
-  const size_t fixed = fused_dyn_offset() + kMaxK * sizeof(ull);
+  const size_t fixed = fused_dyn_offset();
   if ((size_t)optin < fixed) return DSA_ERR_UNSUPPORTED;
   const int64_t room = (int64_t)(((size_t)optin - fixed) / sizeof(float)) & ~int64_t(3);
   int stage_cap = 0;

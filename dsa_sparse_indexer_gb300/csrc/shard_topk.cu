@@ -24,6 +24,7 @@ using RT = RegTopk<kTopkThreads, kVec>;
 struct TopkSmem {
   LocalTopkSmem loc;
   RegEmitSmem<kTopkThreads, kVec> es;
+  uint32_t list[kListCap];   // keys of the threshold bin
 };
 
 __host__ __device__ constexpr size_t topk_stage_offset() {
@@ -81,14 +82,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
   if (hi - base <= RT::kCap) {
     uint32_t key[kVec][4];
     load_keys<kTopkThreads, kVec>(row, lo, hi, key);
-    auto visit = [&](auto&& f) {
-#pragma unroll
-      for (int j = 0; j < kVec; ++j)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (key[j][c]) f(key[j][c]);
-    };
-    const SelectResult res = radix_select_visit<kTopkThreads>(K, visit, sm.loc.sel);
+    int eq;
+    const SelectResult res = select_regs<kTopkThreads, kVec>(key, K, sm.loc.sel, sm.list, sm.es,
+                                                             &eq);
     emit_winners<kTopkThreads, kVec>(key, res.thr, res.take_eq, sm.es,
                                      [&](int p, int e, uint32_t) {
       if (p >= K) return;
