@@ -46,6 +46,10 @@ using RT = RegTopk<kNT, kVec>;
 using ull = unsigned long long;
 
 constexpr int kGatherCap = 2 * kMaxK;   // threshold-bin candidates gathered from the cluster
+constexpr int kBinCap = 64;             // larger winner-holding bins take the select-and-sort path
+constexpr int kNB = 1024;               // fine bins of the one-pass merge
+constexpr int kCoarse = 512;            // coarse bins: one per binade of the score (top 9 key bits)
+constexpr int kScratch = 3 * kMaxK + kBinCap;   // LB + LS + others, or the heavy-tie gather
 
 struct FusedSmem {
   LocalTopkSmem loc;                 // select scratch (also the staged path's barriers)
@@ -55,13 +59,25 @@ struct FusedSmem {
   ull cand[kMaxK];                   // this shard's candidates; later its threshold-bin list
   // Reused in turn: the local select's compacted list (as uint32), the
   // gathered threshold-bin candidates, then win[kMaxK] + others[kMaxK].
-  ull scratch[kGatherCap];
+  alignas(16) ull scratch[kScratch];
   int scan[64];
   int wr[kMaxCluster], off[kMaxCluster];
   int m, w, total, tied, nwin, ncl, bin, above, count;
+  uint32_t kmin, kmax;             // this CTA's candidate score keys, lowest and highest
+  int bstar, bneed, bmax, nown;    // fine-bin merge: threshold bin, rank in it, largest bin
+  ull thr64;                       // fine-bin merge: the K-th candidate's rank key
+  uint32_t rk_min[kMaxCluster], rk_max[kMaxCluster];
+  int rk_m[kMaxCluster], moff[kMaxCluster + 1];
 };
 
 static_assert(offsetof(FusedSmem, chist) % 16 == 0, "uint4 reads of the histograms");
+static_assert(offsetof(FusedSmem, scratch) % 16 == 0, "uint4 reads of the bin ends");
+static_assert((offsetof(FusedSmem, loc) + offsetof(LocalTopkSmem, sel) +
+               offsetof(SelectSmem, hist)) % 16 == 0, "uint4 reads of the coarse histogram");
+
+constexpr int kBinsPerThread = kNB / kNT;   // 2
+static_assert(3 * kNB * sizeof(uint32_t) <= sizeof(FusedSmem::chist), "OFF, END, CNT in chist");
+static_assert(kScratch >= kGatherCap, "the heavy-tie path gathers into scratch");
 
 __host__ __device__ constexpr size_t fused_dyn_offset() {
   return (sizeof(FusedSmem) + 127) & ~size_t(127);
@@ -331,6 +347,230 @@ __device__ __forceinline__ void finish_winners(const FusedArgs& a, cg::cluster_g
   }
 }
 
+// Merge and convert by one fine histogram (the common case).  Candidates whose
+// score key is at least floor_key (no candidate below it can win) are binned by
+// bin(x) = (score_key(x) - floor_key) >> sh, highest bin first.  Each CTA
+// counting-sorts its binned candidates into bin order, then sorts each (small)
+// bin by placing every element at its bin start plus the number of same-bin
+// elements ranked above it, and publishes the sorted list LS with the bin
+// starts OFF and sizes CNT.  After one cluster barrier every CTA sums the bin
+// sizes over the cluster (DSMEM) to find the bin b* holding the K-th
+// candidate, copies every other CTA's sorted list down to the end of b*
+// (coalesced DSMEM reads, at most K - 1 + kBinCap entries in all), and works
+// in its own shared memory: the threshold among b*'s few members; then its
+// winner i (LS[i]) has compacted-slot position i and merged-id position
+// i + (entries above it in each other CTA's sorted list, by binary search).
+// Returns false, before writing any output, when a bin holding winners has
+// more than kBinCap candidates (heavy ties); the decision is the same in every
+// CTA.  On false the caller must pass a cluster barrier before reusing chist,
+// scratch or cand, which other CTAs may still be reading.
+__device__ __forceinline__ int fine_bin(ull x, uint32_t floor_key, int sh) {
+  return (int)(((uint32_t)(x >> 32) - floor_key) >> sh);
+}
+
+__device__ bool merge_by_bins(const FusedArgs& a, cg::cluster_group& cluster, FusedSmem& sm,
+                              const ull (&ck)[kCandPerThread], int s, int r, int total,
+                              uint32_t floor_key, int sh) {
+  const int tid = threadIdx.x;
+  const int K = a.K;
+  uint32_t* OFF = &sm.chist[0][0];        // bin start in the lists
+  uint32_t* END = OFF + kNB;               // fill cursor, then bin end
+  uint32_t* CNT = OFF + 2 * kNB;           // bin size (what other CTAs sum)
+  ull* LB = sm.scratch;                    // candidates in bin order
+  ull* LS = sm.scratch + kMaxK;            // ... sorted (published)
+  ull* others = sm.scratch + 2 * kMaxK;    // other CTAs' sorted lists, down to b*
+  ull* M = reinterpret_cast<ull*>(sm.loc.sel.hist);
+
+  // Own histogram (END as counters), then the descending-bin exclusive prefix.
+  for (int b = tid; b < kNB; b += kNT) END[b] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < kCandPerThread; ++q)
+    if (ck[q] && (uint32_t)(ck[q] >> 32) >= floor_key) atomicAdd(&END[fine_bin(ck[q], floor_key, sh)], 1u);
+  __syncthreads();
+  const int g = kNB - kBinsPerThread * (tid + 1);   // bins g, g+1, taken highest first
+  int c[kBinsPerThread];
+  int local = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    c[j] = (int)END[g + kBinsPerThread - 1 - j];
+    local += c[j];
+  }
+  int nbin;
+  int run = block_exclusive_scan(local, sm.scan, &nbin);
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    const int b = g + kBinsPerThread - 1 - j;
+    OFF[b] = (uint32_t)run;
+    END[b] = (uint32_t)run;     // becomes the fill cursor, then the bin end
+    CNT[b] = (uint32_t)c[j];
+    run += c[j];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < kCandPerThread; ++q)
+    if (ck[q] && (uint32_t)(ck[q] >> 32) >= floor_key)
+      LB[atomicAdd(&END[fine_bin(ck[q], floor_key, sh)], 1u)] = ck[q];
+  __syncthreads();
+  for (int p = tid; p < nbin; p += kNT) {          // sort within bins
+    const ull x = LB[p];
+    const int b = fine_bin(x, floor_key, sh);
+    int pos = (int)OFF[b];
+    for (uint32_t q = OFF[b]; q < END[b]; ++q) pos += LB[q] > x;
+    LS[pos] = x;
+  }
+  cluster.sync();   // every CTA's LS, OFF and CNT are published
+
+  // Global counts of this thread's bins, from the top: the K-th candidate's bin.
+  int G[kBinsPerThread];
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) G[j] = 0;
+  for (int rk = 0; rk < a.S; ++rk) {
+    const uint2 q = *reinterpret_cast<const uint2*>(cluster.map_shared_rank(CNT, rk) + g);
+    G[0] += (int)q.y;
+    G[1] += (int)q.x;
+  }
+  local = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) local += G[j];
+  if (tid == 0) sm.bstar = 0;        // all binned candidates win when total <= K
+  __syncthreads();
+  int tot;
+  run = block_exclusive_scan(local, sm.scan, &tot);
+  int mx = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    const int b = g + kBinsPerThread - 1 - j;
+    if (run < K && G[j] > mx) mx = G[j];            // a bin holding winners
+    if (total > K && run < K && run + G[j] >= K) {
+      sm.bstar = b;
+      sm.bneed = K - run;
+    }
+    run += G[j];
+  }
+  if (mx > kBinCap) atomicMax(&sm.bmax, mx);
+  __syncthreads();
+  if (sm.bmax > kBinCap) return false;
+  const int bstar = sm.bstar;
+
+  // Copy every other CTA's sorted list down to the end of bin b*.
+  if (tid < a.S) {
+    const uint32_t o = cluster.map_shared_rank(OFF, tid)[bstar];
+    const uint32_t n = cluster.map_shared_rank(CNT, tid)[bstar];
+    sm.wr[tid] = (int)(o + n);           // entries in bins >= b*
+    sm.moff[tid] = (int)n;               // of which in b*
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int o = 0;
+    for (int rk = 0; rk < a.S; ++rk) {
+      sm.off[rk] = o;
+      if (rk != s) o += sm.wr[rk];
+    }
+  }
+  __syncthreads();
+  for (int rk = 0; rk < a.S; ++rk) {
+    if (rk == s) continue;
+    const ull* remote = cluster.map_shared_rank(LS, rk);
+    const int len = sm.wr[rk], o = sm.off[rk];
+#pragma unroll 4
+    for (int j = tid; j < len; j += kNT)
+      if (o + j < kMaxK + kBinCap) others[o + j] = remote[j];
+  }
+  __syncthreads();
+
+  // The K-th candidate's rank key: winners are the keys >= thr.
+  ull thr = 1ull;                                   // all candidates (keys are > 0)
+  if (total > K) {
+    const int warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+      int o = 0;
+      for (int rk = 0; rk < a.S; ++rk) {
+        sm.rk_m[rk] = o;                 // where rank rk's members go in M
+        o += sm.moff[rk];
+      }
+      sm.total = o;
+    }
+    __syncthreads();
+    if (warp < a.S) {     // b*'s members: the tail of every CTA's (copied) list
+      const ull* src = warp == s ? LS + OFF[bstar]
+                                 : others + sm.off[warp] + sm.wr[warp] - sm.moff[warp];
+      for (int j = lane; j < sm.moff[warp]; j += 32) M[sm.rk_m[warp] + j] = src[j];
+    }
+    __syncthreads();
+    const int nm = sm.total, need = sm.bneed;
+    if (tid < nm) {
+      const ull x = M[tid];
+      int above = 0;
+      for (int j = 0; j < nm; ++j) above += M[j] > x;
+      if (above == need - 1) sm.thr64 = x;
+    }
+    __syncthreads();
+    thr = sm.thr64;
+  }
+
+  // Winner i of this CTA is LS[i]: compacted-slot position i; merged-id
+  // position i + the entries above it in every other CTA's sorted list.
+  int nmine = 0;
+  for (int i = tid; i < nbin; i += kNT) nmine += LS[i] >= thr;
+  nmine = __reduce_add_sync(kFull, nmine);
+  if ((tid & 31) == 0 && nmine) atomicAdd(&sm.nown, nmine);
+  __syncthreads();
+  const int w = min(sm.nown, K);
+  const int req = a.row_to_req ? a.row_to_req[r] : r;
+  const bool req_ok = req >= 0 && req < a.reqs;
+  const int32_t* table = a.bt + ((int64_t)s * a.reqs + (req_ok ? req : 0)) * a.max_blocks;
+  int32_t* dst = a.slots + ((int64_t)s * a.rows + r) * K;
+  int32_t* out_ids = a.ids + (int64_t)r * K;
+  float* out_sc = a.scores ? a.scores + (int64_t)r * K : nullptr;
+  int blk[kCandPerThread];
+  uint32_t boff[kCandPerThread];
+  bool bad = false;
+#pragma unroll
+  for (int u = 0; u < kCandPerThread; ++u) {     // every table load first
+    const int i = tid + u * kNT;
+    blk[u] = -1;
+    boff[u] = 0;
+    if (i < w) {
+      const uint32_t l = a.sh.local_slot(~(uint32_t)LS[i]);
+      const uint32_t col = fdivmod(l, a.fbs, &boff[u]);
+      if (req_ok && col < (uint32_t)a.max_blocks) blk[u] = __ldg(table + col);
+      else bad = true;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kCandPerThread; ++u) {
+    const int i = tid + u * kNT;
+    if (i < K) {
+      int32_t v = -1;
+      if (i < w) {
+        const ull x = LS[i];
+        int grank = i;
+        for (int rk = 0; rk < a.S; ++rk)
+          if (rk != s) grank += count_above(others + sm.off[rk], sm.wr[rk], x);
+        const int64_t slot = (int64_t)blk[u] * a.bs + boff[u];
+        const bool ok = blk[u] >= 0 && slot <= (int64_t)INT32_MAX;
+        bad |= !ok;
+        v = ok ? (int32_t)slot : -1;
+        if (grank < K) {
+          out_ids[grank] = (int32_t)~(uint32_t)x;
+          if (out_sc) out_sc[grank] = key_score((uint32_t)(x >> 32));
+        }
+      }
+      dst[i] = v;
+    }
+  }
+  if (bad) raise_flag(a.flags, DSA_FLAG_BOUNDS);
+  if (tid == 0 && a.counts) a.counts[(int64_t)s * a.rows + r] = w;
+  if (s == 0) {
+    for (int j = min(total, K) + tid; j < K; j += kNT) {
+      out_ids[j] = -1;
+      if (out_sc) out_sc[j] = -INFINITY;
+    }
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -358,6 +598,10 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
     sm.nwin = 0;
     sm.ncl = 0;
     sm.es.nout = 0;
+    sm.kmin = 0xffffffffu;
+    sm.kmax = 0u;
+    sm.bmax = 0;
+    sm.nown = 0;
   }
   int32_t* out_idx = a.local_idx ? a.local_idx + ((int64_t)s * a.rows + r) * K : nullptr;
   float2* out_cand = a.cand_out ? reinterpret_cast<float2*>(a.cand_out) + ((int64_t)r * a.S + s) * K
@@ -411,22 +655,83 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
       if (out_cand) out_cand[p] = make_float2(v, __int_as_float((int)gid));
     });
   }
-  cluster.sync();  // every CTA's candidates are in place
-
-  // ---- a3: which candidates are global winners ------------------------------
-  if (tid == 0) {
-    int t = 0;
-    for (int rk = 0; rk < a.S; ++rk) t += *cluster.map_shared_rank(&sm.m, rk);
-    sm.total = t;
-  }
   __syncthreads();
-  const int total = sm.total, m = sm.m;
+  const int m = sm.m;
   ull ck[kCandPerThread];
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
 #pragma unroll
   for (int q = 0; q < kCandPerThread; ++q) {
     const int i = tid + q * kNT;
     ck[q] = i < m ? sm.cand[i] : 0ull;    // 0: no candidate (valid keys are > 0)
+    if (ck[q]) {
+      kmin = min(kmin, (uint32_t)(ck[q] >> 32));
+      kmax = max(kmax, (uint32_t)(ck[q] >> 32));
+    }
   }
+  kmin = __reduce_min_sync(kFull, kmin);
+  kmax = __reduce_max_sync(kFull, kmax);
+  if (lane == 0) {
+    atomicMin(&sm.kmin, kmin);
+    atomicMax(&sm.kmax, kmax);
+  }
+  // Coarse histogram (one bin per binade: top 9 key bits) of this CTA's
+  // candidates: summed over the cluster it locates the binade of the K-th
+  // candidate, the floor of the fine bins.
+  uint32_t* coarse = sm.loc.sel.hist;
+  for (int b = tid; b < kCoarse; b += kNT) coarse[b] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < kCandPerThread; ++q)
+    if (ck[q]) atomicAdd(&coarse[(uint32_t)(ck[q] >> 55)], 1u);
+  cluster.sync();  // every CTA's candidates are in place
+
+  // ---- a3 + a4: global winners, their ranks and this shard's slots ---------
+  if (tid < a.S) {
+    sm.rk_m[tid] = *cluster.map_shared_rank(&sm.m, tid);
+    sm.rk_min[tid] = *cluster.map_shared_rank(&sm.kmin, tid);
+    sm.rk_max[tid] = *cluster.map_shared_rank(&sm.kmax, tid);
+  }
+  __syncthreads();
+  int total = 0;
+  uint32_t gmin = 0xffffffffu, gmax = 0u;
+  for (int rk = 0; rk < a.S; ++rk) {
+    total += sm.rk_m[rk];
+    gmin = min(gmin, sm.rk_min[rk]);
+    gmax = max(gmax, sm.rk_max[rk]);
+  }
+  if (total == 0) {   // every shard is empty
+    int32_t* dst = a.slots + ((int64_t)s * a.rows + r) * K;
+    for (int i = tid; i < K; i += kNT) dst[i] = -1;
+    if (tid == 0 && a.counts) a.counts[(int64_t)s * a.rows + r] = 0;
+    if (s == 0)
+      for (int j = tid; j < K; j += kNT) {
+        a.ids[(int64_t)r * K + j] = -1;
+        if (a.scores) a.scores[(int64_t)r * K + j] = -INFINITY;
+      }
+    cluster.sync();
+    return;
+  }
+  uint32_t floor_key = gmin;
+  if (total > K) {
+    static_assert(kCoarse == kNT, "one coarse bin per thread");
+    const int gc = kCoarse - 1 - tid;       // bins from the top
+    int c = 0;
+    for (int rk = 0; rk < a.S; ++rk) c += (int)cluster.map_shared_rank(coarse, rk)[gc];
+    int tot;
+    const int run = block_exclusive_scan(c, sm.scan, &tot);
+    if (run < K && run + c >= K) sm.bin = gc;
+    __syncthreads();
+    floor_key = max(gmin, (uint32_t)sm.bin << 23);
+  }
+  int sh = 0;
+  while (((gmax - floor_key) >> sh) >= (uint32_t)kNB) ++sh;
+  if (merge_by_bins(a, cluster, sm, ck, s, r, total, floor_key, sh)) {
+    cluster.sync();  // no CTA leaves while another still reads its shared memory
+    return;
+  }
+  cluster.sync();    // other CTAs are done reading this CTA's bins
+
+  // ---- heavy ties: select across the cluster, then sort ---------------------
   const bool all = total <= K;
   bool tie = false;
   uint32_t thr1 = 0, thr2 = 0;
