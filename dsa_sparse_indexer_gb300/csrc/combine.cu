@@ -12,8 +12,10 @@
 // weights are taken with exp2 on the base-2 values and only the final LSE is
 // converted; that is the same quantity with one rounding fewer per weight.
 //
-// One warp per (row, head); each lane streams 8 bf16 (16 bytes) per shard per
-// 256-wide slice of D; shards whose LSE is -inf are not read.
+// Up to 8 shards: one warp per (row, head, 256-wide slice of D), every shard's
+// 16-byte load in flight at once.  More shards: one warp per (row, head), each
+// lane streaming 8 bf16 per shard per slice; shards whose LSE is -inf are not
+// read.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -101,6 +103,105 @@ __global__ void __launch_bounds__(kCombThreads)
   if (lse_out && lane == 0) lse_out[rh] = (M + log2f(wsum)) * kLn2;
 }
 
+// Up to 8 shards: a persistent grid; each warp walks (row, head, 256-element
+// slice of D) items and, while it combines one item, already has the next
+// item's loads in flight (every shard's 16-byte load per lane, issued
+// unconditionally: an empty shard's values are loaded but not used, and its
+// LSE).  SN >= S shards are held in registers.
+// Resident blocks per SM: fewer when each warp holds more shards in flight, so
+// the double-buffered loads stay in registers.
+template <int SN>
+constexpr int persist_blocks() { return SN <= 4 ? 4 : 2; }
+
+template <int SN>
+__device__ __forceinline__ void load_item(const uint16_t* __restrict__ part,
+                                          const float* __restrict__ lse2, int S, int64_t RH,
+                                          int D, int nsl, int64_t item, uint4 (&v)[SN],
+                                          float& a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rh = item / nsl;
+  const int d = (int)(item - rh * nsl) * 256 + lane * 8;
+#pragma unroll
+  for (int s = 0; s < SN; ++s)
+    v[s] = (s < S && d < D)
+               ? __ldg(reinterpret_cast<const uint4*>(part + ((int64_t)s * RH + rh) * D + d))
+               : make_uint4(0u, 0u, 0u, 0u);
+  a = lane < S ? __ldg(lse2 + lane * RH + rh) : -INFINITY;
+}
+
+template <int SN>
+__global__ void __launch_bounds__(kCombThreads, persist_blocks<SN>())
+    lse_combine_persist_kernel(const uint16_t* __restrict__ part, const float* __restrict__ lse2,
+                               int S, int rows, int H, int D, uint16_t* __restrict__ out,
+                               float* __restrict__ lse_out) {
+  const int nsl = (D + 255) >> 8;
+  const int64_t RH = (int64_t)rows * H;
+  const int64_t nitems = RH * nsl;
+  const int64_t stride = (int64_t)gridDim.x * kCombWarps;
+  const int lane = threadIdx.x & 31;
+  int64_t item = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5);
+  uint4 cur[SN], nxt[SN];
+  float a_cur = -INFINITY, a_nxt = -INFINITY;
+  if (item < nitems) load_item<SN>(part, lse2, S, RH, D, nsl, item, cur, a_cur);
+  for (; item < nitems; item += stride) {
+    const int64_t next = item + stride;
+    if (next < nitems) load_item<SN>(part, lse2, S, RH, D, nsl, next, nxt, a_nxt);
+    const int64_t rh = item / nsl;
+    const int sl = (int)(item - rh * nsl);
+    const int d = sl * 256 + lane * 8;
+    uint16_t* dst = out + rh * D;
+    float M = a_cur;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    if (M == -INFINITY) {  // no shard holds anything
+      if (d < D) *reinterpret_cast<uint4*>(dst + d) = make_uint4(0u, 0u, 0u, 0u);
+      if (lse_out && sl == 0 && lane == 0) lse_out[rh] = -INFINITY;
+    } else {
+      const float w0 = a_cur == -INFINITY ? 0.f : exp2f(a_cur - M);
+      float wsum = w0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(kFull, wsum, o);
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll
+      for (int s = 0; s < SN; ++s) {
+        const float ws = __shfl_sync(kFull, w0, s);
+        if (s < S && ws != 0.f) accum8(acc, cur[s], ws);
+      }
+      const float inv = 1.f / wsum;
+      if (d < D) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+        o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+        *reinterpret_cast<uint4*>(dst + d) = o;
+      }
+      if (lse_out && sl == 0 && lane == 0) lse_out[rh] = (M + log2f(wsum)) * kLn2;
+    }
+#pragma unroll
+    for (int s = 0; s < SN; ++s) cur[s] = nxt[s];
+    a_cur = a_nxt;
+  }
+}
+
+template <int SN>
+dsa_status launch_persist(const uint16_t* part, const float* lse2, int S, int rows, int H, int D,
+                          uint16_t* out, float* lse_out, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  const int64_t items = (int64_t)rows * H * ((D + 255) / 256);
+  const int64_t need = (items + kCombWarps - 1) / kCombWarps;
+  const int64_t cap = (int64_t)sms * persist_blocks<SN>();
+  const int blocks = (int)(need < cap ? need : cap);
+  lse_combine_persist_kernel<SN><<<blocks, kCombThreads, 0, stream>>>(part, lse2, S, rows, H, D,
+                                                                      out, lse_out);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -116,10 +217,15 @@ extern "C" dsa_status dsa_lse_combine(const uint16_t* partial_out, const float* 
   if (rows == 0) return DSA_OK;
   if (!partial_out || !lse2 || !out || !aligned16(partial_out) || !aligned16(out))
     return DSA_ERR_INVALID_ARG;
-  const int64_t warps = (int64_t)rows * H;
-  const int64_t blocks = (warps + kCombWarps - 1) / kCombWarps;
-  if (blocks > INT32_MAX) return DSA_ERR_UNSUPPORTED;
-  lse_combine_kernel<<<(unsigned)blocks, kCombThreads, 0, stream>>>(partial_out, lse2, S, rows, H,
-                                                                    D, out, lse_out);
+  if (S <= 2) return launch_persist<2>(partial_out, lse2, S, rows, H, D, out, lse_out, stream);
+  if (S <= 4) return launch_persist<4>(partial_out, lse2, S, rows, H, D, out, lse_out, stream);
+  if (S <= 8) return launch_persist<8>(partial_out, lse2, S, rows, H, D, out, lse_out, stream);
+  {
+    const int64_t warps = (int64_t)rows * H;
+    const int64_t blocks = (warps + kCombWarps - 1) / kCombWarps;
+    if (blocks > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+    lse_combine_kernel<<<(unsigned)blocks, kCombThreads, 0, stream>>>(partial_out, lse2, S, rows,
+                                                                      H, D, out, lse_out);
+  }
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
