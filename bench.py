@@ -43,9 +43,9 @@ sys.path.insert(0, ROOT)
 
 import workloads as W  # noqa: E402
 
-WORKLOAD = "decode"
+DEFAULT_WORKLOAD = "decode"
 METRIC = "merged top-K rows/s"
-REPLICAS = 8                 # rotating input sets: 8 x ~52 MB > 2 x L2 (126 MB)
+L2_BYTES = 126 * 2**20       # GB300 L2; rotating input sets together exceed 2.5x this
 PATHS = {
     # one kernel for steps a1-a4 (a cluster of S CTAs per row), then the combine
     "fused": ("indexer_fused", "lse_combine"),
@@ -98,12 +98,32 @@ def max_over_ranks(x: float, world: int) -> float:
 # workload
 # ---------------------------------------------------------------------------
 def host_inputs(cfg, replica: int):
-    """Seeded host arrays for one input set of the workload."""
+    """Seeded host arrays for one input set of the workload.
+
+    Per-shard logits are drawn i.i.d. N(0,1) directly (the recipes' ties and
+    the prefill mask beyond each row's end do not change the work; tests use
+    the exact recipes).  Every shard of a decode row holds >= 2048 tokens, so
+    no combine input is empty there."""
     starts, ends = W.row_ranges(cfg, replica)
     logits = W.iid_local_logits(cfg, replica)
     bt = W.block_tables(cfg, replica=replica)
-    part, lse2 = W.combine_inputs(cfg, replica=replica)   # decode rows hold >= 8192 tokens
-    return dict(starts=starts, ends=ends, logits=logits, bt=bt, part=part, lse2=lse2)
+    r2q = None if cfg.reqs == cfg.rows else np.zeros(cfg.rows, np.int32)
+    d = dict(starts=starts, ends=ends, logits=logits, bt=bt, r2q=r2q)
+    if cfg.H:
+        d["part"], d["lse2"] = W.combine_inputs(cfg, replica=replica)
+    return d
+
+
+def set_bytes(cfg) -> int:
+    b = cfg.S * cfg.rows * cfg.ld * 4
+    if cfg.H:
+        b += cfg.S * cfg.rows * cfg.H * (cfg.D * 2 + 4)
+    return b
+
+
+def replicas_for(cfg) -> int:
+    """Rotating input sets so that a set is out of L2 when it is used again."""
+    return int(min(8, max(2, -(-int(2.5 * L2_BYTES) // set_bytes(cfg)))))
 
 
 def algorithmic_bytes(cfg, ends: np.ndarray) -> dict:
@@ -225,10 +245,10 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str) -> float | None:
+def profiled_traffic(kernel: str, workload: str = DEFAULT_WORKLOAD) -> float | None:
     """DRAM bytes per launch from the committed ncu summary of this kernel on
     this workload, if the kernel's source still matches the one profiled."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
@@ -247,8 +267,9 @@ def oracle_rows(inp: dict, cfg, rows: np.ndarray):
     from oracle import combine as OC
     from oracle import pipeline as OP
     res = OP.run_rows(inp["logits"], inp["starts"], inp["ends"], cfg.S, cfg.I, cfg.K, rows=rows,
-                      tables=inp["bt"], block_size=cfg.block_size)
-    OC.lse_combine(OC.bf16_to_f64(inp["part"][:, rows]), inp["lse2"][:, rows])
+                      tables=inp["bt"], row_to_req=inp["r2q"], block_size=cfg.block_size)
+    if cfg.H:
+        OC.lse_combine(OC.bf16_to_f64(inp["part"][:, rows]), inp["lse2"][:, rows])
     return res
 
 
@@ -265,15 +286,15 @@ def cpu_baseline(cfg, inp: dict, budget_s: float = 10.0) -> dict:
             break
     dt = time.perf_counter() - t0
     return {"value": done / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} rows of the decode batch (all four steps + LSE combine per "
-                      f"row, numpy, one thread), {dt:.1f} s"}
+            "sample": f"{done} rows of the {cfg.name} batch (all steps per row, numpy, one "
+                      f"thread), {dt:.1f} s"}
 
 
 def run_reference(args, world, rank):
     """Reference arm: the oracle timed on the host cores, same workload/metric."""
     if rank != 0:
         return 0
-    cfg = W.CONFIGS[WORKLOAD]
+    cfg = W.CONFIGS[args.workload]
     inp = host_inputs(cfg, 0)
     t = time.perf_counter()
     oracle_rows(inp, cfg, np.array([0]))
@@ -295,8 +316,8 @@ def run_reference(args, world, rank):
         step()
     dt = time.perf_counter() - t0
     value = rows_per_step * args.steps / dt
-    sample = (f"{rows_per_step} row(s) of the 64-row decode batch per step (all four steps "
-              f"+ LSE combine), numpy, one thread")
+    sample = (f"{rows_per_step} row(s) of the {cfg.rows}-row {cfg.name} batch per step (all "
+              f"steps), numpy, one thread")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -311,14 +332,18 @@ def run_reference(args, world, rank):
     return 0
 
 
+def kernels_for(cfg, path: str) -> tuple:
+    return tuple(k for k in PATHS[path] if cfg.H or k != "lse_combine")
+
+
 def config_block(cfg, path: str = "fused") -> dict:
-    return {"workload": "decode batch: 64 rows, S=4, I=1, K=2048, seq_len U[8192, 65536], "
-                        "N(0,1) fp32 logits, block_size 64 permuted per shard, combine "
-                        "[4, 64, 128, 512] bf16 with base-2 LSE U[-5, 20]",
+    return {"workload": f"{cfg.name}: {cfg.description}",
             "rows": cfg.rows, "S": cfg.S, "I": cfg.I, "K": cfg.K, "block_size": cfg.block_size,
             "H": cfg.H, "D": cfg.D,
-            "path": " -> ".join(PATHS[path]) + " (C ABI, one stream)",
-            "l2": f"{REPLICAS} rotating input sets (> 2x L2); no flush",
+            "path": " -> ".join(kernels_for(cfg, path)) + " (C ABI, one stream)",
+            "l2": f"{replicas_for(cfg)} rotating input sets of {set_bytes(cfg) / 1e6:.0f} MB "
+                  f"(> 2.5x L2 together); no flush",
+            "logits": "i.i.d. N(0,1) per shard (work-equivalent to the recipe)",
             "parallelism": "replicas (rows independent, no collective)"}
 
 
@@ -333,6 +358,8 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(W.CONFIGS), default=DEFAULT_WORKLOAD,
+                    help="timed workload (the metric is quoted on decode)")
     ap.add_argument("--path", choices=sorted(PATHS), default="fused",
                     help="fused: one cluster kernel for steps a1-a4; steps: one kernel per step")
     args = ap.parse_args(argv)
@@ -353,49 +380,59 @@ def main(argv=None) -> int:
     barrier(world)
     lib = _lib.load()
     dev = torch.device("cuda", torch.cuda.current_device())
-    cfg = W.CONFIGS[WORKLOAD]
+    cfg = W.CONFIGS[args.workload]
     S, R, K, H, D = cfg.S, cfg.rows, cfg.K, cfg.H, cfg.D
+    REPLICAS = replicas_for(cfg)
+    if args.path == "fused" and S > 8:
+        raise SystemExit("the fused path takes at most 8 shards")
 
     # --- resident inputs (rotating sets; each rank its own seeds) -----------
     host = [host_inputs(cfg, rank * REPLICAS + i) for i in range(REPLICAS)]
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     sets = []
     for h in host:
-        sets.append(dict(logits=d(h["logits"]), starts=d(h["starts"]), ends=d(h["ends"]),
-                         bt=d(h["bt"]), part=d(h["part"].view(np.int16)), lse2=d(h["lse2"])))
+        st = dict(logits=d(h["logits"]), starts=d(h["starts"]), ends=d(h["ends"]),
+                  bt=d(h["bt"]))
+        if h["r2q"] is not None:
+            st["r2q"] = d(h["r2q"])
+        if H:
+            st["part"] = d(h["part"].view(np.int16))
+            st["lse2"] = d(h["lse2"])
+        sets.append(st)
     cand = torch.empty((R, S * K, 2), dtype=torch.float32, device=dev)
     ids = torch.empty((R, K), dtype=torch.int32, device=dev)
     slots = torch.empty((S, R, K), dtype=torch.int32, device=dev)
     counts = torch.empty((S, R), dtype=torch.int32, device=dev)
-    out = torch.empty((R, H, D), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+    out = torch.empty((R, max(H, 1), max(D, 8)), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, max(H, 1)), dtype=torch.float32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     P = lambda t: t.data_ptr()
     ld = cfg.ld
 
-    KERNELS = PATHS[args.path]
+    KERNELS = kernels_for(cfg, args.path)
     calls = []
     for st in sets:
-        combine = (lib.dsa_lse_combine, (P(st["part"]), P(st["lse2"]), S, R, H, D, P(out),
-                                         P(lse), sp))
+        r2q = P(st["r2q"]) if "r2q" in st else None
+        tail = ()
+        if H:
+            tail = ((lib.dsa_lse_combine, (P(st["part"]), P(st["lse2"]), S, R, H, D, P(out),
+                                           P(lse), P(err), sp)),)
         if args.path == "fused":
             calls.append((
                 (lib.dsa_indexer_fused, (P(st["logits"]), ld, R, S, cfg.I, K, P(st["starts"]),
                                          P(st["ends"]), P(st["bt"]), cfg.reqs, cfg.max_blocks,
-                                         cfg.block_size, None, P(ids), None, P(slots),
-                                         P(counts), None, None, P(err), sp)),
-                combine))
+                                         cfg.block_size, r2q, P(ids), None, P(slots),
+                                         P(counts), None, None, P(err), sp)),) + tail)
         else:
             calls.append((
                 (lib.dsa_shard_topk_pack, (P(st["logits"]), ld, R, S, cfg.I, K, P(st["starts"]),
                                            P(st["ends"]), None, P(cand), P(err), sp)),
                 (lib.dsa_merge_topk_stable, (P(cand), R, S * K, K, P(ids), None, P(err), sp)),
                 (lib.dsa_convert_index_compact, (P(ids), R, K, S, cfg.I, P(st["bt"]), cfg.reqs,
-                                                 cfg.max_blocks, cfg.block_size, None,
-                                                 P(slots), P(counts), P(err), sp)),
-                combine))
+                                                 cfg.max_blocks, cfg.block_size, r2q,
+                                                 P(slots), P(counts), P(err), sp))) + tail)
 
     def launch(fn, a):
         status = fn(*a)
@@ -495,15 +532,20 @@ def main(argv=None) -> int:
 
     # --- e2e through host buffers --------------------------------------------
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    hsets = [dict(logits=pin(h["logits"]), starts=pin(h["starts"]), ends=pin(h["ends"]),
-                  bt=pin(h["bt"]), part=pin(h["part"].view(np.int16)), lse2=pin(h["lse2"]))
-             for h in host[:2]]
-    h_slots = torch.empty(slots.shape, dtype=slots.dtype).pin_memory()
-    h_counts = torch.empty(counts.shape, dtype=counts.dtype).pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    hsets = []
+    for h in host[:2]:
+        hs = dict(logits=pin(h["logits"]), starts=pin(h["starts"]), ends=pin(h["ends"]),
+                  bt=pin(h["bt"]))
+        if h["r2q"] is not None:
+            hs["r2q"] = pin(h["r2q"])
+        if H:
+            hs["part"] = pin(h["part"].view(np.int16))
+            hs["lse2"] = pin(h["lse2"])
+        hsets.append(hs)
+    results = [slots, counts] + ([out, lse] if H else [])
+    h_results = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]
     h2d = sum(t.numel() * t.element_size() for t in hsets[0].values())
-    d2h = sum(t.numel() * t.element_size() for t in (h_slots, h_counts, h_out, h_lse))
+    d2h = sum(t.numel() * t.element_size() for t in h_results)
 
     def e2e_step(i):
         hs, ds = hsets[i % 2], sets[i % 2]
@@ -511,10 +553,8 @@ def main(argv=None) -> int:
             ds[k].copy_(hs[k], non_blocking=True)
         for fn, a in calls[i % 2]:
             launch(fn, a)
-        h_slots.copy_(slots, non_blocking=True)
-        h_counts.copy_(counts, non_blocking=True)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        for hr, dr in zip(h_results, results):
+            hr.copy_(dr, non_blocking=True)
 
     for i in range(3):
         e2e_step(i)
@@ -539,7 +579,7 @@ def main(argv=None) -> int:
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                      "bytes_per_launch": nbytes[dominant],
-                     "traffic": profiled_traffic(dominant)},
+                     "traffic": profiled_traffic(dominant, args.workload)},
         "kernels": kernels,
         "graph_ms_per_step": graph_ms,
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": int(h2d),

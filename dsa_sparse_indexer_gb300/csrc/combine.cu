@@ -197,9 +197,10 @@ dsa_status launch_persist(const uint16_t* part, const float* lse2, int S, int ro
   const int64_t need = (items + kCombWarps - 1) / kCombWarps;
   const int64_t cap = (int64_t)sms * persist_blocks<SN>();
   const int blocks = (int)(need < cap ? need : cap);
-  lse_combine_persist_kernel<SN><<<blocks, kCombThreads, 0, stream>>>(part, lse2, S, rows, H, D,
-                                                                      out, lse_out);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  const cudaError_t e = launch_kernel(lse_combine_persist_kernel<SN>, dim3((unsigned)blocks),
+                                      dim3(kCombThreads), 0, stream, 0, part, lse2, S, rows, H, D,
+                                      out, lse_out);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -211,7 +212,8 @@ using namespace dsa;
 
 extern "C" dsa_status dsa_lse_combine(const uint16_t* partial_out, const float* lse2, int S,
                                       int rows, int H, int D, uint16_t* out, float* lse_out,
-                                      cudaStream_t stream) {
+                                      uint32_t* err_flags, cudaStream_t stream) {
+  (void)err_flags;   // no asynchronous copies on this path: nothing can stall
   if (rows < 0 || H < 1 || D < 8 || (D & 7)) return DSA_ERR_INVALID_ARG;
   if (S < 1 || S > DSA_MAX_SHARDS) return DSA_ERR_UNSUPPORTED;
   if (rows == 0) return DSA_OK;
@@ -224,8 +226,9 @@ extern "C" dsa_status dsa_lse_combine(const uint16_t* partial_out, const float* 
     const int64_t warps = (int64_t)rows * H;
     const int64_t blocks = (warps + kCombWarps - 1) / kCombWarps;
     if (blocks > INT32_MAX) return DSA_ERR_UNSUPPORTED;
-    lse_combine_kernel<<<(unsigned)blocks, kCombThreads, 0, stream>>>(partial_out, lse2, S, rows,
-                                                                      H, D, out, lse_out);
+    const cudaError_t e = launch_kernel(lse_combine_kernel, dim3((unsigned)blocks),
+                                        dim3(kCombThreads), 0, stream, 0, partial_out, lse2, S,
+                                        rows, H, D, out, lse_out);
+    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -23,10 +23,11 @@ constexpr int kConvWarps = kConvThreads / 32;
 constexpr int kMaxChunks = 2048 / kConvThreads;   // 32-id chunks per warp for K <= 2048
 
 __global__ void __launch_bounds__(kConvThreads)
-    convert_kernel(const int32_t* __restrict__ ids, int rows, int K, int S, int I,
+    convert_kernel(const int32_t* __restrict__ ids, int rows, int K, int S,
                    const int32_t* __restrict__ bt, int reqs, int max_blocks, int bs,
                    const int32_t* __restrict__ row_to_req, int32_t* __restrict__ slots,
-                   int32_t* __restrict__ counts, uint32_t* flags) {
+                   int32_t* __restrict__ counts, uint32_t* flags, const ShardMath sh,
+                   const FastDiv fbs) {
   __shared__ int cnt[kConvWarps][DSA_MAX_SHARDS];
   __shared__ int total[DSA_MAX_SHARDS];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -41,14 +42,25 @@ __global__ void __launch_bounds__(kConvThreads)
   const int32_t* mine = ids + (int64_t)r * K + warp * seg;
   const unsigned lt = lanemask_lt();
 
-  int id_c[kMaxChunks], own_c[kMaxChunks];
+  // Pass 1: owner and local slot of every id; per-warp counts per shard.
+  int own_c[kMaxChunks];
+  uint32_t loc_c[kMaxChunks];
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) {
+    own_c[c] = -1;
+    loc_c[c] = 0;
+    if (c < nch) {
+      const int id = __ldg(mine + c * 32 + lane);
+      if (id >= 0) {
+        own_c[c] = sh.owner((uint32_t)id);
+        loc_c[c] = sh.local_slot((uint32_t)id);
+      }
+    }
+  }
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     if (c < nch) {
-      const int id = mine[c * 32 + lane];
-      const int o = id >= 0 ? (int)owner_of(id, S, I) : -1;
-      id_c[c] = id;
-      own_c[c] = o;
+      const int o = own_c[c];
       const unsigned peers = __match_any_sync(kFull, o);
       if (o >= 0 && lane == __ffs(peers) - 1) cnt[warp][o] += __popc(peers);
       __syncwarp();
@@ -64,21 +76,19 @@ __global__ void __launch_bounds__(kConvThreads)
     }
     total[s] = run;
   }
-  __syncthreads();
 
-  // Issue every block-table load of this warp before the dependent compaction.
+  // Every block-table load of this thread is issued before the compaction.
   bool bad = !req_ok;
   int slot_c[kMaxChunks];
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     slot_c[c] = -1;
     if (c < nch && own_c[c] >= 0) {
-      const int id = id_c[c], o = own_c[c];
-      const int64_t l = local_slot_of(id, S, I);
-      const int64_t col = l / bs;
-      if (req_ok && col < max_blocks) {
-        const int blk = __ldg(bt + ((int64_t)o * reqs + req) * max_blocks + col);
-        const int64_t v = (int64_t)blk * bs + l % bs;
+      uint32_t off;
+      const uint32_t col = fdivmod(loc_c[c], fbs, &off);
+      if (req_ok && col < (uint32_t)max_blocks) {
+        const int blk = __ldg(bt + ((int64_t)own_c[c] * reqs + req) * max_blocks + col);
+        const int64_t v = (int64_t)blk * bs + off;
         if (blk >= 0 && v <= (int64_t)INT32_MAX) slot_c[c] = (int)v;
         else bad = true;
       } else {
@@ -86,12 +96,14 @@ __global__ void __launch_bounds__(kConvThreads)
       }
     }
   }
+  __syncthreads();
+  // Pass 2: each id at its final position (merged order within its shard).
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     if (c < nch) {
-      const int o = own_c[c], slot = slot_c[c];
+      const int o = own_c[c];
       const unsigned peers = __match_any_sync(kFull, o);
-      if (o >= 0) slots[((int64_t)o * rows + r) * K + cnt[warp][o] + __popc(peers & lt)] = slot;
+      if (o >= 0) slots[((int64_t)o * rows + r) * K + cnt[warp][o] + __popc(peers & lt)] = slot_c[c];
       __syncwarp();
       if (o >= 0 && lane == __ffs(peers) - 1) cnt[warp][o] += __popc(peers);
       __syncwarp();
@@ -99,10 +111,18 @@ __global__ void __launch_bounds__(kConvThreads)
   }
   if (bad) raise_flag(flags, DSA_FLAG_BOUNDS);
 
-  // -1 after each shard's valid slots.
+  // -1 after each shard's valid slots, 16 bytes per store where aligned.
   for (int s = 0; s < S; ++s) {
     int32_t* dst = slots + ((int64_t)s * rows + r) * K;
-    for (int j = total[s] + tid; j < K; j += kConvThreads) dst[j] = -1;
+    const int t0 = total[s];
+    if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+      const int a0 = min(K, (t0 + 3) & ~3);
+      if (tid < a0 - t0) dst[t0 + tid] = -1;
+      int4* d4 = reinterpret_cast<int4*>(dst + a0);
+      for (int j = tid; j < (K - a0) / 4; j += kConvThreads) d4[j] = make_int4(-1, -1, -1, -1);
+    } else {
+      for (int j = t0 + tid; j < K; j += kConvThreads) dst[j] = -1;
+    }
   }
   if (counts)
     for (int s = tid; s < S; s += kConvThreads) counts[(int64_t)s * rows + r] = total[s];
@@ -124,8 +144,10 @@ extern "C" dsa_status dsa_convert_index_compact(const int32_t* ids, int rows, in
   if (K != 512 && K != 1024 && K != 2048) return DSA_ERR_UNSUPPORTED;
   if (rows == 0) return DSA_OK;
   if (!ids || !block_table || !slots) return DSA_ERR_INVALID_ARG;
-  convert_kernel<<<rows, kConvThreads, 0, stream>>>(ids, rows, K, S, I, block_table, reqs,
-                                                    max_blocks, block_size, row_to_req, slots,
-                                                    counts, err_flags);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  if ((int64_t)I * S > (int64_t)INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  const cudaError_t e = launch_kernel(convert_kernel, dim3((unsigned)rows), dim3(kConvThreads), 0,
+                                      stream, 0, ids, rows, K, S, block_table, reqs, max_blocks,
+                                      block_size, row_to_req, slots, counts, err_flags,
+                                      ShardMath(S, I), FastDiv((uint32_t)block_size));
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -42,6 +42,7 @@ constexpr int kVec = 8;                      // 32 keys per thread: local ranges
 constexpr int kMaxK = 2048;
 constexpr int kCandPerThread = kMaxK / kNT;  // 4
 constexpr int kMaxCluster = 8;
+constexpr int kTableCap = 2048;               // block-table columns kept in shared memory
 using RT = RegTopk<kNT, kVec>;
 using ull = unsigned long long;
 
@@ -60,6 +61,7 @@ struct FusedSmem {
   // Reused in turn: the local select's compacted list (as uint32), the
   // gathered threshold-bin candidates, then win[kMaxK] + others[kMaxK].
   alignas(16) ull scratch[kScratch];
+  int32_t sbt[kTableCap];            // this shard's block-table row for the row's request
   int scan[64];
   int wr[kMaxCluster], off[kMaxCluster];
   int m, w, total, tied, nwin, ncl, bin, above, count;
@@ -283,7 +285,8 @@ __device__ __forceinline__ void finish_winners(const FusedArgs& a, cg::cluster_g
     if (tid * E + e < w) {
       const uint32_t l = a.sh.local_slot(~(uint32_t)v[e]);
       const uint32_t col = fdivmod(l, a.fbs, &off[e]);
-      if (req_ok && col < (uint32_t)a.max_blocks) blk[e] = __ldg(table + col);
+      if (req_ok && col < (uint32_t)a.max_blocks)
+        blk[e] = col < (uint32_t)kTableCap ? sm.sbt[col] : __ldg(table + col);
       else bad = true;
     }
   }
@@ -534,7 +537,8 @@ __device__ bool merge_by_bins(const FusedArgs& a, cg::cluster_group& cluster, Fu
     if (i < w) {
       const uint32_t l = a.sh.local_slot(~(uint32_t)LS[i]);
       const uint32_t col = fdivmod(l, a.fbs, &boff[u]);
-      if (req_ok && col < (uint32_t)a.max_blocks) blk[u] = __ldg(table + col);
+      if (req_ok && col < (uint32_t)a.max_blocks)
+        blk[u] = col < (uint32_t)kTableCap ? sm.sbt[col] : __ldg(table + col);
       else bad = true;
     }
   }
@@ -607,6 +611,16 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
   float2* out_cand = a.cand_out ? reinterpret_cast<float2*>(a.cand_out) + ((int64_t)r * a.S + s) * K
                                 : nullptr;
   const bool ordered = out_idx || out_cand;   // intermediates are written in slot order
+  {
+    // This shard's block-table row, fetched now so the slot conversion at the
+    // end does not wait on it.
+    const int req = a.row_to_req ? a.row_to_req[r] : r;
+    if (req >= 0 && req < a.reqs) {
+      const int32_t* table = a.bt + ((int64_t)s * a.reqs + req) * a.max_blocks;
+      const int ncol = min(a.max_blocks, kTableCap);
+      for (int c = tid; c < ncol; c += kNT) sm.sbt[c] = __ldg(table + c);
+    }
+  }
   __syncthreads();
 
   // ---- a1 + a2: local top-K, kept as rank keys -----------------------------
@@ -900,18 +914,7 @@ extern "C" dsa_status dsa_indexer_fused(const float* logits, int64_t ld, int row
   FusedArgs args{logits, ld, rows, S, I, K, row_starts, row_ends, block_table, reqs, max_blocks,
                  block_size, row_to_req, ids, scores, slots, counts, local_idx, cand, err_flags,
                  stage_cap, ShardMath(S, I), FastDiv((uint32_t)block_size)};
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(rows * S));
-  cfg.blockDim = dim3(kNT);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)S;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel, args);
+  const cudaError_t e = launch_kernel(fused_kernel, dim3((unsigned)(rows * S)), dim3(kNT), smem,
+                                      stream, (unsigned)S, args);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

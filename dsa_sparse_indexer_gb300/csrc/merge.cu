@@ -11,6 +11,7 @@
 // tied candidates (ties go to the smaller id).  The K winners are then put in
 // rank order by a bitonic sort of their 64-bit keys (score_key << 32 | ~id).
 #include "common.cuh"
+#include "reg_topk.cuh"
 #include "select.cuh"
 
 namespace dsa {
@@ -173,6 +174,233 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Throughput path (C <= 32 * NT): each thread keeps 32 candidates' score keys
+// in registers; a radix select with threshold-bin compaction (reg_topk.cuh)
+// finds the K-th score, ties on it are broken by a select on ~id (ids
+// reloaded from L2); the winners' 64-bit rank keys are then put in order by a
+// 1024-bin counting sort over their score range plus a sort inside each (small)
+// bin, and written straight to their output positions.  Rows whose winners
+// crowd a bin (heavy ties) are sorted by a bitonic network instead.  Small
+// shared memory and 64 registers per thread keep 1024 / NT rows per SM.
+// ---------------------------------------------------------------------------
+using ull = unsigned long long;
+constexpr int kFineBins = 1024;
+constexpr int kFineCap = 64;          // larger bins take the bitonic sort
+constexpr int kFastListCap = 2048;
+constexpr int kFastVec = 8;           // 32 candidates per thread
+
+struct MergeFastSmem {
+  SelectSmem sel;
+  uint32_t off[kFineBins], end[kFineBins];
+  ull win[kMaxK];
+  union {
+    uint32_t list[kFastListCap];      // threshold-bin keys during the select
+    ull lb[kMaxK];                    // winners in bin order
+  } u;
+  int nlist, nwin, nvalid, bmax;
+  uint32_t kmin, kmax;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT)
+    merge_fast_kernel(const float* __restrict__ cand, int C, int K, int32_t* __restrict__ ids,
+                      float* __restrict__ scores) {
+  __shared__ __align__(16) MergeFastSmem sm;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int r = blockIdx.x;
+  const float4* row4 = reinterpret_cast<const float4*>(cand + (int64_t)r * C * 2);
+  const int32_t* rowi = reinterpret_cast<const int32_t*>(cand + (int64_t)r * C * 2);
+  if (tid == 0) {
+    sm.nwin = 0;
+    sm.nvalid = 0;
+    sm.bmax = 0;
+    sm.kmin = 0xffffffffu;
+    sm.kmax = 0u;
+  }
+
+  // Candidate u of this thread: float4 q = (u / 2) * NT + tid, half u % 2;
+  // element e = 2 q + u % 2.
+  // C is a multiple of 4, so a float4 holds two whole candidates or none.
+  uint32_t key[kFastVec][4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    constexpr int kHalf = kFastVec;
+    float4 v[kHalf];
+#pragma unroll
+    for (int j = 0; j < kHalf; ++j) {
+      const int q = (h * kHalf + j) * NT + tid;
+      v[j] = 2 * q < C ? __ldg(row4 + q)
+                       : make_float4(0.f, __int_as_float(-1), 0.f, __int_as_float(-1));
+    }
+#pragma unroll
+    for (int j = 0; j < kHalf; ++j) {
+      const int jj = h * kHalf + j;
+      key[jj >> 1][(jj & 1) * 2] = __float_as_int(v[j].y) >= 0 ? score_key(v[j].x) : 0u;
+      key[jj >> 1][(jj & 1) * 2 + 1] = __float_as_int(v[j].w) >= 0 ? score_key(v[j].z) : 0u;
+    }
+  }
+  int nv = 0;
+#pragma unroll
+  for (int j = 0; j < kFastVec; ++j)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) nv += key[j][c] != 0u;
+  nv = __reduce_add_sync(kFull, nv);
+  __syncthreads();
+  if (lane == 0 && nv) atomicAdd(&sm.nvalid, nv);
+  __syncthreads();
+  const int valid = sm.nvalid;
+  auto elem = [&](int j, int c) { return 2 * ((2 * j + (c >> 1)) * NT + tid) + (c & 1); };
+
+  // Winner rule: key > thr, or key == thr and (!tie or ~id >= thr2).
+  uint32_t thr = 0u, thr2 = 0u;
+  bool eq_in = false, tie = false;
+  if (valid > K) {
+    int eq;
+    const SelectResult res = select_regs_into<NT, kFastVec, kFastListCap>(key, K, sm.sel, sm.u.list,
+                                                                          &sm.nlist, &eq);
+    thr = res.thr;
+    if (res.take_eq > 0) {
+      eq_in = true;
+      if (res.take_eq < eq) {
+        auto visit = [&](auto&& f) {
+#pragma unroll
+          for (int j = 0; j < kFastVec; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if (key[j][c] == thr) f(~(uint32_t)__ldg(rowi + 2 * elem(j, c) + 1));
+        };
+        const SelectResult b = radix_select_visit<NT>(res.take_eq, visit, sm.sel);
+        thr2 = b.take_eq > 0 ? b.thr : b.thr + 1u;
+        tie = true;
+      }
+    }
+  } else {
+    eq_in = true;   // thr = 0 and key 0 marks padding: every valid candidate wins
+    thr = 1u;
+  }
+  __syncthreads();
+
+  // Gather the winners' 64-bit rank keys (any order) and their score range.
+  {
+    uint32_t wins = 0u;   // bit 4 j + c: key[j][c] wins
+#pragma unroll
+    for (int j = 0; j < kFastVec; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t k = key[j][c];
+        bool w = k > thr || (eq_in && k == thr && k != 0u);
+        if (tie && k == thr && ~(uint32_t)__ldg(rowi + 2 * elem(j, c) + 1) < thr2) w = false;
+        wins |= (uint32_t)w << (4 * j + c);
+      }
+    const int mine = __popc(wins);
+    uint32_t kmn = 0xffffffffu, kmx = 0u;
+    const int incl = warp_inclusive_scan(mine);
+    int base = 0;
+    if (lane == 31 && incl) base = atomicAdd(&sm.nwin, incl);
+    int p = __shfl_sync(kFull, base, 31) + incl - mine;
+#pragma unroll
+    for (int j = 0; j < kFastVec; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t k = key[j][c];
+        if (wins >> (4 * j + c) & 1u) {
+          const uint32_t nid = ~(uint32_t)__ldg(rowi + 2 * elem(j, c) + 1);
+          if (p < kMaxK) sm.win[p] = ((ull)k << 32) | nid;
+          ++p;
+          kmn = min(kmn, k);
+          kmx = max(kmx, k);
+        }
+      }
+    kmn = __reduce_min_sync(kFull, kmn);
+    kmx = __reduce_max_sync(kFull, kmx);
+    if (lane == 0) {
+      atomicMin(&sm.kmin, kmn);
+      atomicMax(&sm.kmax, kmx);
+    }
+  }
+  __syncthreads();
+  const int nwin = min(sm.nwin, K);
+  int32_t* out_ids = ids + (int64_t)r * K;
+  float* out_sc = scores ? scores + (int64_t)r * K : nullptr;
+
+  // 1024-bin counting sort of the winners by score key, highest bin first.
+  const uint32_t kmin = sm.kmin;
+  int sh = 0;
+  while (((sm.kmax - kmin) >> sh) >= (uint32_t)kFineBins) ++sh;
+  for (int b = tid; b < kFineBins; b += NT) sm.end[b] = 0u;
+  __syncthreads();
+  for (int i = tid; i < nwin; i += NT)
+    atomicAdd(&sm.end[((uint32_t)(sm.win[i] >> 32) - kmin) >> sh], 1u);
+  __syncthreads();
+  {
+    constexpr int per = kFineBins / NT;
+    const int g = kFineBins - per * (tid + 1);
+    int c[per];
+    int local = 0, mx = 0;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      c[j] = (int)sm.end[g + per - 1 - j];
+      local += c[j];
+      mx = max(mx, c[j]);
+    }
+    int tot;
+    int run = block_exclusive_scan(local, sm.sel.scan, &tot);
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      const int b = g + per - 1 - j;
+      sm.off[b] = (uint32_t)run;
+      sm.end[b] = (uint32_t)run;
+      run += c[j];
+    }
+    if (mx > kFineCap) atomicMax(&sm.bmax, mx);
+  }
+  __syncthreads();
+  if (sm.bmax <= kFineCap) {
+    for (int i = tid; i < nwin; i += NT) {
+      const ull x = sm.win[i];
+      sm.u.lb[atomicAdd(&sm.end[((uint32_t)(x >> 32) - kmin) >> sh], 1u)] = x;
+    }
+    __syncthreads();
+    for (int p = tid; p < nwin; p += NT) {
+      const ull x = sm.u.lb[p];
+      const int b = (int)(((uint32_t)(x >> 32) - kmin) >> sh);
+      int pos = (int)sm.off[b];
+      for (uint32_t q = sm.off[b]; q < sm.end[b]; ++q) pos += sm.u.lb[q] > x;
+      out_ids[pos] = (int32_t)~(uint32_t)x;
+      if (out_sc) out_sc[pos] = key_score((uint32_t)(x >> 32));
+    }
+  } else {
+    // Heavy ties: a descending bitonic sort of the winners padded with 0 to
+    // a power of two (at most kMaxK).
+    int P = 1;
+    while (P < nwin) P <<= 1;
+    for (int j = nwin + tid; j < P; j += NT) sm.win[j] = 0ull;
+    __syncthreads();
+    for (int k = 2; k <= P; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int p = tid; p < (P >> 1); p += NT) {
+          const int i = 2 * p - (p & (j - 1));
+          const int ixj = i + j;
+          const bool desc = (i & k) == 0;
+          const ull a = sm.win[i], b = sm.win[ixj];
+          if ((a < b) == desc) { sm.win[i] = b; sm.win[ixj] = a; }
+        }
+        __syncthreads();
+      }
+    }
+    for (int p = tid; p < nwin; p += NT) {
+      const ull x = sm.win[p];
+      out_ids[p] = (int32_t)~(uint32_t)x;
+      if (out_sc) out_sc[p] = key_score((uint32_t)(x >> 32));
+    }
+  }
+  for (int j = nwin + tid; j < K; j += NT) {
+    out_ids[j] = -1;
+    if (out_sc) out_sc[j] = -INFINITY;
+  }
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -188,12 +416,27 @@ extern "C" dsa_status dsa_merge_topk_stable(const float* cand, int rows, int C, 
   if (C < K || (C & 3)) return DSA_ERR_INVALID_ARG;
   if (rows == 0) return DSA_OK;
   if (!cand || !ids || !aligned16(cand)) return DSA_ERR_INVALID_ARG;
+  if (C <= 32 * 256) {
+    const cudaError_t e = launch_kernel(merge_fast_kernel<256>, dim3((unsigned)rows), dim3(256), 0,
+                                        stream, 0, cand, C, K, ids, scores);
+    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
+  if (C <= 32 * 512) {
+    const cudaError_t e = launch_kernel(merge_fast_kernel<512>, dim3((unsigned)rows), dim3(512), 0,
+                                        stream, 0, cand, C, K, ids, scores);
+    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
+  if (C <= 32 * 1024) {
+    const cudaError_t e = launch_kernel(merge_fast_kernel<1024>, dim3((unsigned)rows), dim3(1024),
+                                        0, stream, 0, cand, C, K, ids, scores);
+    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
   const int stage_cap = kStageCapCand;
   const size_t smem = merge_stage_offset() + (size_t)min(C, stage_cap) * sizeof(float2);
   if (cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return DSA_ERR_CUDA;
-  merge_kernel<<<rows, kMergeThreads, smem, stream>>>(cand, C, K, ids, scores, err_flags,
-                                                      stage_cap);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  const cudaError_t e = launch_kernel(merge_kernel, dim3((unsigned)rows), dim3(kMergeThreads), smem,
+                                      stream, 0, cand, C, K, ids, scores, err_flags, stage_cap);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -82,13 +82,14 @@ __device__ __forceinline__ int warp_scan_small(int v, int* total) {
 }
 
 // The need-th largest key among the register keys (1 <= need < number of keys).
-// `list` holds kListCap keys of shared memory.  *eq as radix_select_from.
-template <int NT, int VEC>
-__device__ SelectResult select_regs(const uint32_t (&key)[VEC][4], int need, SelectSmem& sm,
-                                    uint32_t* list, RegEmitSmem<NT, VEC>& es, int* eq) {
+// `list` holds LIST_CAP keys of shared memory; *nlist is a shared counter.
+// *eq as radix_select_from.
+template <int NT, int VEC, int LIST_CAP = kListCap>
+__device__ SelectResult select_regs_into(const uint32_t (&key)[VEC][4], int need, SelectSmem& sm,
+                                         uint32_t* list, int* nlist, int* eq) {
   const int tid = threadIdx.x, lane = tid & 31;
   for (int b = tid; b < 2048; b += NT) sm.hist[b] = 0u;
-  if (tid == 0) es.nlist = 0;
+  if (tid == 0) *nlist = 0;
   __syncthreads();
 #pragma unroll
   for (int j = 0; j < VEC; ++j)
@@ -103,7 +104,7 @@ __device__ SelectResult select_regs(const uint32_t (&key)[VEC][4], int need, Sel
   *eq = count;
   if (count == need) return SelectResult{(b << 21) - 1u, 0};
   const uint32_t prefix = b << 21, mask = 0x7ffu << 21;
-  if (count <= kListCap) {
+  if (count <= LIST_CAP) {
     int mine = 0;
 #pragma unroll
     for (int j = 0; j < VEC; ++j)
@@ -111,7 +112,7 @@ __device__ SelectResult select_regs(const uint32_t (&key)[VEC][4], int need, Sel
       for (int c = 0; c < 4; ++c) mine += key[j][c] && (key[j][c] & mask) == prefix;
     const int incl = warp_inclusive_scan(mine);
     int base = 0;
-    if (lane == 31 && incl) base = atomicAdd(&es.nlist, incl);
+    if (lane == 31 && incl) base = atomicAdd(nlist, incl);
     int p = __shfl_sync(kFull, base, 31) + incl - mine;
 #pragma unroll
     for (int j = 0; j < VEC; ++j)
@@ -132,6 +133,13 @@ __device__ SelectResult select_regs(const uint32_t (&key)[VEC][4], int need, Sel
         if (key[j][c]) f(key[j][c]);
   };
   return radix_select_from<NT>(1, prefix, mask, need, visit, sm, eq);
+}
+
+template <int NT, int VEC>
+__device__ __forceinline__ SelectResult select_regs(const uint32_t (&key)[VEC][4], int need,
+                                                    SelectSmem& sm, uint32_t* list,
+                                                    RegEmitSmem<NT, VEC>& es, int* eq) {
+  return select_regs_into<NT, VEC>(key, need, sm, list, &es.nlist, eq);
 }
 
 // Winners in any order: every key >= lo_key (the caller has made sure no tie

@@ -164,10 +164,10 @@ dsa_status launch_topk(const float* logits, int64_t ld, int rows, int S, int I, 
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return DSA_ERR_CUDA;
-  kern<<<rows * S, kTopkThreads, smem, stream>>>(logits, ld, rows, S, I, K, row_starts, row_ends,
-                                                 local_idx, cand, err_flags, stage_cap,
-                                                 ShardMath(S, I));
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  const cudaError_t e = launch_kernel(kern, dim3((unsigned)(rows * S)), dim3(kTopkThreads), smem,
+                                      stream, 0, logits, ld, rows, S, I, K, row_starts, row_ends,
+                                      local_idx, cand, err_flags, stage_cap, ShardMath(S, I));
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // namespace
@@ -211,7 +211,7 @@ extern "C" dsa_status dsa_pack_candidates(const float* logits, int64_t ld,
   const int64_t quads = (int64_t)S * rows * K / 4;
   const int64_t blocks = (quads + 255) / 256;
   if (blocks > INT32_MAX) return DSA_ERR_UNSUPPORTED;
-  pack_kernel<<<(unsigned)blocks, 256, 0, stream>>>(logits, ld, local_idx, rows, S, I, K, cand,
-                                                    err_flags);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  const cudaError_t e = launch_kernel(pack_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, 0,
+                                      logits, ld, local_idx, rows, S, I, K, cand, err_flags);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

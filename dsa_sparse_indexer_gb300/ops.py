@@ -173,7 +173,8 @@ def indexer_fused(logits, row_ends, K: int, I: int, block_table, block_size: int
     return out
 
 
-def lse_combine(partial_out, lse2, out=None, lse_out=None, want_lse: bool = True):
+def lse_combine(partial_out, lse2, out=None, lse_out=None, want_lse: bool = True,
+                err_flags=None):
     """partial_out [S, rows, H, D] bf16, lse2 [S, rows, H] fp32 (base 2)
     -> out [rows, H, D] bf16 (, lse [rows, H] fp32 base e)."""
     _need(partial_out, "partial_out", torch.bfloat16, 4)
@@ -189,5 +190,5 @@ def lse_combine(partial_out, lse2, out=None, lse_out=None, want_lse: bool = True
     if lse_out is not None:
         _need(lse_out, "lse_out", torch.float32, 2)
     _lib.call("dsa_lse_combine", _ptr(partial_out), _ptr(lse2), S, rows, H, D, _ptr(out),
-              _ptr(lse_out), _stream(partial_out))
+              _ptr(lse_out), _ptr(err_flags), _stream(partial_out))
     return out, lse_out

@@ -224,11 +224,13 @@ dsa_status dsa_indexer_fused(const float* logits, int64_t ld, int rows, int S, i
  *   lse2        [S][rows][H] fp32 base-2 LSE
  *   out         [rows][H][D] bf16 out (round to nearest even), 16-byte aligned
  *   lse_out     [rows][H] fp32 out, base e; may be NULL
+ *   err_flags   device word for DSA_FLAG_* bits, may be NULL (no condition of
+ *               this kernel currently sets one; kept for a uniform interface).
  * Errors: D % 8 != 0, H < 1, D < 8 -> INVALID_ARG; S not in [1, 64] -> UNSUPPORTED.
  */
 dsa_status dsa_lse_combine(const uint16_t* partial_out, const float* lse2, int S,
                            int rows, int H, int D, uint16_t* out, float* lse_out,
-                           cudaStream_t stream);
+                           uint32_t* err_flags, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

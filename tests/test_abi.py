@@ -125,20 +125,20 @@ def test_fused_argument_checks(lib):
 def test_zero_rows_accepts_null_arrays(lib):
     assert lib.dsa_shard_topk(NULL, 64, 0, 2, 1, 512, NULL, NULL, NULL, NULL, NULL) == OK
     assert lib.dsa_merge_topk_stable(NULL, 0, 1024, 512, NULL, NULL, NULL, NULL) == OK
-    assert lib.dsa_lse_combine(NULL, NULL, 2, 0, 4, 64, NULL, NULL, NULL) == OK
+    assert lib.dsa_lse_combine(NULL, NULL, 2, 0, 4, 64, NULL, NULL, NULL, NULL) == OK
 
 
 def test_combine_argument_checks(lib):
     f = lib.dsa_lse_combine
-    assert f(P, P, 4, 0, 8, 64, P, NULL, NULL) == OK
-    assert f(NULL, P, 4, 2, 8, 64, P, NULL, NULL) == INVALID
-    assert f(P, NULL, 4, 2, 8, 64, P, NULL, NULL) == INVALID
-    assert f(P, P, 4, 2, 8, 64, NULL, NULL, NULL) == INVALID
-    assert f(P, P, 4, 2, 8, 60, P, NULL, NULL) == INVALID        # D % 8
-    assert f(P, P, 4, 2, 0, 64, P, NULL, NULL) == INVALID
-    assert f(P + 2, P, 4, 2, 8, 64, P, NULL, NULL) == INVALID
-    assert f(P, P, 0, 2, 8, 64, P, NULL, NULL) == UNSUPPORTED
-    assert f(P, P, 65, 2, 8, 64, P, NULL, NULL) == UNSUPPORTED
+    assert f(P, P, 4, 0, 8, 64, P, NULL, NULL, NULL) == OK
+    assert f(NULL, P, 4, 2, 8, 64, P, NULL, NULL, NULL) == INVALID
+    assert f(P, NULL, 4, 2, 8, 64, P, NULL, NULL, NULL) == INVALID
+    assert f(P, P, 4, 2, 8, 64, NULL, NULL, NULL, NULL) == INVALID
+    assert f(P, P, 4, 2, 8, 60, P, NULL, NULL, NULL) == INVALID        # D % 8
+    assert f(P, P, 4, 2, 0, 64, P, NULL, NULL, NULL) == INVALID
+    assert f(P + 2, P, 4, 2, 8, 64, P, NULL, NULL, NULL) == INVALID
+    assert f(P, P, 0, 2, 8, 64, P, NULL, NULL, NULL) == UNSUPPORTED
+    assert f(P, P, 65, 2, 8, 64, P, NULL, NULL, NULL) == UNSUPPORTED
 
 
 def test_binding_rejects_cpu_tensors():

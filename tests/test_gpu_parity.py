@@ -202,7 +202,7 @@ def test_lse_combine_parity_full_size(name):
 
 
 @pytest.mark.parametrize("S,H,D", [(1, 3, 8), (8, 5, 136), (3, 2, 520), (40, 2, 64),
-                                   (64, 1, 256)])
+                                   (64, 1, 256), (4, 2, 2304), (2, 2, 4096), (7, 2, 1024)])
 def test_lse_combine_shapes_and_degenerate_cases(S, H, D):
     import dsa_sparse_indexer_gb300 as dsa
     rng = np.random.default_rng(S * 7 + D)
