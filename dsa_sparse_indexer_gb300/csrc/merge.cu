@@ -175,229 +175,528 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Throughput path (C <= 32 * NT): each thread keeps 32 candidates' score keys
-// in registers; a radix select with threshold-bin compaction (reg_topk.cuh)
-// finds the K-th score, ties on it are broken by a select on ~id (ids
-// reloaded from L2); the winners' 64-bit rank keys are then put in order by a
-// 1024-bin counting sort over their score range plus a sort inside each (small)
-// bin, and written straight to their output positions.  Rows whose winners
-// crowd a bin (heavy ties) are sorted by a bitonic network instead.  Small
-// shared memory and 64 registers per thread keep 1024 / NT rows per SM.
+// Throughput path (C <= 32 * NT).  Each candidate becomes the 64-bit rank key
+// (score key << 32 | ~id), so that one unsigned compare orders two candidates
+// (higher score first, then the smaller id).  Each thread loads 16 float4
+// (32 candidates) in four batches of 4, batch b holding float4 rows
+// 4 i + (i + b) mod 4, so every batch spans all shard blocks and all parts of
+// each block.  While the second batch is in flight, a 256-bin histogram of the
+// first batch's keys (one candidate per float4), refined by a second 256-bin
+// histogram inside its selected bin when that bin is crowded, proposes a floor
+// a little below the K-th score key; each batch's
+// candidates whose score is at or above it (about 1.15 K in all) are appended
+// to a shared list as raw (score, id) pairs by warp ballots, and turned into
+// rank keys by the first histogram pass.  If fewer than K made it, the row is
+// filtered again with no floor.
+//
+// On the list, a histogram of 2048 bins spread over [min, max] of its score
+// keys does two jobs: a scan from the top bin finds the bin b* holding the
+// K-th key and gives every bin above b* its output range, since all of those
+// candidates win.  Winners above b* go into their bin's range and are ranked
+// inside it (bins hold a few keys); the members of b* are ranked among
+// themselves.  If a bin above b* or b* itself is crowded, a second level
+// spreads the bins over [bottom of b*, max].  Rows still crowded (heavy ties,
+// an outlier stretching the range) or whose list overflowed take a radix
+// select for the threshold and a bitonic sort.  Ranked winners are staged in
+// shared memory and written with 16-byte stores.
 // ---------------------------------------------------------------------------
 using ull = unsigned long long;
-constexpr int kFineBins = 1024;
-constexpr int kFineCap = 64;          // larger bins take the bitonic sort
-constexpr int kFastListCap = 2048;
-constexpr int kFastVec = 8;           // 32 candidates per thread
+constexpr int kMBins = 2048;
+constexpr int kSBins = 256;         // bins of the sample histogram
+constexpr int kMListCap = 3072;     // candidates at or above the floor
+constexpr int kRankCap = 256;       // most members of b* for the pairwise ranking
+constexpr int kFineCap = 64;        // most keys in one bin above b*
+constexpr int kQuarter = 4;         // float4 per thread per batch
 
-struct MergeFastSmem {
-  SelectSmem sel;
-  uint32_t off[kFineBins], end[kFineBins];
-  ull win[kMaxK];
+struct alignas(16) MergeFastSmem {
   union {
-    uint32_t list[kFastListCap];      // threshold-bin keys during the select
-    ull lb[kMaxK];                    // winners in bin order
+    ull l[kMListCap];               // rank keys with score key at or above the floor
+    float2 f[kMListCap];            // the same as raw (score, id) before the first pass
+    ull lb[kMaxK];                  // crowded rows: all winners
+    ull out[kMaxK];                 // ranked winners by output position
   } u;
-  int nlist, nwin, nvalid, bmax;
-  uint32_t kmin, kmax;
+  union {
+    // Keys per bin; after the scan the start of the bin's output range
+    // (bins are output from the top down), after the scatter its end, which
+    // is also the start of the bin below.
+    uint32_t end[kMBins];
+    SelectSmem sel;                 // crowded rows only
+  } h;
+  ull win[kMaxK];                   // winners above b*, by output range
+  ull bst[kRankCap];                // members of b*
+  uint32_t scnt[kSBins];            // sample histogram
+  int scan[33];
+  int nsv, nslots, nlist, nlist2, nb, nwin, bstar, above, bcnt, scount, sabove;
+  int bmax[2];                      // per level, so that no reset races a read
+  uint32_t smin, smax, lmin, lmin2, kmax, kmax2, sfloor;
 };
 
 template <int NT>
-__global__ void __launch_bounds__(NT, 1024 / NT)
-    merge_fast_kernel(const float* __restrict__ cand, int C, int K, int32_t* __restrict__ ids,
-                      float* __restrict__ scores) {
-  __shared__ __align__(16) MergeFastSmem sm;
+constexpr int merge_fast_min_blocks() { return NT == 256 ? 4 : (NT == 512 ? 2 : 1); }
+
+__device__ __forceinline__ ull rank_key(float score, float id_bits) {
+  const int id = __float_as_int(id_bits);
+  return id >= 0 ? ((ull)score_key(score) << 32) | (uint32_t)~id : 0ull;
+}
+
+// Rows with crowded bins or an overflowing list.  Among the `count` keys with
+// score key >= lo (which hold every winner) the K-th rank key thr64 comes from
+// a radix select over score keys, then over ~id of the keys tied at the
+// threshold; all winners are then sorted by a bitonic network.  Keys are
+// re-read from the row (in L2).
+template <int NT>
+__device__ __noinline__ void merge_crowded(const float* __restrict__ row, int C, uint32_t lo,
+                                           int count, int need, MergeFastSmem& sm,
+                                           int32_t* out_ids, float* out_sc) {
   const int tid = threadIdx.x, lane = tid & 31;
-  const int r = blockIdx.x;
-  const float4* row4 = reinterpret_cast<const float4*>(cand + (int64_t)r * C * 2);
-  const int32_t* rowi = reinterpret_cast<const int32_t*>(cand + (int64_t)r * C * 2);
-  if (tid == 0) {
-    sm.nwin = 0;
-    sm.nvalid = 0;
-    sm.bmax = 0;
-    sm.kmin = 0xffffffffu;
-    sm.kmax = 0u;
-  }
-
-  // Candidate u of this thread: float4 q = (u / 2) * NT + tid, half u % 2;
-  // element e = 2 q + u % 2.
-  // C is a multiple of 4, so a float4 holds two whole candidates or none.
-  uint32_t key[kFastVec][4];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    constexpr int kHalf = kFastVec;
-    float4 v[kHalf];
-#pragma unroll
-    for (int j = 0; j < kHalf; ++j) {
-      const int q = (h * kHalf + j) * NT + tid;
-      v[j] = 2 * q < C ? __ldg(row4 + q)
-                       : make_float4(0.f, __int_as_float(-1), 0.f, __int_as_float(-1));
-    }
-#pragma unroll
-    for (int j = 0; j < kHalf; ++j) {
-      const int jj = h * kHalf + j;
-      key[jj >> 1][(jj & 1) * 2] = __float_as_int(v[j].y) >= 0 ? score_key(v[j].x) : 0u;
-      key[jj >> 1][(jj & 1) * 2 + 1] = __float_as_int(v[j].w) >= 0 ? score_key(v[j].z) : 0u;
-    }
-  }
-  int nv = 0;
-#pragma unroll
-  for (int j = 0; j < kFastVec; ++j)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) nv += key[j][c] != 0u;
-  nv = __reduce_add_sync(kFull, nv);
-  __syncthreads();
-  if (lane == 0 && nv) atomicAdd(&sm.nvalid, nv);
-  __syncthreads();
-  const int valid = sm.nvalid;
-  auto elem = [&](int j, int c) { return 2 * ((2 * j + (c >> 1)) * NT + tid) + (c & 1); };
-
-  // Winner rule: key > thr, or key == thr and (!tie or ~id >= thr2).
-  uint32_t thr = 0u, thr2 = 0u;
-  bool eq_in = false, tie = false;
-  if (valid > K) {
-    int eq;
-    const SelectResult res = select_regs_into<NT, kFastVec, kFastListCap>(key, K, sm.sel, sm.u.list,
-                                                                          &sm.nlist, &eq);
-    thr = res.thr;
-    if (res.take_eq > 0) {
-      eq_in = true;
-      if (res.take_eq < eq) {
-        auto visit = [&](auto&& f) {
-#pragma unroll
-          for (int j = 0; j < kFastVec; ++j)
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              if (key[j][c] == thr) f(~(uint32_t)__ldg(rowi + 2 * elem(j, c) + 1));
-        };
-        const SelectResult b = radix_select_visit<NT>(res.take_eq, visit, sm.sel);
-        thr2 = b.take_eq > 0 ? b.thr : b.thr + 1u;
-        tie = true;
-      }
-    }
+  const float2* row2 = reinterpret_cast<const float2*>(row);
+  auto rk = [&](int e) {
+    const float2 v = __ldg(row2 + e);
+    return rank_key(v.x, v.y);
+  };
+  ull thr64;
+  if (count == need) {
+    thr64 = (ull)lo << 32;
   } else {
-    eq_in = true;   // thr = 0 and key 0 marks padding: every valid candidate wins
-    thr = 1u;
+    auto visit = [&](auto&& f) {
+      for (int e = tid; e < C; e += NT) {
+        const uint32_t k = (uint32_t)(rk(e) >> 32);
+        if (k && k >= lo) f(k);
+      }
+    };
+    int eq;
+    const SelectResult res = radix_select_from<NT>(0, 0u, 0u, need, visit, sm.h.sel, &eq);
+    const uint32_t thr = res.thr;
+    if (res.take_eq == 0) {
+      thr64 = (ull)(thr + 1u) << 32;
+    } else if (res.take_eq == eq) {
+      thr64 = (ull)thr << 32;
+    } else {
+      auto visit_id = [&](auto&& f) {
+        for (int e = tid; e < C; e += NT) {
+          const ull x = rk(e);
+          if ((uint32_t)(x >> 32) == thr) f((uint32_t)x);
+        }
+      };
+      const SelectResult t2 = radix_select_visit<NT>(res.take_eq, visit_id, sm.h.sel);
+      thr64 = ((ull)thr << 32) | (t2.take_eq > 0 ? t2.thr : t2.thr + 1u);
+    }
+  }
+  // Gather the winners (warp-aggregated append).
+  for (int e0 = 0; e0 < C; e0 += NT) {
+    const int e = e0 + tid;
+    const ull x = e < C ? rk(e) : 0ull;
+    const bool w = x != 0ull && x >= thr64;
+    const unsigned bal = __ballot_sync(kFull, w);
+    int base = 0;
+    if (lane == 0 && bal) base = atomicAdd(&sm.nwin, __popc(bal));
+    base = __shfl_sync(kFull, base, 0);
+    const int p = base + __popc(bal & lanemask_lt());
+    if (w && p < kMaxK) sm.u.lb[p] = x;
   }
   __syncthreads();
-
-  // Gather the winners' 64-bit rank keys (any order) and their score range.
-  {
-    uint32_t wins = 0u;   // bit 4 j + c: key[j][c] wins
-#pragma unroll
-    for (int j = 0; j < kFastVec; ++j)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t k = key[j][c];
-        bool w = k > thr || (eq_in && k == thr && k != 0u);
-        if (tie && k == thr && ~(uint32_t)__ldg(rowi + 2 * elem(j, c) + 1) < thr2) w = false;
-        wins |= (uint32_t)w << (4 * j + c);
-      }
-    const int mine = __popc(wins);
-    uint32_t kmn = 0xffffffffu, kmx = 0u;
-    const int incl = warp_inclusive_scan(mine);
-    int base = 0;
-    if (lane == 31 && incl) base = atomicAdd(&sm.nwin, incl);
-    int p = __shfl_sync(kFull, base, 31) + incl - mine;
-#pragma unroll
-    for (int j = 0; j < kFastVec; ++j)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t k = key[j][c];
-        if (wins >> (4 * j + c) & 1u) {
-          const uint32_t nid = ~(uint32_t)__ldg(rowi + 2 * elem(j, c) + 1);
-          if (p < kMaxK) sm.win[p] = ((ull)k << 32) | nid;
-          ++p;
-          kmn = min(kmn, k);
-          kmx = max(kmx, k);
+  const int nwin = min(sm.nwin, need);
+  int P = 1;
+  while (P < nwin) P <<= 1;
+  for (int j = nwin + tid; j < P; j += NT) sm.u.lb[j] = 0ull;
+  __syncthreads();
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int q = tid; q < (P >> 1); q += NT) {
+        const int i = 2 * q - (q & (j - 1));
+        const bool desc = (i & k) == 0;
+        const ull x = sm.u.lb[i], y = sm.u.lb[i + j];
+        if ((x < y) == desc) {
+          sm.u.lb[i] = y;
+          sm.u.lb[i + j] = x;
         }
       }
-    kmn = __reduce_min_sync(kFull, kmn);
-    kmx = __reduce_max_sync(kFull, kmx);
+      __syncthreads();
+    }
+  }
+  for (int q = tid; q < nwin; q += NT) {
+    const ull x = sm.u.lb[q];
+    out_ids[q] = (int32_t)~(uint32_t)x;
+    if (out_sc) out_sc[q] = key_score((uint32_t)(x >> 32));
+  }
+}
+
+// Entries of a[s0, e) above x.  Bins mostly hold a few keys: the first four
+// entries are compared without a loop, so lanes with different bin sizes
+// stay together.
+__device__ __forceinline__ int count_above(const ull* a, int s0, int e, ull x) {
+  int gt = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (s0 + j < e) gt += a[s0 + j] > x;
+  for (int q = s0 + 4; q < e; ++q) gt += a[q] > x;
+  return gt;
+}
+
+// Appends one batch's valid candidates with score >= ffloor to the list as
+// raw (score, id) pairs, one warp ballot per candidate slot, and folds the
+// appended scores' range into fmn / fmx.  NaN scores fail the comparison.
+__device__ __forceinline__ void append_batch(const float4 (&v)[kQuarter], float ffloor,
+                                             MergeFastSmem& sm, int* counter, float& fmn,
+                                             float& fmx) {
+  const int lane = threadIdx.x & 31;
+  unsigned bal[2 * kQuarter];
+  int tot = 0;
+#pragma unroll
+  for (int i = 0; i < kQuarter; ++i) {
+    const bool ok0 = __float_as_int(v[i].y) >= 0, ok1 = __float_as_int(v[i].w) >= 0;
+    const bool p0 = ok0 && v[i].x >= ffloor, p1 = ok1 && v[i].z >= ffloor;
+    if (p0) {
+      fmn = fminf(fmn, v[i].x);
+      fmx = fmaxf(fmx, v[i].x);
+    }
+    if (p1) {
+      fmn = fminf(fmn, v[i].z);
+      fmx = fmaxf(fmx, v[i].z);
+    }
+    bal[2 * i] = __ballot_sync(kFull, p0);
+    bal[2 * i + 1] = __ballot_sync(kFull, p1);
+    tot += __popc(bal[2 * i]) + __popc(bal[2 * i + 1]);
+  }
+  int base = 0;
+  if (lane == 0 && tot) base = atomicAdd(counter, tot);
+  base = __shfl_sync(kFull, base, 0);
+  const unsigned lt = lanemask_lt();
+#pragma unroll
+  for (int i = 0; i < kQuarter; ++i)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const unsigned b = bal[2 * i + h];
+      const int p = base + __popc(b & lt);
+      if ((b >> lane & 1u) && p < kMListCap)
+        sm.u.f[p] = h ? make_float2(v[i].z, v[i].w) : make_float2(v[i].x, v[i].y);
+      base += __popc(b);
+    }
+}
+
+// Retry with no floor: appends every valid candidate as a rank key and folds
+// its score key into the range (NaN scores included, as keys).
+__device__ __forceinline__ void append_all(const float4 (&v)[kQuarter], MergeFastSmem& sm,
+                                           int* counter, uint32_t& kmn, uint32_t& kmx) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = lanemask_lt();
+#pragma unroll
+  for (int i = 0; i < kQuarter; ++i)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const ull x = h ? rank_key(v[i].z, v[i].w) : rank_key(v[i].x, v[i].y);
+      const uint32_t k = (uint32_t)(x >> 32);
+      if (k) {
+        kmn = min(kmn, k);
+        kmx = max(kmx, k);
+      }
+      const unsigned b = __ballot_sync(kFull, k != 0u);
+      int base = 0;
+      if (lane == 0 && b) base = atomicAdd(counter, __popc(b));
+      base = __shfl_sync(kFull, base, 0);
+      const int p = base + __popc(b & lt);
+      if (k && p < kMListCap) sm.u.l[p] = x;
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
+    merge_fast_kernel(const float* __restrict__ cand, int C, int K, int32_t* __restrict__ ids,
+                      float* __restrict__ scores) {
+  extern __shared__ __align__(16) unsigned char merge_smem[];
+  MergeFastSmem& sm = *reinterpret_cast<MergeFastSmem*>(merge_smem);
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int r = blockIdx.x;
+  const float* row = cand + (int64_t)r * C * 2;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  int32_t* out_ids = ids + (int64_t)r * K;
+  float* out_sc = scores ? scores + (int64_t)r * K : nullptr;
+
+  // Float4 q = jj NT + tid holds elements 2 q and 2 q + 1 (C is a multiple of
+  // 4, so a float4 holds two whole candidates or none).  Batch b holds rows
+  // jj = 4 i + (i + b) mod 4.
+  auto load_batch = [&](int b, float4 (&v)[kQuarter]) {
+#pragma unroll
+    for (int i = 0; i < kQuarter; ++i) {
+      const int q = (4 * i + ((i + b) & 3)) * NT + tid;
+      v[i] = 2 * q < C ? __ldg(row4 + q)
+                       : make_float4(0.f, __int_as_float(-1), 0.f, __int_as_float(-1));
+    }
+  };
+  float4 va[kQuarter], vb[kQuarter];
+  load_batch(0, va);
+  load_batch(1, vb);
+
+  for (int b = tid; b < kSBins; b += NT) sm.scnt[b] = 0u;
+  for (int b = tid; b < kMBins; b += NT) sm.h.end[b] = 0u;
+  if (tid == 0) {
+    sm.nsv = 0;
+    sm.nslots = 0;
+    sm.nlist = 0;
+    sm.nlist2 = 0;
+    sm.nb = 0;
+    sm.nwin = 0;
+    sm.bmax[0] = sm.bmax[1] = 0;
+    sm.smin = 0xffffffffu;
+    sm.smax = 0u;
+    sm.lmin = 0xffffffffu;
+    sm.lmin2 = 0xffffffffu;
+    sm.kmax = 0u;
+    sm.kmax2 = 0u;
+  }
+  // Samples: one candidate of each float4 of batch 0, alternating halves.
+  auto sample = [&](int i) {
+    return (uint32_t)(rank_key((i & 1) ? va[i].z : va[i].x, (i & 1) ? va[i].w : va[i].y) >> 32);
+  };
+  {
+    int ns = 0, slots = 0;   // valid samples; sample positions inside the row
+    uint32_t mn = 0xffffffffu, mx = 0u;
+#pragma unroll
+    for (int i = 0; i < kQuarter; ++i) {
+      const uint32_t k = sample(i);
+      ns += k != 0u;
+      slots += 2 * (5 * i * NT + tid) < C;   // batch 0 holds rows 5 i
+      mx = max(mx, k);
+      mn = min(mn, k ? k : 0xffffffffu);
+    }
+    ns = __reduce_add_sync(kFull, ns);
+    slots = __reduce_add_sync(kFull, slots);
+    mn = __reduce_min_sync(kFull, mn);
+    mx = __reduce_max_sync(kFull, mx);
+    __syncthreads();
     if (lane == 0) {
-      atomicMin(&sm.kmin, kmn);
+      atomicAdd(&sm.nslots, slots);
+      if (ns) {
+        atomicAdd(&sm.nsv, ns);
+        atomicMin(&sm.smin, mn);
+        atomicMax(&sm.smax, mx);
+      }
+    }
+  }
+  __syncthreads();
+  uint32_t floor = 1u;   // every valid key
+  {
+    const int nsv = sm.nsv, nslots = sm.nslots;
+    // Estimated valid candidates: the valid fraction of the sample slots times C.
+    const float valid_est = nslots ? (float)nsv * (float)C / (float)nslots : 0.f;
+    if (valid_est > 1.25f * (float)K && nsv >= 64) {
+      const uint32_t smin = sm.smin;
+      const int ssh = max(0, (32 - __clz((int)(sm.smax - smin))) - 8);   // range >> ssh < 256
+#pragma unroll
+      for (int i = 0; i < kQuarter; ++i) {
+        const uint32_t k = sample(i);
+        if (k) atomicAdd(&sm.scnt[(k - smin) >> ssh], 1u);
+      }
+      __syncthreads();
+      // Expected samples among the winners: K * nslots / C; take 1/8 more and 16.
+      const int target = min(nsv, (int)((float)K * (float)nslots * 1.125f / (float)C) + 16);
+      const int local = tid < kSBins ? (int)sm.scnt[kSBins - 1 - tid] : 0;
+      int tot;
+      const int run = block_exclusive_scan(local, sm.scan, &tot);
+      if (tid < kSBins && run < target && run + local >= target) {
+        sm.sfloor = smin + ((uint32_t)(kSBins - 1 - tid) << ssh);
+        sm.scount = local;
+        sm.sabove = run;
+      }
+      __syncthreads();
+      floor = sm.sfloor;
+      if (sm.scount > 16 && ssh > 0) {
+        // Refine inside the selected bin [floor, floor + 2^ssh).
+        const int ssh2 = max(0, ssh - 8);
+        const int target2 = target - sm.sabove;
+        for (int b = tid; b < kSBins; b += NT) sm.scnt[b] = 0u;
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kQuarter; ++i) {
+          const uint32_t k = sample(i);
+          if (k >= floor && ((k - floor) >> ssh) == 0u) atomicAdd(&sm.scnt[(k - floor) >> ssh2], 1u);
+        }
+        __syncthreads();
+        const int local2 = tid < kSBins ? (int)sm.scnt[kSBins - 1 - tid] : 0;
+        const int run2 = block_exclusive_scan(local2, sm.scan, &tot);
+        if (tid < kSBins && run2 < target2 && run2 + local2 >= target2)
+          sm.sfloor = floor + ((uint32_t)(kSBins - 1 - tid) << ssh2);
+        __syncthreads();
+        floor = sm.sfloor;
+      }
+    }
+  }
+
+  // Filter the four batches into the list, the next batch in flight meanwhile.
+  {
+    // Scores >= ffloor are exactly the keys >= floor (keys below that of -inf
+    // are NaN patterns, which the retry handles).
+    const float ffloor = floor <= score_key(-INFINITY) ? -INFINITY : key_score(floor);
+    float fmn = INFINITY, fmx = -INFINITY;
+    append_batch(va, ffloor, sm, &sm.nlist, fmn, fmx);
+    load_batch(2, va);
+    append_batch(vb, ffloor, sm, &sm.nlist, fmn, fmx);
+    load_batch(3, vb);
+    append_batch(va, ffloor, sm, &sm.nlist, fmn, fmx);
+    append_batch(vb, ffloor, sm, &sm.nlist, fmn, fmx);
+    // Fold the range as score keys (order-preserving, -0.0 as +0.0).
+    const uint32_t kmn = __reduce_min_sync(kFull, fmn <= fmx ? score_key(fmn) : 0xffffffffu);
+    const uint32_t kmx = __reduce_max_sync(kFull, fmn <= fmx ? score_key(fmx) : 0u);
+    if (lane == 0 && kmn <= kmx) {
+      atomicMin(&sm.lmin, kmn);
       atomicMax(&sm.kmax, kmx);
     }
   }
   __syncthreads();
-  const int nwin = min(sm.nwin, K);
-  int32_t* out_ids = ids + (int64_t)r * K;
-  float* out_sc = scores ? scores + (int64_t)r * K : nullptr;
-
-  // 1024-bin counting sort of the winners by score key, highest bin first.
-  const uint32_t kmin = sm.kmin;
-  int sh = 0;
-  while (((sm.kmax - kmin) >> sh) >= (uint32_t)kFineBins) ++sh;
-  for (int b = tid; b < kFineBins; b += NT) sm.end[b] = 0u;
-  __syncthreads();
-  for (int i = tid; i < nwin; i += NT)
-    atomicAdd(&sm.end[((uint32_t)(sm.win[i] >> 32) - kmin) >> sh], 1u);
-  __syncthreads();
-  {
-    constexpr int per = kFineBins / NT;
-    const int g = kFineBins - per * (tid + 1);
-    int c[per];
-    int local = 0, mx = 0;
-#pragma unroll
-    for (int j = 0; j < per; ++j) {
-      c[j] = (int)sm.end[g + per - 1 - j];
-      local += c[j];
-      mx = max(mx, c[j]);
+  // With no floor every valid candidate is in the list (NaN scores, outside
+  // the domain, aside); with a floor, K of them in the list settle need = K.
+  int n = sm.nlist;
+  int need = floor == 1u ? min(K, n) : K;
+  uint32_t lmin = sm.lmin, kmax = sm.kmax;
+  bool raw = true;   // list entries still (score, id) pairs
+  if (n < need) {
+    // The sample floor was above the K-th key: every valid key.
+    uint32_t kmn = 0xffffffffu, kmx = 0u;
+    for (int b = 0; b < 4; ++b) {
+      load_batch(b, va);
+      append_all(va, sm, &sm.nlist2, kmn, kmx);
     }
-    int tot;
-    int run = block_exclusive_scan(local, sm.sel.scan, &tot);
-#pragma unroll
-    for (int j = 0; j < per; ++j) {
-      const int b = g + per - 1 - j;
-      sm.off[b] = (uint32_t)run;
-      sm.end[b] = (uint32_t)run;
-      run += c[j];
+    kmn = __reduce_min_sync(kFull, kmn);
+    kmx = __reduce_max_sync(kFull, kmx);
+    if (lane == 0 && kmn <= kmx) {
+      atomicMin(&sm.lmin2, kmn);
+      atomicMax(&sm.kmax2, kmx);
     }
-    if (mx > kFineCap) atomicMax(&sm.bmax, mx);
+    __syncthreads();
+    n = sm.nlist2;
+    need = min(K, n);
+    floor = 1u;
+    lmin = sm.lmin2;
+    kmax = sm.kmax2;
+    raw = false;
   }
-  __syncthreads();
-  if (sm.bmax <= kFineCap) {
-    for (int i = tid; i < nwin; i += NT) {
-      const ull x = sm.win[i];
-      sm.u.lb[atomicAdd(&sm.end[((uint32_t)(x >> 32) - kmin) >> sh], 1u)] = x;
-    }
-    __syncthreads();
-    for (int p = tid; p < nwin; p += NT) {
-      const ull x = sm.u.lb[p];
-      const int b = (int)(((uint32_t)(x >> 32) - kmin) >> sh);
-      int pos = (int)sm.off[b];
-      for (uint32_t q = sm.off[b]; q < sm.end[b]; ++q) pos += sm.u.lb[q] > x;
-      out_ids[pos] = (int32_t)~(uint32_t)x;
-      if (out_sc) out_sc[pos] = key_score((uint32_t)(x >> 32));
-    }
-  } else {
-    // Heavy ties: a descending bitonic sort of the winners padded with 0 to
-    // a power of two (at most kMaxK).
-    int P = 1;
-    while (P < nwin) P <<= 1;
-    for (int j = nwin + tid; j < P; j += NT) sm.win[j] = 0ull;
-    __syncthreads();
-    for (int k = 2; k <= P; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int p = tid; p < (P >> 1); p += NT) {
-          const int i = 2 * p - (p & (j - 1));
-          const int ixj = i + j;
-          const bool desc = (i & k) == 0;
-          const ull a = sm.win[i], b = sm.win[ixj];
-          if ((a < b) == desc) { sm.win[i] = b; sm.win[ixj] = a; }
+
+  bool ranked = false;   // winners staged in out[] by position
+  if (need > 0 && n > kMListCap) {
+    merge_crowded<NT>(row, C, floor, n, need, sm, out_ids, out_sc);
+  } else if (need > 0) {
+    uint32_t lo = lmin;
+    int sh, bstar = 0, above = 0, bcnt = 0;
+#pragma unroll 1
+    for (int level = 0;; ++level) {
+      sh = max(0, (32 - __clz((int)(kmax - lo))) - 11);   // range >> sh < 2048
+      if (raw) {
+        raw = false;
+        for (int i = tid; i < n; i += NT) {
+          const float2 f = sm.u.f[i];
+          const ull x = rank_key(f.x, f.y);
+          sm.u.l[i] = x;
+          atomicAdd(&sm.h.end[((uint32_t)(x >> 32) - lo) >> sh], 1u);
         }
-        __syncthreads();
+      } else {
+        for (int i = tid; i < n; i += NT) {
+          const uint32_t k = (uint32_t)(sm.u.l[i] >> 32);
+          if (k >= lo) atomicAdd(&sm.h.end[min((k - lo) >> sh, (uint32_t)kMBins - 1u)], 1u);
+        }
+      }
+      __syncthreads();
+      // Scan from the top bin down: output ranges, b*, the largest bin above b*.
+      {
+        constexpr int per = kMBins / NT;
+        const int g = kMBins - per * (tid + 1);
+        int cnt[per];
+        int local = 0;
+#pragma unroll
+        for (int j = 0; j < per; ++j) {
+          cnt[j] = (int)sm.h.end[g + per - 1 - j];
+          local += cnt[j];
+        }
+        int tot;
+        int run = block_exclusive_scan(local, sm.scan, &tot);
+        int mx = 0;
+#pragma unroll
+        for (int j = 0; j < per; ++j) {
+          const int b = g + per - 1 - j;
+          sm.h.end[b] = (uint32_t)run;
+          if (run < need && run + cnt[j] >= need) {
+            sm.bstar = b;
+            sm.above = run;
+            sm.bcnt = cnt[j];
+          } else if (run + cnt[j] < need) {
+            mx = max(mx, cnt[j]);
+          }
+          run += cnt[j];
+        }
+        if (mx > kFineCap) atomicMax(&sm.bmax[level], mx);
+      }
+      __syncthreads();
+      bstar = sm.bstar;
+      above = sm.above;
+      bcnt = sm.bcnt;
+      ranked = bcnt <= kRankCap && sm.bmax[level] <= kFineCap;
+      if (ranked || level == 1 || sh == 0) break;
+      // Second level over [bottom of b*, kmax]: every winner is at or above it.
+      lo += (uint32_t)bstar << sh;
+      for (int b = tid; b < kMBins; b += NT) sm.h.end[b] = 0u;
+      __syncthreads();
+    }
+    const int take = need - above;   // members of b* that win
+
+    if (ranked) {
+      // Winners above b* go to their bin's output range, b* to its own list.
+      for (int i = tid; i < n; i += NT) {
+        const ull x = sm.u.l[i];
+        const uint32_t k = (uint32_t)(x >> 32);
+        if (k < lo) continue;
+        const int b = (int)min((k - lo) >> sh, (uint32_t)kMBins - 1u);
+        if (b > bstar) sm.win[atomicAdd(&sm.h.end[b], 1u)] = x;
+        else if (b == bstar) sm.bst[atomicAdd(&sm.nb, 1)] = x;
+      }
+      __syncthreads();
+      for (int p = tid; p < above; p += NT) {
+        const ull x = sm.win[p];
+        const int b = (int)min(((uint32_t)(x >> 32) - lo) >> sh, (uint32_t)kMBins - 1u);
+        const int e = (int)sm.h.end[b], s0 = b == kMBins - 1 ? 0 : (int)sm.h.end[b + 1];
+        sm.u.out[s0 + count_above(sm.win, s0, e, x)] = x;
+      }
+      for (int i = tid; i < bcnt; i += NT) {
+        const ull x = sm.bst[i];
+        const int rank = count_above(sm.bst, 0, bcnt, x);
+        if (rank < take) sm.u.out[above + rank] = x;
+      }
+      __syncthreads();
+    } else {
+      __syncthreads();   // the select reuses the bin counters
+      merge_crowded<NT>(row, C, lo + ((uint32_t)bstar << sh), above + bcnt, need, sm, out_ids,
+                        out_sc);
+    }
+  }
+  // Write the ranked winners and the -1 / -inf padding, 4 positions a thread.
+  const bool vec = ((reinterpret_cast<uintptr_t>(out_ids) | reinterpret_cast<uintptr_t>(out_sc)) &
+                    15u) == 0;
+  const int first = ranked ? 0 : need;   // the crowded path wrote [0, need) itself
+  for (int p0 = 4 * tid; p0 < K; p0 += 4 * NT) {
+    if (p0 + 4 <= first) continue;
+    int32_t oi[4];
+    float os[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int p = p0 + u;
+      if (ranked && p < need) {
+        const ull x = sm.u.out[p];
+        oi[u] = (int32_t)~(uint32_t)x;
+        os[u] = key_score((uint32_t)(x >> 32));
+      } else {
+        oi[u] = -1;
+        os[u] = -INFINITY;
       }
     }
-    for (int p = tid; p < nwin; p += NT) {
-      const ull x = sm.win[p];
-      out_ids[p] = (int32_t)~(uint32_t)x;
-      if (out_sc) out_sc[p] = key_score((uint32_t)(x >> 32));
+    if (vec && p0 >= first) {
+      *reinterpret_cast<int4*>(out_ids + p0) = make_int4(oi[0], oi[1], oi[2], oi[3]);
+      if (out_sc) *reinterpret_cast<float4*>(out_sc + p0) = make_float4(os[0], os[1], os[2], os[3]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (p0 + u < first) continue;
+        out_ids[p0 + u] = oi[u];
+        if (out_sc) out_sc[p0 + u] = os[u];
+      }
     }
-  }
-  for (int j = nwin + tid; j < K; j += NT) {
-    out_ids[j] = -1;
-    if (out_sc) out_sc[j] = -INFINITY;
   }
 }
 
@@ -416,20 +715,19 @@ extern "C" dsa_status dsa_merge_topk_stable(const float* cand, int rows, int C, 
   if (C < K || (C & 3)) return DSA_ERR_INVALID_ARG;
   if (rows == 0) return DSA_OK;
   if (!cand || !ids || !aligned16(cand)) return DSA_ERR_INVALID_ARG;
-  if (C <= 32 * 256) {
-    const cudaError_t e = launch_kernel(merge_fast_kernel<256>, dim3((unsigned)rows), dim3(256), 0,
-                                        stream, 0, cand, C, K, ids, scores);
-    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
-  }
-  if (C <= 32 * 512) {
-    const cudaError_t e = launch_kernel(merge_fast_kernel<512>, dim3((unsigned)rows), dim3(512), 0,
-                                        stream, 0, cand, C, K, ids, scores);
-    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
-  }
   if (C <= 32 * 1024) {
-    const cudaError_t e = launch_kernel(merge_fast_kernel<1024>, dim3((unsigned)rows), dim3(1024),
-                                        0, stream, 0, cand, C, K, ids, scores);
-    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    auto launch_fast = [&](auto kernel, int nt) {
+      const int smem = (int)sizeof(MergeFastSmem);
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+        return DSA_ERR_CUDA;
+      const cudaError_t e = launch_kernel(kernel, dim3((unsigned)rows), dim3((unsigned)nt),
+                                          (size_t)smem, stream, 0, cand, C, K, ids, scores);
+      return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    };
+    if (C <= 32 * 256) return launch_fast(merge_fast_kernel<256>, 256);
+    if (C <= 32 * 512) return launch_fast(merge_fast_kernel<512>, 512);
+    return launch_fast(merge_fast_kernel<1024>, 1024);
   }
   const int stage_cap = kStageCapCand;
   const size_t smem = merge_stage_offset() + (size_t)min(C, stage_cap) * sizeof(float2);
