@@ -104,6 +104,381 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
   });
 }
 
+// ---------------------------------------------------------------------------
+// Throughput path for local ranges of up to 32 * NT slots (NT = 256 or 512).
+// Each thread keeps 8 float4 of the range as score keys in registers (slot e
+// = base + 4 (j NT + tid) + c).  The K-th key is found without a radix pass
+// over all keys: a 256-bin histogram of 4 sampled keys per thread proposes a
+// floor a little below it; the (score key, ~slot) pairs at or above the floor
+// (about 1.15 K) go to a shared list; a 2048-bin histogram of the list over
+// its key range locates the bin b* that holds the K-th key, and ranking the
+// few members of b* gives the exact threshold (score key, slot): a slot wins
+// if its key is above the threshold key, or equal to it at a slot no later
+// than the threshold slot.  The winners are then written in ascending slot
+// order: per-thread counts for each of the 8 float4 rows, packed four to a
+// word, take one warp scan, and a small table gives each (row, warp) its
+// output offset.  Rows where the floor misses, the list overflows or b* is
+// crowded fall back to the radix select over the registers.
+// ---------------------------------------------------------------------------
+using ull = unsigned long long;
+constexpr int kTListCap = 3072;   // (key, ~slot) pairs at or above the floor
+constexpr int kTBins = 2048;
+constexpr int kTSBins = 256;      // sample histogram
+constexpr int kTRankCap = 256;    // most members of b* for the pairwise ranking
+
+template <int NT>
+struct TopkFastSmem {
+  union {
+    struct {
+      ull l[kTListCap];
+      uint32_t bins[kTBins];
+      ull bst[kTRankCap];          // members of b*
+      uint32_t scnt[kTSBins];
+      uint32_t wt[NT / 32][2];     // packed per-row winner counts of each warp
+      int off[8][NT / 32];         // output offset of each (float4 row, warp)
+      int scan[33];
+      int nsv, nlist, nb, bstar, above, bcnt, scount, sabove;
+      uint32_t smin, smax, lmin, kmax, sfloor;
+      ull thr64;
+    } f;
+    struct {                       // fallback: radix select over the registers
+      LocalTopkSmem loc;
+      RegEmitSmem<NT, kVec> es;
+      uint32_t list[kListCap];
+    } g;
+  };
+};
+
+// Writes winner p of a (shard, row): local slot l and the packed candidate.
+template <bool kPack>
+struct TopkEmitter {
+  const float* row;
+  int32_t* out_idx;
+  float2* out_cand;
+  int K, s;
+  ShardMath sh;
+  __device__ __forceinline__ void operator()(int p, uint32_t l, float v) const {
+    if (p >= K) return;
+    if (out_idx) out_idx[p] = (int32_t)l;
+    if (kPack) out_cand[p] = make_float2(v, __int_as_float((int)sh.global_id(s, l)));
+  }
+  // The candidate's score from its key: exact except that both zeros share a
+  // key, so a zero is read back from the row to keep its sign bit.
+  __device__ __forceinline__ void from_key(int p, uint32_t l, uint32_t k) const {
+    (*this)(p, l, k == 0x80000000u ? __ldg(row + l) : key_score(k));
+  }
+};
+
+// Fallback of the throughput path: the radix select over the keys, re-read
+// from the row (in L2) into registers, or over the row in global memory when
+// the range does not fit the registers.
+template <int NT, bool kPack>
+__device__ __noinline__ void topk_fallback(const float* __restrict__ row, int lo, int hi, int K,
+                                           TopkFastSmem<NT>& sm, const TopkEmitter<kPack> emit) {
+  const int base = lo & ~3;
+  if (hi - base > 32 * NT) {
+    local_topk_emit<NT>(row + lo, hi - lo, K, sm.g.loc,
+                        [&](int p, int i, float v) { emit(p, (uint32_t)(lo + i), v); });
+    return;
+  }
+  uint32_t key[kVec][4];
+  load_keys<NT, kVec>(row, lo, hi, key);
+  int eq;
+  const SelectResult res = select_regs<NT, kVec>(key, K, sm.g.loc.sel, sm.g.list, sm.g.es, &eq);
+  emit_winners<NT, kVec>(key, res.thr, res.take_eq, sm.g.es, [&](int p, int e, uint32_t k) {
+    emit.from_key(p, (uint32_t)(base + e), k);
+  });
+}
+
+__device__ __forceinline__ int t_count_above(const ull* a, int n, ull x) {
+  int gt = 0;
+  for (int q = 0; q < n; ++q) gt += a[q] > x;
+  return gt;
+}
+
+template <int NT, bool kPack>
+__global__ void __launch_bounds__(NT, NT == 256 ? 4 : 2)
+    topk_fast_kernel(const float* __restrict__ logits, int64_t ld, int rows, int S, int I, int K,
+                     const int32_t* __restrict__ row_starts, const int32_t* __restrict__ row_ends,
+                     int32_t* __restrict__ local_idx, float* __restrict__ cand, uint32_t* flags,
+                     const ShardMath sh) {
+  constexpr int W = NT / 32;
+  constexpr int kCap = 32 * NT;
+  __shared__ TopkFastSmem<NT> sm;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s = blockIdx.x / rows, r = blockIdx.x - s * rows;
+  const float* row = logits + ((int64_t)s * rows + r) * ld;
+
+  // Global range -> this shard's local range (ld <= INT32_MAX: slots fit int).
+  int64_t st = row_starts ? (int64_t)row_starts[r] : 0, en = row_ends[r];
+  bool bad = false;
+  if (st < 0) { st = 0; bad = true; }
+  if (en < st) { en = st; bad = true; }
+  int64_t lo64 = local_len(st, s, S, I), hi64 = local_len(en, s, S, I);
+  if (hi64 > ld) { hi64 = ld; bad = true; }
+  if (lo64 > hi64) { lo64 = hi64; bad = true; }
+  if (bad && tid == 0) raise_flag(flags, DSA_FLAG_BOUNDS);
+  const int lo = (int)lo64, hi = (int)hi64, n = hi - lo;
+
+  int32_t* out_idx = local_idx ? local_idx + ((int64_t)s * rows + r) * K : nullptr;
+  float2* out_cand = kPack ? reinterpret_cast<float2*>(cand) + ((int64_t)r * S + s) * K : nullptr;
+  const TopkEmitter<kPack> emit{row, out_idx, out_cand, K, s, sh};
+
+  if (n <= K) {  // every slot is selected: slots lo..hi-1 in order, then padding
+    for (int j = tid; j < K; j += NT) {
+      if (j < n) emit(j, (uint32_t)(lo + j), __ldg(row + lo + j));
+      else write_pad(out_idx, out_cand, j);
+    }
+    return;
+  }
+  const int base = lo & ~3;
+  if (hi - base > kCap) {   // only for an unaligned start right at the limit
+    topk_fallback<NT, kPack>(row, lo, hi, K, sm, emit);
+    return;
+  }
+
+  uint32_t key[kVec][4];
+  {
+    float4 v[kVec];
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int e0 = base + (j * NT + tid) * 4;
+      v[j] = e0 < hi ? __ldg(reinterpret_cast<const float4*>(row + e0))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int e0 = base + (j * NT + tid) * 4;
+      const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) key[j][c] = (e0 + c >= lo && e0 + c < hi) ? score_key(f[c]) : 0u;
+    }
+  }
+  auto slot = [&](int j, int c) { return (uint32_t)(base + (j * NT + tid) * 4 + c); };
+
+  for (int b = tid; b < kTSBins; b += NT) sm.f.scnt[b] = 0u;
+  for (int b = tid; b < kTBins; b += NT) sm.f.bins[b] = 0u;
+  if (tid == 0) {
+    sm.f.nsv = 0;
+    sm.f.nlist = 0;
+    sm.f.nb = 0;
+    sm.f.smin = 0xffffffffu;
+    sm.f.smax = 0u;
+    sm.f.lmin = 0xffffffffu;
+    sm.f.kmax = 0u;
+  }
+  // Samples: float4 rows 0, 2, 4, 6, one lane of each.
+  auto sample = [&](int i) { return key[2 * i][i]; };
+  {
+    int ns = 0;
+    uint32_t mn = 0xffffffffu, mx = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t k = sample(i);
+      ns += k != 0u;
+      mx = max(mx, k);
+      mn = min(mn, k ? k : 0xffffffffu);
+    }
+    ns = __reduce_add_sync(kFull, ns);
+    mn = __reduce_min_sync(kFull, mn);
+    mx = __reduce_max_sync(kFull, mx);
+    __syncthreads();
+    if (lane == 0 && ns) {
+      atomicAdd(&sm.f.nsv, ns);
+      atomicMin(&sm.f.smin, mn);
+      atomicMax(&sm.f.smax, mx);
+    }
+  }
+  __syncthreads();
+  uint32_t floor = 1u;   // every slot of the range
+  const int nsv = sm.f.nsv;
+  if (n * 4 > K * 5 && nsv >= 64) {
+    const uint32_t smin = sm.f.smin;
+    const int ssh = max(0, (32 - __clz((int)(sm.f.smax - smin))) - 8);   // range >> ssh < 256
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t k = sample(i);
+      if (k) atomicAdd(&sm.f.scnt[(k - smin) >> ssh], 1u);
+    }
+    __syncthreads();
+    // Expected samples among the winners: nsv * K / n; take 1/8 more and 16.
+    const int target = min(nsv, (int)((float)nsv * (float)K * 1.125f / (float)n) + 16);
+    const int local = tid < kTSBins ? (int)sm.f.scnt[kTSBins - 1 - tid] : 0;
+    int tot;
+    const int run = block_exclusive_scan(local, sm.f.scan, &tot);
+    if (tid < kTSBins && run < target && run + local >= target) {
+      sm.f.sfloor = smin + ((uint32_t)(kTSBins - 1 - tid) << ssh);
+      sm.f.scount = local;
+      sm.f.sabove = run;
+    }
+    __syncthreads();
+    floor = sm.f.sfloor;
+    if (sm.f.scount > 16 && ssh > 0) {
+      // Refine inside the selected bin [floor, floor + 2^ssh).
+      const int ssh2 = max(0, ssh - 8);
+      const int target2 = target - sm.f.sabove;
+      for (int b = tid; b < kTSBins; b += NT) sm.f.scnt[b] = 0u;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t k = sample(i);
+        if (k >= floor && ((k - floor) >> ssh) == 0u) atomicAdd(&sm.f.scnt[(k - floor) >> ssh2], 1u);
+      }
+      __syncthreads();
+      const int local2 = tid < kTSBins ? (int)sm.f.scnt[kTSBins - 1 - tid] : 0;
+      const int run2 = block_exclusive_scan(local2, sm.f.scan, &tot);
+      if (tid < kTSBins && run2 < target2 && run2 + local2 >= target2)
+        sm.f.sfloor = floor + ((uint32_t)(kTSBins - 1 - tid) << ssh2);
+      __syncthreads();
+      floor = sm.f.sfloor;
+    }
+  }
+
+  // (score key, ~slot) of the keys >= floor into the list, one ballot per slot.
+  {
+    uint32_t kmn = 0xffffffffu, kmx = 0u;
+    const unsigned lt = lanemask_lt();
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      unsigned bal[4];
+      int tot = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const bool p = key[j][c] >= floor;
+        if (p) {
+          kmn = min(kmn, key[j][c]);
+          kmx = max(kmx, key[j][c]);
+        }
+        bal[c] = __ballot_sync(kFull, p);
+        tot += __popc(bal[c]);
+      }
+      int b0 = 0;
+      if (lane == 0 && tot) b0 = atomicAdd(&sm.f.nlist, tot);
+      b0 = __shfl_sync(kFull, b0, 0);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int q = b0 + __popc(bal[c] & lt);
+        if ((bal[c] >> lane & 1u) && q < kTListCap)
+          sm.f.l[q] = ((ull)key[j][c] << 32) | ~slot(j, c);
+        b0 += __popc(bal[c]);
+      }
+    }
+    kmn = __reduce_min_sync(kFull, kmn);
+    kmx = __reduce_max_sync(kFull, kmx);
+    if (lane == 0 && kmn <= kmx) {
+      atomicMin(&sm.f.lmin, kmn);
+      atomicMax(&sm.f.kmax, kmx);
+    }
+  }
+  __syncthreads();
+  const int nl = sm.f.nlist;
+  bool fast = nl >= K && nl <= kTListCap;
+  if (fast) {
+    const uint32_t lmin = sm.f.lmin;
+    const int sh2 = max(0, (32 - __clz((int)(sm.f.kmax - lmin))) - 11);   // range >> sh2 < 2048
+    for (int i = tid; i < nl; i += NT)
+      atomicAdd(&sm.f.bins[((uint32_t)(sm.f.l[i] >> 32) - lmin) >> sh2], 1u);
+    __syncthreads();
+    {
+      constexpr int per = kTBins / NT;
+      const int g = kTBins - per * (tid + 1);
+      int cnt[per];
+      int local = 0;
+#pragma unroll
+      for (int j = 0; j < per; ++j) {
+        cnt[j] = (int)sm.f.bins[g + per - 1 - j];
+        local += cnt[j];
+      }
+      int tot;
+      int run = block_exclusive_scan(local, sm.f.scan, &tot);
+#pragma unroll
+      for (int j = 0; j < per; ++j) {
+        if (run < K && run + cnt[j] >= K) {
+          sm.f.bstar = g + per - 1 - j;
+          sm.f.above = run;
+          sm.f.bcnt = cnt[j];
+        }
+        run += cnt[j];
+      }
+    }
+    __syncthreads();
+    const int bstar = sm.f.bstar, above = sm.f.above, bcnt = sm.f.bcnt;
+    fast = bcnt <= kTRankCap;
+    if (fast) {
+      for (int i = tid; i < nl; i += NT) {
+        const ull x = sm.f.l[i];
+        if ((int)(((uint32_t)(x >> 32) - lmin) >> sh2) == bstar) sm.f.bst[atomicAdd(&sm.f.nb, 1)] = x;
+      }
+      __syncthreads();
+      const int take = K - above;   // members of b* that win
+      for (int i = tid; i < bcnt; i += NT) {
+        const ull x = sm.f.bst[i];
+        if (t_count_above(sm.f.bst, bcnt, x) == take - 1) sm.f.thr64 = x;
+      }
+      __syncthreads();
+    }
+  }
+  if (!fast) {
+    __syncthreads();   // the fallback's shared memory overlaps the list
+    topk_fallback<NT, kPack>(row, lo, hi, K, sm, emit);
+    return;
+  }
+
+  // Ordered emission.
+  const ull thr64 = sm.f.thr64;
+  const uint32_t thr = (uint32_t)(thr64 >> 32), last = ~(uint32_t)thr64;
+  auto wins = [&](int j, int c) {
+    const uint32_t k = key[j][c];
+    return k > thr || (k == thr && slot(j, c) <= last);
+  };
+  uint32_t pk[2] = {0u, 0u};   // winners per float4 row j, 8 bits each
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    int c4 = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) c4 += wins(j, c);
+    pk[j >> 2] |= (uint32_t)c4 << (8 * (j & 3));
+  }
+  uint32_t inc[2] = {pk[0], pk[1]};   // fields stay below 256: at most 128 a warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y0 = __shfl_up_sync(kFull, inc[0], o), y1 = __shfl_up_sync(kFull, inc[1], o);
+    if (lane >= o) {
+      inc[0] += y0;
+      inc[1] += y1;
+    }
+  }
+  if (lane == 31) {
+    sm.f.wt[warp][0] = inc[0];
+    sm.f.wt[warp][1] = inc[1];
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // Lane w < W: exclusive prefix over warps of each row's count, then the
+    // rows' totals in order.
+    int c8[kVec];
+#pragma unroll
+    for (int j = 0; j < kVec; ++j)
+      c8[j] = lane < W ? (int)((sm.f.wt[lane][j >> 2] >> (8 * (j & 3))) & 0xffu) : 0;
+    int row_base = 0;
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int incl = warp_inclusive_scan(c8[j]);
+      if (lane < W) sm.f.off[j][lane] = row_base + incl - c8[j];
+      row_base += __shfl_sync(kFull, incl, 31);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    const uint32_t ex = ((inc[j >> 2] - pk[j >> 2]) >> (8 * (j & 3))) & 0xffu;
+    int p = sm.f.off[j][warp] + (int)ex;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (wins(j, c)) emit.from_key(p++, slot(j, c), key[j][c]);
+  }
+}
+
 // Standalone pack: cand[r][s*K + j] from local_idx[s][r][j].  Each thread
 // handles four consecutive j (K % 4 == 0): one 16-byte index load, four
 // gathers from the logits, two 16-byte candidate stores.
@@ -157,6 +532,17 @@ template <bool kPack>
 dsa_status launch_topk(const float* logits, int64_t ld, int rows, int S, int I, int K,
                        const int32_t* row_starts, const int32_t* row_ends, int32_t* local_idx,
                        float* cand, uint32_t* err_flags, cudaStream_t stream) {
+  const ShardMath shm(S, I);
+  if (ld <= 32 * 512) {
+    auto launch_fast = [&](auto kern, int nt) {
+      const cudaError_t e = launch_kernel(kern, dim3((unsigned)(rows * S)), dim3((unsigned)nt), 0,
+                                          stream, 0, logits, ld, rows, S, I, K, row_starts,
+                                          row_ends, local_idx, cand, err_flags, shm);
+      return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    };
+    if (ld <= 32 * 256) return launch_fast(topk_fast_kernel<256, kPack>, 256);
+    return launch_fast(topk_fast_kernel<512, kPack>, 512);
+  }
   // Rows that fit the register path need no staging area.
   const int stage_cap = ld <= RT::kCap ? 0 : (ld < kStageCapElems ? (int)ld : kStageCapElems);
   const size_t smem = topk_stage_offset() + (size_t)stage_cap * sizeof(float);
