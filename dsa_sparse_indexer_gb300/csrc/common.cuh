@@ -76,6 +76,13 @@ struct ShardMath {
     const uint32_t q = fdivmod(l, fI, &r);
     return q * fIS.d + (uint32_t)s * (uint32_t)I + r;
   }
+  // Tokens of the global prefix [0, L) that shard s holds (L < 2^31).
+  __device__ __forceinline__ uint32_t local_len(uint32_t L, int s) const {
+    uint32_t r;
+    const uint32_t q = fdivmod(L, fIS, &r);
+    const int rem = min(max((int)r - s * I, 0), I);
+    return q * (uint32_t)I + (uint32_t)rem;
+  }
 };
 
 __device__ __forceinline__ void raise_flag(uint32_t* flags, uint32_t bit) {

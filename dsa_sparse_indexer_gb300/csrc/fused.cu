@@ -591,7 +591,8 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
   bool bad = false;
   if (st < 0) { st = 0; bad = true; }
   if (en < st) { en = st; bad = true; }
-  int64_t lo = local_len(st, s, a.S, a.I), hi = local_len(en, s, a.S, a.I);
+  // st and en are int32 row bounds clamped to >= 0: the 32-bit map applies.
+  int64_t lo = a.sh.local_len((uint32_t)st, s), hi = a.sh.local_len((uint32_t)en, s);
   if (hi > a.ld) { hi = a.ld; bad = true; }
   if (lo > hi) { lo = hi; bad = true; }
   const int n = (int)(hi - lo);

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
   bool bad = false;
   if (st < 0) { st = 0; bad = true; }
   if (en < st) { en = st; bad = true; }
-  int64_t lo = local_len(st, s, S, I), hi = local_len(en, s, S, I);
+  int64_t lo = sh.local_len((uint32_t)st, s), hi = sh.local_len((uint32_t)en, s);
   if (hi > ld) { hi = ld; bad = true; }
   if (lo > hi) { lo = hi; bad = true; }
   if (bad && tid == 0) raise_flag(flags, DSA_FLAG_BOUNDS);
@@ -105,45 +105,51 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 }
 
 // ---------------------------------------------------------------------------
-// Throughput path for local ranges of up to 32 * NT slots (NT = 256 or 512).
-// Each thread keeps 8 float4 of the range as score keys in registers (slot e
-// = base + 4 (j NT + tid) + c).  The K-th key is found without a radix pass
+// Throughput path for local ranges of up to 4 V NT slots (V = 4 float4 rows
+// per thread; NT = 512 or 1024 threads).  Each thread keeps V float4 of the
+// range as score keys in registers (slot e = base + 4 (j NT + tid) + c).  The K-th key is found without a radix pass
 // over all keys: a 256-bin histogram of 4 sampled keys per thread proposes a
-// floor a little below it; the (score key, ~slot) pairs at or above the floor
-// (about 1.15 K) go to a shared list; a 2048-bin histogram of the list over
-// its key range locates the bin b* that holds the K-th key, and ranking the
-// few members of b* gives the exact threshold (score key, slot): a slot wins
-// if its key is above the threshold key, or equal to it at a slot no later
-// than the threshold slot.  The winners are then written in ascending slot
-// order: per-thread counts for each of the 8 float4 rows, packed four to a
+// floor a little below it (about 1.15 K keys at or above it), a 2048-bin
+// histogram of those keys over [floor, max key] locates the bin b* that holds
+// the K-th key, and ranking the few members of b* on (score key, ~slot) gives
+// the exact threshold: a slot wins if its key is above the threshold key, or
+// equal to it at a slot no later than the threshold slot.  Bins other than b*
+// may be crowded; only b* is ranked.  The winners are then placed in slot
+// order: per-thread counts for each of the V float4 rows, packed into one
 // word, take one warp scan, and a small table gives each (row, warp) its
-// output offset.  Rows where the floor misses, the list overflows or b* is
-// crowded fall back to the radix select over the registers.
+// output offset; each thread drops its winners' (key, slot) at their output
+// positions in shared memory, and all threads then write the outputs with
+// coalesced stores.  Rows where the floor misses or b* is crowded fall back to
+// the radix select over the registers.
 // ---------------------------------------------------------------------------
 using ull = unsigned long long;
-constexpr int kTListCap = 3072;   // (key, ~slot) pairs at or above the floor
+constexpr int kTMaxK = 2048;     // largest K
 constexpr int kTBins = 2048;
 constexpr int kTSBins = 256;      // sample histogram
 constexpr int kTRankCap = 256;    // most members of b* for the pairwise ranking
 
-template <int NT>
+template <int NT, int V>
 struct TopkFastSmem {
   union {
     struct {
-      ull l[kTListCap];
+      // Stores are 32-bit: 64-bit stores of (key, slot) pairs made the
+      // compiler move the register keys to local memory.
+      uint32_t stage_k[kTMaxK];    // winners by output position: score key
+      uint32_t stage_s[kTMaxK];    // and slot
       uint32_t bins[kTBins];
-      ull bst[kTRankCap];          // members of b*
+      uint32_t bst_k[kTRankCap];   // members of b*: score key
+      uint32_t bst_s[kTRankCap];   // and slot
       uint32_t scnt[kTSBins];
-      uint32_t wt[NT / 32][2];     // packed per-row winner counts of each warp
-      int off[8][NT / 32];         // output offset of each (float4 row, warp)
+      uint32_t wt[NT / 32];        // packed per-row winner counts of each warp
+      int off[V][NT / 32];         // output offset of each (float4 row, warp)
       int scan[33];
-      int nsv, nlist, nb, bstar, above, bcnt, scount, sabove;
-      uint32_t smin, smax, lmin, kmax, sfloor;
+      int nsv, nb, bstar, above, bcnt, scount, sabove;
+      uint32_t smin, smax, kmin, kmax, sfloor;
       ull thr64;
     } f;
     struct {                       // fallback: radix select over the registers
       LocalTopkSmem loc;
-      RegEmitSmem<NT, kVec> es;
+      RegEmitSmem<NT, V> es;
       uint32_t list[kListCap];
     } g;
   };
@@ -172,39 +178,35 @@ struct TopkEmitter {
 // Fallback of the throughput path: the radix select over the keys, re-read
 // from the row (in L2) into registers, or over the row in global memory when
 // the range does not fit the registers.
-template <int NT, bool kPack>
+template <int NT, int V, bool kPack>
 __device__ __noinline__ void topk_fallback(const float* __restrict__ row, int lo, int hi, int K,
-                                           TopkFastSmem<NT>& sm, const TopkEmitter<kPack> emit) {
+                                           TopkFastSmem<NT, V>& sm,
+                                           const TopkEmitter<kPack> emit) {
   const int base = lo & ~3;
-  if (hi - base > 32 * NT) {
+  if (hi - base > 4 * V * NT) {
     local_topk_emit<NT>(row + lo, hi - lo, K, sm.g.loc,
                         [&](int p, int i, float v) { emit(p, (uint32_t)(lo + i), v); });
     return;
   }
-  uint32_t key[kVec][4];
-  load_keys<NT, kVec>(row, lo, hi, key);
+  uint32_t key[V][4];
+  load_keys<NT, V>(row, lo, hi, key);
   int eq;
-  const SelectResult res = select_regs<NT, kVec>(key, K, sm.g.loc.sel, sm.g.list, sm.g.es, &eq);
-  emit_winners<NT, kVec>(key, res.thr, res.take_eq, sm.g.es, [&](int p, int e, uint32_t k) {
+  const SelectResult res = select_regs<NT, V>(key, K, sm.g.loc.sel, sm.g.list, sm.g.es, &eq);
+  emit_winners<NT, V>(key, res.thr, res.take_eq, sm.g.es, [&](int p, int e, uint32_t k) {
     emit.from_key(p, (uint32_t)(base + e), k);
   });
 }
 
-__device__ __forceinline__ int t_count_above(const ull* a, int n, ull x) {
-  int gt = 0;
-  for (int q = 0; q < n; ++q) gt += a[q] > x;
-  return gt;
-}
-
-template <int NT, bool kPack>
-__global__ void __launch_bounds__(NT, NT == 256 ? 4 : 2)
+template <int NT, int V, bool kPack>
+__global__ void __launch_bounds__(NT, 1024 / NT)
     topk_fast_kernel(const float* __restrict__ logits, int64_t ld, int rows, int S, int I, int K,
                      const int32_t* __restrict__ row_starts, const int32_t* __restrict__ row_ends,
                      int32_t* __restrict__ local_idx, float* __restrict__ cand, uint32_t* flags,
                      const ShardMath sh) {
+  static_assert(V == 4, "per-row winner counts are packed four to a word");
   constexpr int W = NT / 32;
-  constexpr int kCap = 32 * NT;
-  __shared__ TopkFastSmem<NT> sm;
+  constexpr int kCap = 4 * V * NT;
+  __shared__ TopkFastSmem<NT, V> sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x / rows, r = blockIdx.x - s * rows;
   const float* row = logits + ((int64_t)s * rows + r) * ld;
@@ -214,7 +216,8 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 2)
   bool bad = false;
   if (st < 0) { st = 0; bad = true; }
   if (en < st) { en = st; bad = true; }
-  int64_t lo64 = local_len(st, s, S, I), hi64 = local_len(en, s, S, I);
+  // st and en are int32 row bounds clamped to >= 0: the 32-bit map applies.
+  int64_t lo64 = sh.local_len((uint32_t)st, s), hi64 = sh.local_len((uint32_t)en, s);
   if (hi64 > ld) { hi64 = ld; bad = true; }
   if (lo64 > hi64) { lo64 = hi64; bad = true; }
   if (bad && tid == 0) raise_flag(flags, DSA_FLAG_BOUNDS);
@@ -233,25 +236,33 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 2)
   }
   const int base = lo & ~3;
   if (hi - base > kCap) {   // only for an unaligned start right at the limit
-    topk_fallback<NT, kPack>(row, lo, hi, K, sm, emit);
+    topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, emit);
     return;
   }
 
-  uint32_t key[kVec][4];
+  // Keys of the range (0 outside it) and their range.
+  uint32_t key[V][4];
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
   {
-    float4 v[kVec];
+    float4 v[V];
 #pragma unroll
-    for (int j = 0; j < kVec; ++j) {
+    for (int j = 0; j < V; ++j) {
       const int e0 = base + (j * NT + tid) * 4;
       v[j] = e0 < hi ? __ldg(reinterpret_cast<const float4*>(row + e0))
                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int j = 0; j < kVec; ++j) {
+    for (int j = 0; j < V; ++j) {
       const int e0 = base + (j * NT + tid) * 4;
       const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) key[j][c] = (e0 + c >= lo && e0 + c < hi) ? score_key(f[c]) : 0u;
+      for (int c = 0; c < 4; ++c) {
+        const bool in = e0 + c >= lo && e0 + c < hi;
+        const uint32_t k = score_key(f[c]);
+        key[j][c] = in ? k : 0u;
+        kmn = in ? min(kmn, k) : kmn;
+        kmx = max(kmx, key[j][c]);
+      }
     }
   }
   auto slot = [&](int j, int c) { return (uint32_t)(base + (j * NT + tid) * 4 + c); };
@@ -260,15 +271,14 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 2)
   for (int b = tid; b < kTBins; b += NT) sm.f.bins[b] = 0u;
   if (tid == 0) {
     sm.f.nsv = 0;
-    sm.f.nlist = 0;
     sm.f.nb = 0;
     sm.f.smin = 0xffffffffu;
     sm.f.smax = 0u;
-    sm.f.lmin = 0xffffffffu;
+    sm.f.kmin = 0xffffffffu;
     sm.f.kmax = 0u;
   }
-  // Samples: float4 rows 0, 2, 4, 6, one lane of each.
-  auto sample = [&](int i) { return key[2 * i][i]; };
+  // Samples: one lane of each float4 row.
+  auto sample = [&](int i) { return key[i][i]; };
   {
     int ns = 0;
     uint32_t mn = 0xffffffffu, mx = 0u;
@@ -282,15 +292,22 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 2)
     ns = __reduce_add_sync(kFull, ns);
     mn = __reduce_min_sync(kFull, mn);
     mx = __reduce_max_sync(kFull, mx);
+    kmn = __reduce_min_sync(kFull, kmn);
+    kmx = __reduce_max_sync(kFull, kmx);
     __syncthreads();
-    if (lane == 0 && ns) {
-      atomicAdd(&sm.f.nsv, ns);
-      atomicMin(&sm.f.smin, mn);
-      atomicMax(&sm.f.smax, mx);
+    if (lane == 0) {
+      atomicMin(&sm.f.kmin, kmn);
+      atomicMax(&sm.f.kmax, kmx);
+      if (ns) {
+        atomicAdd(&sm.f.nsv, ns);
+        atomicMin(&sm.f.smin, mn);
+        atomicMax(&sm.f.smax, mx);
+      }
     }
   }
   __syncthreads();
-  uint32_t floor = 1u;   // every slot of the range
+  uint32_t floor = sm.f.kmin;   // without a sample floor: every key of the range
+  const uint32_t kmax = sm.f.kmax;
   const int nsv = sm.f.nsv;
   if (n * 4 > K * 5 && nsv >= 64) {
     const uint32_t smin = sm.f.smin;
@@ -334,149 +351,133 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 2)
     }
   }
 
-  // (score key, ~slot) of the keys >= floor into the list, one ballot per slot.
+  // Histogram of the keys >= floor over [floor, kmax].
+  const int sh2 = max(0, (32 - __clz((int)(kmax - floor))) - 11);   // range >> sh2 < 2048
+  auto bin_of = [&](uint32_t k) { return (int)((k - floor) >> sh2); };
+#pragma unroll
+  for (int j = 0; j < V; ++j)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (key[j][c] >= floor && key[j][c]) atomicAdd(&sm.f.bins[bin_of(key[j][c])], 1u);
+  __syncthreads();
+  int total;
   {
-    uint32_t kmn = 0xffffffffu, kmx = 0u;
-    const unsigned lt = lanemask_lt();
+    constexpr int per = kTBins / NT;
+    const int g = kTBins - per * (tid + 1);
+    int cnt[per];
+    int local = 0;
 #pragma unroll
-    for (int j = 0; j < kVec; ++j) {
-      unsigned bal[4];
-      int tot = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const bool p = key[j][c] >= floor;
-        if (p) {
-          kmn = min(kmn, key[j][c]);
-          kmx = max(kmx, key[j][c]);
-        }
-        bal[c] = __ballot_sync(kFull, p);
-        tot += __popc(bal[c]);
-      }
-      int b0 = 0;
-      if (lane == 0 && tot) b0 = atomicAdd(&sm.f.nlist, tot);
-      b0 = __shfl_sync(kFull, b0, 0);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int q = b0 + __popc(bal[c] & lt);
-        if ((bal[c] >> lane & 1u) && q < kTListCap)
-          sm.f.l[q] = ((ull)key[j][c] << 32) | ~slot(j, c);
-        b0 += __popc(bal[c]);
-      }
+    for (int j = 0; j < per; ++j) {
+      cnt[j] = (int)sm.f.bins[g + per - 1 - j];
+      local += cnt[j];
     }
-    kmn = __reduce_min_sync(kFull, kmn);
-    kmx = __reduce_max_sync(kFull, kmx);
-    if (lane == 0 && kmn <= kmx) {
-      atomicMin(&sm.f.lmin, kmn);
-      atomicMax(&sm.f.kmax, kmx);
+    int run = block_exclusive_scan(local, sm.f.scan, &total);
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      if (run < K && run + cnt[j] >= K) {
+        sm.f.bstar = g + per - 1 - j;
+        sm.f.above = run;
+        sm.f.bcnt = cnt[j];
+      }
+      run += cnt[j];
     }
   }
   __syncthreads();
-  const int nl = sm.f.nlist;
-  bool fast = nl >= K && nl <= kTListCap;
+  bool fast = total >= K && sm.f.bcnt <= kTRankCap;
   if (fast) {
-    const uint32_t lmin = sm.f.lmin;
-    const int sh2 = max(0, (32 - __clz((int)(sm.f.kmax - lmin))) - 11);   // range >> sh2 < 2048
-    for (int i = tid; i < nl; i += NT)
-      atomicAdd(&sm.f.bins[((uint32_t)(sm.f.l[i] >> 32) - lmin) >> sh2], 1u);
-    __syncthreads();
-    {
-      constexpr int per = kTBins / NT;
-      const int g = kTBins - per * (tid + 1);
-      int cnt[per];
-      int local = 0;
+    // Members of b*, then the exact threshold by ranking them.
+    const int bstar = sm.f.bstar, bcnt = sm.f.bcnt, take = K - sm.f.above;
+    uint32_t bm = 0u;   // bit 4 j + c: slot (j, c) is in b*
 #pragma unroll
-      for (int j = 0; j < per; ++j) {
-        cnt[j] = (int)sm.f.bins[g + per - 1 - j];
-        local += cnt[j];
-      }
-      int tot;
-      int run = block_exclusive_scan(local, sm.f.scan, &tot);
+    for (int j = 0; j < V; ++j)
 #pragma unroll
-      for (int j = 0; j < per; ++j) {
-        if (run < K && run + cnt[j] >= K) {
-          sm.f.bstar = g + per - 1 - j;
-          sm.f.above = run;
-          sm.f.bcnt = cnt[j];
-        }
-        run += cnt[j];
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t k = key[j][c];
+        bm |= (uint32_t)(k >= floor && k && bin_of(k) == bstar) << (4 * j + c);
       }
+    if (__any_sync(kFull, bm != 0u)) {   // most warps hold no member
+      const int mine = __popc(bm);
+      const int incl = warp_inclusive_scan(mine);
+      int b0 = 0;
+      if (lane == 31) b0 = atomicAdd(&sm.f.nb, incl);
+      int q = __shfl_sync(kFull, b0, 31) + incl - mine;
+#pragma unroll
+      for (int j = 0; j < V; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (bm >> (4 * j + c) & 1u) {
+            sm.f.bst_k[q] = key[j][c];
+            sm.f.bst_s[q] = slot(j, c);
+            ++q;
+          }
     }
     __syncthreads();
-    const int bstar = sm.f.bstar, above = sm.f.above, bcnt = sm.f.bcnt;
-    fast = bcnt <= kTRankCap;
-    if (fast) {
-      for (int i = tid; i < nl; i += NT) {
-        const ull x = sm.f.l[i];
-        if ((int)(((uint32_t)(x >> 32) - lmin) >> sh2) == bstar) sm.f.bst[atomicAdd(&sm.f.nb, 1)] = x;
-      }
-      __syncthreads();
-      const int take = K - above;   // members of b* that win
-      for (int i = tid; i < bcnt; i += NT) {
-        const ull x = sm.f.bst[i];
-        if (t_count_above(sm.f.bst, bcnt, x) == take - 1) sm.f.thr64 = x;
-      }
-      __syncthreads();
+    // Rank on (score key, ~slot): the member with take - 1 above it.
+    auto member = [&](int i) { return ((ull)sm.f.bst_k[i] << 32) | ~sm.f.bst_s[i]; };
+    for (int i = tid; i < bcnt; i += NT) {
+      const ull x = member(i);
+      int gt = 0;
+      for (int q = 0; q < bcnt; ++q) gt += member(q) > x;
+      if (gt == take - 1) sm.f.thr64 = x;
     }
-  }
-  if (!fast) {
-    __syncthreads();   // the fallback's shared memory overlaps the list
-    topk_fallback<NT, kPack>(row, lo, hi, K, sm, emit);
+    __syncthreads();
+  } else {
+    __syncthreads();   // the fallback's shared memory overlaps the bins
+    topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, emit);
     return;
   }
 
-  // Ordered emission.
+  // Slot-ordered placement of the winners.
   const ull thr64 = sm.f.thr64;
   const uint32_t thr = (uint32_t)(thr64 >> 32), last = ~(uint32_t)thr64;
-  auto wins = [&](int j, int c) {
-    const uint32_t k = key[j][c];
-    return k > thr || (k == thr && slot(j, c) <= last);
-  };
-  uint32_t pk[2] = {0u, 0u};   // winners per float4 row j, 8 bits each
+  uint32_t wmask = 0u;   // bit 4 j + c: slot (j, c) wins
 #pragma unroll
-  for (int j = 0; j < kVec; ++j) {
-    int c4 = 0;
+  for (int j = 0; j < V; ++j)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) c4 += wins(j, c);
-    pk[j >> 2] |= (uint32_t)c4 << (8 * (j & 3));
-  }
-  uint32_t inc[2] = {pk[0], pk[1]};   // fields stay below 256: at most 128 a warp
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t k = key[j][c];
+      wmask |= (uint32_t)(k > thr || (k == thr && slot(j, c) <= last)) << (4 * j + c);
+    }
+  uint32_t pk = 0u;   // winners per float4 row j, 8 bits each
+#pragma unroll
+  for (int j = 0; j < V; ++j) pk |= (uint32_t)__popc((wmask >> (4 * j)) & 0xfu) << (8 * j);
+  uint32_t inc = pk;   // fields stay below 256: at most 128 a warp
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y0 = __shfl_up_sync(kFull, inc[0], o), y1 = __shfl_up_sync(kFull, inc[1], o);
-    if (lane >= o) {
-      inc[0] += y0;
-      inc[1] += y1;
-    }
+    const uint32_t y = __shfl_up_sync(kFull, inc, o);
+    if (lane >= o) inc += y;
   }
-  if (lane == 31) {
-    sm.f.wt[warp][0] = inc[0];
-    sm.f.wt[warp][1] = inc[1];
-  }
+  if (lane == 31) sm.f.wt[warp] = inc;
   __syncthreads();
   if (warp == 0) {
     // Lane w < W: exclusive prefix over warps of each row's count, then the
     // rows' totals in order.
-    int c8[kVec];
-#pragma unroll
-    for (int j = 0; j < kVec; ++j)
-      c8[j] = lane < W ? (int)((sm.f.wt[lane][j >> 2] >> (8 * (j & 3))) & 0xffu) : 0;
+    const uint32_t wt = lane < W ? sm.f.wt[lane] : 0u;
     int row_base = 0;
 #pragma unroll
-    for (int j = 0; j < kVec; ++j) {
-      const int incl = warp_inclusive_scan(c8[j]);
-      if (lane < W) sm.f.off[j][lane] = row_base + incl - c8[j];
+    for (int j = 0; j < V; ++j) {
+      const int c = (int)((wt >> (8 * j)) & 0xffu);
+      const int incl = warp_inclusive_scan(c);
+      if (lane < W) sm.f.off[j][lane] = row_base + incl - c;
       row_base += __shfl_sync(kFull, incl, 31);
     }
   }
   __syncthreads();
 #pragma unroll
-  for (int j = 0; j < kVec; ++j) {
-    const uint32_t ex = ((inc[j >> 2] - pk[j >> 2]) >> (8 * (j & 3))) & 0xffu;
-    int p = sm.f.off[j][warp] + (int)ex;
+  for (int j = 0; j < V; ++j) {
+    int p = sm.f.off[j][warp] + (int)(((inc - pk) >> (8 * j)) & 0xffu);
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      if (wins(j, c)) emit.from_key(p++, slot(j, c), key[j][c]);
+      if (wmask >> (4 * j + c) & 1u) {
+        if (p < K) {
+          sm.f.stage_k[p] = key[j][c];
+          sm.f.stage_s[p] = slot(j, c);
+        }
+        ++p;
+      }
   }
+  __syncthreads();
+  for (int p = tid; p < K; p += NT) emit.from_key(p, sm.f.stage_s[p], sm.f.stage_k[p]);
 }
 
 // Standalone pack: cand[r][s*K + j] from local_idx[s][r][j].  Each thread
@@ -540,8 +541,8 @@ dsa_status launch_topk(const float* logits, int64_t ld, int rows, int S, int I, 
                                           row_ends, local_idx, cand, err_flags, shm);
       return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
     };
-    if (ld <= 32 * 256) return launch_fast(topk_fast_kernel<256, kPack>, 256);
-    return launch_fast(topk_fast_kernel<512, kPack>, 512);
+    if (ld <= 16 * 512) return launch_fast(topk_fast_kernel<512, 4, kPack>, 512);
+    return launch_fast(topk_fast_kernel<1024, 4, kPack>, 1024);
   }
   // Rows that fit the register path need no staging area.
   const int stage_cap = ld <= RT::kCap ? 0 : (ld < kStageCapElems ? (int)ld : kStageCapElems);
