@@ -128,6 +128,121 @@ __global__ void __launch_bounds__(kConvThreads)
     for (int s = tid; s < S; s += kConvThreads) counts[(int64_t)s * rows + r] = total[s];
 }
 
+// ---------------------------------------------------------------------------
+// Few shards (S <= 8): one 128-thread CTA per row, each warp owning a quarter
+// of the id list in chunks of 32.  One pass computes every id's owner and
+// physical slot and, per chunk, its position among the warp's ids of the same
+// shard: a ballot per shard, the lane's own shard's ballot counted below it,
+// plus that shard's running count (held by lane s and read with a shuffle).
+// A scan over the four warps' per-shard totals then gives final positions.
+// ---------------------------------------------------------------------------
+constexpr int kCvThreads = 128;
+constexpr int kCvWarps = kCvThreads / 32;
+constexpr int kCvMaxChunks = 2048 / kCvThreads;   // 16 chunks of 32 ids per warp for K = 2048
+constexpr int kCvMaxS = 8;
+
+__global__ void __launch_bounds__(kCvThreads)
+    convert_few_kernel(const int32_t* __restrict__ ids, int rows, int K, int S,
+                       const int32_t* __restrict__ bt, int reqs, int max_blocks, int bs,
+                       const int32_t* __restrict__ row_to_req, int32_t* __restrict__ slots,
+                       int32_t* __restrict__ counts, uint32_t* flags, const ShardMath sh,
+                       const FastDiv fbs) {
+  __shared__ int wbase[kCvWarps][kCvMaxS];   // per-warp counts, then exclusive bases
+  __shared__ int total[kCvMaxS];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = blockIdx.x;
+  const int req = row_to_req ? __ldg(row_to_req + r) : r;
+  const bool req_ok = req >= 0 && req < reqs;
+  const int nch = K / kCvThreads;            // chunks per warp
+  const int32_t* mine = ids + (int64_t)r * K + warp * nch * 32;
+  const unsigned lt = lanemask_lt();
+
+  // aux_c: the id, then the id's offset inside its block.
+  int aux_c[kCvMaxChunks];
+#pragma unroll
+  for (int c = 0; c < kCvMaxChunks; ++c) aux_c[c] = c < nch ? __ldg(mine + c * 32 + lane) : -1;
+
+  // Owner and block-table entry (-1: none); every table load is issued before use.
+  int own_c[kCvMaxChunks], blk_c[kCvMaxChunks];
+  bool bad = !req_ok;
+#pragma unroll
+  for (int c = 0; c < kCvMaxChunks; ++c) {
+    own_c[c] = -1;
+    blk_c[c] = -1;
+    const int id = aux_c[c];
+    if (id >= 0) {
+      const int o = sh.owner((uint32_t)id);
+      uint32_t off;
+      const uint32_t col = fdivmod(sh.local_slot((uint32_t)id), fbs, &off);
+      own_c[c] = o;
+      aux_c[c] = (int)off;
+      if (req_ok && col < (uint32_t)max_blocks)
+        blk_c[c] = __ldg(bt + ((int64_t)o * reqs + req) * max_blocks + col);
+    }
+  }
+  // Positions among the warp's ids of the same shard, in id order.
+  int run = 0;   // lane s < S: this warp's ids of shard s so far
+#pragma unroll
+  for (int c = 0; c < kCvMaxChunks; ++c) {
+    if (c < nch) {
+      const int o = own_c[c];
+      unsigned mybal = 0u;
+      int add = 0;
+      for (int s = 0; s < S; ++s) {
+        const unsigned b = __ballot_sync(kFull, o == s);
+        if (o == s) mybal = b;
+        if (lane == s) add = __popc(b);
+      }
+      const int base = __shfl_sync(kFull, run, o < 0 ? 0 : o);
+      own_c[c] = o < 0 ? -1 : (o | ((base + __popc(mybal & lt)) << 8));
+      run += add;
+    }
+  }
+  if (lane < S) wbase[warp][lane] = run;
+  __syncthreads();
+  if (tid < S) {
+    int acc = 0;
+#pragma unroll
+    for (int w = 0; w < kCvWarps; ++w) {
+      const int c = wbase[w][tid];
+      wbase[w][tid] = acc;
+      acc += c;
+    }
+    total[tid] = acc;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < kCvMaxChunks; ++c) {
+    const int packed = own_c[c];
+    if (c < nch && packed >= 0) {
+      const int o = packed & 0xff, pos = wbase[warp][o] + (packed >> 8);
+      // A missing or negative table entry, or a slot past INT32_MAX, gives
+      // -1 and raises the bounds flag.
+      int v = -1;
+      const int64_t x = (int64_t)blk_c[c] * bs + aux_c[c];
+      if (blk_c[c] >= 0 && x <= (int64_t)INT32_MAX) v = (int)x;
+      else bad = true;
+      slots[((int64_t)o * rows + r) * K + pos] = v;
+    }
+  }
+  if (bad) raise_flag(flags, DSA_FLAG_BOUNDS);
+
+  // -1 after each shard's valid slots, 16 bytes per store where aligned.
+  for (int s = 0; s < S; ++s) {
+    int32_t* dst = slots + ((int64_t)s * rows + r) * K;
+    const int t0 = total[s];
+    if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+      const int a0 = min(K, (t0 + 3) & ~3);
+      if (tid < a0 - t0) dst[t0 + tid] = -1;
+      int4* d4 = reinterpret_cast<int4*>(dst + a0);
+      for (int j = tid; j < (K - a0) / 4; j += kCvThreads) d4[j] = make_int4(-1, -1, -1, -1);
+    } else {
+      for (int j = t0 + tid; j < K; j += kCvThreads) dst[j] = -1;
+    }
+  }
+  if (counts && tid < S) counts[(int64_t)tid * rows + r] = total[tid];
+}
+
 }  // namespace
 }  // namespace dsa
 
@@ -145,6 +260,13 @@ extern "C" dsa_status dsa_convert_index_compact(const int32_t* ids, int rows, in
   if (rows == 0) return DSA_OK;
   if (!ids || !block_table || !slots) return DSA_ERR_INVALID_ARG;
   if ((int64_t)I * S > (int64_t)INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  if (S <= kCvMaxS) {
+    const cudaError_t e = launch_kernel(convert_few_kernel, dim3((unsigned)rows), dim3(kCvThreads),
+                                        0, stream, 0, ids, rows, K, S, block_table, reqs,
+                                        max_blocks, block_size, row_to_req, slots, counts,
+                                        err_flags, ShardMath(S, I), FastDiv((uint32_t)block_size));
+    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  }
   const cudaError_t e = launch_kernel(convert_kernel, dim3((unsigned)rows), dim3(kConvThreads), 0,
                                       stream, 0, ids, rows, K, S, block_table, reqs, max_blocks,
                                       block_size, row_to_req, slots, counts, err_flags,

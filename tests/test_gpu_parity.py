@@ -76,12 +76,10 @@ def test_reads_stay_inside_each_rows_range():
     assert np.all(np.isfinite(got["cand_scores"]) | np.isneginf(got["cand_scores"]))
 
 
-@pytest.mark.parametrize("K", [512, 1024, 2048])
-@pytest.mark.parametrize("S,I", [(1, 1), (3, 2), (8, 1), (5, 7)])
-def test_small_shapes_ties_and_tails(K, S, I):
-    """Many ties (coarse grid with -0.0), ragged ends around K, I*S and tile sizes."""
+def _ties_and_tails_case(K, S, I, rows=24):
+    """Many ties (coarse grid with -0.0), ragged ends around K, I*S and tile
+    sizes, a row of equal scores, a row of -inf, a few nonzero starts."""
     rng = np.random.default_rng(K + 10 * S + I)
-    rows = 24
     Lmax = 3 * K * S + 37
     x = (np.rint(rng.standard_normal((rows, Lmax)) * 4) / 4).astype(np.float32)
     x[rng.random((rows, Lmax)) < 0.05] = -0.0
@@ -99,11 +97,29 @@ def test_small_shapes_ties_and_tails(K, S, I):
     local = OL.shard_rows(x, ends, S, I, ld, fill=np.nan)
     bt = np.stack([rng.permutation(rows * cfg.max_blocks).astype(np.int32).reshape(rows, -1)
                    for _ in range(S)])
-    case = dict(cfg=cfg, x=x, local=local, starts=starts, ends=ends, bt=bt, r2q=None)
+    return dict(cfg=cfg, x=x, local=local, starts=starts, ends=ends, bt=bt, r2q=None)
+
+
+@pytest.mark.parametrize("K", [512, 1024, 2048])
+@pytest.mark.parametrize("S,I", [(1, 1), (3, 2), (8, 1), (5, 7)])
+def test_small_shapes_ties_and_tails(K, S, I):
+    """Ties and tails through the step kernels (both packings) and the fused kernel."""
+    case = _ties_and_tails_case(K, S, I)
+    rows = case["cfg"].rows
     for fused in (True, False):
         got = G.run_gpu(case, fused=fused)
         G.assert_indexer_parity(case, got, np.arange(rows))
     G.assert_indexer_parity(case, G.run_gpu_fused(case), np.arange(rows))
+
+
+@pytest.mark.parametrize("K", [512, 2048])
+@pytest.mark.parametrize("S,I", [(16, 3), (12, 1)])
+def test_many_shards_step_kernels(K, S, I):
+    """More shards than the fused kernel's cluster holds (S > 8): the step
+    kernels alone, including the general convert and the widest merge."""
+    case = _ties_and_tails_case(K, S, I, rows=16)
+    got = G.run_gpu(case, fused=True)
+    G.assert_indexer_parity(case, got, np.arange(case["cfg"].rows))
 
 
 @pytest.mark.parametrize("ld", [24000, 60000])
