@@ -52,9 +52,10 @@ PATHS = {
     # one kernel per step (a1+a2 fused), then the combine
     "steps": ("shard_topk_pack", "merge_topk_stable", "convert_index_compact", "lse_combine"),
 }
-KERNEL_SOURCES = {"shard_topk_pack": ("shard_topk.cu", "local_topk.cuh"),
-                  "merge_topk_stable": ("merge.cu",), "convert_index_compact": ("convert.cu",),
-                  "indexer_fused": ("fused.cu", "local_topk.cuh"),
+KERNEL_SOURCES = {"shard_topk_pack": ("shard_topk.cu", "local_topk.cuh", "reg_topk.cuh"),
+                  "merge_topk_stable": ("merge.cu", "reg_topk.cuh"),
+                  "convert_index_compact": ("convert.cu",),
+                  "indexer_fused": ("fused.cu", "local_topk.cuh", "reg_topk.cuh"),
                   "lse_combine": ("combine.cu",)}
 
 
@@ -238,7 +239,7 @@ def measured_peak() -> tuple[float, str]:
 def kernel_source_hash(kernel: str) -> str:
     csrc = os.path.join(ROOT, "dsa_sparse_indexer_gb300", "csrc")
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES[kernel] + ("common.cuh", "select.cuh"):
+    for f in KERNEL_SOURCES[kernel] + ("common.cuh", "fastdiv.h", "select.cuh"):
         p = os.path.join(csrc, f)
         if os.path.exists(p):
             h.update(open(p, "rb").read())
