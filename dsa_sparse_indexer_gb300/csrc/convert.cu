@@ -141,6 +141,25 @@ constexpr int kCvWarps = kCvThreads / 32;
 constexpr int kCvMaxChunks = 2048 / kCvThreads;   // 16 chunks of 32 ids per warp for K = 2048
 constexpr int kCvMaxS = 8;
 
+// id -> (owner, local slot / block size, local slot mod block size).  When S,
+// I and the block size are powers of two (kPow2) the divisions are shifts by
+// the log2 sizes held in the divisors' shift fields.
+template <bool kPow2>
+__device__ __forceinline__ void map_id(uint32_t id, const ShardMath& sh, const FastDiv& fbs,
+                                       int* owner, uint32_t* col, uint32_t* off) {
+  if (kPow2) {
+    const uint32_t lI = sh.fI.l, lS = sh.fS.l, lb = fbs.l;
+    *owner = (int)((id >> lI) & (uint32_t)(sh.S - 1));
+    const uint32_t local = ((id >> (lI + lS)) << lI) | (id & (uint32_t)(sh.I - 1));
+    *col = local >> lb;
+    *off = local & (fbs.d - 1u);
+  } else {
+    *owner = sh.owner(id);
+    *col = fdivmod(sh.local_slot(id), fbs, off);
+  }
+}
+
+template <bool kPow2>
 __global__ void __launch_bounds__(kCvThreads)
     convert_few_kernel(const int32_t* __restrict__ ids, int rows, int K, int S,
                        const int32_t* __restrict__ bt, int reqs, int max_blocks, int bs,
@@ -171,9 +190,9 @@ __global__ void __launch_bounds__(kCvThreads)
     blk_c[c] = -1;
     const int id = aux_c[c];
     if (id >= 0) {
-      const int o = sh.owner((uint32_t)id);
-      uint32_t off;
-      const uint32_t col = fdivmod(sh.local_slot((uint32_t)id), fbs, &off);
+      int o;
+      uint32_t col, off;
+      map_id<kPow2>((uint32_t)id, sh, fbs, &o, &col, &off);
       own_c[c] = o;
       aux_c[c] = (int)off;
       if (req_ok && col < (uint32_t)max_blocks)
@@ -261,10 +280,13 @@ extern "C" dsa_status dsa_convert_index_compact(const int32_t* ids, int rows, in
   if (!ids || !block_table || !slots) return DSA_ERR_INVALID_ARG;
   if ((int64_t)I * S > (int64_t)INT32_MAX) return DSA_ERR_UNSUPPORTED;
   if (S <= kCvMaxS) {
-    const cudaError_t e = launch_kernel(convert_few_kernel, dim3((unsigned)rows), dim3(kCvThreads),
-                                        0, stream, 0, ids, rows, K, S, block_table, reqs,
-                                        max_blocks, block_size, row_to_req, slots, counts,
-                                        err_flags, ShardMath(S, I), FastDiv((uint32_t)block_size));
+    auto pow2 = [](int v) { return (v & (v - 1)) == 0; };
+    auto kern = pow2(S) && pow2(I) && pow2(block_size) ? convert_few_kernel<true>
+                                                        : convert_few_kernel<false>;
+    const cudaError_t e = launch_kernel(kern, dim3((unsigned)rows), dim3(kCvThreads), 0, stream,
+                                        0, ids, rows, K, S, block_table, reqs, max_blocks,
+                                        block_size, row_to_req, slots, counts, err_flags,
+                                        ShardMath(S, I), FastDiv((uint32_t)block_size));
     return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   }
   const cudaError_t e = launch_kernel(convert_kernel, dim3((unsigned)rows), dim3(kConvThreads), 0,
