@@ -334,44 +334,29 @@ __device__ __forceinline__ int count_above(const ull* a, int s0, int e, ull x) {
 }
 
 // Appends one batch's valid candidates with score >= ffloor to the list as
-// raw (score, id) pairs, one warp ballot per candidate slot, and folds the
-// appended scores' range into fmn / fmx.  NaN scores fail the comparison.
+// raw (score, id) pairs: one pass mask per thread, one warp scan and one
+// shared atomic per warp for the positions.  NaN scores fail the comparison.
 __device__ __forceinline__ void append_batch(const float4 (&v)[kQuarter], float ffloor,
-                                             MergeFastSmem& sm, int* counter, float& fmn,
-                                             float& fmx) {
+                                             MergeFastSmem& sm, int* counter) {
   const int lane = threadIdx.x & 31;
-  unsigned bal[2 * kQuarter];
-  int tot = 0;
+  uint32_t mask = 0u;   // bit 2 i + h: candidate h of float4 i passes
 #pragma unroll
   for (int i = 0; i < kQuarter; ++i) {
-    const bool ok0 = __float_as_int(v[i].y) >= 0, ok1 = __float_as_int(v[i].w) >= 0;
-    const bool p0 = ok0 && v[i].x >= ffloor, p1 = ok1 && v[i].z >= ffloor;
-    if (p0) {
-      fmn = fminf(fmn, v[i].x);
-      fmx = fmaxf(fmx, v[i].x);
-    }
-    if (p1) {
-      fmn = fminf(fmn, v[i].z);
-      fmx = fmaxf(fmx, v[i].z);
-    }
-    bal[2 * i] = __ballot_sync(kFull, p0);
-    bal[2 * i + 1] = __ballot_sync(kFull, p1);
-    tot += __popc(bal[2 * i]) + __popc(bal[2 * i + 1]);
+    mask |= (uint32_t)(__float_as_int(v[i].y) >= 0 && v[i].x >= ffloor) << (2 * i);
+    mask |= (uint32_t)(__float_as_int(v[i].w) >= 0 && v[i].z >= ffloor) << (2 * i + 1);
   }
+  const int m = __popc(mask);
+  const int incl = warp_inclusive_scan(m);
   int base = 0;
-  if (lane == 0 && tot) base = atomicAdd(counter, tot);
-  base = __shfl_sync(kFull, base, 0);
-  const unsigned lt = lanemask_lt();
+  if (lane == 31 && incl) base = atomicAdd(counter, incl);
+  int p = __shfl_sync(kFull, base, 31) + incl - m;
 #pragma unroll
-  for (int i = 0; i < kQuarter; ++i)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const unsigned b = bal[2 * i + h];
-      const int p = base + __popc(b & lt);
-      if ((b >> lane & 1u) && p < kMListCap)
-        sm.u.f[p] = h ? make_float2(v[i].z, v[i].w) : make_float2(v[i].x, v[i].y);
-      base += __popc(b);
-    }
+  for (int i = 0; i < kQuarter; ++i) {
+    if ((mask >> (2 * i) & 1u) && p < kMListCap) sm.u.f[p] = make_float2(v[i].x, v[i].y);
+    p += mask >> (2 * i) & 1u;
+    if ((mask >> (2 * i + 1) & 1u) && p < kMListCap) sm.u.f[p] = make_float2(v[i].z, v[i].w);
+    p += mask >> (2 * i + 1) & 1u;
+  }
 }
 
 // Retry with no floor: appends every valid candidate as a rank key and folds
@@ -527,27 +512,22 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
     // Scores >= ffloor are exactly the keys >= floor (keys below that of -inf
     // are NaN patterns, which the retry handles).
     const float ffloor = floor <= score_key(-INFINITY) ? -INFINITY : key_score(floor);
-    float fmn = INFINITY, fmx = -INFINITY;
-    append_batch(va, ffloor, sm, &sm.nlist, fmn, fmx);
+    append_batch(va, ffloor, sm, &sm.nlist);
     load_batch(2, va);
-    append_batch(vb, ffloor, sm, &sm.nlist, fmn, fmx);
+    append_batch(vb, ffloor, sm, &sm.nlist);
     load_batch(3, vb);
-    append_batch(va, ffloor, sm, &sm.nlist, fmn, fmx);
-    append_batch(vb, ffloor, sm, &sm.nlist, fmn, fmx);
-    // Fold the range as score keys (order-preserving, -0.0 as +0.0).
-    const uint32_t kmn = __reduce_min_sync(kFull, fmn <= fmx ? score_key(fmn) : 0xffffffffu);
-    const uint32_t kmx = __reduce_max_sync(kFull, fmn <= fmx ? score_key(fmx) : 0u);
-    if (lane == 0 && kmn <= kmx) {
-      atomicMin(&sm.lmin, kmn);
-      atomicMax(&sm.kmax, kmx);
-    }
+    append_batch(va, ffloor, sm, &sm.nlist);
+    append_batch(vb, ffloor, sm, &sm.nlist);
   }
   __syncthreads();
   // With no floor every valid candidate is in the list (NaN scores, outside
   // the domain, aside); with a floor, K of them in the list settle need = K.
   int n = sm.nlist;
   int need = floor == 1u ? min(K, n) : K;
-  uint32_t lmin = sm.lmin, kmax = sm.kmax;
+  // Bin range: with a floor, [floor, largest sample] (every list key is >=
+  // floor; the few above the largest sample share the top bin); without one,
+  // the list's exact range, taken below.
+  uint32_t lmin = floor, kmax = max(sm.smax, floor);
   bool raw = true;   // list entries still (score, id) pairs
   if (n < need) {
     // The sample floor was above the K-th key: every valid key.
@@ -571,6 +551,28 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
     raw = false;
   }
 
+  if (raw && floor == 1u && need > 0 && n <= kMListCap) {
+    // No floor: convert the list to rank keys and take its exact key range.
+    uint32_t kmn = 0xffffffffu, kmx = 0u;
+    for (int i = tid; i < n; i += NT) {
+      const float2 f = sm.u.f[i];
+      const ull x = rank_key(f.x, f.y);
+      sm.u.l[i] = x;
+      kmn = min(kmn, (uint32_t)(x >> 32));
+      kmx = max(kmx, (uint32_t)(x >> 32));
+    }
+    kmn = __reduce_min_sync(kFull, kmn);
+    kmx = __reduce_max_sync(kFull, kmx);
+    if (lane == 0) {
+      atomicMin(&sm.lmin, kmn);
+      atomicMax(&sm.kmax, kmx);
+    }
+    __syncthreads();
+    lmin = sm.lmin;
+    kmax = sm.kmax;
+    raw = false;
+  }
+
   bool ranked = false;   // winners staged in out[] by position
   if (need > 0 && n > kMListCap) {
     merge_crowded<NT>(row, C, floor, n, need, sm, out_ids, out_sc);
@@ -586,7 +588,7 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
           const float2 f = sm.u.f[i];
           const ull x = rank_key(f.x, f.y);
           sm.u.l[i] = x;
-          atomicAdd(&sm.h.end[((uint32_t)(x >> 32) - lo) >> sh], 1u);
+          atomicAdd(&sm.h.end[min(((uint32_t)(x >> 32) - lo) >> sh, (uint32_t)kMBins - 1u)], 1u);
         }
       } else {
         for (int i = tid; i < n; i += NT) {
