@@ -52,7 +52,8 @@ PATHS = {
     # one kernel per step (a1+a2 fused), then the combine
     "steps": ("shard_topk_pack", "merge_topk_stable", "convert_index_compact", "lse_combine"),
 }
-KERNEL_SOURCES = {"shard_topk_pack": ("shard_topk.cu", "local_topk.cuh", "reg_topk.cuh"),
+KERNEL_SOURCES = {"shard_topk_pack": ("shard_topk.cu", "fast_select.cuh", "local_topk.cuh",
+                                      "reg_topk.cuh"),
                   "merge_topk_stable": ("merge.cu", "reg_topk.cuh"),
                   "convert_index_compact": ("convert.cu",),
                   "indexer_fused": ("fused.cu", "local_topk.cuh", "reg_topk.cuh"),

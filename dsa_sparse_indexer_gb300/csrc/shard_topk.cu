@@ -11,6 +11,7 @@
 // order (ties on the score go to the smaller slot, i.e. the smaller global id);
 // see local_topk.cuh.
 #include "common.cuh"
+#include "fast_select.cuh"
 #include "local_topk.cuh"
 #include "reg_topk.cuh"
 
@@ -107,45 +108,32 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 // ---------------------------------------------------------------------------
 // Throughput path for local ranges of up to 4 V NT slots (V = 4 float4 rows
 // per thread; NT = 512 or 1024 threads).  Each thread keeps V float4 of the
-// range as score keys in registers (slot e = base + 4 (j NT + tid) + c).  The K-th key is found without a radix pass
-// over all keys: a 256-bin histogram of 4 sampled keys per thread proposes a
-// floor a little below it (about 1.15 K keys at or above it), a 2048-bin
-// histogram of those keys over [floor, max key] locates the bin b* that holds
-// the K-th key, and ranking the few members of b* on (score key, ~slot) gives
-// the exact threshold: a slot wins if its key is above the threshold key, or
-// equal to it at a slot no later than the threshold slot.  Bins other than b*
-// may be crowded; only b* is ranked.  The winners are then placed in slot
-// order: per-thread counts for each of the V float4 rows, packed into one
-// word, take one warp scan, and a small table gives each (row, warp) its
-// output offset; each thread drops its winners' (key, slot) at their output
-// positions in shared memory, and all threads then write the outputs with
-// coalesced stores.  Rows where the floor misses or b* is crowded fall back to
-// the radix select over the registers.
+// range as score keys in registers (slot e = base + 4 (j NT + tid) + c).  The
+// exact threshold (key, slot) comes from fast_select (fast_select.cuh: a
+// sampled floor, a histogram over the keys above it, a ranking of the
+// threshold bin): a slot wins if its key is above the threshold key, or equal
+// to it at a slot no later than the threshold slot.  The winners are then
+// placed in slot order: per-thread counts for each of the V float4 rows,
+// packed into one word, take one warp scan, and a small table gives each
+// (row, warp) its output offset; each thread drops its winners' (key, slot)
+// at their output positions in shared memory, and all threads then write the
+// outputs with coalesced stores.  Rows where the floor misses or the
+// threshold bin is crowded fall back to the radix select over the registers.
 // ---------------------------------------------------------------------------
 using ull = unsigned long long;
 constexpr int kTMaxK = 2048;     // largest K
-constexpr int kTBins = 2048;
-constexpr int kTSBins = 256;      // sample histogram
-constexpr int kTRankCap = 256;    // most members of b* for the pairwise ranking
 
 template <int NT, int V>
 struct TopkFastSmem {
   union {
     struct {
-      // Stores are 32-bit: 64-bit stores of (key, slot) pairs made the
-      // compiler move the register keys to local memory.
-      uint32_t stage_k[kTMaxK];    // winners by output position: score key
-      uint32_t stage_s[kTMaxK];    // and slot
-      uint32_t bins[kTBins];
-      uint32_t bst_k[kTRankCap];   // members of b*: score key
-      uint32_t bst_s[kTRankCap];   // and slot
-      uint32_t scnt[kTSBins];
+      FastSelectSmem sel;
+      // Winners by output position, as separate 32-bit words (64-bit pair
+      // stores made the compiler move the register keys to local memory).
+      uint32_t stage_k[kTMaxK];
+      uint32_t stage_s[kTMaxK];
       uint32_t wt[NT / 32];        // packed per-row winner counts of each warp
       int off[V][NT / 32];         // output offset of each (float4 row, warp)
-      int scan[33];
-      int nsv, nb, bstar, above, bcnt, scount, sabove;
-      uint32_t smin, smax, kmin, kmax, sfloor;
-      ull thr64;
     } f;
     struct {                       // fallback: radix select over the registers
       LocalTopkSmem loc;
@@ -267,169 +255,15 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
   }
   auto slot = [&](int j, int c) { return (uint32_t)(base + (j * NT + tid) * 4 + c); };
 
-  for (int b = tid; b < kTSBins; b += NT) sm.f.scnt[b] = 0u;
-  for (int b = tid; b < kTBins; b += NT) sm.f.bins[b] = 0u;
-  if (tid == 0) {
-    sm.f.nsv = 0;
-    sm.f.nb = 0;
-    sm.f.smin = 0xffffffffu;
-    sm.f.smax = 0u;
-    sm.f.kmin = 0xffffffffu;
-    sm.f.kmax = 0u;
-  }
-  // Samples: one lane of each float4 row.
-  auto sample = [&](int i) { return key[i][i]; };
-  {
-    int ns = 0;
-    uint32_t mn = 0xffffffffu, mx = 0u;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t k = sample(i);
-      ns += k != 0u;
-      mx = max(mx, k);
-      mn = min(mn, k ? k : 0xffffffffu);
-    }
-    ns = __reduce_add_sync(kFull, ns);
-    mn = __reduce_min_sync(kFull, mn);
-    mx = __reduce_max_sync(kFull, mx);
-    kmn = __reduce_min_sync(kFull, kmn);
-    kmx = __reduce_max_sync(kFull, kmx);
-    __syncthreads();
-    if (lane == 0) {
-      atomicMin(&sm.f.kmin, kmn);
-      atomicMax(&sm.f.kmax, kmx);
-      if (ns) {
-        atomicAdd(&sm.f.nsv, ns);
-        atomicMin(&sm.f.smin, mn);
-        atomicMax(&sm.f.smax, mx);
-      }
-    }
-  }
-  __syncthreads();
-  uint32_t floor = sm.f.kmin;   // without a sample floor: every key of the range
-  const uint32_t kmax = sm.f.kmax;
-  const int nsv = sm.f.nsv;
-  if (n * 4 > K * 5 && nsv >= 64) {
-    const uint32_t smin = sm.f.smin;
-    const int ssh = max(0, (32 - __clz((int)(sm.f.smax - smin))) - 8);   // range >> ssh < 256
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t k = sample(i);
-      if (k) atomicAdd(&sm.f.scnt[(k - smin) >> ssh], 1u);
-    }
-    __syncthreads();
-    // Expected samples among the winners: nsv * K / n; take 1/8 more and 16.
-    const int target = min(nsv, (int)((float)nsv * (float)K * 1.125f / (float)n) + 16);
-    const int local = tid < kTSBins ? (int)sm.f.scnt[kTSBins - 1 - tid] : 0;
-    int tot;
-    const int run = block_exclusive_scan(local, sm.f.scan, &tot);
-    if (tid < kTSBins && run < target && run + local >= target) {
-      sm.f.sfloor = smin + ((uint32_t)(kTSBins - 1 - tid) << ssh);
-      sm.f.scount = local;
-      sm.f.sabove = run;
-    }
-    __syncthreads();
-    floor = sm.f.sfloor;
-    if (sm.f.scount > 16 && ssh > 0) {
-      // Refine inside the selected bin [floor, floor + 2^ssh).
-      const int ssh2 = max(0, ssh - 8);
-      const int target2 = target - sm.f.sabove;
-      for (int b = tid; b < kTSBins; b += NT) sm.f.scnt[b] = 0u;
-      __syncthreads();
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t k = sample(i);
-        if (k >= floor && ((k - floor) >> ssh) == 0u) atomicAdd(&sm.f.scnt[(k - floor) >> ssh2], 1u);
-      }
-      __syncthreads();
-      const int local2 = tid < kTSBins ? (int)sm.f.scnt[kTSBins - 1 - tid] : 0;
-      const int run2 = block_exclusive_scan(local2, sm.f.scan, &tot);
-      if (tid < kTSBins && run2 < target2 && run2 + local2 >= target2)
-        sm.f.sfloor = floor + ((uint32_t)(kTSBins - 1 - tid) << ssh2);
-      __syncthreads();
-      floor = sm.f.sfloor;
-    }
-  }
-
-  // Histogram of the keys >= floor over [floor, kmax].
-  const int sh2 = max(0, (32 - __clz((int)(kmax - floor))) - 11);   // range >> sh2 < 2048
-  auto bin_of = [&](uint32_t k) { return (int)((k - floor) >> sh2); };
-#pragma unroll
-  for (int j = 0; j < V; ++j)
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (key[j][c] >= floor && key[j][c]) atomicAdd(&sm.f.bins[bin_of(key[j][c])], 1u);
-  __syncthreads();
-  int total;
-  {
-    constexpr int per = kTBins / NT;
-    const int g = kTBins - per * (tid + 1);
-    int cnt[per];
-    int local = 0;
-#pragma unroll
-    for (int j = 0; j < per; ++j) {
-      cnt[j] = (int)sm.f.bins[g + per - 1 - j];
-      local += cnt[j];
-    }
-    int run = block_exclusive_scan(local, sm.f.scan, &total);
-#pragma unroll
-    for (int j = 0; j < per; ++j) {
-      if (run < K && run + cnt[j] >= K) {
-        sm.f.bstar = g + per - 1 - j;
-        sm.f.above = run;
-        sm.f.bcnt = cnt[j];
-      }
-      run += cnt[j];
-    }
-  }
-  __syncthreads();
-  bool fast = total >= K && sm.f.bcnt <= kTRankCap;
-  if (fast) {
-    // Members of b*, then the exact threshold by ranking them.
-    const int bstar = sm.f.bstar, bcnt = sm.f.bcnt, take = K - sm.f.above;
-    uint32_t bm = 0u;   // bit 4 j + c: slot (j, c) is in b*
-#pragma unroll
-    for (int j = 0; j < V; ++j)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t k = key[j][c];
-        bm |= (uint32_t)(k >= floor && k && bin_of(k) == bstar) << (4 * j + c);
-      }
-    if (__any_sync(kFull, bm != 0u)) {   // most warps hold no member
-      const int mine = __popc(bm);
-      const int incl = warp_inclusive_scan(mine);
-      int b0 = 0;
-      if (lane == 31) b0 = atomicAdd(&sm.f.nb, incl);
-      int q = __shfl_sync(kFull, b0, 31) + incl - mine;
-#pragma unroll
-      for (int j = 0; j < V; ++j)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (bm >> (4 * j + c) & 1u) {
-            sm.f.bst_k[q] = key[j][c];
-            sm.f.bst_s[q] = slot(j, c);
-            ++q;
-          }
-    }
-    __syncthreads();
-    // Rank on (score key, ~slot): the member with take - 1 above it.
-    auto member = [&](int i) { return ((ull)sm.f.bst_k[i] << 32) | ~sm.f.bst_s[i]; };
-    for (int i = tid; i < bcnt; i += NT) {
-      const ull x = member(i);
-      int gt = 0;
-      for (int q = 0; q < bcnt; ++q) gt += member(q) > x;
-      if (gt == take - 1) sm.f.thr64 = x;
-    }
-    __syncthreads();
-  } else {
-    __syncthreads();   // the fallback's shared memory overlaps the bins
+  FastSelectResult fs;
+  if (!fast_select<NT, V>(key, n, K, kmn, kmx, slot, sm.f.sel, &fs)) {
+    __syncthreads();   // the fallback's shared memory overlaps the selection's
     topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, emit);
     return;
   }
 
   // Slot-ordered placement of the winners.
-  const ull thr64 = sm.f.thr64;
-  const uint32_t thr = (uint32_t)(thr64 >> 32), last = ~(uint32_t)thr64;
+  const uint32_t thr = fs.thr, last = fs.last;
   uint32_t wmask = 0u;   // bit 4 j + c: slot (j, c) wins
 #pragma unroll
   for (int j = 0; j < V; ++j)
