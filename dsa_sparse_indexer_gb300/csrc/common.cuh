@@ -85,6 +85,18 @@ struct ShardMath {
   }
 };
 
+// 4-byte asynchronous copy global -> shared (cp.async); completion is waited
+// for by cp_async_wait_all, after which a barrier makes it visible to the CTA.
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void raise_flag(uint32_t* flags, uint32_t bit) {
   if (flags) atomicOr(flags, bit);
 }

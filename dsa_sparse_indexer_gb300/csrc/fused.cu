@@ -612,20 +612,33 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
   float2* out_cand = a.cand_out ? reinterpret_cast<float2*>(a.cand_out) + ((int64_t)r * a.S + s) * K
                                 : nullptr;
   const bool ordered = out_idx || out_cand;   // intermediates are written in slot order
+  // Rows on the register path issue their logit loads first, so that they
+  // are in flight during the block-table fetch below.
+  const int64_t base = lo & ~int64_t(3);
+  const bool reg_path = n > K && hi - base <= RT::kCap;
+  float4 v[kVec];
+  if (reg_path) {
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int64_t e0 = base + ((int64_t)j * kNT + tid) * 4;
+      v[j] = e0 < hi ? __ldg(reinterpret_cast<const float4*>(row + e0))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   {
-    // This shard's block-table row, fetched now so the slot conversion at the
-    // end does not wait on it.
+    // This shard's block-table row, copied asynchronously now so the slot
+    // conversion at the end does not wait on it; completed before the barrier
+    // that ends the local top-K.  The barriers inside the local top-K order
+    // thread 0's initialisation above before any use.
     const int req = a.row_to_req ? a.row_to_req[r] : r;
     if (req >= 0 && req < a.reqs) {
       const int32_t* table = a.bt + ((int64_t)s * a.reqs + req) * a.max_blocks;
       const int ncol = min(a.max_blocks, kTableCap);
-      for (int c = tid; c < ncol; c += kNT) sm.sbt[c] = __ldg(table + c);
+      for (int c = tid; c < ncol; c += kNT) cp_async4(&sm.sbt[c], table + c);
     }
   }
-  __syncthreads();
 
   // ---- a1 + a2: local top-K, kept as rank keys -----------------------------
-  const int64_t base = lo & ~int64_t(3);
   if (n <= K) {
     for (int j = tid; j < K; j += kNT) {
       if (j < n) {
@@ -640,25 +653,44 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
         if (out_cand) out_cand[j] = make_float2(-INFINITY, __int_as_float(-1));
       }
     }
-  } else if (hi - base <= RT::kCap) {
+  } else if (reg_path) {
     uint32_t key[kVec][4];
-    load_keys<kNT, kVec>(row, lo, hi, key);
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int64_t e0 = base + ((int64_t)j * kNT + tid) * 4;
+      const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) key[j][c] = (e0 + c >= lo && e0 + c < hi) ? score_key(f[c]) : 0u;
+    }
     int eq;
     const SelectResult res = select_regs<kNT, kVec>(key, K, sm.loc.sel,
                                                     reinterpret_cast<uint32_t*>(sm.scratch),
                                                     sm.es, &eq);
+    // Winners are staged as (score key, slot) words in the scratch area (the
+    // select's list is dead by now), then turned into rank keys and written
+    // out by all threads together: the per-winner work runs with full warps.
+    uint32_t* stage_k = reinterpret_cast<uint32_t*>(sm.scratch);
+    uint32_t* stage_l = stage_k + kMaxK;
     auto put = [&](int p, int e, uint32_t k) {
       if (p >= K) return;
-      const uint32_t l = (uint32_t)(base + e);
-      const uint32_t gid = a.sh.global_id(s, l);
-      sm.cand[p] = rank_key(k, gid);
-      if (out_idx) out_idx[p] = (int32_t)l;
-      if (out_cand) out_cand[p] = make_float2(row[l], __int_as_float((int)gid));
+      stage_k[p] = k;
+      stage_l[p] = (uint32_t)(base + e);
     };
     if (!ordered && (res.take_eq == 0 || res.take_eq == eq))
       emit_unordered<kNT, kVec>(key, res.take_eq == 0 ? res.thr + 1u : res.thr, sm.es, put);
     else
       emit_winners<kNT, kVec>(key, res.thr, res.take_eq, sm.es, put);
+    __syncthreads();
+    for (int p = tid; p < K; p += kNT) {
+      const uint32_t k = stage_k[p], l = stage_l[p];
+      const uint32_t gid = a.sh.global_id(s, l);
+      sm.cand[p] = rank_key(k, gid);
+      if (out_idx) out_idx[p] = (int32_t)l;
+      // A zero key stands for both zeros: read the value back for its sign.
+      if (out_cand)
+        out_cand[p] = make_float2(k == 0x80000000u ? row[l] : key_score(k),
+                                  __int_as_float((int)gid));
+    }
   } else {
     bool ok;
     const float* data = stage_local_range(row, lo, hi, stage, a.stage_cap, sm.loc, a.flags, &ok);
@@ -670,6 +702,7 @@ __global__ void __launch_bounds__(kNT, 2) fused_kernel(const FusedArgs a) {
       if (out_cand) out_cand[p] = make_float2(v, __int_as_float((int)gid));
     });
   }
+  cp_async_wait_all();   // this thread's block-table words; the barrier publishes them
   __syncthreads();
   const int m = sm.m;
   ull ck[kCandPerThread];
