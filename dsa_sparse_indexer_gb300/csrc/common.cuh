@@ -22,9 +22,11 @@ constexpr unsigned kFull = 0xffffffffu;
 // free to mean "padding".
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t score_key(float f) {
-  uint32_t b = __float_as_uint(f);
-  if (b == 0x80000000u) b = 0u;
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  // f + 0 turns -0.0 into +0.0 (round to nearest, no flush of denormals);
+  // then negative patterns are inverted and positive ones get the top bit:
+  // b ^ (sign-extended sign | 0x80000000).
+  const uint32_t b = __float_as_uint(__fadd_rn(f, 0.0f));
+  return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
 }
 
 __device__ __forceinline__ float key_score(uint32_t k) {

@@ -243,13 +243,22 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     for (int j = 0; j < V; ++j) {
       const int e0 = base + (j * NT + tid) * 4;
       const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      if (e0 >= lo && e0 + 4 <= hi) {   // the whole float4 is inside the range
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const bool in = e0 + c >= lo && e0 + c < hi;
-        const uint32_t k = score_key(f[c]);
-        key[j][c] = in ? k : 0u;
-        kmn = in ? min(kmn, k) : kmn;
-        kmx = max(kmx, key[j][c]);
+        for (int c = 0; c < 4; ++c) {
+          key[j][c] = score_key(f[c]);
+          kmn = min(kmn, key[j][c]);
+          kmx = max(kmx, key[j][c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const bool in = e0 + c >= lo && e0 + c < hi;
+          const uint32_t k = score_key(f[c]);
+          key[j][c] = in ? k : 0u;
+          kmn = in ? min(kmn, k) : kmn;
+          kmx = max(kmx, key[j][c]);
+        }
       }
     }
   }
@@ -264,14 +273,21 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
 
   // Slot-ordered placement of the winners.
   const uint32_t thr = fs.thr, last = fs.last;
-  uint32_t wmask = 0u;   // bit 4 j + c: slot (j, c) wins
+  uint32_t wmask = 0u, tmask = 0u;   // bit 4 j + c: slot (j, c) is above / at thr
 #pragma unroll
   for (int j = 0; j < V; ++j)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const uint32_t k = key[j][c];
-      wmask |= (uint32_t)(k > thr || (k == thr && slot(j, c) <= last)) << (4 * j + c);
+      wmask |= (uint32_t)(key[j][c] > thr) << (4 * j + c);
+      tmask |= (uint32_t)(key[j][c] == thr) << (4 * j + c);
     }
+  if (__any_sync(kFull, tmask != 0u)) {   // ties at the threshold: slots up to `last` win
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        wmask |= (uint32_t)((tmask >> (4 * j + c) & 1u) && slot(j, c) <= last) << (4 * j + c);
+  }
   uint32_t pk = 0u;   // winners per float4 row j, 8 bits each
 #pragma unroll
   for (int j = 0; j < V; ++j) pk |= (uint32_t)__popc((wmask >> (4 * j)) & 0xfu) << (8 * j);
