@@ -464,21 +464,33 @@ __device__ bool merge_by_bins(const FusedArgs& a, cg::cluster_group& cluster, Fu
     sm.moff[tid] = (int)n;               // of which in b*
   }
   __syncthreads();
-  if (tid == 0) {
+  // Every thread forms the (at most kMaxCluster) copy offsets itself, and per
+  // chunk of kNT positions issues the loads from all ranks before any store:
+  // the remote (DSMEM) reads then overlap instead of queueing behind stores.
+  int len[kMaxCluster], off[kMaxCluster], maxlen = 0;
+  {
     int o = 0;
-    for (int rk = 0; rk < a.S; ++rk) {
-      sm.off[rk] = o;
-      if (rk != s) o += sm.wr[rk];
+#pragma unroll
+    for (int rk = 0; rk < kMaxCluster; ++rk) {
+      len[rk] = (rk < a.S && rk != s) ? sm.wr[rk] : 0;
+      off[rk] = o;
+      o += len[rk];
+      maxlen = max(maxlen, len[rk]);
     }
   }
-  __syncthreads();
-  for (int rk = 0; rk < a.S; ++rk) {
-    if (rk == s) continue;
-    const ull* remote = cluster.map_shared_rank(LS, rk);
-    const int len = sm.wr[rk], o = sm.off[rk];
-#pragma unroll 4
-    for (int j = tid; j < len; j += kNT)
-      if (o + j < kMaxK + kBinCap) others[o + j] = remote[j];
+  if (tid < kMaxCluster) sm.off[tid] = off[tid];
+  for (int j0 = 0; j0 < maxlen; j0 += kNT) {
+    const int j = j0 + tid;
+    ull v[kMaxCluster];
+#pragma unroll
+    for (int rk = 0; rk < kMaxCluster; ++rk) {
+      // Ranks past the cluster map to this CTA (len 0: nothing is read).
+      const ull* remote = cluster.map_shared_rank(LS, rk < a.S ? rk : s);
+      v[rk] = j < len[rk] ? remote[j] : 0ull;
+    }
+#pragma unroll
+    for (int rk = 0; rk < kMaxCluster; ++rk)
+      if (j < len[rk] && off[rk] + j < kMaxK + kBinCap) others[off[rk] + j] = v[rk];
   }
   __syncthreads();
 
