@@ -12,19 +12,21 @@
 //     shared memory, local_topk.cuh), and the winners are kept in shared memory
 //     as 64-bit rank keys (score_key << 32 | ~global_id).
 //  2. The pages' all_gather becomes reads of the other CTAs' shared memory
-//     (DSMEM).  The first digit of a radix select over all S*K candidates sums
-//     the CTAs' histograms across the cluster; every CTA then gathers the
-//     candidates of the threshold bin from all CTAs and finishes the select on
-//     its own (the same data, so the same answer everywhere).  Ties on the
-//     score are broken by a select on ~global_id: the smaller id wins.
-//  3. Each CTA sorts the winners it holds (bitonic network over registers,
-//     warp shuffles and shared memory).  A shard's winners in rank order are
-//     exactly its compacted slots, so each CTA maps them through its own block
-//     table and writes them.
-//  4. A winner's global rank is its position among its CTA's winners plus, for
-//     every other CTA, the number of that CTA's winners ranked above it
-//     (binary search in a local copy of their sorted lists); it writes its id
-//     at that rank.
+//     (DSMEM).  A per-binade histogram summed over the cluster sets the floor
+//     of 1024 fine bins; each CTA counting-sorts its candidates above the
+//     floor into those bins and sorts inside each (small) bin; the fine bins
+//     summed over the cluster give the bin b* holding the K-th candidate.
+//     Every CTA copies the other CTAs' sorted lists down to b* and resolves
+//     the threshold among b*'s few members (the same data, so the same answer
+//     everywhere).  Ties on the score go to the smaller global id.
+//  3. A shard's winners in rank order are exactly its compacted slots, so
+//     each CTA maps them through its own block table and writes them.
+//  4. A winner's global rank is its position among its CTA's winners plus,
+//     for every other CTA, the number of that CTA's winners ranked above it
+//     (binary search in the copied lists); it writes its id at that rank.
+//  Rows where a winner-holding bin is crowded (heavy ties) take the exact
+//  path instead: a radix select finished over the cluster's gathered
+//  threshold bin and a bitonic sort of each CTA's winners.
 #include <cooperative_groups.h>
 #include <cstddef>
 

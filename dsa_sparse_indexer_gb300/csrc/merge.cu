@@ -5,11 +5,15 @@
 // radix selector) and section 关键源码片段 (the all_gathered [batch, S*topk, 2]
 // buffer; topk_indices overwritten with global ids, -1 for padding).
 //
-// One CTA per row.  The row's C candidates are staged in shared memory by bulk
-// async copies.  Selection is a radix select on the score key, and, only when
-// the K-th score is tied, a second radix select on the inverted id among the
-// tied candidates (ties go to the smaller id).  The K winners are then put in
-// rank order by a bitonic sort of their 64-bit keys (score_key << 32 | ~id).
+// One CTA per row; every candidate is ranked by its 64-bit key
+// (score_key << 32 | ~id), so ties go to the smaller id.  Rows of up to 32
+// candidates per thread (C <= 32768) take the throughput kernel
+// (merge_fast_kernel): a sampled floor, a compact list of the candidates above
+// it, bins over the list's key range that give the winners' output ranges,
+// and ranking inside each (small) bin.  Larger rows are staged in shared
+// memory by bulk async copies (merge_kernel): a radix select on the score key,
+// and, only when the K-th score is tied, a second one on the inverted id; the
+// K winners are then put in rank order by a bitonic sort.
 #include "common.cuh"
 #include "reg_topk.cuh"
 #include "select.cuh"

@@ -5,11 +5,15 @@
 // each rank, then (score, global_id) candidates packed as [batch, topk, 2]
 // fp32) and section 实现拆解 item 1 (`pack_dcp_topk_candidates_cutedsl`).
 //
-// One CTA per (shard, row).  The row's local range is staged in shared memory
-// with bulk async copies (TMA), a radix select finds the K-th best score key,
-// and one ordered sweep with warp ballots writes the winners in ascending slot
-// order (ties on the score go to the smaller slot, i.e. the smaller global id);
-// see local_topk.cuh.
+// One CTA per (shard, row); the winners are written in ascending slot order
+// (ties on the score go to the smaller slot, i.e. the smaller global id).
+// Local ranges of up to 16384 slots take the throughput kernel below
+// (topk_fast_kernel): keys in registers, the exact threshold from a sampled
+// floor (fast_select.cuh), slot-ordered placement through shared memory.
+// Longer ranges are staged in shared memory with bulk async copies (TMA) or
+// read from global memory, and a radix select with an ordered ballot sweep
+// picks the winners (shard_topk_kernel, local_topk.cuh).  The standalone pack
+// gathers candidates for given local indices.
 #include "common.cuh"
 #include "fast_select.cuh"
 #include "local_topk.cuh"
