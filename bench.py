@@ -1,20 +1,25 @@
 """Benchmark of the DCP sparse-indexer hot path on one GB300 (or N, as replicas).
 
-One step = one pass of the whole path over one batch of the decode workload
-(64 rows, S=4 shards, interleave 1, K=2048, per-row sequence length uniform in
-[8192, 65536], N(0,1) fp32 logits, paged block tables of 64-token blocks with
-per-shard random permutations, and the shards' [64, 128, 512] bf16 partial
-attention outputs with base-2 LSE in [-5, 20]):
+One step = one pass of the whole path over one batch.  Default: the decode
+workload (64 rows, S=4 shards, interleave 1, K=2048, per-row sequence length
+uniform in [8192, 65536], N(0,1) fp32 logits, paged block tables of 64-token
+blocks with per-shard random permutations, and the shards' [64, 128, 512] bf16
+partial attention outputs with base-2 LSE in [-5, 20]) on the fused path:
 
-    dsa_shard_topk_pack -> dsa_merge_topk_stable -> dsa_convert_index_compact
-    -> dsa_lse_combine
+    dsa_indexer_fused -> dsa_lse_combine
 
-called through the C ABI (ctypes) on the current stream.  Prints one JSON line.
+(`--path steps`: dsa_shard_topk_pack -> dsa_merge_topk_stable ->
+dsa_convert_index_compact [-> dsa_lse_combine]; `--workload` picks another of
+the five workloads), called through the C ABI (ctypes).  Prints one JSON line.
 
-  value        merged top-K rows/s, device time, inputs resident in HBM
+  value        merged top-K rows/s, device time, inputs resident in HBM: K steps
+               replayed as CUDA graphs (one per rotating input set), timed with
+               events on the launch stream
+  kernels      per-kernel mean times from K more steps launched one by one with
+               events between kernels (`launch_loop_ms_per_step` is that loop)
   e2e          the same through host buffers: per step, H2D of the step's inputs
-               from pinned memory, the four calls, D2H of slots, counts, the
-               combined output and its LSE
+               from pinned memory, the calls, D2H of slots, counts and (with the
+               combine) the combined output and its LSE
   roofline     the step's dominant kernel: algorithmic bytes per launch /
                its mean CUDA-event duration, against the measured HBM peak
   cpu_baseline the oracle (numpy, one core) on a bounded sample of the same batch
@@ -453,44 +458,83 @@ def main(argv=None) -> int:
     if int(err.item()) != 0:
         raise SystemExit(f"device error flags set during warm-up: {int(err.item())}")
 
-    # --- timed region: K steps, events between kernels on the launch stream --
+    # --- one CUDA graph per rotating input set (the step's launches) --------
+    graphs, graph_err = [], None
+    try:
+        gs = torch.cuda.Stream(dev)
+        with torch.cuda.stream(gs):
+            for i in range(REPLICAS):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=gs):
+                    gsp = torch.cuda.current_stream(dev).cuda_stream
+                    for fn, a in calls[i]:
+                        launch(fn, a[:-1] + (gsp,))
+                graphs.append(g)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup) * REPLICAS):
+                graphs[i % REPLICAS].replay()
+        torch.cuda.synchronize()
+    except Exception as exc:  # report, never hide: the launch loop is then the headline
+        graphs, graph_err = [], f"{type(exc).__name__}: {exc}"
+
     nk = len(KERNELS)
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * nk + 1)]
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.2)
+
+    # --- timed region: K steps as graph replays on the launch stream ---------
+    graph_ms = None
+    if graphs:
+        barrier(world)
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_wall0 = time.time()
+        with torch.cuda.stream(stream):
+            g0.record(stream)
+            for i in range(args.steps):
+                graphs[i % REPLICAS].replay()
+            g1.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        barrier(world)
+        graph_ms = g0.elapsed_time(g1)
+
+    # --- per-kernel times: K more steps, events between kernels -------------
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * nk + 1)]
     barrier(world)
     torch.cuda.synchronize()
     # Give the GPU a head start so kernel launches queue up behind a bounded
     # spin and the per-kernel events measure device time, not launch gaps.
     prime_s = min(3.0, 0.01 + args.steps * cpu_per_step * 1.5)
     torch.cuda._sleep(int(prime_s * 2.0e9))
-    t_wall0 = time.time()
+    t_loop0 = time.time()
     e = 0
     for i in range(args.steps):
         for fn, a in calls[i % REPLICAS]:
             evs[e].record(stream)
             launch(fn, a)
             e += 1
-        clocks.poll()
     evs[e].record(stream)
     torch.cuda.synchronize()
-    t_wall1 = time.time()
+    t_loop1 = time.time()
     barrier(world)
-    clocks.poll()
     time.sleep(0.1)
     clocks.stop()
     if int(err.item()) != 0:
         raise SystemExit(f"device error flags set in the timed region: {int(err.item())}")
 
-    total_ms = evs[0].elapsed_time(evs[e])
+    loop_ms = evs[0].elapsed_time(evs[e])
     per_kernel = {k: [] for k in KERNELS}
     for i in range(args.steps):
         for j, k in enumerate(KERNELS):
             per_kernel[k].append(evs[i * nk + j].elapsed_time(evs[i * nk + j + 1]))
     mean_ms = {k: float(np.mean(v)) for k, v in per_kernel.items()}
-    total_ms = max_over_ranks(total_ms, world)
+    if graph_ms is None:                      # no graphs: the launch loop is the timed region
+        graph_ms, t_wall0, t_wall1 = loop_ms, t_loop0, t_loop1
+    total_ms = max_over_ranks(graph_ms, world)
     ms_per_step = total_ms / args.steps
+    loop_ms_per_step = max_over_ranks(loop_ms, world) / args.steps
     value = world * R * args.steps / (total_ms / 1e3)
 
     # algorithmic bytes, averaged over the rotating sets
@@ -503,34 +547,6 @@ def main(argv=None) -> int:
     kernels = {k: {"ms": mean_ms[k], "algorithmic_bytes": nbytes[k],
                    "gbs": nbytes[k] / (mean_ms[k] / 1e3) / 1e9,
                    "frac": nbytes[k] / (mean_ms[k] / 1e3) / 1e9 / peak} for k in KERNELS}
-
-    # --- CUDA-graph variant (launch overhead shown separately) --------------
-    graph_ms = None
-    try:
-        graphs = []
-        gs = torch.cuda.Stream(dev)
-        with torch.cuda.stream(gs):
-            for i in range(REPLICAS):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=gs):
-                    gsp = torch.cuda.current_stream(dev).cuda_stream
-                    for fn, a in calls[i]:
-                        launch(fn, a[:-1] + (gsp,))
-                graphs.append(g)
-        torch.cuda.synchronize()
-        for i in range(3 * REPLICAS):
-            graphs[i % REPLICAS].replay()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_rep = max(REPLICAS, min(args.steps, 2000))
-        torch.cuda.synchronize()
-        g0.record(stream)
-        for i in range(n_rep):
-            graphs[i % REPLICAS].replay()
-        g1.record(stream)
-        torch.cuda.synchronize()
-        graph_ms = g0.elapsed_time(g1) / n_rep
-    except Exception as exc:  # report, never hide
-        graph_ms = f"unavailable: {type(exc).__name__}: {exc}"
 
     # --- e2e through host buffers --------------------------------------------
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -583,7 +599,11 @@ def main(argv=None) -> int:
                      "bytes_per_launch": nbytes[dominant],
                      "traffic": profiled_traffic(dominant, args.workload)},
         "kernels": kernels,
-        "graph_ms_per_step": graph_ms,
+        "timing": ("K steps as CUDA-graph replays, one graph per rotating input set; "
+                   "per-kernel times from K more steps launched one by one with events "
+                   "between kernels" if not graph_err else
+                   f"K steps launched one by one (graph capture failed: {graph_err})"),
+        "launch_loop_ms_per_step": loop_ms_per_step,
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "gpu_launches": nk * args.steps,
