@@ -4,10 +4,11 @@
 // Each of the NT threads holds V float4 rows of keys, key[j][c] at a slot
 // given by the caller (slots order ties: the smaller slot ranks first); key 0
 // marks an empty slot.  Steps:
-//   1. a 256-bin histogram of one key per float4 row per thread (V samples)
-//      over the samples' range proposes a floor a little below the K-th key
-//      (about 1.15 K keys at or above it); when the selected sample bin is
-//      crowded a second 256-bin histogram inside it refines the floor;
+//   1. a 256-bin histogram of one key per float4 row per thread (V samples),
+//      linear in the score over the samples' range, proposes a floor a little
+//      below the K-th key (about 1.15 K keys at or above it); when the
+//      selected sample bin is crowded (an outlier stretching the range) a
+//      second 256-bin histogram inside it, linear in the key, refines it;
 //   2. a 2048-bin histogram of the keys at or above the floor, spread over
 //      [floor, max key], locates the bin b* holding the K-th key;
 //   3. the members of b* (at most kFsRankCap) are ranked on (key, ~slot); the
@@ -34,7 +35,7 @@ struct FastSelectSmem {
   uint32_t bst_k[kFsRankCap];   // members of b*: score key
   uint32_t bst_s[kFsRankCap];   // and slot
   int scan[33];
-  int nsv, nb, bstar, above, bcnt, scount, sabove, gt, eq;
+  int nsv, nb, bstar, above, bcnt, scount, sabove, sbin, gt, eq;
   uint32_t smin, smax, kmin, kmax, sfloor;
   unsigned long long thr64;
 };
@@ -99,12 +100,17 @@ __device__ bool fast_select(const uint32_t (&key)[V][4], int n, int K, uint32_t 
   const uint32_t kmax = sm.kmax;
   const int nsv = sm.nsv;
   if (n * 4 > K * 5 && nsv >= 64) {
-    const uint32_t smin = sm.smin;
-    const int ssh = max(0, (32 - __clz((int)(sm.smax - smin))) - 8);   // range >> ssh < 256
+    const uint32_t smin = sm.smin, smax = sm.smax;
+    // Bins linear in the score: bin(k) = (score(k) - fmin) * fscale, clamped.
+    const float fmin = key_score(smin), fspan = key_score(smax) - fmin;
+    const float fscale = fspan > 0.f ? (float)kFsSampleBins / fspan : 0.f;
+    auto sbin = [&](uint32_t k) {
+      return min(kFsSampleBins - 1, max(0, (int)((key_score(k) - fmin) * fscale)));
+    };
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t k = sample(i);
-      if (k) atomicAdd(&sm.scnt[(k - smin) >> ssh], 1u);
+      if (k) atomicAdd(&sm.scnt[sbin(k)], 1u);
     }
     __syncthreads();
     // Expected samples among the winners: nsv * K / n; take 1/8 more and 16.
@@ -113,22 +119,34 @@ __device__ bool fast_select(const uint32_t (&key)[V][4], int n, int K, uint32_t 
     int tot;
     const int run = block_exclusive_scan(local, sm.scan, &tot);
     if (tid < kFsSampleBins && run < target && run + local >= target) {
-      sm.sfloor = smin + ((uint32_t)(kFsSampleBins - 1 - tid) << ssh);
+      sm.sbin = kFsSampleBins - 1 - tid;
       sm.scount = local;
       sm.sabove = run;
+      sm.sfloor = 0xffffffffu;
+    }
+    __syncthreads();
+    // The floor: the smallest sample in the selected bin (so every sample of
+    // the bin, and the target-th from the top, is at or above it).
+    const int selbin = sm.sbin;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t k = sample(i);
+      if (k && sbin(k) == selbin) atomicMin(&sm.sfloor, k);
     }
     __syncthreads();
     floor = sm.sfloor;
-    if (sm.scount > 16 && ssh > 0) {
-      // Refine inside the selected bin [floor, floor + 2^ssh).
-      const int ssh2 = max(0, ssh - 8);
+    if (sm.scount > 32) {
+      // Crowded bin: refine inside [floor, largest sample of the bin], linear in the key.
+      const uint32_t top = fscale > 0.f ? score_key(fmin + (float)(selbin + 1) / fscale) : smax;
+      const int ssh2 = max(0, (32 - __clz((int)(max(top, floor) - floor))) - 8);
       const int target2 = target - sm.sabove;
       for (int b = tid; b < kFsSampleBins; b += NT) sm.scnt[b] = 0u;
       __syncthreads();
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t k = sample(i);
-        if (k >= floor && ((k - floor) >> ssh) == 0u) atomicAdd(&sm.scnt[(k - floor) >> ssh2], 1u);
+        if (k && sbin(k) == selbin)
+          atomicAdd(&sm.scnt[min(kFsSampleBins - 1, (int)((k - floor) >> ssh2))], 1u);
       }
       __syncthreads();
       const int local2 = tid < kFsSampleBins ? (int)sm.scnt[kFsSampleBins - 1 - tid] : 0;
