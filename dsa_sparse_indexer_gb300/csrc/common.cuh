@@ -37,26 +37,15 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // Interleaved DCP sharding, closed forms of the ownership rule
 // owner(t) = (t / I) mod S (PR #46076 report, "[Attention][DSA] support dcp for
 // FLASHINFER_MLA_SPARSE", section 关键源码片段, `_dcp_localize_decode_seq_lens`).
-// A shard keeps its tokens in increasing global order.
+// A shard keeps its tokens in increasing global order: token t is local slot
+// (t / (I S)) I + t mod I of shard (t / I) mod S, and local slot l of shard s
+// is token (l / I) I S + s I + l mod I.
 // ---------------------------------------------------------------------------
-__host__ __device__ __forceinline__ int64_t owner_of(int64_t t, int S, int I) {
-  return (t / I) % S;
-}
-__host__ __device__ __forceinline__ int64_t local_slot_of(int64_t t, int S, int I) {
-  return (t / ((int64_t)I * S)) * I + t % I;
-}
 __host__ __device__ __forceinline__ int64_t global_of(int s, int64_t l, int S, int I) {
   return (l / I) * ((int64_t)I * S) + (int64_t)s * I + l % I;
 }
-// Tokens of the global prefix [0, L) that shard s holds.
-__host__ __device__ __forceinline__ int64_t local_len(int64_t L, int s, int S, int I) {
-  const int64_t round = (int64_t)I * S;
-  int64_t rem = L % round - (int64_t)s * I;
-  rem = rem < 0 ? 0 : (rem > I ? I : rem);
-  return (L / round) * I + rem;
-}
 
-// The same maps on 32-bit ids (< 2^31) with the divisions by I, I*S and S
+// The maps on 32-bit ids (< 2^31) with the divisions by I, I*S and S
 // precomputed on the host (fastdiv.h).
 struct ShardMath {
   int S, I;
