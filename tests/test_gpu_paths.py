@@ -1,0 +1,130 @@
+"""GPU parity of the throughput kernels' fallback paths on crafted rows.
+
+The throughput merge and local top-K set a floor from keys at fixed sample
+positions.  These rows are built so that the estimate misses in each way the
+kernels handle: the floor lands above the K-th key (the merge takes every
+valid candidate again, the local top-K its radix select), too many keys sit
+at or above it (the merge's list overflows into its radix path), no floor is
+needed at all, and the threshold bin is crowded with ties.  Each result is
+compared element by element with the oracle.
+"""
+import numpy as np
+import pytest
+
+from oracle import indexer as OX
+
+pytestmark = pytest.mark.gpu
+
+
+def _merge_check(scores: np.ndarray, ids: np.ndarray, K: int) -> None:
+    import torch
+
+    import dsa_sparse_indexer_gb300 as dsa
+    cand = np.stack([scores.astype(np.float32), ids.astype(np.int32).view(np.float32)], -1)
+    t = torch.from_numpy(np.ascontiguousarray(cand[None])).cuda()
+    err = dsa.new_error_flags("cuda")
+    got_ids, got_sc = dsa.merge_topk_stable(t, K, want_scores=True, err_flags=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    want_ids, want_sc = OX.merge(scores, ids, K)
+    np.testing.assert_array_equal(got_ids.cpu().numpy()[0], want_ids)
+    np.testing.assert_array_equal(got_sc.cpu().numpy()[0], want_sc)
+
+
+def _merge_sampled(C: int, nt: int = 256) -> np.ndarray:
+    """Candidates the throughput merge samples in a row of C <= 32 nt candidates:
+    candidate i % 2 of float4 (5 i) nt + t of the row, for i < 4, t < nt."""
+    t = np.arange(nt)
+    pos = np.concatenate([2 * ((5 * i) * nt + t) + (i & 1) for i in range(4)])
+    return np.sort(pos[pos < C])
+
+
+def _unique_ids(rng, n: int) -> np.ndarray:
+    return rng.permutation(10 * n)[:n].astype(np.int64)
+
+
+def test_merge_floor_above_the_kth_key_retries():
+    """Sampled candidates score high, the rest low: the sample floor is above
+    the K-th key, so the merge takes every valid candidate (fewer than its list
+    holds) and ranks them."""
+    rng = np.random.default_rng(1)
+    C, K, valid = 4096, 2048, 2900
+    scores = rng.standard_normal(C).astype(np.float32)
+    samp = _merge_sampled(C)
+    scores[samp] = 100.0 + np.arange(len(samp), dtype=np.float32) / 8
+    ids = _unique_ids(rng, C)
+    ids[valid:] = -1
+    scores[valid:] = -np.inf
+    _merge_check(scores, ids, K)
+
+
+def test_merge_list_overflow_takes_the_radix_path():
+    """5000 equal candidates at the sampled quantile: more keys at or above the
+    floor than the list holds, and ties broken by id."""
+    rng = np.random.default_rng(2)
+    C, K = 8192, 2048
+    scores = rng.standard_normal(C).astype(np.float32)
+    scores[rng.permutation(C)[:5000]] = 0.5
+    _merge_check(scores, _unique_ids(rng, C), K)
+
+
+def test_merge_without_a_floor():
+    """Fewer valid candidates than 1.25 K: no sample floor; every valid one is
+    ranked (padding interleaved with the candidates)."""
+    rng = np.random.default_rng(3)
+    C, K = 8192, 2048
+    scores = rng.standard_normal(C).astype(np.float32)
+    ids = _unique_ids(rng, C)
+    pad = rng.permutation(C)[:C - 2300]
+    ids[pad] = -1
+    scores[pad] = -np.inf
+    _merge_check(scores, ids, K)
+
+
+@pytest.mark.parametrize("K", [512, 2048])
+def test_merge_crowded_threshold_bin(K):
+    """Scores on a coarse grid: bins around the K-th key hold many ties."""
+    rng = np.random.default_rng(4 + K)
+    C = 4 * K
+    scores = (np.rint(rng.standard_normal(C) * 2) / 2).astype(np.float32)
+    _merge_check(scores, _unique_ids(rng, C), K)
+
+
+def _topk_check(row: np.ndarray, n: int, K: int) -> None:
+    """One shard (S = 1, I = 1), one row with local range [0, n)."""
+    import torch
+
+    import dsa_sparse_indexer_gb300 as dsa
+    ld = (len(row) + 3) // 4 * 4
+    logits = np.full((1, 1, ld), np.nan, np.float32)
+    logits[0, 0, :len(row)] = row
+    ends = torch.tensor([n], dtype=torch.int32, device="cuda")
+    err = dsa.new_error_flags("cuda")
+    local_idx = dsa.shard_topk(torch.from_numpy(logits).cuda(), ends, K, 1, err_flags=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    np.testing.assert_array_equal(local_idx.cpu().numpy()[0, 0], OX.shard_topk(row, 0, n, K))
+
+
+def test_local_topk_floor_above_the_kth_key_falls_back():
+    """Local ranges up to 8192 slots run 512 threads holding four float4 rows;
+    thread t samples lane i of row i, slot 4 (512 i + t) + i.  Those slots
+    score high: fewer than K keys lie at or above the floor, so the radix
+    select over the registers takes over."""
+    rng = np.random.default_rng(5)
+    n, K = 7000, 2048
+    row = rng.standard_normal(8192).astype(np.float32)
+    t = np.arange(512)
+    samp = np.concatenate([4 * (512 * i + t) + i for i in range(4)])
+    samp = samp[samp < n]
+    row[samp] = 50.0 + np.arange(len(samp), dtype=np.float32) / 64
+    _topk_check(row, n, K)
+
+
+def test_local_topk_crowded_threshold_bin():
+    """Coarse-grid values: the bin of the K-th key holds more keys than the
+    ranking handles, so the radix select takes over (ties by slot)."""
+    rng = np.random.default_rng(6)
+    n, K = 8000, 1024
+    row = (np.rint(rng.standard_normal(8192) * 2) / 2).astype(np.float32)
+    _topk_check(row, n, K)
