@@ -113,14 +113,31 @@ __global__ void __launch_bounds__(kCombThreads)
 template <int SN>
 constexpr int persist_blocks() { return SN <= 4 ? 4 : 2; }
 
-template <int SN>
+// Item -> (row * H + head, 256-element slice).  Below 2^31 items (k32) the
+// division by the slice count uses its host-computed invariant divisor.
+template <bool k32>
+__device__ __forceinline__ int64_t split_item(int64_t item, int nsl, const FastDiv& fnsl,
+                                              int* sl) {
+  if (k32) {
+    uint32_t r;
+    const uint32_t q = fdivmod((uint32_t)item, fnsl, &r);
+    *sl = (int)r;
+    return q;
+  }
+  const int64_t rh = item / nsl;
+  *sl = (int)(item - rh * nsl);
+  return rh;
+}
+
+template <int SN, bool k32>
 __device__ __forceinline__ void load_item(const uint16_t* __restrict__ part,
                                           const float* __restrict__ lse2, int S, int64_t RH,
-                                          int D, int nsl, int64_t item, uint4 (&v)[SN],
-                                          float& a) {
+                                          int D, int nsl, const FastDiv& fnsl, int64_t item,
+                                          uint4 (&v)[SN], float& a) {
   const int lane = threadIdx.x & 31;
-  const int64_t rh = item / nsl;
-  const int d = (int)(item - rh * nsl) * 256 + lane * 8;
+  int sl;
+  const int64_t rh = split_item<k32>(item, nsl, fnsl, &sl);
+  const int d = sl * 256 + lane * 8;
 #pragma unroll
   for (int s = 0; s < SN; ++s)
     v[s] = (s < S && d < D)
@@ -129,11 +146,11 @@ __device__ __forceinline__ void load_item(const uint16_t* __restrict__ part,
   a = lane < S ? __ldg(lse2 + lane * RH + rh) : -INFINITY;
 }
 
-template <int SN>
+template <int SN, bool k32>
 __global__ void __launch_bounds__(kCombThreads, persist_blocks<SN>())
     lse_combine_persist_kernel(const uint16_t* __restrict__ part, const float* __restrict__ lse2,
                                int S, int rows, int H, int D, uint16_t* __restrict__ out,
-                               float* __restrict__ lse_out) {
+                               float* __restrict__ lse_out, const FastDiv fnsl) {
   const int nsl = (D + 255) >> 8;
   const int64_t RH = (int64_t)rows * H;
   const int64_t nitems = RH * nsl;
@@ -142,12 +159,12 @@ __global__ void __launch_bounds__(kCombThreads, persist_blocks<SN>())
   int64_t item = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5);
   uint4 cur[SN], nxt[SN];
   float a_cur = -INFINITY, a_nxt = -INFINITY;
-  if (item < nitems) load_item<SN>(part, lse2, S, RH, D, nsl, item, cur, a_cur);
+  if (item < nitems) load_item<SN, k32>(part, lse2, S, RH, D, nsl, fnsl, item, cur, a_cur);
   for (; item < nitems; item += stride) {
     const int64_t next = item + stride;
-    if (next < nitems) load_item<SN>(part, lse2, S, RH, D, nsl, next, nxt, a_nxt);
-    const int64_t rh = item / nsl;
-    const int sl = (int)(item - rh * nsl);
+    if (next < nitems) load_item<SN, k32>(part, lse2, S, RH, D, nsl, fnsl, next, nxt, a_nxt);
+    int sl;
+    const int64_t rh = split_item<k32>(item, nsl, fnsl, &sl);
     const int d = sl * 256 + lane * 8;
     uint16_t* dst = out + rh * D;
     float M = a_cur;
@@ -197,9 +214,14 @@ dsa_status launch_persist(const uint16_t* part, const float* lse2, int S, int ro
   const int64_t need = (items + kCombWarps - 1) / kCombWarps;
   const int64_t cap = (int64_t)sms * persist_blocks<SN>();
   const int blocks = (int)(need < cap ? need : cap);
-  const cudaError_t e = launch_kernel(lse_combine_persist_kernel<SN>, dim3((unsigned)blocks),
-                                      dim3(kCombThreads), 0, stream, 0, part, lse2, S, rows, H, D,
-                                      out, lse_out);
+  const int nsl = (D + 255) / 256;
+  // 32-bit items when every item index (and the index one stride past the
+  // last) stays below 2^31.
+  const bool k32 = items + (int64_t)blocks * kCombWarps < ((int64_t)1 << 31);
+  auto kern = k32 ? lse_combine_persist_kernel<SN, true> : lse_combine_persist_kernel<SN, false>;
+  const cudaError_t e = launch_kernel(kern, dim3((unsigned)blocks), dim3(kCombThreads), 0, stream,
+                                      0, part, lse2, S, rows, H, D, out, lse_out,
+                                      FastDiv((uint32_t)nsl));
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
