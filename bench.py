@@ -59,7 +59,7 @@ PATHS = {
 }
 KERNEL_SOURCES = {"shard_topk_pack": ("shard_topk.cu", "fast_select.cuh", "local_topk.cuh",
                                       "reg_topk.cuh"),
-                  "merge_topk_stable": ("merge.cu", "reg_topk.cuh"),
+                  "merge_topk_stable": ("merge.cu", "reg_topk.cuh", "binmap.cuh"),
                   "convert_index_compact": ("convert.cu",),
                   "indexer_fused": ("fused.cu", "local_topk.cuh", "reg_topk.cuh"),
                   "lse_combine": ("combine.cu",)}

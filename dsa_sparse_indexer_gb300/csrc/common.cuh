@@ -39,14 +39,10 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // FLASHINFER_MLA_SPARSE", section 关键源码片段, `_dcp_localize_decode_seq_lens`).
 // A shard keeps its tokens in increasing global order: token t is local slot
 // (t / (I S)) I + t mod I of shard (t / I) mod S, and local slot l of shard s
-// is token (l / I) I S + s I + l mod I.
+// is token (l / I) I S + s I + l mod I.  The maps work on 32-bit ids (row
+// ends are int32), with the divisions by I, I*S and S precomputed on the host
+// (fastdiv.h).
 // ---------------------------------------------------------------------------
-__host__ __device__ __forceinline__ int64_t global_of(int s, int64_t l, int S, int I) {
-  return (l / I) * ((int64_t)I * S) + (int64_t)s * I + l % I;
-}
-
-// The maps on 32-bit ids (< 2^31) with the divisions by I, I*S and S
-// precomputed on the host (fastdiv.h).
 struct ShardMath {
   int S, I;
   FastDiv fI, fIS, fS;

@@ -14,6 +14,7 @@
 // memory by bulk async copies (merge_kernel): a radix select on the score key,
 // and, only when the K-th score is tied, a second one on the inverted id; the
 // K winners are then put in rank order by a bitonic sort.
+#include "binmap.cuh"
 #include "common.cuh"
 #include "reg_topk.cuh"
 #include "select.cuh"
@@ -581,23 +582,22 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
   if (need > 0 && n > kMListCap) {
     merge_crowded<NT>(row, C, floor, n, need, sm, out_ids, out_sc);
   } else if (need > 0) {
-    uint32_t lo = lmin;
-    int sh, bstar = 0, above = 0, bcnt = 0;
+    BinMap<kMBins> bin(lmin, kmax);
+    int bstar = 0, above = 0, bcnt = 0;
 #pragma unroll 1
     for (int level = 0;; ++level) {
-      sh = max(0, (32 - __clz((int)(kmax - lo))) - 11);   // range >> sh < 2048
       if (raw) {
         raw = false;
         for (int i = tid; i < n; i += NT) {
           const float2 f = sm.u.f[i];
           const ull x = rank_key(f.x, f.y);
           sm.u.l[i] = x;
-          atomicAdd(&sm.h.end[min(((uint32_t)(x >> 32) - lo) >> sh, (uint32_t)kMBins - 1u)], 1u);
+          atomicAdd(&sm.h.end[bin((uint32_t)(x >> 32))], 1u);
         }
       } else {
         for (int i = tid; i < n; i += NT) {
           const uint32_t k = (uint32_t)(sm.u.l[i] >> 32);
-          if (k >= lo) atomicAdd(&sm.h.end[min((k - lo) >> sh, (uint32_t)kMBins - 1u)], 1u);
+          if (k >= bin.lo) atomicAdd(&sm.h.end[bin(k)], 1u);
         }
       }
       __syncthreads();
@@ -635,9 +635,9 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
       above = sm.above;
       bcnt = sm.bcnt;
       ranked = bcnt <= kRankCap && sm.bmax[level] <= kFineCap;
-      if (ranked || level == 1 || sh == 0) break;
+      if (ranked || level == 1 || kmax - bin.lo < (uint32_t)kMBins) break;
       // Second level over [bottom of b*, kmax]: every winner is at or above it.
-      lo += (uint32_t)bstar << sh;
+      bin = BinMap<kMBins>(bin.bottom(bstar), kmax);
       for (int b = tid; b < kMBins; b += NT) sm.h.end[b] = 0u;
       __syncthreads();
     }
@@ -648,15 +648,15 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
       for (int i = tid; i < n; i += NT) {
         const ull x = sm.u.l[i];
         const uint32_t k = (uint32_t)(x >> 32);
-        if (k < lo) continue;
-        const int b = (int)min((k - lo) >> sh, (uint32_t)kMBins - 1u);
+        if (k < bin.lo) continue;
+        const int b = bin(k);
         if (b > bstar) sm.win[atomicAdd(&sm.h.end[b], 1u)] = x;
         else if (b == bstar) sm.bst[atomicAdd(&sm.nb, 1)] = x;
       }
       __syncthreads();
       for (int p = tid; p < above; p += NT) {
         const ull x = sm.win[p];
-        const int b = (int)min(((uint32_t)(x >> 32) - lo) >> sh, (uint32_t)kMBins - 1u);
+        const int b = bin((uint32_t)(x >> 32));
         const int e = (int)sm.h.end[b], s0 = b == kMBins - 1 ? 0 : (int)sm.h.end[b + 1];
         sm.u.out[s0 + count_above(sm.win, s0, e, x)] = x;
       }
@@ -668,8 +668,7 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
       __syncthreads();
     } else {
       __syncthreads();   // the select reuses the bin counters
-      merge_crowded<NT>(row, C, lo + ((uint32_t)bstar << sh), above + bcnt, need, sm, out_ids,
-                        out_sc);
+      merge_crowded<NT>(row, C, bin.bottom(bstar), above + bcnt, need, sm, out_ids, out_sc);
     }
   }
   // Write the ranked winners and the -1 / -inf padding, 4 positions a thread.

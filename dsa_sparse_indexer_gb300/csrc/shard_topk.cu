@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
       if (j < n) {
         const int64_t l = lo + j;
         if (out_idx) out_idx[j] = (int32_t)l;
-        if (kPack) out_cand[j] = make_float2(row[l], __int_as_float((int)global_of(s, l, S, I)));
+        if (kPack) out_cand[j] = make_float2(row[l], __int_as_float((int)sh.global_id(s, (uint32_t)l)));
       } else {
         write_pad(out_idx, out_cand, j);
       }
@@ -339,8 +339,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
 // gathers from the logits, two 16-byte candidate stores.
 __global__ void __launch_bounds__(256)
     pack_kernel(const float* __restrict__ logits, int64_t ld,
-                const int32_t* __restrict__ local_idx, int rows, int S, int I, int K,
-                float* __restrict__ cand, uint32_t* flags) {
+                const int32_t* __restrict__ local_idx, int rows, int S, int K,
+                float* __restrict__ cand, uint32_t* flags, const ShardMath sh) {
   const int64_t quads = (int64_t)S * rows * K / 4;
   const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (q >= quads) return;
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(256)
   for (int u = 0; u < 4; ++u) {
     const int l = l4[u];
     if (l >= 0 && l < ld) {
-      o[u] = make_float2(__ldg(row + l), __int_as_float((int)global_of(s, l, S, I)));
+      o[u] = make_float2(__ldg(row + l), __int_as_float((int)sh.global_id(s, (uint32_t)l)));
     } else {
       bad |= l >= ld;
       o[u] = make_float2(-INFINITY, __int_as_float(-1));
@@ -453,6 +453,7 @@ extern "C" dsa_status dsa_pack_candidates(const float* logits, int64_t ld,
   const int64_t blocks = (quads + 255) / 256;
   if (blocks > INT32_MAX) return DSA_ERR_UNSUPPORTED;
   const cudaError_t e = launch_kernel(pack_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, 0,
-                                      logits, ld, local_idx, rows, S, I, K, cand, err_flags);
+                                      logits, ld, local_idx, rows, S, K, cand, err_flags,
+                                      ShardMath(S, I));
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
