@@ -10,10 +10,10 @@
 // candidates per thread (C <= 32768) take the throughput kernel
 // (merge_fast_kernel): a sampled floor, a compact list of the candidates above
 // it, bins over the list's key range that give the winners' output ranges,
-// and ranking inside each (small) bin.  Larger rows are staged in shared
-// memory by bulk async copies (merge_kernel): a radix select on the score key,
-// and, only when the K-th score is tied, a second one on the inverted id; the
-// K winners are then put in rank order by a bitonic sort.
+// and ranking inside each (small) bin.  Larger rows (merge_kernel) are read
+// from global memory (L2 after the first pass): a radix select on the score
+// key, and, only when the K-th score is tied, a second one on the inverted
+// id; the K winners are then put in rank order by a bitonic sort.
 #include "binmap.cuh"
 #include "common.cuh"
 #include "reg_topk.cuh"
@@ -23,13 +23,9 @@ namespace dsa {
 namespace {
 
 constexpr int kMergeThreads = 1024;
-constexpr int kMaxChunks = 16;
-constexpr uint32_t kChunkBytes = 16384;
-constexpr int kStageCapCand = 20 * 1024;   // 160 KB of staged candidates at most
 constexpr int kMaxK = 2048;
 
 struct MergeSmem {
-  uint64_t bars[kMaxChunks];
   SelectSmem sel;
   unsigned long long win[kMaxK];
   int nwin;
@@ -37,49 +33,16 @@ struct MergeSmem {
   int tied;
 };
 
-__host__ __device__ constexpr size_t merge_stage_offset() {
-  return (sizeof(MergeSmem) + 127) & ~size_t(127);
-}
-
 __global__ void __launch_bounds__(kMergeThreads, 1)
     merge_kernel(const float* __restrict__ cand, int C, int K, int32_t* __restrict__ ids,
-                 float* __restrict__ scores, uint32_t* flags, int stage_cap) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  MergeSmem& sm = *reinterpret_cast<MergeSmem*>(smem_raw);
-  float2* stage = reinterpret_cast<float2*>(smem_raw + merge_stage_offset());
+                 float* __restrict__ scores) {
+  __shared__ MergeSmem sm;
   const int tid = threadIdx.x, lane = tid & 31;
   const int r = blockIdx.x;
-  const float2* row = reinterpret_cast<const float2*>(cand) + (int64_t)r * C;
-  const float2* data = row;
+  const float2* data = reinterpret_cast<const float2*>(cand) + (int64_t)r * C;
 
   if (tid == 0) { sm.nwin = 0; sm.valid_count = 0; sm.tied = 0; }
   __syncthreads();
-  if (C <= stage_cap) {
-    const uint32_t bytes = (uint32_t)C * 8u;
-    const int nchunks = (int)((bytes + kChunkBytes - 1) / kChunkBytes);
-    if (tid == 0) {
-      for (int c = 0; c < nchunks; ++c) mbar_init(&sm.bars[c], 1);
-      mbar_init_fence();
-    }
-    __syncthreads();
-    if (tid == 0) {
-      for (int c = 0; c < nchunks; ++c) {
-        const uint32_t off = c * kChunkBytes;
-        const uint32_t len = min(kChunkBytes, bytes - off);
-        mbar_expect_tx(&sm.bars[c], len);
-        bulk_g2s(reinterpret_cast<unsigned char*>(stage) + off,
-                 reinterpret_cast<const unsigned char*>(row) + off, len, &sm.bars[c]);
-      }
-    }
-    bool ok = true;
-    for (int c = 0; c < nchunks; ++c) ok &= mbar_wait(&sm.bars[c], 0);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) raise_flag(flags, DSA_FLAG_TIMEOUT);
-      for (int c = 0; c < nchunks; ++c) mbar_wait(&sm.bars[c], 0);
-      return;
-    }
-    data = stage;
-  }
 
   // Valid candidates (id >= 0).
   int nv = 0;
@@ -734,12 +697,8 @@ extern "C" dsa_status dsa_merge_topk_stable(const float* cand, int rows, int C, 
     if (C <= 32 * 512) return launch_fast(merge_fast_kernel<512>, 512);
     return launch_fast(merge_fast_kernel<1024>, 1024);
   }
-  const int stage_cap = kStageCapCand;
-  const size_t smem = merge_stage_offset() + (size_t)min(C, stage_cap) * sizeof(float2);
-  if (cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
-    return DSA_ERR_CUDA;
-  const cudaError_t e = launch_kernel(merge_kernel, dim3((unsigned)rows), dim3(kMergeThreads), smem,
-                                      stream, 0, cand, C, K, ids, scores, err_flags, stage_cap);
+  (void)err_flags;   // no asynchronous copies on this path: nothing can stall
+  const cudaError_t e = launch_kernel(merge_kernel, dim3((unsigned)rows), dim3(kMergeThreads), 0,
+                                      stream, 0, cand, C, K, ids, scores);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

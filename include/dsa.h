@@ -143,7 +143,8 @@ dsa_status dsa_shard_topk_pack(const float* logits, int64_t ld, int rows, int S,
  *               first; -1 after the valid ones.
  *   scores      [rows][K] fp32 out, may be NULL: their scores (-inf after the
  *               valid ones; a -0.0 score may come back as +0.0).
- *   err_flags   DSA_FLAG_TIMEOUT if staging the row in shared memory stalled.
+ *   err_flags   unused (no step of the merge can stall or go out of bounds);
+ *               kept so that every step has the same trailing arguments.
  * Candidate ids within a row must be distinct (the pack guarantees it).
  */
 dsa_status dsa_merge_topk_stable(const float* cand, int rows, int C, int K,

@@ -122,6 +122,16 @@ def test_many_shards_step_kernels(K, S, I):
     G.assert_indexer_parity(case, got, np.arange(case["cfg"].rows))
 
 
+@pytest.mark.parametrize("K,S,I", [(2048, 64, 1), (1024, 40, 3)])
+def test_widest_rows_take_the_wide_merge(K, S, I):
+    """More than 32768 candidates a row, up to the largest shard count: the
+    merge's select-and-sort kernel for wide rows (ties on a coarse grid, so
+    its second select on the ids runs too), through the step kernels."""
+    case = _ties_and_tails_case(K, S, I, rows=16)
+    got = G.run_gpu(case, fused=True)
+    G.assert_indexer_parity(case, got, np.arange(case["cfg"].rows))
+
+
 @pytest.mark.parametrize("ld", [24000, 60000])
 def test_rows_longer_than_the_register_path(ld):
     """Local rows above the register capacity (16384) are staged in shared
