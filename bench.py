@@ -56,13 +56,18 @@ PATHS = {
     "fused": ("indexer_fused", "lse_combine"),
     # one kernel per step (a1+a2 fused), then the combine
     "steps": ("shard_topk_pack", "merge_topk_stable", "convert_index_compact", "lse_combine"),
+    # the write side of the paged cache: each row's new token mapped to the
+    # slot its owner shard stores it at (not part of the indexer step)
+    "write_slots": ("slot_mapping",),
 }
+PATH_METRIC = {"write_slots": ("slot-mapped new tokens/s", "tokens/s")}
 KERNEL_SOURCES = {"shard_topk_pack": ("shard_topk.cu", "fast_select.cuh", "local_topk.cuh",
                                       "reg_topk.cuh"),
                   "merge_topk_stable": ("merge.cu", "reg_topk.cuh", "binmap.cuh"),
                   "convert_index_compact": ("convert.cu",),
                   "indexer_fused": ("fused.cu", "local_topk.cuh", "reg_topk.cuh"),
-                  "lse_combine": ("combine.cu",)}
+                  "lse_combine": ("combine.cu",),
+                  "slot_mapping": ("slot_mapping.cu",)}
 
 
 # ---------------------------------------------------------------------------
@@ -115,7 +120,9 @@ def host_inputs(cfg, replica: int):
     logits = W.iid_local_logits(cfg, replica)
     bt = W.block_tables(cfg, replica=replica)
     r2q = None if cfg.reqs == cfg.rows else np.zeros(cfg.rows, np.int32)
-    d = dict(starts=starts, ends=ends, logits=logits, bt=bt, r2q=r2q)
+    # the token each row adds: the last position of its range
+    pos = np.maximum(ends.astype(np.int64) - 1, -1).astype(np.int32)
+    d = dict(starts=starts, ends=ends, logits=logits, bt=bt, r2q=r2q, pos=pos)
     if cfg.H:
         d["part"], d["lse2"] = W.combine_inputs(cfg, replica=replica)
     return d
@@ -142,6 +149,8 @@ def algorithmic_bytes(cfg, ends: np.ndarray) -> dict:
     convert: K ids read, one block-table word per id, S*K slots and S counts written.
     lse_combine: S partial rows of H*D bf16 and S*H LSEs read, H*D bf16 and H LSEs
         written, per row.
+    slot_mapping: per new token its position (and request) read, one block-table
+        word read, S slots written.
     """
     S, K, R, H, D = cfg.S, cfg.K, cfg.rows, cfg.H, cfg.D
     logits = 4 * ends.astype(np.int64).sum()
@@ -152,6 +161,7 @@ def algorithmic_bytes(cfg, ends: np.ndarray) -> dict:
         # logits once, one table word per merged id, ids + slots + counts written
         "indexer_fused": int(logits + R * (4 * K + 4 * K + 4 * S * K + 4 * S)),
         "lse_combine": int(R * (S * H * D * 2 + S * H * 4 + H * D * 2 + H * 4)),
+        "slot_mapping": int(R * (4 + (4 if cfg.reqs != cfg.rows else 0) + 4 + 4 * S)),
     }
 
 
@@ -270,7 +280,11 @@ def profiled_traffic(kernel: str, workload: str = DEFAULT_WORKLOAD) -> float | N
 # ---------------------------------------------------------------------------
 # the oracle as CPU baseline / reference arm
 # ---------------------------------------------------------------------------
-def oracle_rows(inp: dict, cfg, rows: np.ndarray):
+def oracle_rows(inp: dict, cfg, rows: np.ndarray, path: str = "fused"):
+    if path == "write_slots":
+        from oracle import kv_write as KW
+        req = rows if inp["r2q"] is None else inp["r2q"][rows]
+        return KW.slot_mapping(inp["pos"][rows], req, cfg.S, cfg.I, inp["bt"], cfg.block_size)
     from oracle import combine as OC
     from oracle import pipeline as OP
     res = OP.run_rows(inp["logits"], inp["starts"], inp["ends"], cfg.S, cfg.I, cfg.K, rows=rows,
@@ -280,20 +294,31 @@ def oracle_rows(inp: dict, cfg, rows: np.ndarray):
     return res
 
 
-def cpu_baseline(cfg, inp: dict, budget_s: float = 10.0) -> dict:
+def metric_for(path: str) -> tuple[str, str]:
+    return PATH_METRIC.get(path, (METRIC, "rows/s"))
+
+
+def dtype_for(path: str) -> str:
+    """The arithmetic the path computes in: fp32 keys and scores (the combine
+    accumulates in fp32), or int32 index maps only."""
+    return "i32" if path == "write_slots" else "f32"
+
+
+def cpu_baseline(cfg, inp: dict, budget_s: float = 10.0, path: str = "fused") -> dict:
     """The oracle, as it stands, over rows of the same batch until ~budget_s."""
     t0 = time.perf_counter()
     done = 0
     r = 0
     while True:
-        oracle_rows(inp, cfg, np.array([r % cfg.rows]))
+        oracle_rows(inp, cfg, np.array([r % cfg.rows]), path)
         done += 1
         r += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": done / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} rows of the {cfg.name} batch (all steps per row, numpy, one "
+    what = "the new token" if path == "write_slots" else "all steps"
+    return {"value": done / dt, "unit": metric_for(path)[1], "cores": 1, "kind": "oracle",
+            "sample": f"{done} rows of the {cfg.name} batch ({what} per row, numpy, one "
                       f"thread), {dt:.1f} s"}
 
 
@@ -303,8 +328,9 @@ def run_reference(args, world, rank):
         return 0
     cfg = W.CONFIGS[args.workload]
     inp = host_inputs(cfg, 0)
+    metric, unit = metric_for(args.path)
     t = time.perf_counter()
-    oracle_rows(inp, cfg, np.array([0]))
+    oracle_rows(inp, cfg, np.array([0]), args.path)
     per_row = max(time.perf_counter() - t, 1e-3)
     budget = 150.0                        # seconds for warm-up + timed steps
     rows_per_step = int(max(1, min(cfg.rows, budget / (args.steps + args.warmup) / per_row)))
@@ -314,7 +340,7 @@ def run_reference(args, world, rank):
         nonlocal r
         rows = (np.arange(rows_per_step) + r) % cfg.rows
         r += rows_per_step
-        oracle_rows(inp, cfg, rows)
+        oracle_rows(inp, cfg, rows, args.path)
 
     for _ in range(args.warmup):
         step()
@@ -323,17 +349,18 @@ def run_reference(args, world, rank):
         step()
     dt = time.perf_counter() - t0
     value = rows_per_step * args.steps / dt
-    sample = (f"{rows_per_step} row(s) of the {cfg.rows}-row {cfg.name} batch per step (all "
-              f"steps), numpy, one thread")
+    what = "the new token" if args.path == "write_slots" else "all steps"
+    sample = (f"{rows_per_step} row(s) of the {cfg.rows}-row {cfg.name} batch per step "
+              f"({what}), numpy, one thread")
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "impl": "reference", "metric": metric, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_block(cfg),
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+        "vs_baseline": None, "dtype": dtype_for(args.path), "data": "synthetic",
+        "config": config_block(cfg, args.path),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }))
     return 0
@@ -348,8 +375,9 @@ def config_block(cfg, path: str = "fused") -> dict:
             "rows": cfg.rows, "S": cfg.S, "I": cfg.I, "K": cfg.K, "block_size": cfg.block_size,
             "H": cfg.H, "D": cfg.D,
             "path": " -> ".join(kernels_for(cfg, path)) + " (C ABI, one stream)",
-            "l2": f"{replicas_for(cfg)} rotating input sets of {set_bytes(cfg) / 1e6:.0f} MB "
-                  f"(> 2.5x L2 together); no flush",
+            "l2": (f"{replicas_for(cfg)} rotating input sets of {set_bytes(cfg) / 1e6:.0f} MB "
+                   f"(> 2.5x L2 together); no flush" if path != "write_slots" else
+                   "positions and block tables (a few MB at most) stay in L2; no flush"),
             "logits": "i.i.d. N(0,1) per shard (work-equivalent to the recipe)",
             "parallelism": "replicas (rows independent, no collective)"}
 
@@ -368,7 +396,9 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", choices=sorted(W.CONFIGS), default=DEFAULT_WORKLOAD,
                     help="timed workload (the metric is quoted on decode)")
     ap.add_argument("--path", choices=sorted(PATHS), default="fused",
-                    help="fused: one cluster kernel for steps a1-a4; steps: one kernel per step")
+                    help="fused: one cluster kernel for steps a1-a4; steps: one kernel per "
+                         "step; write_slots: the write-side slot mapping of each row's new "
+                         "token")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -399,7 +429,7 @@ def main(argv=None) -> int:
     sets = []
     for h in host:
         st = dict(logits=d(h["logits"]), starts=d(h["starts"]), ends=d(h["ends"]),
-                  bt=d(h["bt"]))
+                  bt=d(h["bt"]), pos=d(h["pos"]))
         if h["r2q"] is not None:
             st["r2q"] = d(h["r2q"])
         if H:
@@ -412,6 +442,7 @@ def main(argv=None) -> int:
     counts = torch.empty((S, R), dtype=torch.int32, device=dev)
     out = torch.empty((R, max(H, 1), max(D, 8)), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((R, max(H, 1)), dtype=torch.float32, device=dev)
+    slotmap = torch.empty((S, R), dtype=torch.int32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
@@ -426,7 +457,11 @@ def main(argv=None) -> int:
         if H:
             tail = ((lib.dsa_lse_combine, (P(st["part"]), P(st["lse2"]), S, R, H, D, P(out),
                                            P(lse), P(err), sp)),)
-        if args.path == "fused":
+        if args.path == "write_slots":
+            calls.append(((lib.dsa_slot_mapping, (P(st["pos"]), r2q, R, S, cfg.I, P(st["bt"]),
+                                                  cfg.reqs, cfg.max_blocks, cfg.block_size,
+                                                  P(slotmap), P(err), sp)),))
+        elif args.path == "fused":
             calls.append((
                 (lib.dsa_indexer_fused, (P(st["logits"]), ld, R, S, cfg.I, K, P(st["starts"]),
                                          P(st["ends"]), P(st["bt"]), cfg.reqs, cfg.max_blocks,
@@ -552,15 +587,21 @@ def main(argv=None) -> int:
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     hsets = []
     for h in host[:2]:
-        hs = dict(logits=pin(h["logits"]), starts=pin(h["starts"]), ends=pin(h["ends"]),
-                  bt=pin(h["bt"]))
+        if args.path == "write_slots":       # the new tokens and the tables they go through
+            hs = dict(pos=pin(h["pos"]), bt=pin(h["bt"]))
+        else:
+            hs = dict(logits=pin(h["logits"]), starts=pin(h["starts"]), ends=pin(h["ends"]),
+                      bt=pin(h["bt"]))
         if h["r2q"] is not None:
             hs["r2q"] = pin(h["r2q"])
-        if H:
+        if H and args.path != "write_slots":
             hs["part"] = pin(h["part"].view(np.int16))
             hs["lse2"] = pin(h["lse2"])
         hsets.append(hs)
-    results = [slots, counts] + ([out, lse] if H else [])
+    if args.path == "write_slots":
+        results = [slotmap]
+    else:
+        results = [slots, counts] + ([out, lse] if H else [])
     h_results = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]
     h2d = sum(t.numel() * t.element_size() for t in hsets[0].values())
     d2h = sum(t.numel() * t.element_size() for t in h_results)
@@ -587,11 +628,12 @@ def main(argv=None) -> int:
     e2e_ms = max_over_ranks(x0.elapsed_time(x1), world) / args.e2e_steps
     e2e_value = world * R / (e2e_ms / 1e3)
 
+    metric, unit = metric_for(args.path)
     result = {
-        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": config_block(cfg, args.path),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": dtype_for(args.path), "data": "synthetic", "config": config_block(cfg, args.path),
         "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
         "hbm_frac_step": step_bytes / (ms_per_step / 1e3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
@@ -604,14 +646,14 @@ def main(argv=None) -> int:
                    "between kernels" if not graph_err else
                    f"K steps launched one by one (graph capture failed: {graph_err})"),
         "launch_loop_ms_per_step": loop_ms_per_step,
-        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "gpu_launches": nk * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(cfg, host[0])
+            result["cpu_baseline"] = cpu_baseline(cfg, host[0], path=args.path)
         print(json.dumps(result))
     if world > 1:
         import torch.distributed as dist

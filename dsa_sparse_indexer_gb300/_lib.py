@@ -31,6 +31,7 @@ SIGNATURES = {
     "dsa_indexer_fused": ([_p, _i64, _i, _i, _i, _i, _p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p,
                            _p, _p, _p, _p], _i),
     "dsa_lse_combine": ([_p, _p, _i, _i, _i, _i, _p, _p, _p, _p], _i),
+    "dsa_slot_mapping": ([_p, _p, _i, _i, _i, _p, _i, _i, _i, _p, _p, _p], _i),
 }
 
 _lib = None

@@ -12,8 +12,8 @@ import torch
 from . import _lib
 
 __all__ = ["shard_topk", "pack_candidates", "shard_topk_pack", "merge_topk_stable",
-           "convert_index_compact", "indexer_fused", "lse_combine", "new_error_flags",
-           "SUPPORTED_K"]
+           "convert_index_compact", "indexer_fused", "lse_combine", "slot_mapping",
+           "new_error_flags", "SUPPORTED_K"]
 
 SUPPORTED_K = (512, 1024, 2048)
 
@@ -192,3 +192,24 @@ def lse_combine(partial_out, lse2, out=None, lse_out=None, want_lse: bool = True
     _lib.call("dsa_lse_combine", _ptr(partial_out), _ptr(lse2), S, rows, H, D, _ptr(out),
               _ptr(lse_out), _ptr(err_flags), _stream(partial_out))
     return out, lse_out
+
+
+def slot_mapping(positions, block_table, block_size: int, I: int, token_req=None, out=None,
+                 err_flags=None):
+    """Write-side KV slots of new tokens: positions [n] int32 (and token_req [n],
+    default token i = request i) -> [S, n] int32, -1 where a shard does not
+    store the token."""
+    _need(positions, "positions", torch.int32, 1)
+    _need(block_table, "block_table", torch.int32, 3)
+    S, reqs, max_blocks = block_table.shape
+    n = positions.shape[0]
+    if token_req is not None:
+        _need(token_req, "token_req", torch.int32, 1)
+        if token_req.shape[0] != n:
+            raise ValueError("token_req must have one entry per position")
+    if out is None:
+        out = torch.empty((S, n), dtype=torch.int32, device=positions.device)
+    _need(out, "out", torch.int32, 2)
+    _lib.call("dsa_slot_mapping", _ptr(positions), _ptr(token_req), n, S, I, _ptr(block_table),
+              reqs, max_blocks, block_size, _ptr(out), _ptr(err_flags), _stream(positions))
+    return out

@@ -15,9 +15,11 @@
  *   dsa_lse_combine       LSE-weighted combine of the shards' partial
  *                         attention outputs, base-2 LSE converted to base e
  *
- * plus dsa_shard_topk_pack (the first two steps in one kernel) and
+ * plus dsa_shard_topk_pack (the first two steps in one kernel),
  * dsa_indexer_fused (the first four steps in one kernel per row, a thread-block
- * cluster of S CTAs exchanging candidates through distributed shared memory).
+ * cluster of S CTAs exchanging candidates through distributed shared memory)
+ * and dsa_slot_mapping (the write side of the paged cache: where each shard
+ * stores the KV of new tokens).
  *
  * Sharding (PR #46076 report, section 关键源码片段, comment in
  * `_dcp_localize_decode_seq_lens`): global token t lives on shard
@@ -232,6 +234,37 @@ dsa_status dsa_indexer_fused(const float* logits, int64_t ld, int rows, int S, i
 dsa_status dsa_lse_combine(const uint16_t* partial_out, const float* lse2, int S,
                            int rows, int H, int D, uint16_t* out, float* lse_out,
                            uint32_t* err_flags, cudaStream_t stream);
+
+/*
+ * dsa_slot_mapping - where each shard writes the KV of new tokens (the write
+ * side of the paged cache; dsa_convert_index_compact is the read side).
+ * PR #40996 report, "DCP supports hybrid attention", section 实现拆解 item 2
+ * (per-rank token -> KV-slot mapping over rank-local block tables with
+ * allocation blocks of KV_CACHE_BLOCK_SIZE tokens) and item 1; the ownership
+ * rule of the PR #46076 report, section 关键源码片段.
+ *
+ * Token i at global position t = positions[i] of request q = token_req[i] is
+ * stored by shard s = (t / I) mod S at its local slot l = (t / (I*S))*I +
+ * t mod I, i.e. at block_table[s][q][l / block_size] * block_size +
+ * l % block_size; every other shard's entry is -1.
+ *
+ *   positions    [n] int32 global positions; a negative one is a padding token
+ *                (-1 on every shard, no error)
+ *   token_req    [n] int32 request of each token (NULL: token i is request i)
+ *   block_table  [S][reqs][max_blocks] int32 physical block numbers per shard,
+ *                in allocation blocks of block_size tokens (a kernel block of
+ *                block_size / m tokens inside one does not change the slot)
+ *   slot_mapping [S][n] int32 out
+ *   err_flags    DSA_FLAG_BOUNDS if a request is outside [0, reqs), a column
+ *                is >= max_blocks, a table entry is negative or a slot does not
+ *                fit in int32; that token is then -1 on every shard.
+ * Errors: n < 0, reqs < 1, max_blocks < 1, block_size < 1, null pointers ->
+ *         INVALID_ARG; S not in [1, 64], I < 1, I*S > INT32_MAX -> UNSUPPORTED.
+ */
+dsa_status dsa_slot_mapping(const int32_t* positions, const int32_t* token_req, int n,
+                            int S, int I, const int32_t* block_table, int reqs,
+                            int max_blocks, int block_size, int32_t* slot_mapping,
+                            uint32_t* err_flags, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -51,12 +51,15 @@ def slot_mapping(positions, token_req, S: int, I: int, tables, block_size: int):
     n = positions.shape[0]
     out = np.full((S, n), -1, np.int64)
     error = False
+    real = positions >= 0                      # negative positions: padding tokens
+    shard = np.full(n, -1, np.int64)
+    local = np.full(n, -1, np.int64)
+    if real.any():
+        shard[real], local[real] = dcp_layout.global_to_local(positions[real], S, I)
     for i in range(n):
-        t = int(positions[i])
-        if t < 0:
+        if not real[i]:
             continue
-        s, l = dcp_layout.global_to_local(np.array([t]), S, I)
-        s, l = int(s[0]), int(l[0])
+        s, l = int(shard[i]), int(local[i])
         req = int(token_req[i])
         col = l // block_size
         if not (0 <= req < reqs) or col >= max_blocks:

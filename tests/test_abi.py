@@ -141,6 +141,22 @@ def test_combine_argument_checks(lib):
     assert f(P, P, 65, 2, 8, 64, P, NULL, NULL, NULL) == UNSUPPORTED
 
 
+def test_slot_mapping_argument_checks(lib):
+    f = lib.dsa_slot_mapping
+    assert f(NULL, NULL, 0, 4, 1, NULL, 2, 8, 64, NULL, NULL, NULL) == OK      # n == 0
+    assert f(NULL, NULL, 5, 4, 1, P, 2, 8, 64, P, NULL, NULL) == INVALID
+    assert f(P, NULL, 5, 4, 1, NULL, 2, 8, 64, P, NULL, NULL) == INVALID
+    assert f(P, NULL, 5, 4, 1, P, 2, 8, 64, NULL, NULL, NULL) == INVALID
+    assert f(P, NULL, -1, 4, 1, P, 2, 8, 64, P, NULL, NULL) == INVALID
+    assert f(P, NULL, 5, 4, 1, P, 0, 8, 64, P, NULL, NULL) == INVALID          # reqs
+    assert f(P, NULL, 5, 4, 1, P, 2, 0, 64, P, NULL, NULL) == INVALID          # max_blocks
+    assert f(P, NULL, 5, 4, 1, P, 2, 8, 0, P, NULL, NULL) == INVALID           # block size
+    assert f(P, NULL, 5, 0, 1, P, 2, 8, 64, P, NULL, NULL) == UNSUPPORTED
+    assert f(P, NULL, 5, 65, 1, P, 2, 8, 64, P, NULL, NULL) == UNSUPPORTED
+    assert f(P, NULL, 5, 4, 0, P, 2, 8, 64, P, NULL, NULL) == UNSUPPORTED
+    assert f(P, NULL, 5, 64, 2 ** 30, P, 2, 8, 64, P, NULL, NULL) == UNSUPPORTED  # I*S
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
     import dsa_sparse_indexer_gb300 as dsa
