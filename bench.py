@@ -493,8 +493,10 @@ def main(argv=None) -> int:
     if int(err.item()) != 0:
         raise SystemExit(f"device error flags set during warm-up: {int(err.item())}")
 
-    # --- one CUDA graph per rotating input set (the step's launches) --------
-    graphs, graph_err = [], None
+    # --- CUDA graphs: one step on each rotating input set back to back (as a
+    # model-forward graph holds the indexer of every layer), and one graph per
+    # set for the remainder of K steps and for the one-step-per-replay figure
+    graphs, rotation, graph_err = [], None, None
     try:
         gs = torch.cuda.Stream(dev)
         with torch.cuda.stream(gs):
@@ -505,21 +507,30 @@ def main(argv=None) -> int:
                     for fn, a in calls[i]:
                         launch(fn, a[:-1] + (gsp,))
                 graphs.append(g)
+            rotation = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(rotation, stream=gs):
+                gsp = torch.cuda.current_stream(dev).cuda_stream
+                for i in range(REPLICAS):
+                    for fn, a in calls[i]:
+                        launch(fn, a[:-1] + (gsp,))
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup)):
+                rotation.replay()
             for i in range(max(3, args.warmup) * REPLICAS):
                 graphs[i % REPLICAS].replay()
         torch.cuda.synchronize()
     except Exception as exc:  # report, never hide: the launch loop is then the headline
-        graphs, graph_err = [], f"{type(exc).__name__}: {exc}"
+        graphs, rotation, graph_err = [], None, f"{type(exc).__name__}: {exc}"
 
     nk = len(KERNELS)
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.2)
 
-    # --- timed region: K steps as graph replays on the launch stream ---------
-    graph_ms = None
+    # --- timed region: exactly K steps, K // R replays of the rotation graph
+    # and K mod R one-step graphs, on the launch stream ----------------------
+    graph_ms = single_ms = None
     if graphs:
         barrier(world)
         torch.cuda.synchronize()
@@ -527,13 +538,24 @@ def main(argv=None) -> int:
         t_wall0 = time.time()
         with torch.cuda.stream(stream):
             g0.record(stream)
-            for i in range(args.steps):
-                graphs[i % REPLICAS].replay()
+            for i in range(args.steps // REPLICAS):
+                rotation.replay()
+            for i in range(args.steps % REPLICAS):
+                graphs[i].replay()
             g1.record(stream)
         torch.cuda.synchronize()
         t_wall1 = time.time()
         barrier(world)
         graph_ms = g0.elapsed_time(g1)
+        # the same K steps with one replay per step (launch gap between steps)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            g0.record(stream)
+            for i in range(args.steps):
+                graphs[i % REPLICAS].replay()
+            g1.record(stream)
+        torch.cuda.synchronize()
+        single_ms = g0.elapsed_time(g1)
 
     # --- per-kernel times: K more steps, events between kernels -------------
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * nk + 1)]
@@ -641,10 +663,14 @@ def main(argv=None) -> int:
                      "bytes_per_launch": nbytes[dominant],
                      "traffic": profiled_traffic(dominant, args.workload)},
         "kernels": kernels,
-        "timing": ("K steps as CUDA-graph replays, one graph per rotating input set; "
+        "timing": (f"K steps as CUDA-graph replays: a graph of one step on each of the {REPLICAS} "
+                   "rotating input sets back to back (as a model-forward graph holds the "
+                   "indexer of every layer), K // R replays of it and K mod R one-step graphs; "
                    "per-kernel times from K more steps launched one by one with events "
                    "between kernels" if not graph_err else
                    f"K steps launched one by one (graph capture failed: {graph_err})"),
+        "one_step_per_replay_ms_per_step": (None if single_ms is None else
+                                            max_over_ranks(single_ms, world) / args.steps),
         "launch_loop_ms_per_step": loop_ms_per_step,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
