@@ -32,6 +32,8 @@ SIGNATURES = {
                            _p, _p, _p, _p], _i),
     "dsa_lse_combine": ([_p, _p, _i, _i, _i, _i, _p, _p, _p, _p], _i),
     "dsa_slot_mapping": ([_p, _p, _i, _i, _i, _p, _i, _i, _i, _p, _p, _p], _i),
+    "dsa_sparse_mla_decode": ([_p, _p, _i64, _p, _p, _i, _i, _i, _i, ctypes.c_float, _p, _p, _p,
+                               _p], _i),
 }
 
 _lib = None

@@ -13,9 +13,10 @@ from . import _lib
 
 __all__ = ["shard_topk", "pack_candidates", "shard_topk_pack", "merge_topk_stable",
            "convert_index_compact", "indexer_fused", "lse_combine", "slot_mapping",
-           "new_error_flags", "SUPPORTED_K"]
+           "sparse_mla_decode", "new_error_flags", "SUPPORTED_K", "MLA_DQK", "MLA_DV"]
 
 SUPPORTED_K = (512, 1024, 2048)
+MLA_DQK, MLA_DV = 576, 512       # DSA_MLA_DQK, DSA_MLA_DV of include/dsa.h
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
@@ -213,3 +214,33 @@ def slot_mapping(positions, block_table, block_size: int, I: int, token_req=None
     _lib.call("dsa_slot_mapping", _ptr(positions), _ptr(token_req), n, S, I, _ptr(block_table),
               reqs, max_blocks, block_size, _ptr(out), _ptr(err_flags), _stream(positions))
     return out
+
+
+def sparse_mla_decode(q, kv_cache, slots, counts, scale: float, out=None, lse2=None,
+                      err_flags=None):
+    """Each shard's sparse MLA decode attention over its compacted slots.
+
+    q [rows, H, 576] bf16, kv_cache [S, n_slots, 576] bf16, slots [S, rows, K]
+    int32, counts [S, rows] int32 -> (out [S, rows, H, 512] bf16, lse2 [S, rows, H]
+    fp32, base 2)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(kv_cache, "kv_cache", torch.bfloat16, 3)
+    _need(slots, "slots", torch.int32, 3)
+    _need(counts, "counts", torch.int32, 2)
+    rows, H, dqk = q.shape
+    S, n_slots, dqk2 = kv_cache.shape
+    if dqk != MLA_DQK or dqk2 != MLA_DQK:
+        raise ValueError(f"q and kv_cache rows must have {MLA_DQK} entries")
+    if slots.shape[:2] != (S, rows) or tuple(counts.shape) != (S, rows):
+        raise ValueError("slots must be [S, rows, K] and counts [S, rows]")
+    K = slots.shape[2]
+    if out is None:
+        out = torch.empty((S, rows, H, MLA_DV), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, 4)
+    if lse2 is None:
+        lse2 = torch.empty((S, rows, H), dtype=torch.float32, device=q.device)
+    _need(lse2, "lse2", torch.float32, 3)
+    _lib.call("dsa_sparse_mla_decode", _ptr(q), _ptr(kv_cache), n_slots, _ptr(slots),
+              _ptr(counts), rows, S, H, K, float(scale), _ptr(out), _ptr(lse2), _ptr(err_flags),
+              _stream(q))
+    return out, lse2

@@ -18,8 +18,9 @@
  * plus dsa_shard_topk_pack (the first two steps in one kernel),
  * dsa_indexer_fused (the first four steps in one kernel per row, a thread-block
  * cluster of S CTAs exchanging candidates through distributed shared memory)
- * and dsa_slot_mapping (the write side of the paged cache: where each shard
- * stores the KV of new tokens).
+ * dsa_slot_mapping (the write side of the paged cache: where each shard
+ * stores the KV of new tokens) and dsa_sparse_mla_decode (each shard's sparse
+ * attention over its compacted slots, whose outputs dsa_lse_combine merges).
  *
  * Sharding (PR #46076 report, section 关键源码片段, comment in
  * `_dcp_localize_decode_seq_lens`): global token t lives on shard
@@ -73,6 +74,11 @@ enum {
 /* Supported top-K sizes: the pages' set, PR #46076 report, section 关键源码片段,
  * `_assert_cutedsl_dcp_merge_supported` (index_topk in 512/1024/2048). */
 #define DSA_MAX_SHARDS 64
+/* Sparse MLA decode (dsa_sparse_mla_decode): a cache row and a query head are
+ * the latent kv_c (DSA_MLA_DV values) followed by the rope part, DSA_MLA_DQK
+ * values in all. */
+#define DSA_MLA_DQK 576
+#define DSA_MLA_DV 512
 
 /* Human-readable name of a status code (static string). */
 const char* dsa_status_string(dsa_status status);
@@ -265,6 +271,42 @@ dsa_status dsa_slot_mapping(const int32_t* positions, const int32_t* token_req, 
                             int S, int I, const int32_t* block_table, int reqs,
                             int max_blocks, int block_size, int32_t* slot_mapping,
                             uint32_t* err_flags, cudaStream_t stream);
+
+/*
+ * dsa_sparse_mla_decode - every shard's sparse MLA decode attention over its
+ * compacted KV slots: the partial outputs and base-2 LSEs dsa_lse_combine merges.
+ * PR #52046 report, "DSV3.2 PCP sharding", section 关键源码片段
+ * (`_fused_norm_rope_kernel`: a cache row is the normed latent kv_c followed by
+ * the roped k_pe; `_sparse_indexer_and_attn`: the MQA query is its parts
+ * concatenated on the last dimension, `forward_mqa(q, kv_cache, ...)` returns
+ * output and LSE per shard); PR #46076 report, section 实现拆解 items 4 and 5
+ * (compacted slots in, base-2 LSE out).
+ *
+ * For shard s, row r, head h, over j in slots[s][r][0 .. counts[s][r]):
+ *   x_j = scale * (q[r][h] . kv_cache[s][slot_j]),
+ *   out[s][r][h] = sum_j exp(x_j) v_j / sum_j exp(x_j),  v_j = first DSA_MLA_DV
+ *   entries of the row; lse2[s][r][h] = log2 sum_j exp(x_j).
+ * A shard with no slot gives out = 0 and lse2 = -inf.  Scores accumulate in
+ * fp32 from bf16 products; the softmax weights enter the value product as bf16.
+ *
+ *   q          [rows][H][DSA_MLA_DQK] bf16 (uint16 bit patterns), 16-byte aligned
+ *   kv_cache   [S][n_slots][DSA_MLA_DQK] bf16, 16-byte aligned: each shard's
+ *              paged cache by physical slot (block * block_size + offset)
+ *   slots      [S][rows][K] int32, counts [S][rows] int32: the compacted slots
+ *              and their number, as dsa_convert_index_compact writes them
+ *   scale      softmax scale (finite)
+ *   out        [S][rows][H][DSA_MLA_DV] bf16 out, 16-byte aligned
+ *   lse2       [S][rows][H] fp32 out
+ *   err_flags  DSA_FLAG_BOUNDS if a count is outside [0, K] (clamped) or a slot
+ *              below it is outside [0, n_slots) (that token is left out).
+ * Errors: rows < 0, K < 1, n_slots < 1, non-finite scale, null pointers,
+ *         misalignment -> INVALID_ARG; S not in [1, 64], H not a multiple of
+ *         32 -> UNSUPPORTED.
+ */
+dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache, int64_t n_slots,
+                                 const int32_t* slots, const int32_t* counts, int rows, int S,
+                                 int H, int K, float scale, uint16_t* out, float* lse2,
+                                 uint32_t* err_flags, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -157,6 +157,22 @@ def test_slot_mapping_argument_checks(lib):
     assert f(P, NULL, 5, 64, 2 ** 30, P, 2, 8, 64, P, NULL, NULL) == UNSUPPORTED  # I*S
 
 
+def test_sparse_mla_decode_argument_checks(lib):
+    f = lib.dsa_sparse_mla_decode
+    ok = (P, P, 1000, P, P, 2, 4, 128, 2048, 0.07, P, P, NULL, NULL)
+    assert f(*ok[:5], 0, *ok[6:]) == OK                                   # rows == 0
+    for i, bad in [(0, NULL), (1, NULL), (3, NULL), (4, NULL), (10, NULL), (11, NULL),
+                   (0, P + 8), (1, P + 4), (10, P + 2), (2, 0), (8, 0),
+                   (9, float("inf")), (9, float("nan")), (5, -1)]:
+        args = list(ok)
+        args[i] = bad
+        assert f(*args) == INVALID, (i, bad)
+    for i, bad in [(6, 0), (6, 65), (7, 96 + 16), (7, 16)]:
+        args = list(ok)
+        args[i] = bad
+        assert f(*args) == UNSUPPORTED, (i, bad)
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
     import dsa_sparse_indexer_gb300 as dsa

@@ -200,6 +200,21 @@ def combine_inputs(cfg: Config, empty: np.ndarray | None = None, replica: int = 
     return out, lse2
 
 
+MLA_DQK, MLA_DV = 576, 512     # a cache row / query head: latent 512 + rope 64
+
+
+def mla_query(rows: int, H: int, seed: int) -> np.ndarray:
+    """[rows, H, 576] MQA queries (latent + rope parts), N(0,1) in bf16 bits."""
+    rng = np.random.default_rng(seed)
+    return f32_to_bf16_bits(rng.standard_normal((rows, H, MLA_DQK), dtype=np.float32))
+
+
+def mla_cache(S: int, n_slots: int, seed: int) -> np.ndarray:
+    """[S, n_slots, 576] paged KV caches by slot, N(0,1) in bf16 bits."""
+    rng = np.random.default_rng(seed)
+    return f32_to_bf16_bits(rng.standard_normal((S, n_slots, MLA_DQK), dtype=np.float32))
+
+
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 to bf16 (round to nearest, ties to even); returns uint16 bits.
     Inputs are finite."""
