@@ -14,14 +14,20 @@
 // sum_j 2^(s_j log2 e) with v_j the first 512 entries of row_j, and
 // lse2 = log2 sum_j exp(s_j).
 //
-// One CTA per (row, shard, group of 32 heads), 8 warps, tensor cores through
-// mma.sync m16n8k16 (bf16 in, fp32 accumulate).  The group's 32 query rows
-// sit in shared memory; the selected cache rows are gathered by slot into
-// double-buffered tiles of 16 tokens with cp.async (invalid tokens are
-// zero-filled and masked).  Per tile: the 32 x 16 scores, split over the two
-// halves of the 576 dimensions, then an online softmax in the exp2 domain and
-// O += P V, each warp owning 16 heads x 128 output dimensions (64 fp32
-// accumulators per thread).
+// One CTA per (row, shard, group of 64 heads), tensor cores through mma.sync
+// m16n8k16 (bf16 in, fp32 accumulate), warp-specialised:
+//  * a producer warp gathers the shard's selected cache rows by slot, one row
+//    per lane and one bulk asynchronous copy (TMA, non-tensor form) per row,
+//    into two stages of 32 tokens guarded by full / empty mbarriers (invalid
+//    tokens are zeroed and masked);
+//  * eight consumer warps, a pair per 16 heads: each warp of a pair computes
+//    the scores of its 16 heads against half of the tile's tokens (all 576
+//    dimensions), the pair swaps them through shared memory under one
+//    64-thread named barrier, and each warp then runs the online softmax (exp2
+//    domain) on all 32 tokens and O += P V for its half of the 512 output
+//    dimensions (128 fp32 accumulators per thread); the softmax weights go
+//    from the score registers straight into the operand layout of P V.
+// No block-wide barrier runs inside the token loop; every wait is bounded.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -31,32 +37,34 @@ namespace {
 
 constexpr int kDqk = DSA_MLA_DQK;            // 576: latent 512 + rope 64
 constexpr int kDv = DSA_MLA_DV;              // 512
-constexpr int kHeads = 32;                   // heads per CTA
-constexpr int kTile = 16;                    // tokens per tile
-constexpr int kAttnThreads = 256;
+constexpr int kHeads = 64;                   // heads per CTA: four blocks of 16
+constexpr int kHalfDv = kDv / 2;             // output dimensions per consumer warp
+constexpr int kTile = 32;                    // tokens per stage (one per producer lane)
+constexpr int kStages = 2;
+constexpr int kConsumers = 8;                // warps 0..7; warp 8 produces
+constexpr int kAttnThreads = (kConsumers + 1) * 32;
 constexpr int kStride = kDqk + 8;            // smem row stride (elements): rows 16 B apart in banks
 constexpr int kChunks = kDqk / 8;            // 16-byte chunks per row
-constexpr int kKHalf = kDqk / 2;             // 288 dims per score half
-constexpr int kSpStride = kTile + 1;
+constexpr uint32_t kRowBytes = kDqk * 2;     // one cache row, one bulk copy
 constexpr float kLog2e = 1.4426950408889634f;
 
-static_assert(kDqk % 32 == 0 && kDv % 128 == 0, "tile shapes");
+static_assert(kDqk % 32 == 0 && kHalfDv % 16 == 0, "tile shapes");
+static_assert(kTile == 32 && kStages == 2, "one token per producer lane; parity = tile & 1");
 
 struct AttnSmem {
+  uint64_t full[kStages];                    // a stage's rows have landed
+  uint64_t empty[kStages];                   // every consumer warp is done with a stage
   alignas(16) __nv_bfloat16 q[kHeads * kStride];
-  alignas(16) __nv_bfloat16 kv[2][kTile * kStride];
-  float sp[2][kHeads * kSpStride];           // score halves
-  int tokv[2][kTile];                        // token valid in this tile
+  alignas(16) __nv_bfloat16 kv[kStages][kTile * kStride];
+  // Score swap between the two warps of a head block: [block][token half]
+  // [tile parity][value][lane], each lane's eight scores of its half.
+  float xs[kHeads / 16][2][2][8][32];
+  int tokv[kStages][kTile];                  // token valid in this stage
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t (&r)[2]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
                : "r"(addr));
 }
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
@@ -72,18 +80,29 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// 16-byte global -> shared copy; with valid == false the 16 bytes are zero
-// filled and nothing is read.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
-               "r"(valid ? 16 : 0)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_wait_one() {
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Named barrier over `count` threads that also returns whether any of them
+// passed pred = true.
+__device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -103,7 +122,46 @@ struct AttnArgs {
   uint32_t* flags;
 };
 
-__global__ void __launch_bounds__(kAttnThreads, 2) sparse_mla_decode_kernel(const AttnArgs a) {
+// Producer warp: tile t of 32 tokens into stage t & 1, lane i taking token i.
+__device__ __forceinline__ void produce(const AttnArgs& a, AttnSmem& sm, int count, int ntiles,
+                                        const int32_t* slot_row,
+                                        const __nv_bfloat16* shard_cache) {
+  const int lane = threadIdx.x & 31;
+  bool bad = false, ok = true;
+  int issued = 0;
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t & 1;
+    if (t >= kStages) ok = mbar_wait(&sm.empty[st], (uint32_t)(t / kStages - 1) & 1u);
+    if (!__all_sync(kFull, ok)) {
+      ok = false;
+      break;
+    }
+    const int idx = t * kTile + lane;
+    const int slot = idx < count ? __ldg(slot_row + idx) : -1;
+    const bool in = slot >= 0 && (int64_t)slot < a.n_slots;
+    bad |= idx < count && !in;
+    __nv_bfloat16* dst = &sm.kv[st][lane * kStride];
+    if (!in)
+      for (int c = 0; c < kChunks; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+    sm.tokv[st][lane] = in;
+    const unsigned valid = __ballot_sync(kFull, in);
+    // The consumers' reads of this stage (generic proxy) before the copies.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    // Arm first (zeroed rows and flags published by this arrival), then copy.
+    if (lane == 0) mbar_expect_tx(&sm.full[st], (uint32_t)__popc(valid) * kRowBytes);
+    __syncwarp();
+    if (in) bulk_g2s(dst, shard_cache + (int64_t)slot * kDqk, kRowBytes, &sm.full[st]);
+    issued = t + 1;
+  }
+  if (!ok && lane == 0) raise_flag(a.flags, DSA_FLAG_TIMEOUT);
+  if (bad) raise_flag(a.flags, DSA_FLAG_BOUNDS);
+  // Copies still in flight land before this warp, and so the block, exits.
+  for (int t = max(0, issued - kStages); t < issued; ++t)
+    mbar_wait(&sm.full[t & 1], (uint32_t)(t / kStages) & 1u);
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1) sparse_mla_decode_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) unsigned char attn_smem[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(attn_smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -115,180 +173,194 @@ __global__ void __launch_bounds__(kAttnThreads, 2) sparse_mla_decode_kernel(cons
   int count = __ldg(a.counts + pair);
   if ((count < 0 || count > a.K) && tid == 0) raise_flag(a.flags, DSA_FLAG_BOUNDS);
   count = min(max(count, 0), a.K);
-  const int32_t* slot_row = a.slots + (int64_t)pair * a.K;
-  const __nv_bfloat16* shard_cache = a.cache + (int64_t)s * a.n_slots * kDqk;
-
-  // Warp roles.  Scores: head half hh, token octet nt, dimension half kh.
-  // Softmax and P V: head half hh2, output quarter dq.
-  const int nt = warp & 1, hh = (warp >> 1) & 1, kh = warp >> 2;
-  const int dq = warp & 3, hh2 = warp >> 2;
-  const int h_lo = hg * kHeads + hh2 * 16 + g;         // rows g and g + 8 of this warp
-  const int64_t obase = (int64_t)pair * a.H;           // (s, r) in [S][rows][H]
+  const int64_t obase = (int64_t)pair * a.H + hg * kHeads;   // first head of the group
 
   if (count == 0) {
     // Nothing selected on this shard: O = 0, lse2 = -inf.
-    for (int i = tid; i < kHeads * kDv / 8; i += kAttnThreads) {
-      const int h = hg * kHeads + i / (kDv / 8), c = i % (kDv / 8);
-      *reinterpret_cast<uint4*>(a.out + (obase + h) * kDv + c * 8) = make_uint4(0, 0, 0, 0);
-    }
-    if (tid < kHeads) a.lse2[obase + hg * kHeads + tid] = -INFINITY;
+    for (int i = tid; i < kHeads * kDv / 8; i += kAttnThreads)
+      *reinterpret_cast<uint4*>(a.out + (obase + i / (kDv / 8)) * kDv + (i % (kDv / 8)) * 8) =
+          make_uint4(0, 0, 0, 0);
+    if (tid < kHeads) a.lse2[obase + tid] = -INFINITY;
     return;
   }
 
-  // Query rows of the group (their own cp.async group, with the first tile).
+  // The group's query rows (cp.async by every thread) and the barriers.
   {
     const __nv_bfloat16* qg = a.q + ((int64_t)r * a.H + hg * kHeads) * kDqk;
     for (int c = tid; c < kHeads * kChunks; c += kAttnThreads) {
       const int h = c / kChunks, j = c - h * kChunks;
-      cp_async16(&sm.q[h * kStride + j * 8], qg + (int64_t)h * kDqk + j * 8, true);
+      cp_async16(&sm.q[h * kStride + j * 8], qg + (int64_t)h * kDqk + j * 8);
     }
+    cp_async_commit();
   }
-  const int ntiles = (count + kTile - 1) / kTile;
-  bool bad = false;
-  auto load_tile = [&](int tile, int buf) {
-    for (int c = tid; c < kTile * kChunks; c += kAttnThreads) {
-      const int i = c / kChunks, j = c - i * kChunks;
-      const int idx = tile * kTile + i;
-      int slot = idx < count ? __ldg(slot_row + idx) : -1;
-      const bool in = slot >= 0 && (int64_t)slot < a.n_slots;
-      bad |= idx < count && !in;
-      const __nv_bfloat16* src = in ? shard_cache + (int64_t)slot * kDqk + j * 8 : a.cache;
-      cp_async16(&sm.kv[buf][i * kStride + j * 8], src, in);
-      if (j == 0) sm.tokv[buf][i] = in;
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&sm.full[st], 1);
+      mbar_init(&sm.empty[st], kConsumers);
     }
-  };
-  load_tile(0, 0);
-  cp_async_commit();
+    mbar_init_fence();
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  const int ntiles = (count + kTile - 1) / kTile;
 
-  float acc[kDv / 4 / 8][4];                 // 16 n-tiles of 8 dims x (rows g, g + 8)
+  if (warp == kConsumers) {
+    produce(a, sm, count, ntiles, a.slots + (int64_t)pair * a.K,
+            a.cache + (int64_t)s * a.n_slots * kDqk);
+    return;
+  }
+
+  // ---- consumer warps: head block hb (16 heads), half dh -------------------
+  const int hb = warp >> 1, dh = warp & 1;
+  const uint32_t qa = smem_u32(&sm.q[(hb * 16 + (lane & 15)) * kStride + (lane >> 4) * 8]);
+  float acc[kHalfDv / 8][4];                 // 32 n-tiles of 8 dims x (rows g, g + 8)
 #pragma unroll
-  for (int j = 0; j < kDv / 4 / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  for (int j = 0; j < kHalfDv / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
   // Running max and two row sums: of the fp32 weights (for the LSE) and of
   // the bf16-rounded weights that enter P V (to normalise O, which is then an
   // exact convex mix of what was multiplied).
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, w0 = 0.f, w1 = 0.f;
+  bool ok = true;
 
-  for (int tile = 0; tile < ntiles; ++tile) {
-    const int buf = tile & 1;
-    __syncthreads();                         // the other buffer and the scores are free
-    if (tile + 1 < ntiles) load_tile(tile + 1, buf ^ 1);
-    cp_async_commit();                       // possibly empty: keeps the group count uniform
-    cp_async_wait_one();                     // this thread's copies of this tile are done
-    __syncthreads();                         // ... and everyone's
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t & 1;
+    const bool landed = mbar_wait(&sm.full[st], (uint32_t)(t / kStages) & 1u);
 
-    // ---- scores: one m16n8 tile per warp over half of the dimensions ------
-    {
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t qa = smem_u32(&sm.q[(hh * 16 + (lane & 15)) * kStride + kh * kKHalf +
-                                         (lane >> 4) * 8]);
-      const uint32_t kb = smem_u32(&sm.kv[buf][(nt * 8 + (lane & 7)) * kStride + kh * kKHalf +
-                                               ((lane >> 3) & 1) * 8]);
-#pragma unroll 6
-      for (int ks = 0; ks < kKHalf / 16; ++ks) {
-        uint32_t af[4], bf[2];
-        ldsm_x4(qa + ks * 32, af);
-        ldsm_x2(kb + ks * 32, bf);
-        mma_bf16(c, af, bf[0], bf[1]);
-      }
-      float* sp = sm.sp[kh];
-      const int row = hh * 16 + g, col = nt * 8 + 2 * t4;
-      sp[row * kSpStride + col] = c[0];
-      sp[row * kSpStride + col + 1] = c[1];
-      sp[(row + 8) * kSpStride + col] = c[2];
-      sp[(row + 8) * kSpStride + col + 1] = c[3];
+    // Scores of the 16 heads against tokens dh*16 .. dh*16+15 (two n-tiles),
+    // even and odd k-steps in separate accumulators.
+    float c[2][2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) c[n][e][0] = c[n][e][1] = c[n][e][2] = c[n][e][3] = 0.f;
+    const uint32_t kb = smem_u32(&sm.kv[st][(dh * 16 + (lane & 7) + ((lane >> 4) & 1) * 8) *
+                                                kStride + ((lane >> 3) & 1) * 8]);
+#pragma unroll 3
+    for (int ks = 0; ks < kDqk / 16; ks += 2) {
+      uint32_t af[4], bf[4], ag[4], bg[4];
+      ldsm_x4(qa + ks * 32, af);
+      ldsm_x4(kb + ks * 32, bf);
+      ldsm_x4(qa + ks * 32 + 32, ag);
+      ldsm_x4(kb + ks * 32 + 32, bg);
+      mma_bf16(c[0][0], af, bf[0], bf[1]);
+      mma_bf16(c[1][0], af, bf[2], bf[3]);
+      mma_bf16(c[0][1], ag, bg[0], bg[1]);
+      mma_bf16(c[1][1], ag, bg[2], bg[3]);
     }
-    __syncthreads();
-
-    // ---- online softmax (exp2 domain) and O += P V --------------------------
-    {
-      const int R0 = hh2 * 16 + g, R1 = R0 + 8;
-      const int cols[4] = {2 * t4, 2 * t4 + 1, 2 * t4 + 8, 2 * t4 + 9};
-      float x0[4], x1[4];
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+    // x[kk][v]: k-step kk (tokens kk*16 ..); v in A-fragment order: rows g
+    // (v = 0, 1, 4, 5) and g + 8 (v = 2, 3, 6, 7) at tokens 2t, 2t+1, 2t+8, 2t+9.
+    float own[8], oth[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int cc = cols[u];
-        const bool v = sm.tokv[buf][cc] != 0;
-        x0[u] = v ? (sm.sp[0][R0 * kSpStride + cc] + sm.sp[1][R0 * kSpStride + cc]) * a.c2
-                  : -INFINITY;
-        x1[u] = v ? (sm.sp[0][R1 * kSpStride + cc] + sm.sp[1][R1 * kSpStride + cc]) * a.c2
-                  : -INFINITY;
-        mx0 = fmaxf(mx0, x0[u]);
-        mx1 = fmaxf(mx1, x1[u]);
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      // Rows with nothing valid yet keep m = -inf: use 0 as the reference.
-      const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;
-      const float al0 = exp2f(m0 - ref0), al1 = exp2f(m1 - ref1);
-      m0 = n0;
-      m1 = n1;
-      float e0[4], e1[4], p0[4], p1[4];
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        e0[u] = exp2f(x0[u] - ref0);
-        e1[u] = exp2f(x1[u] - ref1);
-      }
-      uint32_t pa[4];
-      pa[0] = pack_bf16(e0[0], e0[1]);
-      pa[1] = pack_bf16(e1[0], e1[1]);
-      pa[2] = pack_bf16(e0[2], e0[3]);
-      pa[3] = pack_bf16(e1[2], e1[3]);
-      {
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(pa);
-        const float2 f0 = __bfloat1622float2(h[0]), f1 = __bfloat1622float2(h[1]);
-        const float2 f2 = __bfloat1622float2(h[2]), f3 = __bfloat1622float2(h[3]);
-        p0[0] = f0.x; p0[1] = f0.y; p0[2] = f2.x; p0[3] = f2.y;
-        p1[0] = f1.x; p1[1] = f1.y; p1[2] = f3.x; p1[3] = f3.y;
-      }
-      float s0 = e0[0] + e0[1] + e0[2] + e0[3], s1 = e1[0] + e1[1] + e1[2] + e1[3];
-      float r0 = p0[0] + p0[1] + p0[2] + p0[3], r1 = p1[0] + p1[1] + p1[2] + p1[3];
+      for (int u = 0; u < 4; ++u) own[4 * n + u] = (c[n][0][u] + c[n][1][u]) * a.c2;
+    float* mine = &sm.xs[hb][dh][st][0][lane];
 #pragma unroll
-      for (int o = 1; o <= 2; o <<= 1) {
-        s0 += __shfl_xor_sync(kFull, s0, o);
-        s1 += __shfl_xor_sync(kFull, s1, o);
-        r0 += __shfl_xor_sync(kFull, r0, o);
-        r1 += __shfl_xor_sync(kFull, r1, o);
-      }
-      l0 = l0 * al0 + s0;
-      l1 = l1 * al1 + s1;
-      w0 = w0 * al0 + r0;
-      w1 = w1 * al1 + r1;
+    for (int v = 0; v < 8; ++v) mine[v * 32] = own[v];
+    if (bar_any(1 + hb, 64, !landed)) {      // both warps of the block see the same answer
+      ok = false;
+      break;
+    }
+    const float* other = &sm.xs[hb][dh ^ 1][st][0][lane];
 #pragma unroll
-      for (int j = 0; j < kDv / 4 / 8; ++j) {
+    for (int v = 0; v < 8; ++v) oth[v] = other[v * 32];
+    float x[2][8];                           // by k-step, selected without indexing by dh
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      x[0][v] = dh ? oth[v] : own[v];
+      x[1][v] = dh ? own[v] : oth[v];
+    }
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const int tok = kk * 16 + 2 * t4 + (v & 1) + ((v >> 2) << 3);
+        if (!sm.tokv[st][tok]) x[kk][v] = -INFINITY;
+        if ((v >> 1) & 1) mx1 = fmaxf(mx1, x[kk][v]);
+        else mx0 = fmaxf(mx0, x[kk][v]);
+      }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
+    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+    // Rows with nothing valid yet keep m = -inf: use 0 as the reference.
+    const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;
+    const float al0 = exp2f(m0 - ref0), al1 = exp2f(m1 - ref1);
+    m0 = n0;
+    m1 = n1;
+    uint32_t pa[2][4];
+    float s0 = 0.f, s1 = 0.f, r0 = 0.f, r1 = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      float e[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) e[v] = exp2f(x[kk][v] - (((v >> 1) & 1) ? ref1 : ref0));
+#pragma unroll
+      for (int q2 = 0; q2 < 4; ++q2) {
+        pa[kk][q2] = pack_bf16(e[2 * q2], e[2 * q2 + 1]);
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa[kk][q2]));
+        if (q2 & 1) {
+          s1 += e[2 * q2] + e[2 * q2 + 1];
+          r1 += f.x + f.y;
+        } else {
+          s0 += e[2 * q2] + e[2 * q2 + 1];
+          r0 += f.x + f.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      s0 += __shfl_xor_sync(kFull, s0, o);
+      s1 += __shfl_xor_sync(kFull, s1, o);
+      r0 += __shfl_xor_sync(kFull, r0, o);
+      r1 += __shfl_xor_sync(kFull, r1, o);
+    }
+    l0 = l0 * al0 + s0;
+    l1 = l1 * al1 + s1;
+    w0 = w0 * al0 + r0;
+    w1 = w1 * al1 + r1;
+    if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {   // the max moved: rescale O
+#pragma unroll
+      for (int j = 0; j < kHalfDv / 8; ++j) {
         acc[j][0] *= al0;
         acc[j][1] *= al0;
         acc[j][2] *= al1;
         acc[j][3] *= al1;
       }
-      const uint32_t vb = smem_u32(&sm.kv[buf][((lane & 7) + ((lane >> 3) & 1) * 8) * kStride +
-                                               dq * (kDv / 4) + (lane >> 4) * 8]);
+    }
+    // O += P V over this warp's 256 output dimensions.
 #pragma unroll
-      for (int jj = 0; jj < kDv / 4 / 16; ++jj) {
+    for (int kk = 0; kk < 2; ++kk) {
+      const uint32_t vb = smem_u32(&sm.kv[st][(kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) *
+                                                  kStride + dh * kHalfDv + (lane >> 4) * 8]);
+#pragma unroll
+      for (int j = 0; j < kHalfDv / 16; ++j) {
         uint32_t bf[4];
-        ldsm_x4_t(vb + jj * 32, bf);
-        mma_bf16(acc[2 * jj], pa, bf[0], bf[1]);
-        mma_bf16(acc[2 * jj + 1], pa, bf[2], bf[3]);
+        ldsm_x4_t(vb + j * 32, bf);
+        mma_bf16(acc[2 * j], pa[kk], bf[0], bf[1]);
+        mma_bf16(acc[2 * j + 1], pa[kk], bf[2], bf[3]);
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[st]);   // this warp is done with the stage
   }
-  if (bad) raise_flag(a.flags, DSA_FLAG_BOUNDS);
+  if (!ok && lane == 0) raise_flag(a.flags, DSA_FLAG_TIMEOUT);
 
-  // ---- O / l in bf16, lse2 = m + log2 l --------------------------------------
+  // ---- O / w in bf16, lse2 = m + log2 l ----------------------------------------
   const float inv0 = w0 > 0.f ? 1.f / w0 : 0.f, inv1 = w1 > 0.f ? 1.f / w1 : 0.f;
-  __nv_bfloat16* o0 = a.out + (obase + h_lo) * kDv + dq * (kDv / 4) + 2 * t4;
+  const int64_t h0 = obase + hb * 16 + g;
+  __nv_bfloat16* o0 = a.out + h0 * kDv + dh * kHalfDv + 2 * t4;
   __nv_bfloat16* o1 = o0 + 8 * kDv;
 #pragma unroll
-  for (int j = 0; j < kDv / 4 / 8; ++j) {
+  for (int j = 0; j < kHalfDv / 8; ++j) {
     *reinterpret_cast<uint32_t*>(o0 + j * 8) = pack_bf16(acc[j][0] * inv0, acc[j][1] * inv0);
     *reinterpret_cast<uint32_t*>(o1 + j * 8) = pack_bf16(acc[j][2] * inv1, acc[j][3] * inv1);
   }
-  if (dq == 0 && t4 == 0) {
-    a.lse2[obase + h_lo] = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
-    a.lse2[obase + h_lo + 8] = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
+  if (dh == 0 && t4 == 0) {
+    a.lse2[h0] = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
+    a.lse2[h0 + 8] = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
   }
 }
 

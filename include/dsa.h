@@ -301,7 +301,7 @@ dsa_status dsa_slot_mapping(const int32_t* positions, const int32_t* token_req, 
  *              below it is outside [0, n_slots) (that token is left out).
  * Errors: rows < 0, K < 1, n_slots < 1, non-finite scale, null pointers,
  *         misalignment -> INVALID_ARG; S not in [1, 64], H not a multiple of
- *         32 -> UNSUPPORTED.
+ *         64 -> UNSUPPORTED.
  */
 dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache, int64_t n_slots,
                                  const int32_t* slots, const int32_t* counts, int rows, int S,

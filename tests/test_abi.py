@@ -167,7 +167,7 @@ def test_sparse_mla_decode_argument_checks(lib):
         args = list(ok)
         args[i] = bad
         assert f(*args) == INVALID, (i, bad)
-    for i, bad in [(6, 0), (6, 65), (7, 96 + 16), (7, 16)]:
+    for i, bad in [(6, 0), (6, 65), (7, 96), (7, 32), (7, 16)]:
         args = list(ok)
         args[i] = bad
         assert f(*args) == UNSUPPORTED, (i, bad)
