@@ -59,7 +59,7 @@ struct AttnSmem {
   // Score swap between the two warps of a head block: [block][token half]
   // [tile parity][value][lane], each lane's eight scores of its half.
   float xs[kHeads / 16][2][2][8][32];
-  int tokv[kStages][kTile];                  // token valid in this stage
+  uint32_t vmask[kStages];                   // bit i: token i of the stage is valid
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -143,8 +143,8 @@ __device__ __forceinline__ void produce(const AttnArgs& a, AttnSmem& sm, int cou
     __nv_bfloat16* dst = &sm.kv[st][lane * kStride];
     if (!in)
       for (int c = 0; c < kChunks; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
-    sm.tokv[st][lane] = in;
     const unsigned valid = __ballot_sync(kFull, in);
+    if (lane == 0) sm.vmask[st] = valid;
     // The consumers' reads of this stage (generic proxy) before the copies.
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
@@ -271,12 +271,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) sparse_mla_decode_kernel(cons
       x[1][v] = dh ? own[v] : oth[v];
     }
     float mx0 = -INFINITY, mx1 = -INFINITY;
+    const uint32_t vm = sm.vmask[st] >> (2 * t4);
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
-        const int tok = kk * 16 + 2 * t4 + (v & 1) + ((v >> 2) << 3);
-        if (!sm.tokv[st][tok]) x[kk][v] = -INFINITY;
+        const int tok = kk * 16 + (v & 1) + ((v >> 2) << 3);   // + 2 t4, folded into vm
+        if (!((vm >> tok) & 1u)) x[kk][v] = -INFINITY;
         if ((v >> 1) & 1) mx1 = fmaxf(mx1, x[kk][v]);
         else mx0 = fmaxf(mx0, x[kk][v]);
       }
