@@ -59,15 +59,22 @@ PATHS = {
     # the write side of the paged cache: each row's new token mapped to the
     # slot its owner shard stores it at (not part of the indexer step)
     "write_slots": ("slot_mapping",),
+    # the decode loop closed: the fused indexer, every shard's sparse MLA
+    # attention over its compacted slots, and the combine of those outputs
+    "attention": ("indexer_fused", "sparse_mla_decode", "lse_combine"),
 }
-PATH_METRIC = {"write_slots": ("slot-mapped new tokens/s", "tokens/s")}
+PATH_METRIC = {"write_slots": ("slot-mapped new tokens/s", "tokens/s"),
+               "attention": ("decode rows/s (indexer, sparse MLA attention, LSE combine)",
+                             "rows/s")}
+MLA_SCALE = 1.0 / np.sqrt(192.0)   # softmax scale of the attention path
 KERNEL_SOURCES = {"shard_topk_pack": ("shard_topk.cu", "fast_select.cuh", "local_topk.cuh",
                                       "reg_topk.cuh"),
                   "merge_topk_stable": ("merge.cu", "reg_topk.cuh", "binmap.cuh"),
                   "convert_index_compact": ("convert.cu",),
                   "indexer_fused": ("fused.cu", "local_topk.cuh", "reg_topk.cuh"),
                   "lse_combine": ("combine.cu",),
-                  "slot_mapping": ("slot_mapping.cu",)}
+                  "slot_mapping": ("slot_mapping.cu",),
+                  "sparse_mla_decode": ("attention.cu",)}
 
 
 # ---------------------------------------------------------------------------
@@ -109,7 +116,7 @@ def max_over_ranks(x: float, world: int) -> float:
 # ---------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------
-def host_inputs(cfg, replica: int):
+def host_inputs(cfg, replica: int, path: str = "fused"):
     """Seeded host arrays for one input set of the workload.
 
     Per-shard logits are drawn i.i.d. N(0,1) directly (the recipes' ties and
@@ -125,7 +132,14 @@ def host_inputs(cfg, replica: int):
     d = dict(starts=starts, ends=ends, logits=logits, bt=bt, r2q=r2q, pos=pos)
     if cfg.H:
         d["part"], d["lse2"] = W.combine_inputs(cfg, replica=replica)
+    if path == "attention":
+        d["q"] = W.mla_query(cfg.rows, cfg.H, seed=1000 * replica + 7)
     return d
+
+
+def mla_cache_slots(cfg) -> int:
+    """Slots of each shard's paged KV cache: every block the tables address."""
+    return cfg.reqs * cfg.max_blocks * cfg.block_size
 
 
 def set_bytes(cfg) -> int:
@@ -151,6 +165,10 @@ def algorithmic_bytes(cfg, ends: np.ndarray) -> dict:
         written, per row.
     slot_mapping: per new token its position (and request) read, one block-table
         word read, S slots written.
+    sparse_mla_decode: per (row, shard) the query (H x 576 bf16) and its count,
+        per selected slot the slot and the cache row (576 bf16) read; per (row,
+        shard) H x 512 bf16 outputs and H LSEs written.  The selected slots of a
+        row number min(K, row length) over all shards.
     """
     S, K, R, H, D = cfg.S, cfg.K, cfg.rows, cfg.H, cfg.D
     logits = 4 * ends.astype(np.int64).sum()
@@ -162,7 +180,20 @@ def algorithmic_bytes(cfg, ends: np.ndarray) -> dict:
         "indexer_fused": int(logits + R * (4 * K + 4 * K + 4 * S * K + 4 * S)),
         "lse_combine": int(R * (S * H * D * 2 + S * H * 4 + H * D * 2 + H * 4)),
         "slot_mapping": int(R * (4 + (4 if cfg.reqs != cfg.rows else 0) + 4 + 4 * S)),
+        "sparse_mla_decode": int(selected(cfg, ends) * (4 + 2 * W.MLA_DQK)
+                                 + R * S * (H * 2 * W.MLA_DQK + 4 + H * (2 * W.MLA_DV + 4))),
     }
+
+
+def selected(cfg, ends: np.ndarray) -> int:
+    """Merged winners of a batch: min(K, row length) per row (row_start = 0)."""
+    return int(np.minimum(cfg.K, ends.astype(np.int64)).sum())
+
+
+def attention_flops(cfg, ends: np.ndarray) -> int:
+    """Scores (576-long dot products) and the weighted sum (512 values) per
+    selected token and head."""
+    return int(2 * cfg.H * selected(cfg, ends) * (W.MLA_DQK + W.MLA_DV))
 
 
 # ---------------------------------------------------------------------------
@@ -252,6 +283,16 @@ def measured_peak() -> tuple[float, str]:
         return 6800.0, "fallback"
 
 
+def measured_tensor_peak() -> float:
+    """Dense bf16 TFLOP/s measured on this machine (burst: a kernel timed alone),
+    else the recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
+
+
 def kernel_source_hash(kernel: str) -> str:
     csrc = os.path.join(ROOT, "dsa_sparse_indexer_gb300", "csrc")
     h = hashlib.sha256()
@@ -281,6 +322,24 @@ def profiled_traffic(kernel: str, workload: str = DEFAULT_WORKLOAD) -> float | N
 # the oracle as CPU baseline / reference arm
 # ---------------------------------------------------------------------------
 def oracle_rows(inp: dict, cfg, rows: np.ndarray, path: str = "fused"):
+    if path == "attention":
+        from oracle import attention as OA
+        from oracle import combine as OC
+        from oracle import pipeline as OP
+        res = OP.run_rows(inp["logits"], inp["starts"], inp["ends"], cfg.S, cfg.I, cfg.K,
+                          rows=rows, tables=inp["bt"], row_to_req=inp["r2q"],
+                          block_size=cfg.block_size)
+        for j, r in enumerate(rows):
+            parts, lses = [], []
+            for s in range(cfg.S):
+                sel = res["slots"][s, j, :res["counts"][s, j]]
+                o, l2 = OA.sparse_mla_decode(OC.bf16_to_f64(inp["q"][r]),
+                                             OC.bf16_to_f64(inp["cache"][s, sel]), MLA_SCALE,
+                                             W.MLA_DV)
+                parts.append(o)
+                lses.append(l2)
+            OC.lse_combine(np.stack(parts), np.stack(lses))
+        return res
     if path == "write_slots":
         from oracle import kv_write as KW
         req = rows if inp["r2q"] is None else inp["r2q"][rows]
@@ -301,7 +360,8 @@ def metric_for(path: str) -> tuple[str, str]:
 def dtype_for(path: str) -> str:
     """The arithmetic the path computes in: fp32 keys and scores (the combine
     accumulates in fp32), or int32 index maps only."""
-    return "i32" if path == "write_slots" else "f32"
+    return {"write_slots": "i32", "attention": "f32 indexer, bf16 attention (fp32 accumulate)"}.get(
+        path, "f32")
 
 
 def cpu_baseline(cfg, inp: dict, budget_s: float = 10.0, path: str = "fused") -> dict:
@@ -316,7 +376,8 @@ def cpu_baseline(cfg, inp: dict, budget_s: float = 10.0, path: str = "fused") ->
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    what = "the new token" if path == "write_slots" else "all steps"
+    what = {"write_slots": "the new token",
+            "attention": "all steps, the shards' attention and the combine"}.get(path, "all steps")
     return {"value": done / dt, "unit": metric_for(path)[1], "cores": 1, "kind": "oracle",
             "sample": f"{done} rows of the {cfg.name} batch ({what} per row, numpy, one "
                       f"thread), {dt:.1f} s"}
@@ -327,7 +388,9 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     cfg = W.CONFIGS[args.workload]
-    inp = host_inputs(cfg, 0)
+    inp = host_inputs(cfg, 0, args.path)
+    if args.path == "attention":
+        inp["cache"] = W.mla_cache_uniform(cfg.S, mla_cache_slots(cfg), seed=4242)
     metric, unit = metric_for(args.path)
     t = time.perf_counter()
     oracle_rows(inp, cfg, np.array([0]), args.path)
@@ -377,7 +440,10 @@ def config_block(cfg, path: str = "fused") -> dict:
             "path": " -> ".join(kernels_for(cfg, path)) + " (C ABI, one stream)",
             "l2": (f"{replicas_for(cfg)} rotating input sets of {set_bytes(cfg) / 1e6:.0f} MB "
                    f"(> 2.5x L2 together); no flush" if path != "write_slots" else
-                   "positions and block tables (a few MB at most) stay in L2; no flush"),
+                   "positions and block tables (a few MB at most) stay in L2; no flush")
+                  + (f"; resident KV caches of {cfg.S * mla_cache_slots(cfg) * 2 * W.MLA_DQK / 1e9:.1f}"
+                     f" GB (bf16, |v| in [0.5, 1)), softmax scale 1/sqrt(192)"
+                     if path == "attention" else ""),
             "logits": "i.i.d. N(0,1) per shard (work-equivalent to the recipe)",
             "parallelism": "replicas (rows independent, no collective)"}
 
@@ -385,6 +451,32 @@ def config_block(cfg, path: str = "fused") -> dict:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def attention_probe() -> int:
+    """A small, fixed case of dsa_sparse_mla_decode for profiler captures: the
+    decode batch's shape (64 rows, 4 shards, 128 heads, 512 selected slots per
+    (row, shard), i.e. its 131 K gathered rows) over caches of 65,536 slots per
+    shard (302 MB, larger than L2; about 0.5 GB on the device in all).  Seeded
+    inputs; three launches; prints the error word."""
+    import torch
+    from dsa_sparse_indexer_gb300 import build as B
+    import dsa_sparse_indexer_gb300 as dsa
+    B.build()
+    dev = torch.device("cuda")
+    S, R, H, K, n_slots, cnt = 4, 64, 128, 2048, 65536, 512
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    q = torch.randn((R, H, W.MLA_DQK), generator=g, device=dev).to(torch.bfloat16)
+    cache = (torch.rand((S, n_slots, W.MLA_DQK), generator=g, device=dev) - 0.5).to(torch.bfloat16)
+    slots = torch.randint(0, n_slots, (S, R, K), generator=g, device=dev, dtype=torch.int32)
+    counts = torch.full((S, R), cnt, dtype=torch.int32, device=dev)
+    err = dsa.new_error_flags(dev)
+    for _ in range(3):
+        dsa.sparse_mla_decode(q, cache, slots, counts, MLA_SCALE, err_flags=err)
+    torch.cuda.synchronize()
+    print(json.dumps({"probe": "sparse_mla_decode", "err": int(err.item())}))
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -399,7 +491,11 @@ def main(argv=None) -> int:
                     help="fused: one cluster kernel for steps a1-a4; steps: one kernel per "
                          "step; write_slots: the write-side slot mapping of each row's new "
                          "token")
+    ap.add_argument("--probe", choices=["attention"], default=None,
+                    help="run a small fixed case of one kernel for a profiler capture, no timing")
     args = ap.parse_args(argv)
+    if args.probe == "attention":
+        return attention_probe()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
@@ -420,11 +516,13 @@ def main(argv=None) -> int:
     cfg = W.CONFIGS[args.workload]
     S, R, K, H, D = cfg.S, cfg.rows, cfg.K, cfg.H, cfg.D
     REPLICAS = replicas_for(cfg)
-    if args.path == "fused" and S > 8:
-        raise SystemExit("the fused path takes at most 8 shards")
+    if args.path in ("fused", "attention") and S > 8:
+        raise SystemExit("the fused indexer takes at most 8 shards")
+    if args.path == "attention" and not H:
+        raise SystemExit("the attention path needs a workload with heads (H > 0)")
 
     # --- resident inputs (rotating sets; each rank its own seeds) -----------
-    host = [host_inputs(cfg, rank * REPLICAS + i) for i in range(REPLICAS)]
+    host = [host_inputs(cfg, rank * REPLICAS + i, args.path) for i in range(REPLICAS)]
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     sets = []
     for h in host:
@@ -435,7 +533,17 @@ def main(argv=None) -> int:
         if H:
             st["part"] = d(h["part"].view(np.int16))
             st["lse2"] = d(h["lse2"])
+        if "q" in h:
+            st["q"] = d(h["q"].view(np.int16))
         sets.append(st)
+    if args.path == "attention":
+        # Each shard's paged KV cache (every block the tables address), drawn
+        # once on the host and kept resident, as a serving cache is.
+        n_slots = mla_cache_slots(cfg)
+        cache_host = W.mla_cache_uniform(S, n_slots, seed=4242 + rank)
+        cache_dev = d(cache_host.view(np.int16))
+        attn_out = torch.empty((S, R, H, W.MLA_DV), dtype=torch.int16, device=dev)
+        attn_lse = torch.empty((S, R, H), dtype=torch.float32, device=dev)
     cand = torch.empty((R, S * K, 2), dtype=torch.float32, device=dev)
     ids = torch.empty((R, K), dtype=torch.int32, device=dev)
     slots = torch.empty((S, R, K), dtype=torch.int32, device=dev)
@@ -457,7 +565,18 @@ def main(argv=None) -> int:
         if H:
             tail = ((lib.dsa_lse_combine, (P(st["part"]), P(st["lse2"]), S, R, H, D, P(out),
                                            P(lse), P(err), sp)),)
-        if args.path == "write_slots":
+        if args.path == "attention":
+            calls.append((
+                (lib.dsa_indexer_fused, (P(st["logits"]), ld, R, S, cfg.I, K, P(st["starts"]),
+                                         P(st["ends"]), P(st["bt"]), cfg.reqs, cfg.max_blocks,
+                                         cfg.block_size, r2q, P(ids), None, P(slots),
+                                         P(counts), None, None, P(err), sp)),
+                (lib.dsa_sparse_mla_decode, (P(st["q"]), P(cache_dev), n_slots, P(slots),
+                                             P(counts), R, S, H, K, MLA_SCALE, P(attn_out),
+                                             P(attn_lse), P(err), sp)),
+                (lib.dsa_lse_combine, (P(attn_out), P(attn_lse), S, R, H, D, P(out), P(lse),
+                                       P(err), sp))))
+        elif args.path == "write_slots":
             calls.append(((lib.dsa_slot_mapping, (P(st["pos"]), r2q, R, S, cfg.I, P(st["bt"]),
                                                   cfg.reqs, cfg.max_blocks, cfg.block_size,
                                                   P(slotmap), P(err), sp)),))
@@ -604,6 +723,14 @@ def main(argv=None) -> int:
     kernels = {k: {"ms": mean_ms[k], "algorithmic_bytes": nbytes[k],
                    "gbs": nbytes[k] / (mean_ms[k] / 1e3) / 1e9,
                    "frac": nbytes[k] / (mean_ms[k] / 1e3) / 1e9 / peak} for k in KERNELS}
+    if "sparse_mla_decode" in kernels:
+        # a contraction too: its tensor-core rate against the measured bf16 peak
+        flops = float(np.mean([attention_flops(cfg, h["ends"]) for h in host]))
+        tflops = flops / (mean_ms["sparse_mla_decode"] / 1e3) / 1e12
+        tpeak = measured_tensor_peak()
+        kernels["sparse_mla_decode"].update(
+            flops=flops, tflops=tflops, tensor_peak_tflops=tpeak,
+            tensor_frac=tflops / tpeak if tpeak else None)
 
     # --- e2e through host buffers --------------------------------------------
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -616,9 +743,11 @@ def main(argv=None) -> int:
                       bt=pin(h["bt"]))
         if h["r2q"] is not None:
             hs["r2q"] = pin(h["r2q"])
-        if H and args.path != "write_slots":
+        if H and args.path in ("fused", "steps"):
             hs["part"] = pin(h["part"].view(np.int16))
             hs["lse2"] = pin(h["lse2"])
+        if "q" in h:
+            hs["q"] = pin(h["q"].view(np.int16))
         hsets.append(hs)
     if args.path == "write_slots":
         results = [slotmap]
@@ -679,7 +808,10 @@ def main(argv=None) -> int:
     }
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(cfg, host[0], path=args.path)
+            base_inp = dict(host[0])
+            if args.path == "attention":
+                base_inp["cache"] = cache_host
+            result["cpu_baseline"] = cpu_baseline(cfg, base_inp, path=args.path)
         print(json.dumps(result))
     if world > 1:
         import torch.distributed as dist
