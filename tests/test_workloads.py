@@ -73,3 +73,17 @@ def test_combine_inputs_respect_empty_mask():
     assert np.isneginf(lse2[2, 1]).all() and np.all(out[2, 1] == 0)
     ok = ~np.isneginf(lse2)
     assert lse2[ok].min() >= -5 and lse2[ok].max() <= 20
+
+
+def test_mla_inputs_are_seeded_bf16_of_the_stated_ranges():
+    from oracle.combine import bf16_to_f64
+    a = W.mla_cache_uniform(2, 300, seed=5)
+    b = W.mla_cache_uniform(2, 300, seed=5)
+    assert a.shape == (2, 300, W.MLA_DQK) and a.dtype == np.uint16
+    assert np.array_equal(a, b)
+    v = np.abs(bf16_to_f64(a))
+    assert v.min() >= 0.5 and v.max() < 1.0
+    q = W.mla_query(3, 64, seed=1)
+    assert q.shape == (3, 64, W.MLA_DQK) and np.array_equal(q, W.mla_query(3, 64, seed=1))
+    c = bf16_to_f64(W.mla_cache(1, 2000, seed=2))
+    assert abs(c.mean()) < 0.01 and abs(c.std() - 1.0) < 0.01

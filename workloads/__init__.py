@@ -215,6 +215,18 @@ def mla_cache(S: int, n_slots: int, seed: int) -> np.ndarray:
     return f32_to_bf16_bits(rng.standard_normal((S, n_slots, MLA_DQK), dtype=np.float32))
 
 
+def mla_cache_uniform(S: int, n_slots: int, seed: int) -> np.ndarray:
+    """[S, n_slots, 576] paged KV caches for benchmark-sized runs (gigabytes):
+    bf16 bit patterns with a random sign, exponent -1 and 7 random mantissa
+    bits, i.e. values of magnitude in [0.5, 1), drawn 16 bits at a time so that
+    several gigabytes take seconds to draw."""
+    rng = np.random.default_rng(seed)
+    w = rng.integers(0, 1 << 16, (S, n_slots, MLA_DQK), dtype=np.uint16)
+    w &= np.uint16(0x807F)
+    w |= np.uint16(0x3F00)
+    return w
+
+
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 to bf16 (round to nearest, ties to even); returns uint16 bits.
     Inputs are finite."""
