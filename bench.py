@@ -776,7 +776,52 @@ def main(argv=None) -> int:
         e2e_step(i)
     x1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(x0.elapsed_time(x1), world) / args.e2e_steps
+    e2e_seq_ms = max_over_ranks(x0.elapsed_time(x1), world) / args.e2e_steps
+
+    # The same steps pipelined as a serving loop runs them: step i+1's inputs go
+    # up on one stream while step i computes and its result comes back on
+    # others.  Input set i % 2 is reused once step i - 2 has computed; the
+    # result buffers once step i - 1's result has been read out.  Every step
+    # still copies all of its inputs and its result inside the timed region.
+    in_s, out_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def e2e_pipelined(n, first=None):
+        comp_done, out_done = {}, {}
+        for i in range(n):
+            hs, ds = hsets[i % 2], sets[i % 2]
+            with torch.cuda.stream(in_s):
+                if i == 0 and first is not None:
+                    first.record(in_s)
+                if i >= 2:
+                    in_s.wait_event(comp_done[i - 2])
+                for k in hs:
+                    ds[k].copy_(hs[k], non_blocking=True)
+                e_in = torch.cuda.Event()
+                e_in.record(in_s)
+            stream.wait_event(e_in)
+            if i >= 1:
+                stream.wait_event(out_done[i - 1])
+            for fn, a in calls[i % 2]:
+                launch(fn, a)
+            e_c = torch.cuda.Event()
+            e_c.record(stream)
+            comp_done[i] = e_c
+            with torch.cuda.stream(out_s):
+                out_s.wait_event(e_c)
+                for hr, dr in zip(h_results, results):
+                    hr.copy_(dr, non_blocking=True)
+                e_o = torch.cuda.Event(enable_timing=True)
+                e_o.record(out_s)
+                out_done[i] = e_o
+        return out_done[n - 1]
+
+    e2e_pipelined(3)
+    torch.cuda.synchronize()
+    barrier(world)
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = e2e_pipelined(args.e2e_steps, first=p0)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(p0.elapsed_time(p1), world) / args.e2e_steps
     e2e_value = world * R / (e2e_ms / 1e3)
 
     metric, unit = metric_for(args.path)
@@ -802,7 +847,10 @@ def main(argv=None) -> int:
                                             max_over_ranks(single_ms, world) / args.steps),
         "launch_loop_ms_per_step": loop_ms_per_step,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+                "schedule": "pinned host buffers through the C ABI; step i+1's inputs copied "
+                            "while step i computes and its result is read back (three streams)",
+                "sequential_ms_per_step": e2e_seq_ms},
         "gpu_launches": nk * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
