@@ -153,6 +153,27 @@ def test_rows_longer_than_the_register_path(ld):
     G.assert_indexer_parity(case, got, np.arange(rows))
 
 
+def test_very_long_local_rows():
+    """Quarter-million-slot local rows (2 shards, 512 K tokens a row): the
+    global-memory select over many radix passes, K = 512 and 2048."""
+    rng = np.random.default_rng(13)
+    for K in (512, 2048):
+        rows, S, I = 2, 2, 3
+        Lmax = 2 * 262144
+        ld = (max(OL.local_count(Lmax, s, S, I) for s in range(S)) + 3) // 4 * 4
+        x = rng.standard_normal((rows, Lmax)).astype(np.float32)
+        ends = np.array([Lmax, Lmax - 77777], np.int32)
+        cfg = W.Config("adhoc", 9, rows=rows, S=S, I=I, K=K, block_size=64, max_len=Lmax,
+                       ld=ld, reqs=rows, max_blocks=(ld + 63) // 64)
+        local = OL.shard_rows(x, ends, S, I, ld)
+        bt = np.stack([rng.permutation(rows * cfg.max_blocks).astype(np.int32).reshape(rows, -1)
+                       for _ in range(S)])
+        case = dict(cfg=cfg, x=x, local=local, starts=np.zeros(rows, np.int32), ends=ends,
+                    bt=bt, r2q=None)
+        G.assert_indexer_parity(case, G.run_gpu(case), np.arange(rows))
+        G.assert_indexer_parity(case, G.run_gpu_fused(case), np.arange(rows))
+
+
 @pytest.mark.parametrize("ld", [30000, 52000])
 def test_fused_rows_longer_than_the_register_path(ld):
     """The fused kernel's staged (ld 30000) and global-memory (ld 52000) paths."""
