@@ -79,6 +79,8 @@ enum {
  * values in all. */
 #define DSA_MLA_DQK 576
 #define DSA_MLA_DV 512
+/* Bytes of the library-owned candidate array of dsa_indexer_steps_noalloc. */
+#define DSA_NOALLOC_SCRATCH_BYTES (64u << 20)
 
 /* Human-readable name of a status code (static string). */
 const char* dsa_status_string(dsa_status status);
@@ -307,6 +309,29 @@ dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache, in
                                  const int32_t* slots, const int32_t* counts, int rows, int S,
                                  int H, int K, float scale, uint16_t* out, float* lse2,
                                  uint32_t* err_flags, cudaStream_t stream);
+
+/*
+ * dsa_indexer_steps_noalloc - dsa_shard_topk_pack, dsa_merge_topk_stable and
+ * dsa_convert_index_compact in turn, with the packed candidates held in a
+ * static device array of this library (DSA_NOALLOC_SCRATCH_BYTES) instead of a
+ * caller buffer.  No counterpart on the pages: a convenience for callers that
+ * cannot allocate the [rows][S*K][2] candidate buffer.
+ *
+ * Arguments as the three entry points it calls (ids [rows][K] is the merge's
+ * output and the convert's input; scores and local_idx are not produced).
+ * It enqueues three kernels on `stream`.  Calls on one device share the array:
+ * they must not overlap in time.
+ * Errors: rows * S * K * 8 > DSA_NOALLOC_SCRATCH_BYTES -> UNSUPPORTED; the
+ *         array's address cannot be looked up -> CUDA; otherwise those of the
+ *         entry points it calls, from the first that fails (nothing after it
+ *         is enqueued).
+ */
+dsa_status dsa_indexer_steps_noalloc(const float* logits, int64_t ld, int rows, int S, int I,
+                                     int K, const int32_t* row_starts, const int32_t* row_ends,
+                                     const int32_t* block_table, int reqs, int max_blocks,
+                                     int block_size, const int32_t* row_to_req, int32_t* ids,
+                                     int32_t* slots, int32_t* counts, uint32_t* err_flags,
+                                     cudaStream_t stream);
 
 #ifdef __cplusplus
 }
