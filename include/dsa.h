@@ -36,9 +36,12 @@
  *
  * Conventions for every entry point:
  *   - All array pointers are DEVICE pointers owned by the caller; the library
- *     allocates nothing, keeps no state between calls and frees nothing.
+ *     allocates nothing, keeps no state between calls and frees nothing (the
+ *     one exception, dsa_indexer_steps_noalloc, uses a static device array
+ *     that exists while the library is loaded).
  *   - Every call is asynchronous on `stream` (0 = legacy default stream) and
- *     enqueues one kernel; results are ready when the stream reaches it.
+ *     enqueues one kernel (dsa_indexer_steps_noalloc: three); results are
+ *     ready when the stream reaches it.
  *   - Arguments are checked on the host before anything is enqueued.  A bad
  *     argument returns DSA_ERR_INVALID_ARG or DSA_ERR_UNSUPPORTED and touches
  *     nothing.  rows == 0 returns DSA_OK and enqueues nothing once the scalar
