@@ -1,8 +1,8 @@
 """ctypes loader for libdsa.so, the C-ABI library of the DCP sparse-indexer path.
 
 The library is built in-tree by `dsa_sparse_indexer_gb300.build` (also run by
-`__graft_entry__.build()`).  There is no fallback: if the library is missing or
-fails to load, every call raises.
+the repository's top-level build entry point).  There is no fallback: if the
+library is missing or fails to load, every call raises.
 """
 from __future__ import annotations
 
