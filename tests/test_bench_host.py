@@ -1,0 +1,64 @@
+"""Host logic of bench.py: the algorithmic bytes and FLOPs it divides by, the
+paths and kernels it times, the rotating input sets, and the rule that an ncu
+summary's traffic is used only while the kernel's sources are unchanged."""
+import numpy as np
+import pytest
+
+import bench
+import workloads as W
+
+
+def test_algorithmic_bytes_by_hand_for_the_decode_shape():
+    cfg = W.CONFIGS["decode"]
+    ends = np.array([8192, 65536, 1000], np.int64)    # 1000 < K: fewer winners than K
+    R = cfg.rows
+    S, K, H, D = cfg.S, cfg.K, cfg.H, cfg.D
+    b = bench.algorithmic_bytes(cfg, ends)
+    logits = 4 * (8192 + 65536 + 1000)
+    assert b["shard_topk_pack"] == logits + R * 8 * S * K
+    assert b["merge_topk_stable"] == R * (8 * S * K + 4 * K)
+    assert b["convert_index_compact"] == R * (4 * K + 4 * K + 4 * S * K + 4 * S)
+    assert b["indexer_fused"] == logits + R * (8 * K + 4 * S * K + 4 * S)
+    assert b["lse_combine"] == R * (S * H * D * 2 + S * H * 4 + H * D * 2 + H * 4)
+    assert b["slot_mapping"] == R * (4 + 4 + 4 * S)               # row r is request r
+    sel = 2048 + 2048 + 1000
+    assert bench.selected(cfg, ends) == sel
+    assert b["sparse_mla_decode"] == sel * (4 + 1152) + R * S * (H * 1152 + 4 + H * 1028)
+    assert bench.attention_flops(cfg, ends) == 2 * H * sel * (576 + 512)
+
+
+def test_prefill_write_side_counts_the_request_word():
+    cfg = W.CONFIGS["prefill"]
+    _, ends = W.row_ranges(cfg)
+    assert bench.algorithmic_bytes(cfg, ends)["slot_mapping"] == cfg.rows * (4 + 4 + 4 + 4 * cfg.S)
+
+
+def test_paths_kernels_metrics():
+    dec, tiny = W.CONFIGS["decode"], W.CONFIGS["tiny"]
+    assert bench.kernels_for(dec, "fused") == ("indexer_fused", "lse_combine")
+    assert bench.kernels_for(tiny, "fused") == ("indexer_fused",)          # no heads: no combine
+    assert bench.kernels_for(dec, "attention") == ("indexer_fused", "sparse_mla_decode",
+                                                   "lse_combine")
+    assert bench.kernels_for(dec, "write_slots") == ("slot_mapping",)
+    assert bench.metric_for("fused") == (bench.METRIC, "rows/s")
+    assert bench.metric_for("write_slots")[1] == "tokens/s"
+    assert bench.dtype_for("write_slots") == "i32" and bench.dtype_for("steps") == "f32"
+    for k in ("indexer_fused", "lse_combine", "shard_topk_pack", "merge_topk_stable",
+              "convert_index_compact", "slot_mapping", "sparse_mla_decode"):
+        assert k in bench.KERNEL_SOURCES
+
+
+@pytest.mark.parametrize("name", sorted(W.CONFIGS))
+def test_rotating_sets_exceed_l2(name):
+    cfg = W.CONFIGS[name]
+    n = bench.replicas_for(cfg)
+    assert 2 <= n <= 8
+    assert n * bench.set_bytes(cfg) > 2.5 * bench.L2_BYTES or n == 8
+
+
+def test_profile_traffic_only_while_sources_match(monkeypatch):
+    got = bench.profiled_traffic("indexer_fused", "decode")
+    assert got is not None and got > 0
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
+    assert bench.profiled_traffic("indexer_fused", "decode") is None
+    assert bench.profiled_traffic("no_such_kernel", "decode") is None
