@@ -4,18 +4,15 @@
 // Each of the NT threads holds V float4 rows of keys, key[j][c] at a slot
 // given by the caller (slots order ties: the smaller slot ranks first); key 0
 // marks an empty slot.  Steps:
-//   1. a 256-bin histogram of one key per float4 row per thread (V samples),
-//      linear in the score over the samples' range, proposes a floor a little
-//      below the K-th key (about 1.15 K keys at or above it); when the
-//      selected sample bin is crowded (an outlier stretching the range) a
-//      second 256-bin histogram inside it, linear in the key, refines it;
-//   2. a 2048-bin histogram of the keys at or above the floor, spread over
-//      [floor, max key], locates the bin b* holding the K-th key;
-//   3. the members of b* (at most kFsRankCap) are ranked on (key, ~slot); the
+//   1. a 2048-bin histogram of every key, the bins linear in the score between
+//      the smallest and the largest key, locates the bin b* holding the K-th
+//      key (a normal-like row leaves a few dozen keys there);
+//   2. the members of b* (at most kFsRankCap) are ranked on (key, ~slot); the
 //      one with K - 1 - (keys above b*) keys above it is the threshold.
-// Bins other than b* may be crowded; only b* is ranked.  Returns false when
-// the floor misses (fewer than K keys at or above it) or b* is crowded: the
-// caller then falls back to a radix select.
+// Bins other than b* may be crowded; only b* is ranked.  Returns false when a
+// score is infinite, the range is empty or b* is crowded (an outlier
+// stretching the range, heavy ties): the caller then falls back to a radix
+// select.
 #pragma once
 
 #include "common.cuh"
@@ -24,19 +21,17 @@
 namespace dsa {
 
 constexpr int kFsBins = 2048;
-constexpr int kFsSampleBins = 256;
 constexpr int kFsRankCap = 256;
 
 struct FastSelectSmem {
   uint32_t bins[kFsBins];
-  uint32_t scnt[kFsSampleBins];
   // Stores are 32-bit: 64-bit stores of (key, slot) pairs made the compiler
   // move the callers' register keys to local memory.
   uint32_t bst_k[kFsRankCap];   // members of b*: score key
   uint32_t bst_s[kFsRankCap];   // and slot
   int scan[33];
-  int nsv, nb, bstar, above, bcnt, scount, sabove, sbin, gt, eq;
-  uint32_t smin, smax, kmin, kmax, sfloor;
+  int nb, bstar, above, bcnt, gt, eq;
+  uint32_t kmin, kmax;
   unsigned long long thr64;
 };
 
@@ -47,125 +42,44 @@ struct FastSelectResult {
   int gt, eq;
 };
 
-// n: the number of nonzero keys (n > K).  kmn / kmx: this thread's smallest
-// nonzero and largest key.  Every thread calls it.  On true it ends with a
-// barrier; on false the caller must synchronise before reusing `sm`.
+// More than K nonzero keys.  kmn / kmx: this thread's smallest nonzero and
+// largest key.  Every thread calls it.  On true it ends with a barrier; on
+// false the caller must synchronise before reusing `sm`.
 template <int NT, int V, bool kCounts = false, typename SlotOf>
-__device__ bool fast_select(const uint32_t (&key)[V][4], int n, int K, uint32_t kmn,
-                            uint32_t kmx, SlotOf slot_of, FastSelectSmem& sm,
-                            FastSelectResult* out) {
-  static_assert(V >= 4, "one sample per float4 row, four rows");
+__device__ bool fast_select(const uint32_t (&key)[V][4], int K, uint32_t kmn, uint32_t kmx,
+                            SlotOf slot_of, FastSelectSmem& sm, FastSelectResult* out) {
   using ull = unsigned long long;
   const int tid = threadIdx.x, lane = tid & 31;
-  for (int b = tid; b < kFsSampleBins; b += NT) sm.scnt[b] = 0u;
   for (int b = tid; b < kFsBins; b += NT) sm.bins[b] = 0u;
   if (tid == 0) {
-    sm.nsv = 0;
     sm.nb = 0;
-    sm.smin = 0xffffffffu;
-    sm.smax = 0u;
     sm.kmin = 0xffffffffu;
     sm.kmax = 0u;
   }
-  // Samples: one lane of each of four spread float4 rows.
-  auto sample = [&](int i) { return key[(i * V) / 4][i]; };
   {
-    int ns = 0;
-    uint32_t mn = 0xffffffffu, mx = 0u;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t k = sample(i);
-      ns += k != 0u;
-      mx = max(mx, k);
-      mn = min(mn, k ? k : 0xffffffffu);
-    }
-    ns = __reduce_add_sync(kFull, ns);
-    mn = __reduce_min_sync(kFull, mn);
-    mx = __reduce_max_sync(kFull, mx);
-    kmn = __reduce_min_sync(kFull, kmn);
-    kmx = __reduce_max_sync(kFull, kmx);
+    const uint32_t mn = __reduce_min_sync(kFull, kmn), mx = __reduce_max_sync(kFull, kmx);
     __syncthreads();
     if (lane == 0) {
-      atomicMin(&sm.kmin, kmn);
-      atomicMax(&sm.kmax, kmx);
-      if (ns) {
-        atomicAdd(&sm.nsv, ns);
-        atomicMin(&sm.smin, mn);
-        atomicMax(&sm.smax, mx);
-      }
+      atomicMin(&sm.kmin, mn);
+      atomicMax(&sm.kmax, mx);
     }
   }
   __syncthreads();
-  uint32_t floor = sm.kmin;   // without a sample floor: every key
-  const uint32_t kmax = sm.kmax;
-  const int nsv = sm.nsv;
-  if (n * 4 > K * 5 && nsv >= 64) {
-    const uint32_t smin = sm.smin, smax = sm.smax;
-    // Bins linear in the score: bin(k) = (score(k) - fmin) * fscale, clamped.
-    const float fmin = key_score(smin), fspan = key_score(smax) - fmin;
-    const float fscale = fspan > 0.f ? (float)kFsSampleBins / fspan : 0.f;
-    auto sbin = [&](uint32_t k) {
-      return min(kFsSampleBins - 1, max(0, (int)((key_score(k) - fmin) * fscale)));
-    };
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t k = sample(i);
-      if (k) atomicAdd(&sm.scnt[sbin(k)], 1u);
-    }
-    __syncthreads();
-    // Expected samples among the winners: nsv * K / n; take 1/8 more and 16.
-    const int target = min(nsv, (int)((float)nsv * (float)K * 1.125f / (float)n) + 16);
-    const int local = tid < kFsSampleBins ? (int)sm.scnt[kFsSampleBins - 1 - tid] : 0;
-    int tot;
-    const int run = block_exclusive_scan(local, sm.scan, &tot);
-    if (tid < kFsSampleBins && run < target && run + local >= target) {
-      sm.sbin = kFsSampleBins - 1 - tid;
-      sm.scount = local;
-      sm.sabove = run;
-      sm.sfloor = 0xffffffffu;
-    }
-    __syncthreads();
-    // The floor: the smallest sample in the selected bin (so every sample of
-    // the bin, and the target-th from the top, is at or above it).
-    const int selbin = sm.sbin;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t k = sample(i);
-      if (k && sbin(k) == selbin) atomicMin(&sm.sfloor, k);
-    }
-    __syncthreads();
-    floor = sm.sfloor;
-    if (sm.scount > 32) {
-      // Crowded bin: refine inside [floor, largest sample of the bin], linear in the key.
-      const uint32_t top = fscale > 0.f ? score_key(fmin + (float)(selbin + 1) / fscale) : smax;
-      const int ssh2 = max(0, (32 - __clz((int)(max(top, floor) - floor))) - 8);
-      const int target2 = target - sm.sabove;
-      for (int b = tid; b < kFsSampleBins; b += NT) sm.scnt[b] = 0u;
-      __syncthreads();
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t k = sample(i);
-        if (k && sbin(k) == selbin)
-          atomicAdd(&sm.scnt[min(kFsSampleBins - 1, (int)((k - floor) >> ssh2))], 1u);
-      }
-      __syncthreads();
-      const int local2 = tid < kFsSampleBins ? (int)sm.scnt[kFsSampleBins - 1 - tid] : 0;
-      const int run2 = block_exclusive_scan(local2, sm.scan, &tot);
-      if (tid < kFsSampleBins && run2 < target2 && run2 + local2 >= target2)
-        sm.sfloor = floor + ((uint32_t)(kFsSampleBins - 1 - tid) << ssh2);
-      __syncthreads();
-      floor = sm.sfloor;
-    }
-  }
-
-  // Histogram of the keys >= floor over [floor, kmax].
-  const int sh2 = max(0, (32 - __clz((int)(kmax - floor))) - 11);   // range >> sh2 < 2048
-  auto bin_of = [&](uint32_t k) { return (int)((k - floor) >> sh2); };
+  // Bins linear in the score over [smallest, largest key]: a normal-like row
+  // leaves a few dozen keys in the bin of the K-th.  Monotone in the key (a
+  // rounded difference, a rounded positive product and a truncation never
+  // reverse the order of two scores).  Same values in every thread.
+  const float fmin = key_score(sm.kmin), fmax = key_score(sm.kmax);
+  const float fscale = __fdividef((float)kFsBins, fmax - fmin);
+  if (!(fmax > fmin) || !isfinite(fmin) || !isfinite(fmax) || !isfinite(fscale)) return false;
+  auto bin_of = [&](uint32_t k) {
+    return min(kFsBins - 1, (int)__float2uint_rz((key_score(k) - fmin) * fscale));
+  };
 #pragma unroll
   for (int j = 0; j < V; ++j)
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      if (key[j][c] >= floor && key[j][c]) atomicAdd(&sm.bins[bin_of(key[j][c])], 1u);
+      if (key[j][c]) atomicAdd(&sm.bins[bin_of(key[j][c])], 1u);
   __syncthreads();
   int total;
   {
@@ -200,7 +114,7 @@ __device__ bool fast_select(const uint32_t (&key)[V][4], int n, int K, uint32_t 
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint32_t k = key[j][c];
-      bm |= (uint32_t)(k >= floor && k && bin_of(k) == bstar) << (4 * j + c);
+      bm |= (uint32_t)(k && bin_of(k) == bstar) << (4 * j + c);
     }
   if (__any_sync(kFull, bm != 0u)) {   // most warps hold no member
     const int mine = __popc(bm);

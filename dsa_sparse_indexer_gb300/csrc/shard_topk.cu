@@ -8,8 +8,9 @@
 // One CTA per (shard, row); the winners are written in ascending slot order
 // (ties on the score go to the smaller slot, i.e. the smaller global id).
 // Local ranges of up to 16384 slots take the throughput kernel below
-// (topk_fast_kernel): keys in registers, the exact threshold from a sampled
-// floor (fast_select.cuh), slot-ordered placement through shared memory.
+// (topk_fast_kernel): keys in registers, the exact threshold from one
+// histogram linear in the score and a ranking of its threshold bin
+// (fast_select.cuh), slot-ordered placement through shared memory.
 // Longer ranges are staged in shared memory with bulk async copies (TMA) or
 // read from global memory, and a radix select with an ordered ballot sweep
 // picks the winners (shard_topk_kernel, local_topk.cuh).  The standalone pack
@@ -114,15 +115,15 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 // per thread; NT = 512 or 1024 threads).  Each thread keeps V float4 of the
 // range as score keys in registers (slot e = base + 4 (j NT + tid) + c).  The
 // exact threshold (key, slot) comes from fast_select (fast_select.cuh: a
-// sampled floor, a histogram over the keys above it, a ranking of the
-// threshold bin): a slot wins if its key is above the threshold key, or equal
+// histogram of the keys linear in the score over their range, a ranking of
+// the threshold bin): a slot wins if its key is above the threshold key, or equal
 // to it at a slot no later than the threshold slot.  The winners are then
 // placed in slot order: per-thread counts for each of the V float4 rows,
 // packed into one word, take one warp scan, and a small table gives each
 // (row, warp) its output offset; each thread drops its winners' (key, slot)
 // at their output positions in shared memory, and all threads then write the
-// outputs with coalesced stores.  Rows where the floor misses or the
-// threshold bin is crowded fall back to the radix select over the registers.
+// outputs with coalesced stores.  Rows with an infinite score or a crowded
+// threshold bin fall back to the radix select over the registers.
 // ---------------------------------------------------------------------------
 using ull = unsigned long long;
 constexpr int kTMaxK = 2048;     // largest K
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
   auto slot = [&](int j, int c) { return (uint32_t)(base + (j * NT + tid) * 4 + c); };
 
   FastSelectResult fs;
-  if (!fast_select<NT, V>(key, n, K, kmn, kmx, slot, sm.f.sel, &fs)) {
+  if (!fast_select<NT, V>(key, K, kmn, kmx, slot, sm.f.sel, &fs)) {
     __syncthreads();   // the fallback's shared memory overlaps the selection's
     topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, emit);
     return;

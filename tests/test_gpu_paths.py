@@ -1,12 +1,14 @@
 """GPU parity of the throughput kernels' fallback paths on crafted rows.
 
-The throughput merge and local top-K set a floor from keys at fixed sample
-positions.  These rows are built so that the estimate misses in each way the
-kernels handle: the floor lands above the K-th key (the merge takes every
-valid candidate again, the local top-K its radix select), too many keys sit
-at or above it (the merge's list overflows into its radix path), no floor is
-needed at all, and the threshold bin is crowded with ties.  Each result is
-compared element by element with the oracle.
+The throughput merge sets a floor from candidates at fixed sample positions;
+these rows make the estimate miss in each way it handles: the floor lands
+above the K-th key (every valid candidate is taken again), too many keys sit
+at or above it (the list overflows into the radix path), no floor is needed
+at all, and the threshold bin is crowded with ties.  The throughput local
+top-K bins the keys linearly in the score over their range; its rows hold an
+infinite score, an outlier that puts nearly every key into one bin, coarse
+ties, and a block of high scores.  Each result is compared element by element
+with the oracle.
 """
 import numpy as np
 import pytest
@@ -106,11 +108,10 @@ def _topk_check(row: np.ndarray, n: int, K: int) -> None:
     np.testing.assert_array_equal(local_idx.cpu().numpy()[0, 0], OX.shard_topk(row, 0, n, K))
 
 
-def test_local_topk_floor_above_the_kth_key_falls_back():
-    """Local ranges up to 8192 slots run 512 threads holding four float4 rows;
-    thread t samples lane i of row i, slot 4 (512 i + t) + i.  Those slots
-    score high: fewer than K keys lie at or above the floor, so the radix
-    select over the registers takes over."""
+def test_local_topk_a_block_of_high_scores():
+    """A quarter of the slots (a regular pattern over the register layout)
+    score far above the rest: the K-th key lies in the bulk, far below the
+    block, and the bins between them stay empty."""
     rng = np.random.default_rng(5)
     n, K = 7000, 2048
     row = rng.standard_normal(8192).astype(np.float32)
@@ -127,4 +128,25 @@ def test_local_topk_crowded_threshold_bin():
     rng = np.random.default_rng(6)
     n, K = 8000, 1024
     row = (np.rint(rng.standard_normal(8192) * 2) / 2).astype(np.float32)
+    _topk_check(row, n, K)
+
+
+@pytest.mark.parametrize("special", [np.inf, -np.inf])
+def test_local_topk_infinite_scores_take_the_radix_select(special):
+    """An infinite score leaves no finite score range to bin: the radix select
+    over the registers takes over (the infinite key still ranks by value)."""
+    rng = np.random.default_rng(7)
+    n, K = 7000, 2048
+    row = rng.standard_normal(8192).astype(np.float32)
+    row[[5, 4000]] = special
+    _topk_check(row, n, K)
+
+
+def test_local_topk_an_outlier_crowds_one_bin():
+    """One score of 1e30: every other key falls into the lowest bin, far more
+    than the ranking handles, so the radix select takes over."""
+    rng = np.random.default_rng(8)
+    n, K = 8000, 512
+    row = rng.standard_normal(8192).astype(np.float32)
+    row[123] = 1e30
     _topk_check(row, n, K)
