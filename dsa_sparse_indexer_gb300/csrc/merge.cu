@@ -668,6 +668,196 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
   }
 }
 
+// ---------------------------------------------------------------------------
+// Rows of up to 16 candidates per thread (C <= 16 NT; NT = 512 or 1024):
+// every candidate stays in registers as (score key, ~id), so neither a floor
+// nor a list is needed.  One pass gives the number of valid candidates and the
+// range of their score keys; one 2048-bin histogram, the bins linear in the
+// score over that range (monotone in the key: a rounded difference, a rounded
+// positive product and a truncation never reverse two scores), and a scan from
+// the top bin down give every bin above the bin b* of the need-th key its
+// output range.  Winners above b* are scattered into those ranges and ranked
+// inside their bins, b*'s members among themselves.  Rows with an infinite
+// score, a single score value or crowded bins take merge_crowded.  Twice the
+// threads of merge_fast_kernel per row: for batches that fit one wave, where a
+// row's latency, not the throughput of many rows, sets the time.
+// ---------------------------------------------------------------------------
+constexpr int kLinPer = 16;   // candidates per thread
+
+template <int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT)
+    merge_lin_kernel(const float* __restrict__ cand, int C, int K, int32_t* __restrict__ ids,
+                     float* __restrict__ scores) {
+  extern __shared__ __align__(16) unsigned char merge_smem[];
+  MergeFastSmem& sm = *reinterpret_cast<MergeFastSmem*>(merge_smem);
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int r = blockIdx.x;
+  const float* row = cand + (int64_t)r * C * 2;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  int32_t* out_ids = ids + (int64_t)r * K;
+  float* out_sc = scores ? scores + (int64_t)r * K : nullptr;
+
+  // Float4 q = j NT + tid holds candidates 2 q and 2 q + 1.
+  uint32_t key[kLinPer], nid[kLinPer];   // score key (0: no candidate) and ~id
+  {
+    float4 v[kLinPer / 2];
+#pragma unroll
+    for (int j = 0; j < kLinPer / 2; ++j) {
+      const int q = j * NT + tid;
+      v[j] = 2 * q < C ? __ldg(row4 + q)
+                       : make_float4(0.f, __int_as_float(-1), 0.f, __int_as_float(-1));
+    }
+#pragma unroll
+    for (int j = 0; j < kLinPer / 2; ++j) {
+      const int i0 = __float_as_int(v[j].y), i1 = __float_as_int(v[j].w);
+      key[2 * j] = i0 >= 0 ? score_key(v[j].x) : 0u;
+      key[2 * j + 1] = i1 >= 0 ? score_key(v[j].z) : 0u;
+      nid[2 * j] = ~(uint32_t)i0;
+      nid[2 * j + 1] = ~(uint32_t)i1;
+    }
+  }
+  for (int b = tid; b < kMBins; b += NT) sm.h.end[b] = 0u;
+  if (tid == 0) {
+    sm.nlist = 0;
+    sm.nb = 0;
+    sm.nwin = 0;
+    sm.bmax[0] = sm.bmax[1] = 0;
+    sm.lmin = 0xffffffffu;
+    sm.kmax = 0u;
+  }
+  {
+    int nv = 0;
+    uint32_t mn = 0xffffffffu, mx = 0u;
+#pragma unroll
+    for (int i = 0; i < kLinPer; ++i)
+      if (key[i]) {
+        ++nv;
+        mn = min(mn, key[i]);
+        mx = max(mx, key[i]);
+      }
+    nv = __reduce_add_sync(kFull, nv);
+    mn = __reduce_min_sync(kFull, mn);
+    mx = __reduce_max_sync(kFull, mx);
+    __syncthreads();
+    if (lane == 0 && nv) {
+      atomicAdd(&sm.nlist, nv);
+      atomicMin(&sm.lmin, mn);
+      atomicMax(&sm.kmax, mx);
+    }
+  }
+  __syncthreads();
+  const int valid = sm.nlist;
+  const int need = min(K, valid);
+  bool ranked = false;   // winners ordered in out[] by position
+  if (need > 0) {
+    const float fmin = key_score(sm.lmin), fmax = key_score(sm.kmax);
+    const float fscale = __fdividef((float)kMBins, fmax - fmin);
+    // Same values in every thread: uniform.
+    const bool lin = fmax > fmin && isfinite(fmin) && isfinite(fmax) && isfinite(fscale);
+    auto bin = [&](uint32_t k) {
+      return min(kMBins - 1, (int)__float2uint_rz((key_score(k) - fmin) * fscale));
+    };
+    if (lin) {
+#pragma unroll
+      for (int i = 0; i < kLinPer; ++i)
+        if (key[i]) atomicAdd(&sm.h.end[bin(key[i])], 1u);
+      __syncthreads();
+      // Scan from the top bin down: output ranges, b*, the largest bin above b*.
+      {
+        constexpr int per = kMBins / NT;
+        const int g = kMBins - per * (tid + 1);
+        int cnt[per];
+        int local = 0;
+#pragma unroll
+        for (int j = 0; j < per; ++j) {
+          cnt[j] = (int)sm.h.end[g + per - 1 - j];
+          local += cnt[j];
+        }
+        int tot;
+        int run = block_exclusive_scan(local, sm.scan, &tot);
+        int mx = 0;
+#pragma unroll
+        for (int j = 0; j < per; ++j) {
+          const int b = g + per - 1 - j;
+          sm.h.end[b] = (uint32_t)run;
+          if (run < need && run + cnt[j] >= need) {
+            sm.bstar = b;
+            sm.above = run;
+            sm.bcnt = cnt[j];
+          } else if (run + cnt[j] < need) {
+            mx = max(mx, cnt[j]);
+          }
+          run += cnt[j];
+        }
+        if (mx > kFineCap) atomicMax(&sm.bmax[0], mx);
+      }
+      __syncthreads();
+      const int bstar = sm.bstar, above = sm.above, bcnt = sm.bcnt;
+      ranked = bcnt <= kRankCap && sm.bmax[0] <= kFineCap;
+      if (ranked) {
+        const int take = need - above;   // members of b* that win
+#pragma unroll
+        for (int i = 0; i < kLinPer; ++i) {
+          if (!key[i]) continue;
+          const int b = bin(key[i]);
+          const ull x = ((ull)key[i] << 32) | nid[i];
+          if (b > bstar) sm.win[atomicAdd(&sm.h.end[b], 1u)] = x;
+          else if (b == bstar) sm.bst[atomicAdd(&sm.nb, 1)] = x;
+        }
+        __syncthreads();
+        for (int p = tid; p < above; p += NT) {
+          const ull x = sm.win[p];
+          const int b = bin((uint32_t)(x >> 32));
+          const int e = (int)sm.h.end[b], s0 = b == kMBins - 1 ? 0 : (int)sm.h.end[b + 1];
+          sm.u.out[s0 + count_above(sm.win, s0, e, x)] = x;
+        }
+        for (int i = tid; i < bcnt; i += NT) {
+          const ull x = sm.bst[i];
+          const int rank = count_above(sm.bst, 0, bcnt, x);
+          if (rank < take) sm.u.out[above + rank] = x;
+        }
+        __syncthreads();
+      }
+    }
+    if (!ranked) {
+      __syncthreads();   // the select reuses the bin counters
+      merge_crowded<NT>(row, C, 1u, valid, need, sm, out_ids, out_sc);
+    }
+  }
+  // Write the ranked winners and the -1 / -inf padding, 4 positions a thread.
+  const bool vec = ((reinterpret_cast<uintptr_t>(out_ids) | reinterpret_cast<uintptr_t>(out_sc)) &
+                    15u) == 0;
+  const int first = ranked ? 0 : need;   // the crowded path wrote [0, need) itself
+  for (int p0 = 4 * tid; p0 < K; p0 += 4 * NT) {
+    if (p0 + 4 <= first) continue;
+    int32_t oi[4];
+    float os[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int p = p0 + u;
+      if (ranked && p < need) {
+        const ull x = sm.u.out[p];
+        oi[u] = (int32_t)~(uint32_t)x;
+        os[u] = key_score((uint32_t)(x >> 32));
+      } else {
+        oi[u] = -1;
+        os[u] = -INFINITY;
+      }
+    }
+    if (vec && p0 >= first) {
+      *reinterpret_cast<int4*>(out_ids + p0) = make_int4(oi[0], oi[1], oi[2], oi[3]);
+      if (out_sc) *reinterpret_cast<float4*>(out_sc + p0) = make_float4(os[0], os[1], os[2], os[3]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (p0 + u < first) continue;
+        out_ids[p0 + u] = oi[u];
+        if (out_sc) out_sc[p0 + u] = os[u];
+      }
+    }
+  }
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -693,6 +883,14 @@ extern "C" dsa_status dsa_merge_topk_stable(const float* cand, int rows, int C, 
                                           (size_t)smem, stream, 0, cand, C, K, ids, scores);
       return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
     };
+    // Batches that fit one wave are latency-bound: more threads per row.
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    if (C <= kLinPer * 512 && rows <= 2 * sms) return launch_fast(merge_lin_kernel<512>, 512);
+    if (C > kLinPer * 512 && C <= kLinPer * 1024 && rows <= sms)
+      return launch_fast(merge_lin_kernel<1024>, 1024);
     if (C <= 32 * 256) return launch_fast(merge_fast_kernel<256>, 256);
     if (C <= 32 * 512) return launch_fast(merge_fast_kernel<512>, 512);
     return launch_fast(merge_fast_kernel<1024>, 1024);

@@ -1,7 +1,10 @@
 """GPU parity of the throughput kernels' fallback paths on crafted rows.
 
-The throughput merge sets a floor from candidates at fixed sample positions;
-these rows make the estimate miss in each way it handles: the floor lands
+Every merge row runs twice: alone (a batch that fits one wave takes the
+latency kernel: all candidates in registers, one histogram linear in the
+score over their range) and tiled to 400 rows (the throughput kernel).  The
+throughput merge sets a floor from candidates at fixed sample positions; these
+rows make the estimate miss in each way it handles: the floor lands
 above the K-th key (every valid candidate is taken again), too many keys sit
 at or above it (the list overflows into the radix path), no floor is needed
 at all, and the threshold bin is crowded with ties.  The throughput local
@@ -18,19 +21,27 @@ from oracle import indexer as OX
 pytestmark = pytest.mark.gpu
 
 
+# Batches that fit one wave take the latency kernel (all candidates in
+# registers); larger ones the throughput kernel (sampled floor and list).
+ROWS_LATENCY, ROWS_THROUGHPUT = 1, 400
+
+
 def _merge_check(scores: np.ndarray, ids: np.ndarray, K: int) -> None:
     import torch
 
     import dsa_sparse_indexer_gb300 as dsa
     cand = np.stack([scores.astype(np.float32), ids.astype(np.int32).view(np.float32)], -1)
-    t = torch.from_numpy(np.ascontiguousarray(cand[None])).cuda()
-    err = dsa.new_error_flags("cuda")
-    got_ids, got_sc = dsa.merge_topk_stable(t, K, want_scores=True, err_flags=err)
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
     want_ids, want_sc = OX.merge(scores, ids, K)
-    np.testing.assert_array_equal(got_ids.cpu().numpy()[0], want_ids)
-    np.testing.assert_array_equal(got_sc.cpu().numpy()[0], want_sc)
+    for rows in (ROWS_LATENCY, ROWS_THROUGHPUT):
+        t = torch.from_numpy(np.tile(cand[None], (rows, 1, 1)))
+        err = dsa.new_error_flags("cuda")
+        got_ids, got_sc = dsa.merge_topk_stable(t.cuda(), K, want_scores=True, err_flags=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        got_ids, got_sc = got_ids.cpu().numpy(), got_sc.cpu().numpy()
+        for r in (0, rows - 1):
+            np.testing.assert_array_equal(got_ids[r], want_ids)
+            np.testing.assert_array_equal(got_sc[r], want_sc)
 
 
 def _merge_sampled(C: int, nt: int = 256) -> np.ndarray:
@@ -89,6 +100,27 @@ def test_merge_crowded_threshold_bin(K):
     rng = np.random.default_rng(4 + K)
     C = 4 * K
     scores = (np.rint(rng.standard_normal(C) * 2) / 2).astype(np.float32)
+    _merge_check(scores, _unique_ids(rng, C), K)
+
+
+@pytest.mark.parametrize("special", [np.inf, -np.inf])
+def test_merge_infinite_scores(special):
+    """Valid candidates scoring +-inf: no finite range to bin, so the latency
+    kernel takes the exact radix path; the throughput kernel's floor handles them."""
+    rng = np.random.default_rng(9)
+    C, K = 8192, 2048
+    scores = rng.standard_normal(C).astype(np.float32)
+    scores[[3, 4000, 8000]] = special
+    _merge_check(scores, _unique_ids(rng, C), K)
+
+
+def test_merge_an_outlier_crowds_one_bin():
+    """One candidate at 1e30: every other key falls into the lowest bin of a
+    range-wide histogram."""
+    rng = np.random.default_rng(10)
+    C, K = 8192, 512
+    scores = rng.standard_normal(C).astype(np.float32)
+    scores[77] = 1e30
     _merge_check(scores, _unique_ids(rng, C), K)
 
 
