@@ -6,11 +6,14 @@
 // buffer; topk_indices overwritten with global ids, -1 for padding).
 //
 // One CTA per row; every candidate is ranked by its 64-bit key
-// (score_key << 32 | ~id), so ties go to the smaller id.  Rows of up to 32
-// candidates per thread (C <= 32768) take the throughput kernel
-// (merge_fast_kernel): a sampled floor, a compact list of the candidates above
-// it, bins over the list's key range that give the winners' output ranges,
-// and ranking inside each (small) bin.  Larger rows (merge_kernel) are read
+// (score_key << 32 | ~id), so ties go to the smaller id.  Batches that fit one
+// wave (up to 16 candidates per thread) take the latency kernel
+// (merge_lin_kernel): every candidate in registers, one histogram linear in
+// the score over their range.  Otherwise rows of up to 32 candidates per
+// thread (C <= 32768) take the throughput kernel (merge_fast_kernel): a
+// sampled floor, a compact list of the candidates above it, bins over the
+// list's key range that give the winners' output ranges, and ranking inside
+// each (small) bin (both kernels rank the same way).  Larger rows (merge_kernel) are read
 // from global memory (L2 after the first pass): a radix select on the score
 // key, and, only when the K-th score is tied, a second one on the inverted
 // id; the K winners are then put in rank order by a bitonic sort.
