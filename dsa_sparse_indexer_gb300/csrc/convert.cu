@@ -129,17 +129,16 @@ __global__ void __launch_bounds__(kConvThreads)
 }
 
 // ---------------------------------------------------------------------------
-// Few shards (S <= 8): one 128-thread CTA per row, each warp owning a quarter
-// of the id list in chunks of 32.  One pass computes every id's owner and
-// physical slot and, per chunk, its position among the warp's ids of the same
-// shard: a ballot per shard, the lane's own shard's ballot counted below it,
-// plus that shard's running count (held by lane s and read with a shuffle).
-// A scan over the four warps' per-shard totals then gives final positions.
+// Few shards (S <= 8): one CTA per row (128 threads, or 512 for a batch that
+// fits one wave), each warp owning a contiguous piece of the id list in
+// chunks of 32.  One pass computes every id's owner and physical slot and,
+// per chunk, its position among the warp's ids of the same shard: a ballot per
+// shard, the lane's own shard's ballot counted below it, plus that shard's
+// running count (held by lane s and read with a shuffle).  A scan over the
+// warps' per-shard totals then gives final positions.
 // ---------------------------------------------------------------------------
-constexpr int kCvThreads = 128;
-constexpr int kCvWarps = kCvThreads / 32;
-constexpr int kCvMaxChunks = 2048 / kCvThreads;   // 16 chunks of 32 ids per warp for K = 2048
 constexpr int kCvMaxS = 8;
+constexpr int kCvMaxK = 2048;
 
 // id -> (owner, local slot / block size, local slot mod block size).  When S,
 // I and the block size are powers of two (kPow2) the divisions are shifts by
@@ -159,20 +158,24 @@ __device__ __forceinline__ void map_id(uint32_t id, const ShardMath& sh, const F
   }
 }
 
-template <bool kPow2>
-__global__ void __launch_bounds__(kCvThreads)
+// NT threads per row: 128 for large batches, 512 for batches that fit one wave
+// (where a row's latency sets the time).
+template <int NT, bool kPow2>
+__global__ void __launch_bounds__(NT)
     convert_few_kernel(const int32_t* __restrict__ ids, int rows, int K, int S,
                        const int32_t* __restrict__ bt, int reqs, int max_blocks, int bs,
                        const int32_t* __restrict__ row_to_req, int32_t* __restrict__ slots,
                        int32_t* __restrict__ counts, uint32_t* flags, const ShardMath sh,
                        const FastDiv fbs) {
+  constexpr int kCvWarps = NT / 32;
+  constexpr int kCvMaxChunks = kCvMaxK / NT;   // chunks of 32 ids per warp for K = 2048
   __shared__ int wbase[kCvWarps][kCvMaxS];   // per-warp counts, then exclusive bases
   __shared__ int total[kCvMaxS];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.x;
   const int req = row_to_req ? __ldg(row_to_req + r) : r;
   const bool req_ok = req >= 0 && req < reqs;
-  const int nch = K / kCvThreads;            // chunks per warp
+  const int nch = K / NT;                    // chunks per warp
   const int32_t* mine = ids + (int64_t)r * K + warp * nch * 32;
   const unsigned lt = lanemask_lt();
 
@@ -254,9 +257,9 @@ __global__ void __launch_bounds__(kCvThreads)
       const int a0 = min(K, (t0 + 3) & ~3);
       if (tid < a0 - t0) dst[t0 + tid] = -1;
       int4* d4 = reinterpret_cast<int4*>(dst + a0);
-      for (int j = tid; j < (K - a0) / 4; j += kCvThreads) d4[j] = make_int4(-1, -1, -1, -1);
+      for (int j = tid; j < (K - a0) / 4; j += NT) d4[j] = make_int4(-1, -1, -1, -1);
     } else {
-      for (int j = t0 + tid; j < K; j += kCvThreads) dst[j] = -1;
+      for (int j = t0 + tid; j < K; j += NT) dst[j] = -1;
     }
   }
   if (counts && tid < S) counts[(int64_t)tid * rows + r] = total[tid];
@@ -281,9 +284,16 @@ extern "C" dsa_status dsa_convert_index_compact(const int32_t* ids, int rows, in
   if ((int64_t)I * S > (int64_t)INT32_MAX) return DSA_ERR_UNSUPPORTED;
   if (S <= kCvMaxS) {
     auto pow2 = [](int v) { return (v & (v - 1)) == 0; };
-    auto kern = pow2(S) && pow2(I) && pow2(block_size) ? convert_few_kernel<true>
-                                                        : convert_few_kernel<false>;
-    const cudaError_t e = launch_kernel(kern, dim3((unsigned)rows), dim3(kCvThreads), 0, stream,
+    const bool p2 = pow2(S) && pow2(I) && pow2(block_size);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    // Batches that fit one wave are latency-bound: more threads per row.
+    const bool wide = rows <= 2 * sms;
+    auto kern = wide ? (p2 ? convert_few_kernel<512, true> : convert_few_kernel<512, false>)
+                     : (p2 ? convert_few_kernel<128, true> : convert_few_kernel<128, false>);
+    const cudaError_t e = launch_kernel(kern, dim3((unsigned)rows), dim3(wide ? 512 : 128), 0, stream,
                                         0, ids, rows, K, S, block_table, reqs, max_blocks,
                                         block_size, row_to_req, slots, counts, err_flags,
                                         ShardMath(S, I), FastDiv((uint32_t)block_size));
