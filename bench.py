@@ -22,7 +22,8 @@ the five workloads), called through the C ABI (ctypes).  Prints one JSON line.
                combine) the combined output and its LSE
   roofline     the step's dominant kernel: algorithmic bytes per launch /
                its mean CUDA-event duration, against the measured HBM peak
-  cpu_baseline the oracle (numpy, one core) on a bounded sample of the same batch
+  cpu_baseline the oracle (numpy, one core) on a bounded sample of the same batch;
+               cpu_baseline_all_cores the same over rows on every host core
 
 `--impl reference` times the oracle itself as the reference arm.
 Under torchrun (N > 1) each rank runs its own batch (replicas, weak scaling);
@@ -381,6 +382,92 @@ def cpu_baseline(cfg, inp: dict, budget_s: float = 10.0, path: str = "fused") ->
     return {"value": done / dt, "unit": metric_for(path)[1], "cores": 1, "kind": "oracle",
             "sample": f"{done} rows of the {cfg.name} batch ({what} per row, numpy, one "
                       f"thread), {dt:.1f} s"}
+
+
+# The oracle over rows on every host core: one spawned process per core (the
+# GPU context is already open, so no fork), each reading the batch from shared
+# memory and running whole rows until the budget is spent.
+_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+_WORKER: dict = {}
+
+
+def _share_arrays(inp: dict):
+    from multiprocessing import shared_memory
+    blocks, spec = [], {}
+    for k, a in inp.items():
+        if isinstance(a, np.ndarray):
+            shm = shared_memory.SharedMemory(create=True, size=max(1, a.nbytes))
+            np.ndarray(a.shape, a.dtype, buffer=shm.buf)[...] = a
+            blocks.append(shm)
+            spec[k] = ("shm", shm.name, a.shape, a.dtype.str)
+        else:
+            spec[k] = ("obj", a)
+    return blocks, spec
+
+
+def _oracle_worker_init(workload: str, path: str, spec: dict, barrier) -> None:
+    from multiprocessing import shared_memory
+    inp, blocks = {}, []
+    for k, v in spec.items():
+        if v[0] == "shm":   # spawned children share the parent's resource tracker,
+            shm = shared_memory.SharedMemory(name=v[1])   # which unlinks at the end
+            blocks.append(shm)
+            inp[k] = np.ndarray(v[2], np.dtype(v[3]), buffer=shm.buf)
+        else:
+            inp[k] = v[1]
+    cfg = W.CONFIGS[workload]
+    oracle_rows(inp, cfg, np.array([0]), path)          # imports and first-call costs
+    _WORKER.update(cfg=cfg, inp=inp, path=path, barrier=barrier, blocks=blocks)
+
+
+def _oracle_worker_rows(task):
+    first, budget_s = task
+    w = _WORKER
+    w["barrier"].wait(timeout=300)
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        oracle_rows(w["inp"], w["cfg"], np.array([(first + done) % w["cfg"].rows]), w["path"])
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return done, time.perf_counter() - t0
+
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def cpu_baseline_all_cores(cfg, inp: dict, budget_s: float = 10.0,
+                           path: str = "fused", cores: int | None = None) -> dict:
+    """The oracle, as it stands, over rows of the same batch on every host core."""
+    import multiprocessing as mp
+    n = cores or host_cores()
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(n)
+    blocks, spec = _share_arrays(inp)
+    saved = {k: os.environ.get(k) for k in _THREAD_VARS}
+    os.environ.update({k: "1" for k in _THREAD_VARS})
+    try:
+        with ctx.Pool(n, initializer=_oracle_worker_init,
+                      initargs=(cfg.name, path, spec, barrier)) as pool:
+            res = pool.map(_oracle_worker_rows,
+                           [(i * max(1, cfg.rows // n), budget_s) for i in range(n)], chunksize=1)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+        for b in blocks:
+            b.close()
+            b.unlink()
+    done = sum(d for d, _ in res)
+    dt = max(t for _, t in res)
+    return {"value": done / dt, "unit": metric_for(path)[1], "cores": n, "kind": "oracle",
+            "sample": f"{done} rows of the {cfg.name} batch on {n} processes (all steps per "
+                      f"row, numpy single-threaded in each; {host_cores()} host cores), "
+                      f"{dt:.1f} s"}
 
 
 def run_reference(args, world, rank):
@@ -766,17 +853,14 @@ def main(argv=None) -> int:
         for hr, dr in zip(h_results, results):
             hr.copy_(dr, non_blocking=True)
 
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    barrier(world)
-    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    x0.record(stream)
-    for i in range(args.e2e_steps):
-        e2e_step(i)
-    x1.record(stream)
-    torch.cuda.synchronize()
-    e2e_seq_ms = max_over_ranks(x0.elapsed_time(x1), world) / args.e2e_steps
+    def e2e_sequential(n):
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for i in range(n):
+            e2e_step(i)
+        x1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(x0.elapsed_time(x1), world) / n
 
     # The same steps pipelined as a serving loop runs them: step i+1's inputs go
     # up on one stream while step i computes and its result comes back on
@@ -815,13 +899,27 @@ def main(argv=None) -> int:
                 out_done[i] = e_o
         return out_done[n - 1]
 
+    def e2e_overlapped(n):
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = e2e_pipelined(n, first=p0)
+        torch.cuda.synchronize()
+        return max_over_ranks(p0.elapsed_time(p1), world) / n
+
+    # Warm both schedules, pick the faster on a short trial (the host link's
+    # rate under overlapping copies varies from box to box), then time both in
+    # full; the trial decides which one is reported, not the full timings.
+    for i in range(3):
+        e2e_step(i)
     e2e_pipelined(3)
     torch.cuda.synchronize()
     barrier(world)
-    p0 = torch.cuda.Event(enable_timing=True)
-    p1 = e2e_pipelined(args.e2e_steps, first=p0)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(p0.elapsed_time(p1), world) / args.e2e_steps
+    trial = max(3, min(10, args.e2e_steps // 10))
+    pipelined_won = e2e_overlapped(trial) <= e2e_sequential(trial)
+    barrier(world)
+    e2e_seq_ms = e2e_sequential(args.e2e_steps)
+    barrier(world)
+    e2e_pipe_ms = e2e_overlapped(args.e2e_steps)
+    e2e_ms = e2e_pipe_ms if pipelined_won else e2e_seq_ms
     e2e_value = world * R / (e2e_ms / 1e3)
 
     metric, unit = metric_for(args.path)
@@ -848,8 +946,13 @@ def main(argv=None) -> int:
         "launch_loop_ms_per_step": loop_ms_per_step,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
-                "schedule": "pinned host buffers through the C ABI; step i+1's inputs copied "
-                            "while step i computes and its result is read back (three streams)",
+                "schedule": ("pinned host buffers through the C ABI; step i+1's inputs copied "
+                             "while step i computes and its result is read back (three streams)"
+                             if pipelined_won else
+                             "pinned host buffers through the C ABI; each step's input copy, "
+                             "kernels and result copy in order on one stream"),
+                "schedule_choice": f"the faster of the two on a {trial}-step trial after warm-up",
+                "pipelined_ms_per_step": e2e_pipe_ms,
                 "sequential_ms_per_step": e2e_seq_ms},
         "gpu_launches": nk * args.steps,
         "clocks": clocks.summary(t_wall0, t_wall1),
@@ -860,6 +963,11 @@ def main(argv=None) -> int:
             if args.path == "attention":
                 base_inp["cache"] = cache_host
             result["cpu_baseline"] = cpu_baseline(cfg, base_inp, path=args.path)
+            try:
+                result["cpu_baseline_all_cores"] = cpu_baseline_all_cores(cfg, base_inp,
+                                                                          path=args.path)
+            except Exception as e:   # the single-thread figure above still stands
+                result["cpu_baseline_all_cores"] = {"unavailable": f"{type(e).__name__}: {e}"}
         print(json.dumps(result))
     if world > 1:
         import torch.distributed as dist

@@ -62,3 +62,13 @@ def test_profile_traffic_only_while_sources_match(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
     assert bench.profiled_traffic("indexer_fused", "decode") is None
     assert bench.profiled_traffic("no_such_kernel", "decode") is None
+
+
+def test_oracle_over_all_cores_counts_rows_of_every_process():
+    """The all-cores CPU baseline: spawned processes read the batch from shared
+    memory, run whole rows and report how many they finished."""
+    cfg = W.CONFIGS["tiny"]
+    inp = bench.host_inputs(cfg, 0, "steps")
+    res = bench.cpu_baseline_all_cores(cfg, inp, budget_s=0.3, path="steps", cores=2)
+    assert res["cores"] == 2 and res["kind"] == "oracle" and res["unit"] == "rows/s"
+    assert res["value"] > 0 and "processes" in res["sample"]
