@@ -1,18 +1,30 @@
-// The K-th largest of register-resident score keys, exactly, without a radix
-// pass over all keys (sm_103a).
+// The K-th largest of register-resident scores, exactly, without a radix pass
+// over all of them (sm_103a).
 //
-// Each of the NT threads holds V float4 rows of keys, key[j][c] at a slot
-// given by the caller (slots order ties: the smaller slot ranks first); key 0
-// marks an empty slot.  Steps:
-//   1. a 2048-bin histogram of every key, the bins linear in the score between
-//      the smallest and the largest key, locates the bin b* holding the K-th
-//      key (a normal-like row leaves a few dozen keys there);
-//   2. the members of b* (at most kFsRankCap) are ranked on (key, ~slot); the
-//      one with K - 1 - (keys above b*) keys above it is the threshold.
+// Each of the NT threads holds V float4 rows of scores, f[j][c] at a slot
+// given by the caller (slots order ties: the smaller slot ranks first); -inf
+// marks an empty slot (the fast path runs only when every real score is
+// finite).  Steps:
+//   1. a 2048-bin histogram of every score, the bins linear in the score
+//      between the smallest and the largest, locates the bin b* holding the
+//      K-th score (a normal-like row leaves a few dozen scores there);
+//   2. the members of b* (at most kFsRankCap) are ranked on (score key, ~slot);
+//      the one with K - 1 - (scores above b*) members above it is the
+//      threshold.
 // Bins other than b* may be crowded; only b* is ranked.  Returns false when a
-// score is infinite, the range is empty or b* is crowded (an outlier
-// stretching the range, heavy ties): the caller then falls back to a radix
-// select.
+// score is infinite, the range is empty or too narrow for the bin map, b* is
+// the lowest bin or crowded (an outlier stretching the range, heavy ties):
+// the caller then falls back to a radix select.
+//
+// The bin of a score f is read off the bits of v = fma(f, scale, c), where c
+// puts the smallest score at 2^23 + 1 and scale = 2045 / range keeps the
+// largest below 2^23 + 2047: every float in [2^23, 2^24) is an integer, so the
+// FFMA's rounding replaces a float-to-int conversion and the low 11 bits of v
+// are the bin (the exponent field of 2^23 has none set).  A rounded product
+// and sum never reverse two scores, so bins are monotone in the score; the
+// two ends are checked once, which bounds every score in between.  An empty
+// slot (-inf) gives v = -inf, whose low 11 bits are 0: it only adds to bin 0,
+// which is never b* on this path.
 #pragma once
 
 #include "common.cuh"
@@ -26,28 +38,38 @@ constexpr int kFsRankCap = 256;
 struct FastSelectSmem {
   uint32_t bins[kFsBins];
   // Stores are 32-bit: 64-bit stores of (key, slot) pairs made the compiler
-  // move the callers' register keys to local memory.
+  // move the callers' register scores to local memory.
   uint32_t bst_k[kFsRankCap];   // members of b*: score key
   uint32_t bst_s[kFsRankCap];   // and slot
   int scan[33];
-  int nb, bstar, above, bcnt, gt, eq;
+  int nb, bstar, above, bcnt, eq;
   uint32_t kmin, kmax;
   unsigned long long thr64;
 };
 
-// Outcome: a slot wins iff key > thr or (key == thr and slot <= last); with
-// kCounts, gt keys are above thr and eq keys equal it (K - gt of the ties win).
+// Outcome: a slot wins iff f > thr or (f == thr and slot <= last); eq scores
+// equal thr (eq == 1: the threshold's own, so every f >= thr wins).
 struct FastSelectResult {
-  uint32_t thr, last;
-  int gt, eq;
+  float thr;
+  uint32_t last;
+  int eq;
 };
 
-// More than K nonzero keys.  kmn / kmx: this thread's smallest nonzero and
-// largest key.  Every thread calls it.  On true it ends with a barrier; on
-// false the caller must synchronise before reusing `sm`.
-template <int NT, int V, bool kCounts = false, typename SlotOf>
-__device__ bool fast_select(const uint32_t (&key)[V][4], int K, uint32_t kmn, uint32_t kmx,
-                            SlotOf slot_of, FastSelectSmem& sm, FastSelectResult* out) {
+// The bin of a score: the low 11 bits of fma(f, scale, c) (see above).
+struct LinearBins {
+  float scale, c;
+  __device__ __forceinline__ float v(float f) const { return __fmaf_rn(f, scale, c); }
+  __device__ __forceinline__ int operator()(float f) const {
+    return (int)(__float_as_uint(v(f)) & (uint32_t)(kFsBins - 1));
+  }
+};
+
+// More than K real scores.  fmn / fmx: this thread's smallest and largest real
+// score (+inf / -inf if it holds none).  Every thread calls it.  On true it
+// ends with a barrier; on false the caller must synchronise before reusing sm.
+template <int NT, int V, typename SlotOf>
+__device__ bool fast_select(const float (&f)[V][4], int K, float fmn, float fmx, SlotOf slot_of,
+                            FastSelectSmem& sm, FastSelectResult* out) {
   using ull = unsigned long long;
   const int tid = threadIdx.x, lane = tid & 31;
   for (int b = tid; b < kFsBins; b += NT) sm.bins[b] = 0u;
@@ -57,7 +79,8 @@ __device__ bool fast_select(const uint32_t (&key)[V][4], int K, uint32_t kmn, ui
     sm.kmax = 0u;
   }
   {
-    const uint32_t mn = __reduce_min_sync(kFull, kmn), mx = __reduce_max_sync(kFull, kmx);
+    const uint32_t mn = __reduce_min_sync(kFull, score_key(fmn));
+    const uint32_t mx = __reduce_max_sync(kFull, score_key(fmx));
     __syncthreads();
     if (lane == 0) {
       atomicMin(&sm.kmin, mn);
@@ -65,23 +88,19 @@ __device__ bool fast_select(const uint32_t (&key)[V][4], int K, uint32_t kmn, ui
     }
   }
   __syncthreads();
-  // Bins linear in the score over [smallest, largest key]: a normal-like row
-  // leaves a few dozen keys in the bin of the K-th.  Monotone in the key (a
-  // rounded difference, a rounded positive product and a truncation never
-  // reverse the order of two scores).  Same values in every thread.
   const float fmin = key_score(sm.kmin), fmax = key_score(sm.kmax);
-  const float fscale = __fdividef((float)kFsBins, fmax - fmin);
-  if (!(fmax > fmin) || !isfinite(fmin) || !isfinite(fmax) || !isfinite(fscale)) return false;
-  auto bin_of = [&](uint32_t k) {
-    return min(kFsBins - 1, (int)__float2uint_rz((key_score(k) - fmin) * fscale));
-  };
+  constexpr float kTwo23 = 8388608.0f;
+  const float scale = __fdividef(2045.0f, fmax - fmin);
+  const LinearBins bin_of{scale, (kTwo23 + 1.0f) - fmin * scale};
+  // Same values in every thread: all of them return here or none.
+  if (!(fmax > fmin) || !isfinite(fmin) || !isfinite(fmax) || !isfinite(scale) ||
+      !(bin_of.v(fmin) >= kTwo23) || !(bin_of.v(fmax) <= kTwo23 + (float)(kFsBins - 1)))
+    return false;
 #pragma unroll
   for (int j = 0; j < V; ++j)
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (key[j][c]) atomicAdd(&sm.bins[bin_of(key[j][c])], 1u);
+    for (int c = 0; c < 4; ++c) atomicAdd(&sm.bins[bin_of(f[j][c])], 1u);
   __syncthreads();
-  int total;
   {
     constexpr int per = kFsBins / NT;
     const int g = kFsBins - per * (tid + 1);
@@ -92,6 +111,7 @@ __device__ bool fast_select(const uint32_t (&key)[V][4], int K, uint32_t kmn, ui
       cnt[j] = (int)sm.bins[g + per - 1 - j];
       local += cnt[j];
     }
+    int total;
     int run = block_exclusive_scan(local, sm.scan, &total);
 #pragma unroll
     for (int j = 0; j < per; ++j) {
@@ -104,18 +124,18 @@ __device__ bool fast_select(const uint32_t (&key)[V][4], int K, uint32_t kmn, ui
     }
   }
   __syncthreads();
-  if (total < K || sm.bcnt > kFsRankCap) return false;
+  // Bin 0 also counts the empty slots: the K-th score must lie above it.
+  if (sm.bstar == 0 || sm.bcnt > kFsRankCap) return false;
 
-  // Members of b*, then the exact threshold by ranking them.
-  const int bstar = sm.bstar, bcnt = sm.bcnt, take = K - sm.above;
+  // Members of b* (v is an integer-valued float: the bin test is one compare),
+  // then the exact threshold by ranking them.
+  const int bcnt = sm.bcnt, take = K - sm.above;
+  const float vstar = kTwo23 + (float)sm.bstar;
   uint32_t bm = 0u;   // bit 4 j + c: slot (j, c) is in b*
 #pragma unroll
   for (int j = 0; j < V; ++j)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t k = key[j][c];
-      bm |= (uint32_t)(k && bin_of(k) == bstar) << (4 * j + c);
-    }
+    for (int c = 0; c < 4; ++c) bm |= (uint32_t)(bin_of.v(f[j][c]) == vstar) << (4 * j + c);
   if (__any_sync(kFull, bm != 0u)) {   // most warps hold no member
     const int mine = __popc(bm);
     const int incl = warp_inclusive_scan(mine);
@@ -127,40 +147,33 @@ __device__ bool fast_select(const uint32_t (&key)[V][4], int K, uint32_t kmn, ui
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         if (bm >> (4 * j + c) & 1u) {
-          sm.bst_k[q] = key[j][c];
+          sm.bst_k[q] = score_key(f[j][c]);
           sm.bst_s[q] = slot_of(j, c);
           ++q;
         }
   }
   __syncthreads();
-  // Rank on (score key, ~slot): the member with take - 1 above it.
+  // Rank on (score key, ~slot): the member with take - 1 above it.  It also
+  // counts the members with its score.
   auto member = [&](int i) { return ((ull)sm.bst_k[i] << 32) | ~sm.bst_s[i]; };
   for (int i = tid; i < bcnt; i += NT) {
     const ull x = member(i);
-    int gt = 0;
-    for (int q = 0; q < bcnt; ++q) gt += member(q) > x;
-    if (gt == take - 1) sm.thr64 = x;
+    const uint32_t xk = (uint32_t)(x >> 32);
+    int gt = 0, eq = 0;
+    for (int q = 0; q < bcnt; ++q) {
+      gt += member(q) > x;
+      eq += sm.bst_k[q] == xk;
+    }
+    if (gt == take - 1) {
+      sm.thr64 = x;
+      sm.eq = eq;
+    }
   }
   __syncthreads();
   const ull thr64 = sm.thr64;
-  const uint32_t thr = (uint32_t)(thr64 >> 32);
-  out->thr = thr;
+  out->thr = key_score((uint32_t)(thr64 >> 32));
   out->last = ~(uint32_t)thr64;
-  out->gt = out->eq = -1;
-  if (kCounts) {
-    if (tid == 0) {
-      int gt = 0, eq = 0;
-      for (int q = 0; q < bcnt; ++q) {
-        gt += sm.bst_k[q] > thr;
-        eq += sm.bst_k[q] == thr;
-      }
-      sm.gt = sm.above + gt;
-      sm.eq = eq;
-    }
-    __syncthreads();
-    out->gt = sm.gt;
-    out->eq = sm.eq;
-  }
+  out->eq = sm.eq;
   return true;
 }
 

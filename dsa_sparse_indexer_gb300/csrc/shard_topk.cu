@@ -113,14 +113,16 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 // ---------------------------------------------------------------------------
 // Throughput path for local ranges of up to 4 V NT slots (V = 4 float4 rows
 // per thread; NT = 512 or 1024 threads).  Each thread keeps V float4 of the
-// range as score keys in registers (slot e = base + 4 (j NT + tid) + c).  The
-// exact threshold (key, slot) comes from fast_select (fast_select.cuh: a
-// histogram of the keys linear in the score over their range, a ranking of
-// the threshold bin): a slot wins if its key is above the threshold key, or equal
-// to it at a slot no later than the threshold slot.  The winners are then
+// range as scores in registers (slot e = base + 4 (j NT + tid) + c; -inf
+// outside the range).  The exact threshold (score, slot) comes from
+// fast_select (fast_select.cuh: a histogram of the scores linear in the score
+// over their range, a ranking of the threshold bin): a slot wins if its score
+// is above the threshold score, or equal to it at a slot no later than the
+// threshold slot (scores compare as floats: -0.0 ties +0.0, as their keys do,
+// and each keeps its own sign in the candidate).  The winners are then
 // placed in slot order: per-thread counts for each of the V float4 rows,
 // packed into one word, take one warp scan, and a small table gives each
-// (row, warp) its output offset; each thread drops its winners' (key, slot)
+// (row, warp) its output offset; each thread drops its winners' (score, slot)
 // at their output positions in shared memory, and all threads then write the
 // outputs with coalesced stores.  Rows with an infinite score or a crowded
 // threshold bin fall back to the radix select over the registers.
@@ -134,8 +136,8 @@ struct TopkFastSmem {
     struct {
       FastSelectSmem sel;
       // Winners by output position, as separate 32-bit words (64-bit pair
-      // stores made the compiler move the register keys to local memory).
-      uint32_t stage_k[kTMaxK];
+      // stores made the compiler move the register scores to local memory).
+      float stage_v[kTMaxK];
       uint32_t stage_s[kTMaxK];
       uint32_t wt[NT / 32];        // packed per-row winner counts of each warp
       int off[V][NT / 32];         // output offset of each (float4 row, warp)
@@ -233,36 +235,37 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     return;
   }
 
-  // Keys of the range (0 outside it) and their range.
-  uint32_t key[V][4];
-  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  // Scores of the range (-inf outside it) and their range.
+  float f[V][4];
+  float fmn = INFINITY, fmx = -INFINITY;
   {
     float4 v[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) {
       const int e0 = base + (j * NT + tid) * 4;
       v[j] = e0 < hi ? __ldg(reinterpret_cast<const float4*>(row + e0))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 #pragma unroll
     for (int j = 0; j < V; ++j) {
       const int e0 = base + (j * NT + tid) * 4;
-      const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      f[j][0] = v[j].x;
+      f[j][1] = v[j].y;
+      f[j][2] = v[j].z;
+      f[j][3] = v[j].w;
       if (e0 >= lo && e0 + 4 <= hi) {   // the whole float4 is inside the range
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          key[j][c] = score_key(f[c]);
-          kmn = min(kmn, key[j][c]);
-          kmx = max(kmx, key[j][c]);
+          fmn = fminf(fmn, f[j][c]);
+          fmx = fmaxf(fmx, f[j][c]);
         }
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const bool in = e0 + c >= lo && e0 + c < hi;
-          const uint32_t k = score_key(f[c]);
-          key[j][c] = in ? k : 0u;
-          kmn = in ? min(kmn, k) : kmn;
-          kmx = max(kmx, key[j][c]);
+          f[j][c] = in ? f[j][c] : -INFINITY;
+          fmn = in ? fminf(fmn, f[j][c]) : fmn;
+          fmx = in ? fmaxf(fmx, f[j][c]) : fmx;
         }
       }
     }
@@ -270,28 +273,29 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
   auto slot = [&](int j, int c) { return (uint32_t)(base + (j * NT + tid) * 4 + c); };
 
   FastSelectResult fs;
-  if (!fast_select<NT, V>(key, K, kmn, kmx, slot, sm.f.sel, &fs)) {
+  if (!fast_select<NT, V>(f, K, fmn, fmx, slot, sm.f.sel, &fs)) {
     __syncthreads();   // the fallback's shared memory overlaps the selection's
     topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, emit);
     return;
   }
 
-  // Slot-ordered placement of the winners.
-  const uint32_t thr = fs.thr, last = fs.last;
-  uint32_t wmask = 0u, tmask = 0u;   // bit 4 j + c: slot (j, c) is above / at thr
+  // Slot-ordered placement of the winners.  With one score at the threshold
+  // (the threshold's own) every score at or above it wins.
+  const float thr = fs.thr;
+  const uint32_t last = fs.last;
+  uint32_t wmask = 0u;   // bit 4 j + c: slot (j, c) wins
+  if (fs.eq == 1) {
 #pragma unroll
-  for (int j = 0; j < V; ++j)
+    for (int j = 0; j < V; ++j)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      wmask |= (uint32_t)(key[j][c] > thr) << (4 * j + c);
-      tmask |= (uint32_t)(key[j][c] == thr) << (4 * j + c);
-    }
-  if (__any_sync(kFull, tmask != 0u)) {   // ties at the threshold: slots up to `last` win
+      for (int c = 0; c < 4; ++c) wmask |= (uint32_t)(f[j][c] >= thr) << (4 * j + c);
+  } else {
 #pragma unroll
     for (int j = 0; j < V; ++j)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        wmask |= (uint32_t)((tmask >> (4 * j + c) & 1u) && slot(j, c) <= last) << (4 * j + c);
+        wmask |= (uint32_t)(f[j][c] > thr || (f[j][c] == thr && slot(j, c) <= last))
+                 << (4 * j + c);
   }
   uint32_t pk = 0u;   // winners per float4 row j, 8 bits each
 #pragma unroll
@@ -325,14 +329,14 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
     for (int c = 0; c < 4; ++c)
       if (wmask >> (4 * j + c) & 1u) {
         if (p < K) {
-          sm.f.stage_k[p] = key[j][c];
+          sm.f.stage_v[p] = f[j][c];
           sm.f.stage_s[p] = slot(j, c);
         }
         ++p;
       }
   }
   __syncthreads();
-  for (int p = tid; p < K; p += NT) emit.from_key(p, sm.f.stage_s[p], sm.f.stage_k[p]);
+  for (int p = tid; p < K; p += NT) emit(p, sm.f.stage_s[p], sm.f.stage_v[p]);
 }
 
 // Standalone pack: cand[r][s*K + j] from local_idx[s][r][j].  Each thread
