@@ -56,12 +56,30 @@ def test_rotating_sets_exceed_l2(name):
     assert n * bench.set_bytes(cfg) > 2.5 * bench.L2_BYTES or n == 8
 
 
-def test_profile_traffic_only_while_sources_match(monkeypatch):
-    got = bench.profiled_traffic("indexer_fused", "decode")
-    assert got is not None and got > 0
+def test_profile_traffic_only_while_sources_match(monkeypatch, tmp_path):
+    (tmp_path / "profiles").mkdir()
+    h = bench.kernel_source_hash("indexer_fused")
+    (tmp_path / "profiles" / "indexer_fused_decode.md").write_text(
+        f"# summary\n\nsource_sha256_16: {h}\ndram_bytes_per_launch: 10274816\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: h)
+    assert bench.profiled_traffic("indexer_fused", "decode") == 10274816
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
     assert bench.profiled_traffic("indexer_fused", "decode") is None
     assert bench.profiled_traffic("no_such_kernel", "decode") is None
+
+
+def test_committed_profiles_name_their_sources():
+    """Every committed kernel summary states the source hash and DRAM bytes it
+    was taken with (bench.py uses the bytes only while the hash matches)."""
+    import glob
+    import os
+    for path in glob.glob(os.path.join(bench.ROOT, "profiles", "*.md")):
+        name = os.path.basename(path)[:-3]
+        if name.startswith("launches_"):
+            continue
+        text = open(path, encoding="utf-8").read()
+        assert "source_sha256_16:" in text and "dram_bytes_per_launch:" in text, name
 
 
 def test_oracle_over_all_cores_counts_rows_of_every_process():
