@@ -4,13 +4,15 @@ One step = one pass of the whole path over one batch.  Default: the decode
 workload (64 rows, S=4 shards, interleave 1, K=2048, per-row sequence length
 uniform in [8192, 65536], N(0,1) fp32 logits, paged block tables of 64-token
 blocks with per-shard random permutations, and the shards' [64, 128, 512] bf16
-partial attention outputs with base-2 LSE in [-5, 20]) on the fused path:
+partial attention outputs with base-2 LSE in [-5, 20]) on the step kernels,
+the faster path at every batch size:
 
-    dsa_indexer_fused -> dsa_lse_combine
+    dsa_shard_topk_pack -> dsa_merge_topk_stable -> dsa_convert_index_compact
+    -> dsa_lse_combine
 
-(`--path steps`: dsa_shard_topk_pack -> dsa_merge_topk_stable ->
-dsa_convert_index_compact [-> dsa_lse_combine]; `--workload` picks another of
-the five workloads), called through the C ABI (ctypes).  Prints one JSON line.
+(`--path fused`: dsa_indexer_fused [-> dsa_lse_combine], steps a1-a4 in one
+cluster kernel; `--workload` picks another of the five workloads), called
+through the C ABI (ctypes).  Prints one JSON line.
 
   value        merged top-K rows/s, device time, inputs resident in HBM: K steps
                replayed as CUDA graphs (one per rotating input set), timed with
@@ -574,7 +576,7 @@ def main(argv=None) -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=sorted(W.CONFIGS), default=DEFAULT_WORKLOAD,
                     help="timed workload (the metric is quoted on decode)")
-    ap.add_argument("--path", choices=sorted(PATHS), default="fused",
+    ap.add_argument("--path", choices=sorted(PATHS), default="steps",
                     help="fused: one cluster kernel for steps a1-a4; steps: one kernel per "
                          "step; write_slots: the write-side slot mapping of each row's new "
                          "token")
