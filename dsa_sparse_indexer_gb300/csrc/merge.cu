@@ -886,11 +886,13 @@ extern "C" dsa_status dsa_merge_topk_stable(const float* cand, int rows, int C, 
                                           (size_t)smem, stream, 0, cand, C, K, ids, scores);
       return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
     };
-    // Batches that fit one wave are latency-bound: more threads per row.
+    // Batches that fit one wave are latency-bound: more threads per row
+    // (1024 whenever a row per SM is enough, 512 for up to two rows per SM).
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return DSA_ERR_CUDA;
+    if (C <= kLinPer * 1024 && rows <= sms) return launch_fast(merge_lin_kernel<1024>, 1024);
     if (C <= kLinPer * 512 && rows <= 2 * sms) return launch_fast(merge_lin_kernel<512>, 512);
     if (C > kLinPer * 512 && C <= kLinPer * 1024 && rows <= sms)
       return launch_fast(merge_lin_kernel<1024>, 1024);
