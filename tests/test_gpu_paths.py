@@ -182,3 +182,44 @@ def test_local_topk_an_outlier_crowds_one_bin():
     row = rng.standard_normal(8192).astype(np.float32)
     row[123] = 1e30
     _topk_check(row, n, K)
+
+
+@pytest.mark.parametrize("spread", [1e-4, 1e-3, 1e-2])
+def test_local_topk_scores_far_from_zero(spread):
+    """Scores 100 + N(0,1) * spread: the narrower the range next to the scores'
+    size, the coarser the FFMA bin map's offset (at 1e-4 it is off by several
+    bins, and the end check sends the row to the radix select; at 1e-2 the map
+    holds).  Whichever path the end check picks, the selection is exact."""
+    rng = np.random.default_rng(11)
+    n, K = 8100, 2048
+    row = (100.0 + rng.standard_normal(8192) * spread).astype(np.float32)
+    _topk_check(row, n, K)
+
+
+def test_local_topk_signed_zeros_at_the_threshold_keep_their_sign():
+    """The K-th score is a zero shared by 30 slots (-0.0 and +0.0 alternating,
+    equal as scores): the first 8 of them by slot win, and each packed
+    candidate carries its own zero's sign bit."""
+    import torch
+
+    import dsa_sparse_indexer_gb300 as dsa
+    rng = np.random.default_rng(12)
+    n, K = 8192, 2048
+    row = -1.0 - rng.random(n).astype(np.float32)             # the bulk, below -1
+    hi = rng.permutation(n)[:2040 + 30]
+    row[hi[:2040]] = 1.0 + rng.random(2040).astype(np.float32)  # 2040 clear winners
+    zeros = np.sort(hi[2040:])
+    row[zeros] = np.where(np.arange(30) % 2 == 0, -0.0, 0.0).astype(np.float32)
+    _topk_check(row, n, K)
+
+    logits = torch.from_numpy(row.reshape(1, 1, n)).cuda()
+    ends = torch.tensor([n], dtype=torch.int32, device="cuda")
+    err = dsa.new_error_flags("cuda")
+    local_idx, cand = dsa.shard_topk_pack(logits, ends, K, 1, err_flags=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    li = local_idx.cpu().numpy()[0, 0]
+    np.testing.assert_array_equal(li, OX.shard_topk(row, 0, n, K))
+    got = cand.cpu().numpy()[0, :, 0]
+    np.testing.assert_array_equal(got.view(np.uint32), row[li].view(np.uint32))
+    assert np.array_equal(np.intersect1d(li, zeros), zeros[:8])
