@@ -27,7 +27,8 @@ through the C ABI (ctypes).  Prints one JSON line.
   cpu_baseline the oracle (numpy, one core) on a bounded sample of the same batch;
                cpu_baseline_all_cores the same over rows on every host core
 
-`--impl reference` times the oracle itself as the reference arm.
+`--impl reference` times the oracle itself as the reference arm, over rows on
+every host core (one spawned process per core).
 Under torchrun (N > 1) each rank runs its own batch (replicas, weak scaling);
 rows are independent, so there is no collective on the data path.
 """
@@ -472,10 +473,18 @@ def cpu_baseline_all_cores(cfg, inp: dict, budget_s: float = 10.0,
                       f"{dt:.1f} s"}
 
 
+def _oracle_worker_batch(rows) -> int:
+    w = _WORKER
+    oracle_rows(w["inp"], w["cfg"], np.asarray(rows, np.int64), w["path"])
+    return len(rows)
+
+
 def run_reference(args, world, rank):
-    """Reference arm: the oracle timed on the host cores, same workload/metric."""
+    """Reference arm: the oracle timed on the host cores (one spawned process
+    per core, each step's rows split among them), same workload and metric."""
     if rank != 0:
         return 0
+    import multiprocessing as mp
     cfg = W.CONFIGS[args.workload]
     inp = host_inputs(cfg, 0, args.path)
     if args.path == "attention":
@@ -484,33 +493,53 @@ def run_reference(args, world, rank):
     t = time.perf_counter()
     oracle_rows(inp, cfg, np.array([0]), args.path)
     per_row = max(time.perf_counter() - t, 1e-3)
+    cores = host_cores()
     budget = 150.0                        # seconds for warm-up + timed steps
-    rows_per_step = int(max(1, min(cfg.rows, budget / (args.steps + args.warmup) / per_row)))
-    r = 0
+    rows_per_step = int(max(1, min(cfg.rows,
+                                   budget * cores / (args.steps + args.warmup) / per_row)))
+    ctx = mp.get_context("spawn")
+    blocks, spec = _share_arrays(inp)
+    saved = {k: os.environ.get(k) for k in _THREAD_VARS}
+    os.environ.update({k: "1" for k in _THREAD_VARS})
+    try:
+        with ctx.Pool(cores, initializer=_oracle_worker_init,
+                      initargs=(cfg.name, args.path, spec, None)) as pool:
+            r = 0
 
-    def step():
-        nonlocal r
-        rows = (np.arange(rows_per_step) + r) % cfg.rows
-        r += rows_per_step
-        oracle_rows(inp, cfg, rows, args.path)
+            def step():
+                nonlocal r
+                rows = (np.arange(rows_per_step) + r) % cfg.rows
+                r += rows_per_step
+                pool.map(_oracle_worker_batch, [c.tolist() for c in np.array_split(rows, cores)
+                                                if len(c)], chunksize=1)
 
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
+            for _ in range(args.warmup):
+                step()
+            t0 = time.perf_counter()
+            for _ in range(args.steps):
+                step()
+            dt = time.perf_counter() - t0
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+        for b in blocks:
+            b.close()
+            b.unlink()
     value = rows_per_step * args.steps / dt
     what = "the new token" if args.path == "write_slots" else "all steps"
     sample = (f"{rows_per_step} row(s) of the {cfg.rows}-row {cfg.name} batch per step "
-              f"({what}), numpy, one thread")
+              f"({what}), split over {cores} processes (one per host core, numpy "
+              f"single-threaded in each)")
     print(json.dumps({
         "impl": "reference", "metric": metric, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype_for(args.path), "data": "synthetic",
         "config": config_block(cfg, args.path),
-        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

@@ -90,3 +90,15 @@ def test_oracle_over_all_cores_counts_rows_of_every_process():
     res = bench.cpu_baseline_all_cores(cfg, inp, budget_s=0.3, path="steps", cores=2)
     assert res["cores"] == 2 and res["kind"] == "oracle" and res["unit"] == "rows/s"
     assert res["value"] > 0 and "processes" in res["sample"]
+
+
+def test_reference_arm_prints_the_oracle_line(capsys):
+    """`bench.py --impl reference`: the oracle over rows on the host cores,
+    one JSON line with the reference keys and no GPU."""
+    import json
+    assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2",
+                       "--warmup", "3"]) == 0
+    d = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "rows/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
