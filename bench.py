@@ -297,13 +297,20 @@ def measured_tensor_peak() -> float:
         return 1900.0
 
 
+def _code_only(text: str) -> str:
+    """Source text with its C/C++ comments removed: a profile stays valid
+    while only the comments around the profiled code change."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.sub(r"//[^\n]*", "", text)
+
+
 def kernel_source_hash(kernel: str) -> str:
     csrc = os.path.join(ROOT, "dsa_sparse_indexer_gb300", "csrc")
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel] + ("common.cuh", "fastdiv.h", "select.cuh"):
         p = os.path.join(csrc, f)
         if os.path.exists(p):
-            h.update(open(p, "rb").read())
+            h.update(_code_only(open(p, encoding="utf-8").read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

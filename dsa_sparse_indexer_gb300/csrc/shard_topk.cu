@@ -8,9 +8,10 @@
 // One CTA per (shard, row); the winners are written in ascending slot order
 // (ties on the score go to the smaller slot, i.e. the smaller global id).
 // Local ranges of up to 16384 slots take the throughput kernel below
-// (topk_fast_kernel): keys in registers, the exact threshold from one
-// histogram linear in the score and a ranking of its threshold bin
-// (fast_select.cuh), slot-ordered placement through shared memory.
+// (topk_fast_kernel): scores in registers, the exact threshold from one
+// histogram linear in the score (bins read off the bits of one FFMA) and a
+// ranking of its threshold bin (fast_select.cuh), slot-ordered placement
+// through shared memory.
 // Longer ranges are staged in shared memory with bulk async copies (TMA) or
 // read from global memory, and a radix select with an ordered ballot sweep
 // picks the winners (shard_topk_kernel, local_topk.cuh).  The standalone pack

@@ -102,3 +102,16 @@ def test_reference_arm_prints_the_oracle_line(capsys):
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "rows/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_source_hash_ignores_comments_only(monkeypatch, tmp_path):
+    """A profile's hash follows the code: comments may change, code may not."""
+    csrc = tmp_path / "dsa_sparse_indexer_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (csrc / "combine.cu").write_text("// a\nint f() { return 1; } /* b */\n")
+    h0 = bench.kernel_source_hash("lse_combine")
+    (csrc / "combine.cu").write_text("// other words\nint f() { return 1; } /* c\n d */\n")
+    assert bench.kernel_source_hash("lse_combine") == h0
+    (csrc / "combine.cu").write_text("// a\nint f() { return 2; } /* b */\n")
+    assert bench.kernel_source_hash("lse_combine") != h0
