@@ -1,29 +1,31 @@
 """Benchmark of the DCP sparse-indexer hot path on one GB300 (or N, as replicas).
 
-One step = one pass of the whole path over one batch.  Default: the decode
-workload (64 rows, S=4 shards, interleave 1, K=2048, per-row sequence length
-uniform in [8192, 65536], N(0,1) fp32 logits, paged block tables of 64-token
-blocks with per-shard random permutations, and the shards' [64, 128, 512] bf16
-partial attention outputs with base-2 LSE in [-5, 20]) on the step kernels,
-the faster path at every batch size:
+One step = one pass of the whole path over one batch.  Default: the prefill
+workload, the largest that fits one GPU (4096 causal query rows over a
+32768-token context, row i seeing [0, 28672 + i); S=4 shards, interleave 1,
+K=2048; fp32 logits, paged block tables of 64-token blocks) on the step
+kernels, the faster path at every batch size:
 
     dsa_shard_topk_pack -> dsa_merge_topk_stable -> dsa_convert_index_compact
-    -> dsa_lse_combine
+    [-> dsa_lse_combine, for workloads with partial attention outputs]
 
-(`--path fused`: dsa_indexer_fused [-> dsa_lse_combine], steps a1-a4 in one
-cluster kernel; `--workload` picks another of the five workloads), called
-through the C ABI (ctypes).  Prints one JSON line.
+(`--workload decode` times the 64-row decode batch with the combine of its
+[64, 128, 512] bf16 partial outputs; `--path fused`: dsa_indexer_fused
+[-> dsa_lse_combine], steps a1-a4 in one cluster kernel), called through the
+C ABI (ctypes).  Prints one JSON line.
 
   value        merged top-K rows/s, device time, inputs resident in HBM: K steps
                replayed as CUDA graphs (one per rotating input set), timed with
                events on the launch stream
-  kernels      per-kernel mean times from K more steps launched one by one with
-               events between kernels (`launch_loop_ms_per_step` is that loop)
+  kernels      per-kernel mean times, taken the same way: a graph of one kernel
+               on every rotating input set back to back, replayed; their sum is
+               `kernels_sum_ms` (`launch_loop_ms_per_step`: the steps launched
+               one by one, no graph)
   e2e          the same through host buffers: per step, H2D of the step's inputs
                from pinned memory, the calls, D2H of slots, counts and (with the
                combine) the combined output and its LSE
   roofline     the step's dominant kernel: algorithmic bytes per launch /
-               its mean CUDA-event duration, against the measured HBM peak
+               its mean duration, against the measured HBM peak
   cpu_baseline the oracle (numpy, one core) on a bounded sample of the same batch;
                cpu_baseline_all_cores the same over rows on every host core
 
@@ -52,7 +54,7 @@ sys.path.insert(0, ROOT)
 
 import workloads as W  # noqa: E402
 
-DEFAULT_WORKLOAD = "decode"
+DEFAULT_WORKLOAD = "prefill"
 METRIC = "merged top-K rows/s"
 L2_BYTES = 126 * 2**20       # GB300 L2; rotating input sets together exceed 2.5x this
 PATHS = {
@@ -576,32 +578,6 @@ def config_block(cfg, path: str = "fused") -> dict:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def attention_probe() -> int:
-    """A small, fixed case of dsa_sparse_mla_decode for profiler captures: the
-    decode batch's shape (64 rows, 4 shards, 128 heads, 512 selected slots per
-    (row, shard), i.e. its 131 K gathered rows) over caches of 65,536 slots per
-    shard (302 MB, larger than L2; about 0.5 GB on the device in all).  Seeded
-    inputs; three launches; prints the error word."""
-    import torch
-    from dsa_sparse_indexer_gb300 import build as B
-    import dsa_sparse_indexer_gb300 as dsa
-    B.build()
-    dev = torch.device("cuda")
-    S, R, H, K, n_slots, cnt = 4, 64, 128, 2048, 65536, 512
-    g = torch.Generator(device=dev)
-    g.manual_seed(1)
-    q = torch.randn((R, H, W.MLA_DQK), generator=g, device=dev).to(torch.bfloat16)
-    cache = (torch.rand((S, n_slots, W.MLA_DQK), generator=g, device=dev) - 0.5).to(torch.bfloat16)
-    slots = torch.randint(0, n_slots, (S, R, K), generator=g, device=dev, dtype=torch.int32)
-    counts = torch.full((S, R), cnt, dtype=torch.int32, device=dev)
-    err = dsa.new_error_flags(dev)
-    for _ in range(3):
-        dsa.sparse_mla_decode(q, cache, slots, counts, MLA_SCALE, err_flags=err)
-    torch.cuda.synchronize()
-    print(json.dumps({"probe": "sparse_mla_decode", "err": int(err.item())}))
-    return 0
-
-
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -611,16 +587,12 @@ def main(argv=None) -> int:
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=sorted(W.CONFIGS), default=DEFAULT_WORKLOAD,
-                    help="timed workload (the metric is quoted on decode)")
+                    help="timed workload (default: prefill, the largest one-GPU workload)")
     ap.add_argument("--path", choices=sorted(PATHS), default="steps",
                     help="fused: one cluster kernel for steps a1-a4; steps: one kernel per "
                          "step; write_slots: the write-side slot mapping of each row's new "
                          "token")
-    ap.add_argument("--probe", choices=["attention"], default=None,
-                    help="run a small fixed case of one kernel for a profiler capture, no timing")
     args = ap.parse_args(argv)
-    if args.probe == "attention":
-        return attention_probe()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
@@ -740,7 +712,7 @@ def main(argv=None) -> int:
     # --- CUDA graphs: one step on each rotating input set back to back (as a
     # model-forward graph holds the indexer of every layer), and one graph per
     # set for the remainder of K steps and for the one-step-per-replay figure
-    graphs, rotation, graph_err = [], None, None
+    graphs, rotation, graph_err, kernel_graphs = [], None, None, []
     try:
         gs = torch.cuda.Stream(dev)
         with torch.cuda.stream(gs):
@@ -757,6 +729,16 @@ def main(argv=None) -> int:
                 for i in range(REPLICAS):
                     for fn, a in calls[i]:
                         launch(fn, a[:-1] + (gsp,))
+            # one kernel of the step on each rotating set back to back: the
+            # per-kernel times, taken the way the step is timed
+            for j in range(len(KERNELS)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=gs):
+                    gsp = torch.cuda.current_stream(dev).cuda_stream
+                    for i in range(REPLICAS):
+                        fn, a = calls[i][j]
+                        launch(fn, a[:-1] + (gsp,))
+                kernel_graphs.append(g)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             for i in range(max(3, args.warmup)):
@@ -765,7 +747,8 @@ def main(argv=None) -> int:
                 graphs[i % REPLICAS].replay()
         torch.cuda.synchronize()
     except Exception as exc:  # report, never hide: the launch loop is then the headline
-        graphs, rotation, graph_err = [], None, f"{type(exc).__name__}: {exc}"
+        graphs, rotation, kernel_graphs = [], None, []
+        graph_err = f"{type(exc).__name__}: {exc}"
 
     nk = len(KERNELS)
     clocks = ClockSampler(dev.index)
@@ -801,22 +784,45 @@ def main(argv=None) -> int:
         torch.cuda.synchronize()
         single_ms = g0.elapsed_time(g1)
 
-    # --- per-kernel times: K more steps, events between kernels -------------
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps * nk + 1)]
+    # --- per-kernel times: each kernel's graph (that kernel on every rotating
+    # set back to back) replayed max(1, K // R) times, timed like the step ---
+    kernel_ms = {}
+    if kernel_graphs:
+        reps = max(1, args.steps // REPLICAS)
+        with torch.cuda.stream(stream):
+            for k, g in zip(KERNELS, kernel_graphs):
+                for _ in range(3):
+                    g.replay()
+                torch.cuda.synchronize()
+                k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                k0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                k1.record(stream)
+                torch.cuda.synchronize()
+                kernel_ms[k] = max_over_ranks(k0.elapsed_time(k1), world) / (reps * REPLICAS)
+
+    # --- the same K steps launched one by one (no graph); without graphs,
+    # events between kernels give the per-kernel times ------------------------
+    per_kernel_events = not kernel_graphs
+    evs = [torch.cuda.Event(enable_timing=True)
+           for _ in range(args.steps * nk + 1 if per_kernel_events else 2)]
     barrier(world)
     torch.cuda.synchronize()
     # Give the GPU a head start so kernel launches queue up behind a bounded
-    # spin and the per-kernel events measure device time, not launch gaps.
+    # spin and the events measure device time, not launch gaps.
     prime_s = min(3.0, 0.01 + args.steps * cpu_per_step * 1.5)
     torch.cuda._sleep(int(prime_s * 2.0e9))
     t_loop0 = time.time()
     e = 0
+    evs[0].record(stream)
     for i in range(args.steps):
         for fn, a in calls[i % REPLICAS]:
-            evs[e].record(stream)
+            if per_kernel_events and e > 0:
+                evs[e].record(stream)
             launch(fn, a)
             e += 1
-    evs[e].record(stream)
+    evs[e if per_kernel_events else 1].record(stream)
     torch.cuda.synchronize()
     t_loop1 = time.time()
     barrier(world)
@@ -825,12 +831,14 @@ def main(argv=None) -> int:
     if int(err.item()) != 0:
         raise SystemExit(f"device error flags set in the timed region: {int(err.item())}")
 
-    loop_ms = evs[0].elapsed_time(evs[e])
-    per_kernel = {k: [] for k in KERNELS}
-    for i in range(args.steps):
-        for j, k in enumerate(KERNELS):
-            per_kernel[k].append(evs[i * nk + j].elapsed_time(evs[i * nk + j + 1]))
-    mean_ms = {k: float(np.mean(v)) for k, v in per_kernel.items()}
+    loop_ms = evs[0].elapsed_time(evs[e if per_kernel_events else 1])
+    if per_kernel_events:
+        per_kernel = {k: [] for k in KERNELS}
+        for i in range(args.steps):
+            for j, k in enumerate(KERNELS):
+                per_kernel[k].append(evs[i * nk + j].elapsed_time(evs[i * nk + j + 1]))
+        kernel_ms = {k: max_over_ranks(float(np.mean(v)), world) for k, v in per_kernel.items()}
+    mean_ms = kernel_ms
     if graph_ms is None:                      # no graphs: the launch loop is the timed region
         graph_ms, t_wall0, t_wall1 = loop_ms, t_loop0, t_loop1
     total_ms = max_over_ranks(graph_ms, world)
@@ -976,9 +984,11 @@ def main(argv=None) -> int:
         "timing": (f"K steps as CUDA-graph replays: a graph of one step on each of the {REPLICAS} "
                    "rotating input sets back to back (as a model-forward graph holds the "
                    "indexer of every layer), K // R replays of it and K mod R one-step graphs; "
-                   "per-kernel times from K more steps launched one by one with events "
-                   "between kernels" if not graph_err else
-                   f"K steps launched one by one (graph capture failed: {graph_err})"),
+                   "per-kernel times the same way: a graph of that kernel on each rotating set "
+                   "back to back, replayed max(1, K // R) times" if not graph_err else
+                   f"K steps launched one by one (graph capture failed: {graph_err}); per-kernel "
+                   "times from events between the kernels"),
+        "kernels_sum_ms": float(sum(mean_ms.values())),
         "one_step_per_replay_ms_per_step": (None if single_ms is None else
                                             max_over_ranks(single_ms, world) / args.steps),
         "launch_loop_ms_per_step": loop_ms_per_step,

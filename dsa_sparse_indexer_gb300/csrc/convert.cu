@@ -13,6 +13,7 @@
 // row, each warp owns a contiguous piece of the id list, counts per shard,
 // the CTA takes an exclusive scan over warps, and each warp then writes its
 // ids at their final positions using match_any peer groups.
+#include "checks.h"
 #include "common.cuh"
 
 namespace dsa {
@@ -270,18 +271,27 @@ __global__ void __launch_bounds__(NT)
 
 using namespace dsa;
 
+dsa_status dsa::check_convert_index_compact(const int32_t* ids, int rows, int K, int S, int I,
+                                            const int32_t* block_table, int reqs, int max_blocks,
+                                            int block_size, const int32_t* slots) {
+  if (rows < 0 || reqs < 1 || max_blocks < 1 || block_size < 1) return DSA_ERR_INVALID_ARG;
+  if (S < 1 || S > DSA_MAX_SHARDS || I < 1) return DSA_ERR_UNSUPPORTED;
+  if (K != 512 && K != 1024 && K != 2048) return DSA_ERR_UNSUPPORTED;
+  if ((int64_t)I * S > (int64_t)INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  if (rows == 0) return DSA_OK;
+  if (!ids || !block_table || !slots) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
 extern "C" dsa_status dsa_convert_index_compact(const int32_t* ids, int rows, int K, int S,
                                                 int I, const int32_t* block_table, int reqs,
                                                 int max_blocks, int block_size,
                                                 const int32_t* row_to_req, int32_t* slots,
                                                 int32_t* counts, uint32_t* err_flags,
                                                 cudaStream_t stream) {
-  if (rows < 0 || reqs < 1 || max_blocks < 1 || block_size < 1) return DSA_ERR_INVALID_ARG;
-  if (S < 1 || S > DSA_MAX_SHARDS || I < 1) return DSA_ERR_UNSUPPORTED;
-  if (K != 512 && K != 1024 && K != 2048) return DSA_ERR_UNSUPPORTED;
-  if (rows == 0) return DSA_OK;
-  if (!ids || !block_table || !slots) return DSA_ERR_INVALID_ARG;
-  if ((int64_t)I * S > (int64_t)INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  const dsa_status st = check_convert_index_compact(ids, rows, K, S, I, block_table, reqs,
+                                                    max_blocks, block_size, slots);
+  if (st != DSA_OK || rows == 0) return st;
   if (S <= kCvMaxS) {
     auto pow2 = [](int v) { return (v & (v - 1)) == 0; };
     const bool p2 = pow2(S) && pow2(I) && pow2(block_size);

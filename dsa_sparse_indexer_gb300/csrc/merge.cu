@@ -18,6 +18,7 @@
 // key, and, only when the K-th score is tied, a second one on the inverted
 // id; the K winners are then put in rank order by a bitonic sort.
 #include "binmap.cuh"
+#include "checks.h"
 #include "common.cuh"
 #include "reg_topk.cuh"
 #include "select.cuh"
@@ -868,14 +869,21 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 using namespace dsa;
 
-extern "C" dsa_status dsa_merge_topk_stable(const float* cand, int rows, int C, int K,
-                                            int32_t* ids, float* scores, uint32_t* err_flags,
-                                            cudaStream_t stream) {
+dsa_status dsa::check_merge_topk_stable(const float* cand, int rows, int C, int K,
+                                        const int32_t* ids) {
   if (rows < 0 || C < 0) return DSA_ERR_INVALID_ARG;
   if (K != 512 && K != 1024 && K != 2048) return DSA_ERR_UNSUPPORTED;
   if (C < K || (C & 3)) return DSA_ERR_INVALID_ARG;
   if (rows == 0) return DSA_OK;
   if (!cand || !ids || !aligned16(cand)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+extern "C" dsa_status dsa_merge_topk_stable(const float* cand, int rows, int C, int K,
+                                            int32_t* ids, float* scores, uint32_t* err_flags,
+                                            cudaStream_t stream) {
+  const dsa_status st = check_merge_topk_stable(cand, rows, C, K, ids);
+  if (st != DSA_OK || rows == 0) return st;
   if (C <= 32 * 1024) {
     auto launch_fast = [&](auto kernel, int nt) {
       const int smem = (int)sizeof(MergeFastSmem);

@@ -3,11 +3,13 @@
 // dsa_indexer_steps_noalloc runs dsa_shard_topk_pack, dsa_merge_topk_stable
 // and dsa_convert_index_compact, unchanged, with the packed candidates
 // ([rows][S*K][2] fp32) in a static device array of this library instead of a
-// caller buffer, for callers that cannot allocate one.  The array's address is
-// looked up once per device.  Calls that share a device share the array, so
-// they must not overlap in time (one stream, or ordered streams).
-#include <mutex>
-
+// caller buffer, for callers that cannot allocate one.  Every argument of the
+// three calls is checked before the first kernel is queued.  The array's
+// address is looked up on every call (a host-side table lookup), so it stays
+// right when the module is loaded again in a new context.  Calls that share a
+// device share the array, so they must not overlap in time (one stream, or
+// ordered streams).
+#include "checks.h"
 #include "common.cuh"
 
 namespace {
@@ -16,20 +18,11 @@ constexpr size_t kScratchBytes = DSA_NOALLOC_SCRATCH_BYTES;
 
 __device__ __align__(256) unsigned char g_cand_scratch[kScratchBytes];
 
-// Address of the array on the current device, looked up on first use.
+// Address of the array in the current context (nullptr if the lookup fails).
 float* scratch_on_current_device() {
-  constexpr int kMaxDevices = 64;
-  static float* ptrs[kMaxDevices] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_cand_scratch) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<float*>(p);
-  }
-  return ptrs[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_cand_scratch) != cudaSuccess) return nullptr;
+  return static_cast<float*>(p);
 }
 
 }  // namespace
@@ -43,13 +36,26 @@ extern "C" dsa_status dsa_indexer_steps_noalloc(const float* logits, int64_t ld,
                                                 const int32_t* row_to_req, int32_t* ids,
                                                 int32_t* slots, int32_t* counts,
                                                 uint32_t* err_flags, cudaStream_t stream) {
-  if (rows < 0 || S < 1 || K < 1) return rows < 0 ? DSA_ERR_INVALID_ARG : DSA_ERR_UNSUPPORTED;
-  if ((uint64_t)rows * (uint64_t)S * (uint64_t)K * 8u > kScratchBytes) return DSA_ERR_UNSUPPORTED;
+  // The array's size limit and every check of the three calls first, so that
+  // a bad argument queues nothing.  The array stands in for the candidate
+  // pointer: it is 256-byte aligned, so any non-null, 16-byte-aligned value
+  // checks the same way.
+  if (rows > 0 && S > 0 && K > 0 &&
+      (uint64_t)rows * (uint64_t)S * (uint64_t)K * 8u > kScratchBytes)
+    return DSA_ERR_UNSUPPORTED;
+  const float* cand_probe = reinterpret_cast<const float*>(uintptr_t{256});
+  dsa_status st = dsa::check_shard_topk_pack(logits, ld, rows, S, I, K, row_ends, cand_probe);
+  if (st != DSA_OK) return st;
+  st = dsa::check_merge_topk_stable(cand_probe, rows, S * K, K, ids);
+  if (st != DSA_OK) return st;
+  st = dsa::check_convert_index_compact(ids, rows, K, S, I, block_table, reqs, max_blocks,
+                                        block_size, slots);
+  if (st != DSA_OK) return st;
   if (rows == 0) return DSA_OK;
   float* cand = scratch_on_current_device();
   if (!cand) return DSA_ERR_CUDA;
-  dsa_status st = dsa_shard_topk_pack(logits, ld, rows, S, I, K, row_starts, row_ends, nullptr,
-                                      cand, err_flags, stream);
+  st = dsa_shard_topk_pack(logits, ld, rows, S, I, K, row_starts, row_ends, nullptr, cand,
+                           err_flags, stream);
   if (st != DSA_OK) return st;
   st = dsa_merge_topk_stable(cand, rows, S * K, K, ids, nullptr, err_flags, stream);
   if (st != DSA_OK) return st;

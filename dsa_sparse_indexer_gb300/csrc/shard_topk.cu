@@ -16,6 +16,7 @@
 // read from global memory, and a radix select with an ordered ballot sweep
 // picks the winners (shard_topk_kernel, local_topk.cuh).  The standalone pack
 // gathers candidates for given local indices.
+#include "checks.h"
 #include "common.cuh"
 #include "fast_select.cuh"
 #include "local_topk.cuh"
@@ -434,15 +435,21 @@ extern "C" dsa_status dsa_shard_topk(const float* logits, int64_t ld, int rows, 
                             err_flags, stream);
 }
 
+dsa_status dsa::check_shard_topk_pack(const float* logits, int64_t ld, int rows, int S, int I,
+                                      int K, const int32_t* row_ends, const float* cand) {
+  const dsa_status st = check_common(logits, ld, rows, S, I, K);
+  if (st != DSA_OK || rows == 0) return st;
+  if (!row_ends || !cand || !aligned16(cand)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
 extern "C" dsa_status dsa_shard_topk_pack(const float* logits, int64_t ld, int rows, int S,
                                           int I, int K, const int32_t* row_starts,
                                           const int32_t* row_ends, int32_t* local_idx,
                                           float* cand, uint32_t* err_flags,
                                           cudaStream_t stream) {
-  dsa_status st = check_common(logits, ld, rows, S, I, K);
-  if (st != DSA_OK) return st;
-  if (rows == 0) return DSA_OK;
-  if (!row_ends || !cand || !aligned16(cand)) return DSA_ERR_INVALID_ARG;
+  const dsa_status st = check_shard_topk_pack(logits, ld, rows, S, I, K, row_ends, cand);
+  if (st != DSA_OK || rows == 0) return st;
   return launch_topk<true>(logits, ld, rows, S, I, K, row_starts, row_ends, local_idx, cand,
                            err_flags, stream);
 }

@@ -323,11 +323,12 @@ dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache, in
  * Arguments as the three entry points it calls (ids [rows][K] is the merge's
  * output and the convert's input; scores and local_idx are not produced).
  * It enqueues three kernels on `stream`.  Calls on one device share the array:
- * they must not overlap in time.
- * Errors: rows * S * K * 8 > DSA_NOALLOC_SCRATCH_BYTES -> UNSUPPORTED; the
- *         array's address cannot be looked up -> CUDA; otherwise those of the
- *         entry points it calls, from the first that fails (nothing after it
- *         is enqueued).
+ * they must not overlap in time.  The array's address is looked up in the
+ * current context on every call.
+ * Errors: rows * S * K * 8 > DSA_NOALLOC_SCRATCH_BYTES -> UNSUPPORTED; then
+ *         every argument check of the three entry points, before anything is
+ *         enqueued (the first that fails is returned and nothing is touched);
+ *         the array's address cannot be looked up -> CUDA.
  */
 dsa_status dsa_indexer_steps_noalloc(const float* logits, int64_t ld, int rows, int S, int I,
                                      int K, const int32_t* row_starts, const int32_t* row_ends,

@@ -31,6 +31,37 @@ def test_host_checks(lib):
     assert f(*args(rows, 4, 2048)) == UNSUPPORTED
 
 
+# Fake, 16-byte-aligned device addresses: every case below fails a host check
+# before anything is enqueued, so none of them is ever dereferenced.
+_PTR = 1 << 20
+
+
+def _full_args(rows=4, S=4, I=1, K=2048, ld=64, bt=_PTR, reqs=1, max_blocks=1, block_size=64,
+               ids=_PTR, slots=_PTR, row_ends=_PTR, logits=_PTR):
+    return (logits, ld, rows, S, I, K, NULL, row_ends, bt, reqs, max_blocks, block_size, NULL,
+            ids, slots, NULL, NULL, NULL)
+
+
+@pytest.mark.parametrize("rows", [0, 4])
+@pytest.mark.parametrize("bad, want", [
+    (dict(block_size=0), INVALID), (dict(reqs=0), INVALID), (dict(max_blocks=0), INVALID),
+    (dict(I=0), UNSUPPORTED), (dict(ld=6), INVALID), (dict(ld=0), INVALID),
+    (dict(S=65), UNSUPPORTED), (dict(K=777), UNSUPPORTED)])
+def test_scalar_checks_of_every_step_come_first(lib, rows, bad, want):
+    """A bad scalar of any of the three steps (the convert's block size, the
+    local top-K's stride, ...) is reported whether or not there are rows."""
+    assert lib.dsa_indexer_steps_noalloc(*_full_args(rows=rows, **bad)) == want
+
+
+@pytest.mark.parametrize("bad", [dict(bt=NULL), dict(ids=NULL), dict(slots=NULL),
+                                 dict(row_ends=NULL), dict(logits=NULL), dict(logits=_PTR + 4)])
+def test_a_later_steps_pointer_check_runs_before_any_launch(lib, bad):
+    """With rows > 0, a null block table, ids or slots (checked by the merge
+    and the convert) is reported before the local top-K is queued; these
+    calls never reach the GPU (there is none here)."""
+    assert lib.dsa_indexer_steps_noalloc(*_full_args(**bad)) == INVALID
+
+
 @pytest.mark.gpu
 def test_two_calls_match_the_entry_points_with_a_caller_buffer(lib):
     import torch
@@ -61,3 +92,16 @@ def test_two_calls_match_the_entry_points_with_a_caller_buffer(lib):
             np.testing.assert_array_equal(ids.cpu().numpy(), want["ids"])
             np.testing.assert_array_equal(slots.cpu().numpy(), want["slots"])
             np.testing.assert_array_equal(counts.cpu().numpy(), want["counts"])
+
+        # A bad argument of the last step (a zero block size) is found before
+        # the first kernel: the ids, slots and counts keep their fill.
+        ids = torch.full((cfg.rows, cfg.K), 7, dtype=torch.int32, device="cuda")
+        slots = torch.full((cfg.S, cfg.rows, cfg.K), 7, dtype=torch.int32, device="cuda")
+        counts = torch.full((cfg.S, cfg.rows), 7, dtype=torch.int32, device="cuda")
+        st = lib.dsa_indexer_steps_noalloc(
+            P(logits), cfg.ld, cfg.rows, cfg.S, cfg.I, cfg.K, P(starts), P(ends), P(bt),
+            cfg.reqs, cfg.max_blocks, 0, None, P(ids), P(slots), P(counts), None,
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == INVALID
+        torch.cuda.synchronize()
+        assert (ids == 7).all() and (slots == 7).all() and (counts == 7).all()
