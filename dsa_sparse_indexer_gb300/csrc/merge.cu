@@ -147,43 +147,48 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Throughput path (C <= 32 * NT).  Each candidate becomes the 64-bit rank key
-// (score key << 32 | ~id), so that one unsigned compare orders two candidates
-// (higher score first, then the smaller id).  Each thread loads 16 float4
-// (32 candidates) in four batches of 4, batch b holding float4 rows
+// Throughput path (C <= 32 * NT).  Each thread loads 16 float4 (32
+// candidates) in four batches of 4, batch b holding float4 rows
 // 4 i + (i + b) mod 4, so every batch spans all shard blocks and all parts of
-// each block.  While the second batch is in flight, a 256-bin histogram of the
-// first batch's keys (one candidate per float4), refined by a second 256-bin
-// histogram inside its selected bin when that bin is crowded, proposes a floor
-// a little below the K-th score key; each batch's
-// candidates whose score is at or above it (about 1.15 K in all) are appended
-// to a shared list as raw (score, id) pairs by warp ballots, and turned into
-// rank keys by the first histogram pass.  If fewer than K made it, the row is
-// filtered again with no floor.
+// each block.  While the second batch is in flight, a histogram of one
+// candidate per float4 of the first batch (256 bins linear in the score over
+// the samples' range) proposes a floor a little below the K-th score; each
+// batch's valid candidates at or above it (about 1.15 K in all) are appended to
+// a shared list as raw (score, id) pairs.  If fewer than K made it, or no floor
+// could be set (few valid candidates, an infinite sample), every valid
+// candidate is listed instead and the list's exact score range is taken.
 //
-// On the list, a histogram of 2048 bins spread over [min, max] of its score
-// keys does two jobs: a scan from the top bin finds the bin b* holding the
-// K-th key and gives every bin above b* its output range, since all of those
-// candidates win.  Winners above b* go into their bin's range and are ranked
-// inside it (bins hold a few keys); the members of b* are ranked among
-// themselves.  If a bin above b* or b* itself is crowded, a second level
-// spreads the bins over [bottom of b*, max].  Rows still crowded (heavy ties,
-// an outlier stretching the range) or whose list overflowed take a radix
-// select for the threshold and a bitonic sort.  Ranked winners are staged in
-// shared memory and written with 16-byte stores.
+// On the list, a histogram of 2048 bins does two jobs: a scan from the top bin
+// finds the bin b* holding the K-th candidate and gives every bin above b* its
+// output range, since all of those candidates win.  The bins are spaced
+// logarithmically above the floor: the bin of a score f is read off the bit
+// pattern of w = f - floor + delta (delta = range / 15), whose top bits count
+// 512 bins per octave of w from delta to 16 delta.  A rounded sum and the bit
+// pattern of a non-negative float are both monotone, so bins keep the score
+// order; and since candidate scores thin out above the floor (the upper tail
+// of the shards' winners), bins that widen with the distance from the floor
+// hold one or two candidates each, where equal widths hold several near the
+// floor.  Winners above b* go into their bin's range as 64-bit rank keys
+// (score key << 32 | ~id, so one unsigned compare orders two candidates:
+// higher score first, then the smaller id) and are ranked inside it; the
+// members of b* are ranked among themselves.  Rows with a crowded bin (heavy
+// ties, an outlier stretching the range), a non-finite range or an
+// overflowing list take a radix select for the threshold and a bitonic sort.
+// Ranked winners are staged in shared memory and written with 16-byte stores.
 // ---------------------------------------------------------------------------
 using ull = unsigned long long;
 constexpr int kMBins = 2048;
-constexpr int kSBins = 256;         // bins of the sample histogram
+constexpr int kSampBins = 256;      // bins of the sample histogram
 constexpr int kMListCap = 3072;     // candidates at or above the floor
 constexpr int kRankCap = 256;       // most members of b* for the pairwise ranking
 constexpr int kFineCap = 64;        // most keys in one bin above b*
 constexpr int kQuarter = 4;         // float4 per thread per batch
+constexpr int kLogShift = 14;       // 2^(23 - 14) = 512 bins per octave
 
 struct alignas(16) MergeFastSmem {
   union {
-    ull l[kMListCap];               // rank keys with score key at or above the floor
-    float2 f[kMListCap];            // the same as raw (score, id) before the first pass
+    ull l[kMListCap];               // rank keys (latency kernel)
+    float2 f[kMListCap];            // raw (score, id) at or above the floor
     ull lb[kMaxK];                  // crowded rows: all winners
     ull out[kMaxK];                 // ranked winners by output position
   } u;
@@ -194,13 +199,16 @@ struct alignas(16) MergeFastSmem {
     uint32_t end[kMBins];
     SelectSmem sel;                 // crowded rows only
   } h;
-  ull win[kMaxK];                   // winners above b*, by output range
+  union {
+    ull win[kMaxK];                 // winners above b*, by output range
+    uint32_t scnt[kSampBins];       // sample histogram (before the list exists)
+  } w;
   ull bst[kRankCap];                // members of b*
-  uint32_t scnt[kSBins];            // sample histogram
   int scan[33];
-  int nsv, nslots, nlist, nlist2, nb, nwin, bstar, above, bcnt, scount, sabove;
+  int nsv, nslots, nlist, nlist2, nb, nwin, bstar, above, bcnt;
   int bmax[2];                      // per level, so that no reset races a read
-  uint32_t smin, smax, lmin, lmin2, kmax, kmax2, sfloor;
+  uint32_t smin, smax, lmin, lmin2, kmax, kmax2;
+  float sfloor;
 };
 
 template <int NT>
@@ -293,29 +301,87 @@ __device__ __noinline__ void merge_crowded(const float* __restrict__ row, int C,
   }
 }
 
-// Entries of a[s0, e) above x.  Bins mostly hold a few keys: the first four
+// Entries of a[s0, e) above x.  Bins mostly hold a few keys: the first U
 // entries are compared without a loop, so lanes with different bin sizes
 // stay together.
+template <int U = 4>
 __device__ __forceinline__ int count_above(const ull* a, int s0, int e, ull x) {
   int gt = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int j = 0; j < U; ++j)
     if (s0 + j < e) gt += a[s0 + j] > x;
-  for (int q = s0 + 4; q < e; ++q) gt += a[q] > x;
+  for (int q = s0 + U; q < e; ++q) gt += a[q] > x;
   return gt;
 }
 
-// Appends one batch's valid candidates with score >= ffloor to the list as
+// Appends two batches' valid candidates with score >= ffloor to the list as
 // raw (score, id) pairs: one pass mask per thread, one warp scan and one
 // shared atomic per warp for the positions.  NaN scores fail the comparison.
-__device__ __forceinline__ void append_batch(const float4 (&v)[kQuarter], float ffloor,
-                                             MergeFastSmem& sm, int* counter) {
+__device__ __forceinline__ void append_batches(const float4 (&va)[kQuarter],
+                                               const float4 (&vb)[kQuarter], float ffloor,
+                                               MergeFastSmem& sm, int* counter) {
   const int lane = threadIdx.x & 31;
-  uint32_t mask = 0u;   // bit 2 i + h: candidate h of float4 i passes
+  uint32_t mask = 0u;   // bit 2 i + h (+ 8 for vb): candidate h of float4 i passes
 #pragma unroll
   for (int i = 0; i < kQuarter; ++i) {
-    mask |= (uint32_t)(__float_as_int(v[i].y) >= 0 && v[i].x >= ffloor) << (2 * i);
-    mask |= (uint32_t)(__float_as_int(v[i].w) >= 0 && v[i].z >= ffloor) << (2 * i + 1);
+    mask |= (uint32_t)(__float_as_int(va[i].y) >= 0 && va[i].x >= ffloor) << (2 * i);
+    mask |= (uint32_t)(__float_as_int(va[i].w) >= 0 && va[i].z >= ffloor) << (2 * i + 1);
+    mask |= (uint32_t)(__float_as_int(vb[i].y) >= 0 && vb[i].x >= ffloor) << (2 * i + 8);
+    mask |= (uint32_t)(__float_as_int(vb[i].w) >= 0 && vb[i].z >= ffloor) << (2 * i + 9);
+  }
+  const int m = __popc(mask);
+  const int incl = warp_inclusive_scan(m);
+  int base = 0;
+  if (lane == 31 && incl) base = atomicAdd(counter, incl);
+  int p = __shfl_sync(kFull, base, 31) + incl - m;
+  auto put = [&](const float4& v, int bit) {
+    if ((mask >> bit & 1u) && p < kMListCap) sm.u.f[p] = make_float2(v.x, v.y);
+    p += mask >> bit & 1u;
+    if ((mask >> (bit + 1) & 1u) && p < kMListCap) sm.u.f[p] = make_float2(v.z, v.w);
+    p += mask >> (bit + 1) & 1u;
+  };
+#pragma unroll
+  for (int i = 0; i < kQuarter; ++i) put(va[i], 2 * i);
+#pragma unroll
+  for (int i = 0; i < kQuarter; ++i) put(vb[i], 2 * i + 8);
+}
+
+// Log-spaced bins of scores at or above lo (see the throughput path): the
+// top bits of the bit pattern of max(f - lo + delta, 0), delta = (hi - lo) / 15,
+// counted from those of delta; clamped to [0, kMBins).  Monotone in f.
+struct LogBins {
+  float d;          // delta - lo
+  uint32_t base;    // bit pattern of delta
+  __device__ __forceinline__ LogBins(float lo, float hi) {
+    const float delta = (hi - lo) * (1.0f / 15.0f);
+    d = delta - lo;
+    base = __float_as_uint(delta);
+  }
+  __device__ __forceinline__ int operator()(float f) const {
+    const int x = (int)(__float_as_uint(fmaxf(f + d, 0.0f)) - base) >> kLogShift;
+    return min(max(x, 0), kMBins - 1);
+  }
+};
+
+// Appends one batch's valid candidates (id >= 0) as raw (score, id) pairs and
+// folds their score keys into [kmn, kmx] (no floor: the exact range).
+__device__ __forceinline__ void append_valid(const float4 (&v)[kQuarter], MergeFastSmem& sm,
+                                             int* counter, uint32_t& kmn, uint32_t& kmx) {
+  const int lane = threadIdx.x & 31;
+  uint32_t mask = 0u;
+#pragma unroll
+  for (int i = 0; i < kQuarter; ++i) {
+    const bool a = __float_as_int(v[i].y) >= 0, b = __float_as_int(v[i].w) >= 0;
+    mask |= (uint32_t)a << (2 * i);
+    mask |= (uint32_t)b << (2 * i + 1);
+    if (a) {
+      kmn = min(kmn, score_key(v[i].x));
+      kmx = max(kmx, score_key(v[i].x));
+    }
+    if (b) {
+      kmn = min(kmn, score_key(v[i].z));
+      kmx = max(kmx, score_key(v[i].z));
+    }
   }
   const int m = __popc(mask);
   const int incl = warp_inclusive_scan(m);
@@ -329,31 +395,6 @@ __device__ __forceinline__ void append_batch(const float4 (&v)[kQuarter], float 
     if ((mask >> (2 * i + 1) & 1u) && p < kMListCap) sm.u.f[p] = make_float2(v[i].z, v[i].w);
     p += mask >> (2 * i + 1) & 1u;
   }
-}
-
-// Retry with no floor: appends every valid candidate as a rank key and folds
-// its score key into the range (NaN scores included, as keys).
-__device__ __forceinline__ void append_all(const float4 (&v)[kQuarter], MergeFastSmem& sm,
-                                           int* counter, uint32_t& kmn, uint32_t& kmx) {
-  const int lane = threadIdx.x & 31;
-  const unsigned lt = lanemask_lt();
-#pragma unroll
-  for (int i = 0; i < kQuarter; ++i)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const ull x = h ? rank_key(v[i].z, v[i].w) : rank_key(v[i].x, v[i].y);
-      const uint32_t k = (uint32_t)(x >> 32);
-      if (k) {
-        kmn = min(kmn, k);
-        kmx = max(kmx, k);
-      }
-      const unsigned b = __ballot_sync(kFull, k != 0u);
-      int base = 0;
-      if (lane == 0 && b) base = atomicAdd(counter, __popc(b));
-      base = __shfl_sync(kFull, base, 0);
-      const int p = base + __popc(b & lt);
-      if (k && p < kMListCap) sm.u.l[p] = x;
-    }
 }
 
 template <int NT>
@@ -384,7 +425,7 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
   load_batch(0, va);
   load_batch(1, vb);
 
-  for (int b = tid; b < kSBins; b += NT) sm.scnt[b] = 0u;
+  for (int b = tid; b < kSampBins; b += NT) sm.w.scnt[b] = 0u;
   for (int b = tid; b < kMBins; b += NT) sm.h.end[b] = 0u;
   if (tid == 0) {
     sm.nsv = 0;
@@ -392,29 +433,28 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
     sm.nlist = 0;
     sm.nlist2 = 0;
     sm.nb = 0;
-    sm.nwin = 0;
-    sm.bmax[0] = sm.bmax[1] = 0;
+    sm.nwin = 0;   // the crowded path's winner count
+    sm.bmax[0] = 0;
     sm.smin = 0xffffffffu;
     sm.smax = 0u;
-    sm.lmin = 0xffffffffu;
     sm.lmin2 = 0xffffffffu;
-    sm.kmax = 0u;
     sm.kmax2 = 0u;
   }
   // Samples: one candidate of each float4 of batch 0, alternating halves.
-  auto sample = [&](int i) {
-    return (uint32_t)(rank_key((i & 1) ? va[i].z : va[i].x, (i & 1) ? va[i].w : va[i].y) >> 32);
-  };
+  auto samp_f = [&](int i) { return (i & 1) ? va[i].z : va[i].x; };
+  auto samp_ok = [&](int i) { return __float_as_int((i & 1) ? va[i].w : va[i].y) >= 0; };
   {
     int ns = 0, slots = 0;   // valid samples; sample positions inside the row
     uint32_t mn = 0xffffffffu, mx = 0u;
 #pragma unroll
     for (int i = 0; i < kQuarter; ++i) {
-      const uint32_t k = sample(i);
-      ns += k != 0u;
       slots += 2 * (5 * i * NT + tid) < C;   // batch 0 holds rows 5 i
-      mx = max(mx, k);
-      mn = min(mn, k ? k : 0xffffffffu);
+      if (samp_ok(i)) {
+        const uint32_t k = score_key(samp_f(i));
+        ++ns;
+        mx = max(mx, k);
+        mn = min(mn, k);
+      }
     }
     ns = __reduce_add_sync(kFull, ns);
     slots = __reduce_add_sync(kFull, slots);
@@ -431,82 +471,63 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
     }
   }
   __syncthreads();
-  uint32_t floor = 1u;   // every valid key
+  // The floor: the score above which about 1.125 K + 16 sample-equivalents lie.
+  float ffloor = -INFINITY;   // -inf: no floor, every valid candidate is listed
   {
+    const float smax_f = key_score(sm.smax);
     const int nsv = sm.nsv, nslots = sm.nslots;
     // Estimated valid candidates: the valid fraction of the sample slots times C.
     const float valid_est = nslots ? (float)nsv * (float)C / (float)nslots : 0.f;
-    if (valid_est > 1.25f * (float)K && nsv >= 64) {
-      const uint32_t smin = sm.smin;
-      const int ssh = max(0, (32 - __clz((int)(sm.smax - smin))) - 8);   // range >> ssh < 256
+    const float smin_f = key_score(sm.smin);
+    constexpr float kTwo23 = 8388608.0f;
+    const float scale = __fdividef((float)(kSampBins - 3), smax_f - smin_f);
+    const LinearBinsN<kSampBins> sbin{scale, (kTwo23 + 1.0f) - smin_f * scale};
+    // Same values in every thread: uniform.
+    if (valid_est > 1.25f * (float)K && nsv >= 64 && smax_f > smin_f && isfinite(smin_f) &&
+        isfinite(smax_f) && isfinite(scale) && sbin.v(smin_f) >= kTwo23 &&
+        sbin.v(smax_f) <= kTwo23 + (float)(kSampBins - 1)) {
 #pragma unroll
-      for (int i = 0; i < kQuarter; ++i) {
-        const uint32_t k = sample(i);
-        if (k) atomicAdd(&sm.scnt[(k - smin) >> ssh], 1u);
-      }
+      for (int i = 0; i < kQuarter; ++i)
+        if (samp_ok(i)) atomicAdd(&sm.w.scnt[sbin(samp_f(i))], 1u);
       __syncthreads();
       // Expected samples among the winners: K * nslots / C; take 1/8 more and 16.
       const int target = min(nsv, (int)((float)K * (float)nslots * 1.125f / (float)C) + 16);
-      const int local = tid < kSBins ? (int)sm.scnt[kSBins - 1 - tid] : 0;
+      // Thread t < kSampBins takes bin kSampBins - 1 - t (bins from the top).
+      const int local = tid < kSampBins ? (int)sm.w.scnt[kSampBins - 1 - tid] : 0;
       int tot;
       const int run = block_exclusive_scan(local, sm.scan, &tot);
-      if (tid < kSBins && run < target && run + local >= target) {
-        sm.sfloor = smin + ((uint32_t)(kSBins - 1 - tid) << ssh);
-        sm.scount = local;
-        sm.sabove = run;
+      if (tid < kSampBins && run < target && run + local >= target) {
+        // Bin b holds scores from about smin + (b - 1) / scale; one bin lower
+        // for the rounding of the map.
+        const int b = kSampBins - 1 - tid;
+        sm.sfloor = b <= 2 ? smin_f : smin_f + (float)(b - 2) / scale;
       }
       __syncthreads();
-      floor = sm.sfloor;
-      if (sm.scount > 16 && ssh > 0) {
-        // Refine inside the selected bin [floor, floor + 2^ssh).
-        const int ssh2 = max(0, ssh - 8);
-        const int target2 = target - sm.sabove;
-        for (int b = tid; b < kSBins; b += NT) sm.scnt[b] = 0u;
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < kQuarter; ++i) {
-          const uint32_t k = sample(i);
-          if (k >= floor && ((k - floor) >> ssh) == 0u) atomicAdd(&sm.scnt[(k - floor) >> ssh2], 1u);
-        }
-        __syncthreads();
-        const int local2 = tid < kSBins ? (int)sm.scnt[kSBins - 1 - tid] : 0;
-        const int run2 = block_exclusive_scan(local2, sm.scan, &tot);
-        if (tid < kSBins && run2 < target2 && run2 + local2 >= target2)
-          sm.sfloor = floor + ((uint32_t)(kSBins - 1 - tid) << ssh2);
-        __syncthreads();
-        floor = sm.sfloor;
-      }
+      ffloor = sm.sfloor;
     }
   }
 
-  // Filter the four batches into the list, the next batch in flight meanwhile.
-  {
-    // Scores >= ffloor are exactly the keys >= floor (keys below that of -inf
-    // are NaN patterns, which the retry handles).
-    const float ffloor = floor <= score_key(-INFINITY) ? -INFINITY : key_score(floor);
-    append_batch(va, ffloor, sm, &sm.nlist);
+  int n = 0, need = 0;
+  float lo = 0.f, hi = 0.f;
+  if (ffloor > -INFINITY) {
+    // Filter the four batches into the list, the next batch in flight meanwhile.
+    append_batches(va, vb, ffloor, sm, &sm.nlist);
     load_batch(2, va);
-    append_batch(vb, ffloor, sm, &sm.nlist);
     load_batch(3, vb);
-    append_batch(va, ffloor, sm, &sm.nlist);
-    append_batch(vb, ffloor, sm, &sm.nlist);
+    append_batches(va, vb, ffloor, sm, &sm.nlist);
+    __syncthreads();
+    n = sm.nlist;
+    need = K;
+    // Bins over [floor, largest sample]; the few above it share the top bin.
+    lo = ffloor;
+    hi = fmaxf(key_score(sm.smax), ffloor);
   }
-  __syncthreads();
-  // With no floor every valid candidate is in the list (NaN scores, outside
-  // the domain, aside); with a floor, K of them in the list settle need = K.
-  int n = sm.nlist;
-  int need = floor == 1u ? min(K, n) : K;
-  // Bin range: with a floor, [floor, largest sample] (every list key is >=
-  // floor; the few above the largest sample share the top bin); without one,
-  // the list's exact range, taken below.
-  uint32_t lmin = floor, kmax = max(sm.smax, floor);
-  bool raw = true;   // list entries still (score, id) pairs
-  if (n < need) {
-    // The sample floor was above the K-th key: every valid key.
+  if (n < need || ffloor == -INFINITY) {
+    // No floor, or it was above the K-th score: every valid candidate.
     uint32_t kmn = 0xffffffffu, kmx = 0u;
     for (int b = 0; b < 4; ++b) {
       load_batch(b, va);
-      append_all(va, sm, &sm.nlist2, kmn, kmx);
+      append_valid(va, sm, &sm.nlist2, kmn, kmx);
     }
     kmn = __reduce_min_sync(kFull, kmn);
     kmx = __reduce_max_sync(kFull, kmx);
@@ -517,115 +538,69 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
     __syncthreads();
     n = sm.nlist2;
     need = min(K, n);
-    floor = 1u;
-    lmin = sm.lmin2;
-    kmax = sm.kmax2;
-    raw = false;
-  }
-
-  if (raw && floor == 1u && need > 0 && n <= kMListCap) {
-    // No floor: convert the list to rank keys and take its exact key range.
-    uint32_t kmn = 0xffffffffu, kmx = 0u;
-    for (int i = tid; i < n; i += NT) {
-      const float2 f = sm.u.f[i];
-      const ull x = rank_key(f.x, f.y);
-      sm.u.l[i] = x;
-      kmn = min(kmn, (uint32_t)(x >> 32));
-      kmx = max(kmx, (uint32_t)(x >> 32));
-    }
-    kmn = __reduce_min_sync(kFull, kmn);
-    kmx = __reduce_max_sync(kFull, kmx);
-    if (lane == 0) {
-      atomicMin(&sm.lmin, kmn);
-      atomicMax(&sm.kmax, kmx);
-    }
-    __syncthreads();
-    lmin = sm.lmin;
-    kmax = sm.kmax;
-    raw = false;
+    lo = key_score(sm.lmin2);
+    hi = key_score(sm.kmax2);
   }
 
   bool ranked = false;   // winners staged in out[] by position
-  if (need > 0 && n > kMListCap) {
-    merge_crowded<NT>(row, C, floor, n, need, sm, out_ids, out_sc);
+  if (need > 0 && (n > kMListCap || !isfinite(lo) || !isfinite(hi))) {
+    // Every winner's score is at or above lo; n valid candidates are.
+    merge_crowded<NT>(row, C, score_key(lo), n, need, sm, out_ids, out_sc);
   } else if (need > 0) {
-    BinMap<kMBins> bin(lmin, kmax);
-    int bstar = 0, above = 0, bcnt = 0;
-#pragma unroll 1
-    for (int level = 0;; ++level) {
-      if (raw) {
-        raw = false;
-        for (int i = tid; i < n; i += NT) {
-          const float2 f = sm.u.f[i];
-          const ull x = rank_key(f.x, f.y);
-          sm.u.l[i] = x;
-          atomicAdd(&sm.h.end[bin((uint32_t)(x >> 32))], 1u);
-        }
-      } else {
-        for (int i = tid; i < n; i += NT) {
-          const uint32_t k = (uint32_t)(sm.u.l[i] >> 32);
-          if (k >= bin.lo) atomicAdd(&sm.h.end[bin(k)], 1u);
-        }
-      }
-      __syncthreads();
-      // Scan from the top bin down: output ranges, b*, the largest bin above b*.
-      {
-        constexpr int per = kMBins / NT;
-        const int g = kMBins - per * (tid + 1);
-        int cnt[per];
-        int local = 0;
+    const LogBins bin(lo, hi);
+    for (int i = tid; i < n; i += NT) atomicAdd(&sm.h.end[bin(sm.u.f[i].x)], 1u);
+    __syncthreads();
+    // Scan from the top bin down: output ranges, b*, the largest bin above b*.
+    {
+      constexpr int per = kMBins / NT;
+      const int g = kMBins - per * (tid + 1);
+      int cnt[per];
+      int local = 0;
 #pragma unroll
-        for (int j = 0; j < per; ++j) {
-          cnt[j] = (int)sm.h.end[g + per - 1 - j];
-          local += cnt[j];
-        }
-        int tot;
-        int run = block_exclusive_scan(local, sm.scan, &tot);
-        int mx = 0;
-#pragma unroll
-        for (int j = 0; j < per; ++j) {
-          const int b = g + per - 1 - j;
-          sm.h.end[b] = (uint32_t)run;
-          if (run < need && run + cnt[j] >= need) {
-            sm.bstar = b;
-            sm.above = run;
-            sm.bcnt = cnt[j];
-          } else if (run + cnt[j] < need) {
-            mx = max(mx, cnt[j]);
-          }
-          run += cnt[j];
-        }
-        if (mx > kFineCap) atomicMax(&sm.bmax[level], mx);
+      for (int j = 0; j < per; ++j) {
+        cnt[j] = (int)sm.h.end[g + per - 1 - j];
+        local += cnt[j];
       }
-      __syncthreads();
-      bstar = sm.bstar;
-      above = sm.above;
-      bcnt = sm.bcnt;
-      ranked = bcnt <= kRankCap && sm.bmax[level] <= kFineCap;
-      if (ranked || level == 1 || kmax - bin.lo < (uint32_t)kMBins) break;
-      // Second level over [bottom of b*, kmax]: every winner is at or above it.
-      bin = BinMap<kMBins>(bin.bottom(bstar), kmax);
-      for (int b = tid; b < kMBins; b += NT) sm.h.end[b] = 0u;
-      __syncthreads();
+      int tot;
+      int run = block_exclusive_scan(local, sm.scan, &tot);
+      int mx = 0;
+#pragma unroll
+      for (int j = 0; j < per; ++j) {
+        const int b = g + per - 1 - j;
+        sm.h.end[b] = (uint32_t)run;
+        if (run < need && run + cnt[j] >= need) {
+          sm.bstar = b;
+          sm.above = run;
+          sm.bcnt = cnt[j];
+        } else if (run + cnt[j] < need) {
+          mx = max(mx, cnt[j]);
+        }
+        run += cnt[j];
+      }
+      if (mx > kFineCap) atomicMax(&sm.bmax[0], mx);
     }
-    const int take = need - above;   // members of b* that win
-
+    __syncthreads();
+    const int bstar = sm.bstar, above = sm.above, bcnt = sm.bcnt;
+    ranked = bcnt <= kRankCap && sm.bmax[0] <= kFineCap;
     if (ranked) {
+      const int take = need - above;   // members of b* that win
       // Winners above b* go to their bin's output range, b* to its own list.
       for (int i = tid; i < n; i += NT) {
-        const ull x = sm.u.l[i];
-        const uint32_t k = (uint32_t)(x >> 32);
-        if (k < bin.lo) continue;
-        const int b = bin(k);
-        if (b > bstar) sm.win[atomicAdd(&sm.h.end[b], 1u)] = x;
-        else if (b == bstar) sm.bst[atomicAdd(&sm.nb, 1)] = x;
+        const float2 e = sm.u.f[i];
+        const int b = bin(e.x);
+        if (b < bstar) continue;
+        const ull x = rank_key(e.x, e.y);
+        if (b > bstar) sm.w.win[atomicAdd(&sm.h.end[b], 1u)] = x;
+        else sm.bst[atomicAdd(&sm.nb, 1)] = x;
       }
       __syncthreads();
       for (int p = tid; p < above; p += NT) {
-        const ull x = sm.win[p];
-        const int b = bin((uint32_t)(x >> 32));
+        const ull x = sm.w.win[p];
+        // key_score(score_key(f)) is f (a -0.0 comes back as +0.0, which has
+        // the same bin), so this is the bin the scatter used.
+        const int b = bin(key_score((uint32_t)(x >> 32)));
         const int e = (int)sm.h.end[b], s0 = b == kMBins - 1 ? 0 : (int)sm.h.end[b + 1];
-        sm.u.out[s0 + count_above(sm.win, s0, e, x)] = x;
+        sm.u.out[s0 + count_above<2>(sm.w.win, s0, e, x)] = x;
       }
       for (int i = tid; i < bcnt; i += NT) {
         const ull x = sm.bst[i];
@@ -635,7 +610,7 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
       __syncthreads();
     } else {
       __syncthreads();   // the select reuses the bin counters
-      merge_crowded<NT>(row, C, bin.bottom(bstar), above + bcnt, need, sm, out_ids, out_sc);
+      merge_crowded<NT>(row, C, score_key(lo), n, need, sm, out_ids, out_sc);
     }
   }
   // Write the ranked winners and the -1 / -inf padding, 4 positions a thread.
@@ -805,15 +780,15 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
           if (!key[i]) continue;
           const int b = bin(key[i]);
           const ull x = ((ull)key[i] << 32) | nid[i];
-          if (b > bstar) sm.win[atomicAdd(&sm.h.end[b], 1u)] = x;
+          if (b > bstar) sm.w.win[atomicAdd(&sm.h.end[b], 1u)] = x;
           else if (b == bstar) sm.bst[atomicAdd(&sm.nb, 1)] = x;
         }
         __syncthreads();
         for (int p = tid; p < above; p += NT) {
-          const ull x = sm.win[p];
+          const ull x = sm.w.win[p];
           const int b = bin((uint32_t)(x >> 32));
           const int e = (int)sm.h.end[b], s0 = b == kMBins - 1 ? 0 : (int)sm.h.end[b + 1];
-          sm.u.out[s0 + count_above(sm.win, s0, e, x)] = x;
+          sm.u.out[s0 + count_above(sm.w.win, s0, e, x)] = x;
         }
         for (int i = tid; i < bcnt; i += NT) {
           const ull x = sm.bst[i];
