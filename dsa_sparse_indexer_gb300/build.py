@@ -83,6 +83,33 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     return LIB
 
 
+STALLED_COPY_TEST_LIB = os.path.join(BUILD, "libdsa_stalled_copy_test.so")
+
+
+def build_stalled_copy_test(force: bool = False) -> str:
+    """A test-only library, separate from libdsa.so: the local top-K entry
+    points (shard_topk.cu alone) built with DSA_TEST_STALLED_COPY, whose
+    staging wait also waits on an mbarrier that no copy completes, with a
+    short poll bound.  Every real copy still lands; the bounded wait runs out
+    and the kernel returns with DSA_FLAG_TIMEOUT set.  Used by the tests of
+    that flag only."""
+    src = os.path.join(CSRC, "shard_topk.cu")
+    deps = [src, os.path.abspath(__file__), os.path.join(INCLUDE, "dsa.h")] + \
+        [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
+    if (not force and os.path.exists(STALLED_COPY_TEST_LIB) and
+            all(os.path.getmtime(f) <= os.path.getmtime(STALLED_COPY_TEST_LIB) for f in deps)):
+        return STALLED_COPY_TEST_LIB
+    os.makedirs(BUILD, exist_ok=True)
+    tmp = STALLED_COPY_TEST_LIB + ".tmp"
+    cmd = [nvcc(), *ARCH, *FLAGS, "-DDSA_TEST_STALLED_COPY", "-shared", "-cudart", "shared",
+           src, "-o", tmp]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"nvcc failed on the stalled-copy test build:\n{res.stdout}\n{res.stderr}")
+    os.replace(tmp, STALLED_COPY_TEST_LIB)
+    return STALLED_COPY_TEST_LIB
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--force", action="store_true")

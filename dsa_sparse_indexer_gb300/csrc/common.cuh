@@ -137,7 +137,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for phase `parity` of an mbarrier.  Returns false (and the
 // caller raises DSA_FLAG_TIMEOUT) after `limit` polls; each poll may suspend
 // the thread for a hardware-chosen interval, so the bound is generous.
+#ifdef DSA_TEST_STALLED_COPY
+constexpr uint32_t kWaitPolls = 1u << 12;   // the test build's short bound
+#else
 constexpr uint32_t kWaitPolls = 1u << 22;
+#endif
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;

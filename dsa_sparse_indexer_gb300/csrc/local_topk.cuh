@@ -14,8 +14,17 @@ constexpr int kStageChunks = 16;
 constexpr uint32_t kStageChunkBytes = 16384;
 constexpr int kStageCapElems = 48 * 1024;  // 192 KB of staged logits at most
 
+// DSA_TEST_STALLED_COPY (a separate test build, never libdsa.so): one more
+// mbarrier, armed for 16 bytes that no copy delivers, joins the staging wait,
+// so that the bounded wait runs out while every real copy still lands.
+#ifdef DSA_TEST_STALLED_COPY
+constexpr int kStageBars = kStageChunks + 1;
+#else
+constexpr int kStageBars = kStageChunks;
+#endif
+
 struct LocalTopkSmem {
-  uint64_t bars[kStageChunks];
+  uint64_t bars[kStageBars];
   SelectSmem sel;
   int wgt[32], weq[32], eq_before[32], sel_before[32];
 };
@@ -37,6 +46,9 @@ __device__ __forceinline__ const float* stage_local_range(const float* row, int6
   const int nchunks = (int)((bytes + kStageChunkBytes - 1) / kStageChunkBytes);
   if (threadIdx.x == 0) {
     for (int c = 0; c < nchunks; ++c) mbar_init(&sm.bars[c], 1);
+#ifdef DSA_TEST_STALLED_COPY
+    mbar_init(&sm.bars[kStageChunks], 1);
+#endif
     mbar_init_fence();
   }
   __syncthreads();
@@ -49,8 +61,14 @@ __device__ __forceinline__ const float* stage_local_range(const float* row, int6
                reinterpret_cast<const unsigned char*>(row + lo4) + off, len, &sm.bars[c]);
     }
   }
+#ifdef DSA_TEST_STALLED_COPY
+  if (threadIdx.x == 0) mbar_expect_tx(&sm.bars[kStageChunks], 16);
+#endif
   bool good = true;
   for (int c = 0; c < nchunks; ++c) good &= mbar_wait(&sm.bars[c], 0);
+#ifdef DSA_TEST_STALLED_COPY
+  good &= mbar_wait(&sm.bars[kStageChunks], 0);
+#endif
   if (__syncthreads_or(!good)) {
     if (threadIdx.x == 0) raise_flag(flags, DSA_FLAG_TIMEOUT);
     for (int c = 0; c < nchunks; ++c) mbar_wait(&sm.bars[c], 0);

@@ -136,11 +136,12 @@ def convert_index_compact(ids, block_table, block_size: int, I: int, row_to_req=
 def indexer_fused(logits, row_ends, K: int, I: int, block_table, block_size: int,
                   row_starts=None, row_to_req=None, ids=None, slots=None, counts=None,
                   want_scores: bool = False, want_local_idx: bool = False,
-                  want_cand: bool = False, err_flags=None) -> dict:
+                  want_cand: bool = False, err_flags=None, scores=None, local_idx=None,
+                  cand=None) -> dict:
     """Shard top-K, pack, merge and convert in one kernel (S <= 8).
 
     Returns a dict with ids [rows, K], slots [S, rows, K], counts [S, rows] and,
-    when asked for, scores, local_idx and cand."""
+    when asked for (or given as output tensors), scores, local_idx and cand."""
     _need(logits, "logits", torch.float32, 3)
     S, rows, ld = logits.shape
     _need(row_ends, "row_ends", torch.int32, 1)
@@ -158,12 +159,17 @@ def indexer_fused(logits, row_ends, K: int, I: int, block_table, block_size: int
         torch.empty((S, rows, K), dtype=torch.int32, device=dv),
         "counts": counts if counts is not None else
         torch.empty((S, rows), dtype=torch.int32, device=dv),
-        "scores": torch.empty((rows, K), dtype=torch.float32, device=dv) if want_scores else None,
-        "local_idx": torch.empty((S, rows, K), dtype=torch.int32, device=dv)
-        if want_local_idx else None,
-        "cand": torch.empty((rows, S * K, 2), dtype=torch.float32, device=dv)
-        if want_cand else None,
+        "scores": scores if scores is not None else
+        torch.empty((rows, K), dtype=torch.float32, device=dv) if want_scores else None,
+        "local_idx": local_idx if local_idx is not None else
+        torch.empty((S, rows, K), dtype=torch.int32, device=dv) if want_local_idx else None,
+        "cand": cand if cand is not None else
+        torch.empty((rows, S * K, 2), dtype=torch.float32, device=dv) if want_cand else None,
     }
+    for name, dt, nd in (("scores", torch.float32, 2), ("local_idx", torch.int32, 3),
+                         ("cand", torch.float32, 3)):
+        if out[name] is not None:
+            _need(out[name], name, dt, nd)
     _need(out["ids"], "ids", torch.int32, 2)
     _need(out["slots"], "slots", torch.int32, 3)
     _need(out["counts"], "counts", torch.int32, 2)

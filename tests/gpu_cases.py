@@ -34,27 +34,60 @@ def dev(a, dtype=None):
     return t.cuda()
 
 
+GUARD_BYTES = 4096
+POISON = 0xA5
+
+
+class Guards:
+    """Output buffers with a poisoned 4 KB guard before and after each: a
+    kernel that writes past either end of an output changes a guard byte.
+    (Memory checkers are not available on the GPU hosts; these guards stand in
+    for them on every output of the parity tests.)"""
+
+    def __init__(self):
+        self.bufs = []
+
+    def empty(self, shape, dtype) -> torch.Tensor:
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        raw = torch.full((2 * GUARD_BYTES + n,), POISON, dtype=torch.uint8, device="cuda")
+        self.bufs.append((raw, n))
+        return raw[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
+
+    def check(self) -> None:
+        torch.cuda.synchronize()
+        for i, (raw, n) in enumerate(self.bufs):
+            head, tail = raw[:GUARD_BYTES], raw[GUARD_BYTES + n:]
+            assert bool((head == POISON).all()), f"write before output buffer {i}"
+            assert bool((tail == POISON).all()), f"write past output buffer {i}"
+
+
 def run_gpu(case: dict, fused: bool = True) -> dict:
     """The launch sequence the benchmark times: fused shard top-K + pack, merge,
-    convert.  Also returns the error word."""
+    convert, every output guarded.  Also returns the error word."""
     import dsa_sparse_indexer_gb300 as dsa
     cfg = case["cfg"]
+    S, R, K = cfg.S, cfg.rows, cfg.K
     logits = dev(case["local"])
     starts = dev(case["starts"])
     ends = dev(case["ends"])
     bt = dev(case["bt"])
     r2q = None if case["r2q"] is None else dev(case["r2q"])
     err = dsa.new_error_flags("cuda")
+    g = Guards()
+    local_idx = g.empty((S, R, K), torch.int32)
+    cand = g.empty((R, S * K, 2), torch.float32)
     if fused:
-        local_idx, cand = dsa.shard_topk_pack(logits, ends, cfg.K, cfg.I, row_starts=starts,
-                                              err_flags=err)
+        dsa.shard_topk_pack(logits, ends, K, cfg.I, row_starts=starts, local_idx=local_idx,
+                            cand=cand, err_flags=err)
     else:
-        local_idx = dsa.shard_topk(logits, ends, cfg.K, cfg.I, row_starts=starts, err_flags=err)
-        cand = dsa.pack_candidates(logits, local_idx, cfg.I, err_flags=err)
-    ids, scores = dsa.merge_topk_stable(cand, cfg.K, want_scores=True, err_flags=err)
+        dsa.shard_topk(logits, ends, K, cfg.I, row_starts=starts, out=local_idx, err_flags=err)
+        dsa.pack_candidates(logits, local_idx, cfg.I, out=cand, err_flags=err)
+    ids, scores = dsa.merge_topk_stable(cand, K, ids=g.empty((R, K), torch.int32),
+                                        scores=g.empty((R, K), torch.float32), err_flags=err)
     slots, counts = dsa.convert_index_compact(ids, bt, cfg.block_size, cfg.I, row_to_req=r2q,
-                                              err_flags=err)
-    torch.cuda.synchronize()
+                                              slots=g.empty((S, R, K), torch.int32),
+                                              counts=g.empty((S, R), torch.int32), err_flags=err)
+    g.check()
     cand_np = cand.cpu().numpy()
     return dict(local_idx=local_idx.cpu().numpy(), cand_scores=cand_np[..., 0],
                 cand_ids=cand_np[..., 1].view(np.int32), ids=ids.cpu().numpy(),
@@ -68,11 +101,17 @@ def run_gpu_fused(case: dict, with_intermediates: bool = True) -> dict:
     cfg = case["cfg"]
     err = dsa.new_error_flags("cuda")
     r2q = None if case["r2q"] is None else dev(case["r2q"])
-    o = dsa.indexer_fused(dev(case["local"]), dev(case["ends"]), cfg.K, cfg.I, dev(case["bt"]),
+    S, R, K = cfg.S, cfg.rows, cfg.K
+    g = Guards()
+    o = dsa.indexer_fused(dev(case["local"]), dev(case["ends"]), K, cfg.I, dev(case["bt"]),
                           cfg.block_size, row_starts=dev(case["starts"]), row_to_req=r2q,
-                          want_scores=True, want_local_idx=with_intermediates,
-                          want_cand=with_intermediates, err_flags=err)
-    torch.cuda.synchronize()
+                          ids=g.empty((R, K), torch.int32), slots=g.empty((S, R, K), torch.int32),
+                          counts=g.empty((S, R), torch.int32),
+                          scores=g.empty((R, K), torch.float32),
+                          local_idx=g.empty((S, R, K), torch.int32) if with_intermediates else None,
+                          cand=g.empty((R, S * K, 2), torch.float32) if with_intermediates else None,
+                          err_flags=err)
+    g.check()
     got = dict(ids=o["ids"].cpu().numpy(), scores=o["scores"].cpu().numpy(),
                slots=o["slots"].cpu().numpy(), counts=o["counts"].cpu().numpy(),
                err=int(err.item()))
@@ -141,3 +180,58 @@ def assert_combine_parity(out_bf16: torch.Tensor, lse: torch.Tensor, part_bits: 
     assert np.array_equal(np.isneginf(got_lse), inf)
     d = np.abs(got_lse[~inf] - ref_lse[~inf])
     assert np.all(d <= 1e-5 * np.maximum(1.0, np.abs(ref_lse[~inf]))), d.max()
+
+
+# ---------------------------------------------------------------------------
+# Every row of a full-size workload against the oracle, over spawned host
+# processes (spawned, not forked: the parent already holds a GPU context).
+# Each worker rebuilds the workload from its seeds and compares its share of
+# the rows; the definition check (a brute-force sort of the unsharded row) is
+# left to the sampled rows of assert_indexer_parity.
+# ---------------------------------------------------------------------------
+_KEYS_S = ("local_idx", "slots", "counts")          # [S, rows, ...]
+_KEYS_R = ("cand_scores", "cand_ids", "ids", "scores")   # [rows, ...]
+_WORKER: dict = {}
+
+
+def _rows_worker_init(name: str) -> None:
+    case = make_case(name)
+    case.pop("x")                      # only the shards' rows are read
+    _WORKER["case"] = case
+
+
+def _rows_worker_check(task):
+    rows, got = task
+    want = run_oracle(_WORKER["case"], rows)
+    bad = {}
+    for k in _KEYS_S + _KEYS_R:
+        g, w = got[k], want[k]
+        if k in ("cand_scores",):
+            g, w = bits(g), bits(w)
+        if not np.array_equal(g, w):
+            diff = (g != w).reshape((len(rows), -1) if k in _KEYS_R else (g.shape[0], len(rows), -1))
+            first = np.argwhere(diff.any(axis=-1))[0]
+            bad[k] = int(rows[first[-1]])
+    return len(rows), bad
+
+
+def assert_all_rows_match_oracle(name: str, got: dict, procs: int | None = None) -> int:
+    """Every row of workload `name` (as make_case builds it) bit-exact against
+    the oracle's steps; returns the number of rows checked."""
+    import multiprocessing as mp
+    import os
+    cfg = W.CONFIGS[name]
+    n = procs or max(1, min(8, (os.cpu_count() or 2) - 1))
+    chunks = np.array_split(np.arange(cfg.rows), 4 * n)
+    tasks = []
+    for c in chunks:
+        sub = {k: np.ascontiguousarray(got[k][:, c]) for k in _KEYS_S}
+        sub.update({k: np.ascontiguousarray(got[k][c]) for k in _KEYS_R})
+        tasks.append((c, sub))
+    checked = 0
+    with mp.get_context("spawn").Pool(n, initializer=_rows_worker_init, initargs=(name,)) as pool:
+        for cnt, bad in pool.imap_unordered(_rows_worker_check, tasks):
+            assert not bad, f"first mismatching row per output: {bad}"
+            checked += cnt
+    assert checked == cfg.rows
+    return checked

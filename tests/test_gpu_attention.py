@@ -28,11 +28,16 @@ SCALE = 1.0 / np.sqrt(192.0)
 def _attend(q_bits, cache_bits, slots, counts, scale=SCALE):
     import dsa_sparse_indexer_gb300 as dsa
     err = dsa.new_error_flags("cuda")
+    g = G.Guards()
+    S, rows = counts.shape
+    H = q_bits.shape[1]
     out, lse2 = dsa.sparse_mla_decode(G.dev(q_bits.view(np.int16)).view(torch.bfloat16),
                                       G.dev(cache_bits.view(np.int16)).view(torch.bfloat16),
                                       G.dev(slots.astype(np.int32)),
-                                      G.dev(counts.astype(np.int32)), scale, err_flags=err)
-    torch.cuda.synchronize()
+                                      G.dev(counts.astype(np.int32)), scale,
+                                      out=g.empty((S, rows, H, W.MLA_DV), torch.bfloat16),
+                                      lse2=g.empty((S, rows, H), torch.float32), err_flags=err)
+    g.check()
     ob = out.view(torch.int16).cpu().numpy().view(np.uint16)
     return OC.bf16_to_f64(ob), lse2.cpu().numpy(), int(err.item())
 

@@ -19,10 +19,11 @@ pytestmark = pytest.mark.gpu
 def _run(pos, req, S, I, bt, bs):
     import dsa_sparse_indexer_gb300 as dsa
     err = dsa.new_error_flags("cuda")
+    g = G.Guards()
     out = dsa.slot_mapping(G.dev(np.asarray(pos, np.int32)), G.dev(bt), bs, I,
                            token_req=None if req is None else G.dev(np.asarray(req, np.int32)),
-                           err_flags=err)
-    torch.cuda.synchronize()
+                           out=g.empty((S, len(pos)), torch.int32), err_flags=err)
+    g.check()
     return out.cpu().numpy(), int(err.item())
 
 

@@ -30,6 +30,10 @@ def test_indexer_parity_full_size(name, nsample):
     case = G.make_case(name)
     got = G.run_gpu(case, fused=True)
     G.assert_indexer_parity(case, got, sample_rows(case["cfg"], nsample))
+    if case["cfg"].rows > nsample:
+        # every row, over host processes (the sampled rows above also checked
+        # the merged ids against a brute-force sort of the unsharded row)
+        assert G.assert_all_rows_match_oracle(name, got) == case["cfg"].rows
 
 
 @pytest.mark.parametrize("name", ["tiny", "ragged", "long_decode"])
@@ -63,6 +67,8 @@ def test_fused_cluster_kernel_parity_full_size(name, nsample):
     case = G.make_case(name)
     got = G.run_gpu_fused(case)
     G.assert_indexer_parity(case, got, sample_rows(case["cfg"], nsample))
+    if case["cfg"].rows > nsample:
+        assert G.assert_all_rows_match_oracle(name, got) == case["cfg"].rows
     lean = G.run_gpu_fused(case, with_intermediates=False)   # the benchmark's call
     for k in ("ids", "slots", "counts"):
         np.testing.assert_array_equal(lean[k], got[k])
@@ -241,11 +247,15 @@ def test_lse_combine_parity_full_size(name):
     cfg, part, lse2, empty = _combine_case(name)
     if name == "ragged":
         assert empty.any() and (~empty).any()
-    out, lse = dsa.lse_combine(G.dev(part.view(np.int16)).view(torch.bfloat16), G.dev(lse2))
-    torch.cuda.synchronize()
-    rows = sample_rows(cfg, 24, seed=5)
-    rows = np.union1d(rows, np.where(empty.any(axis=0))[0][:8])
-    G.assert_combine_parity(out, lse, part, lse2, rows)
+    g = G.Guards()
+    R, H, D = cfg.rows, cfg.H, cfg.D
+    out, lse = dsa.lse_combine(G.dev(part.view(np.int16)).view(torch.bfloat16), G.dev(lse2),
+                               out=g.empty((R, H, D), torch.bfloat16),
+                               lse_out=g.empty((R, H), torch.float32))
+    g.check()
+    # every row, 32 at a time (the fp64 oracle holds S x 32 x H x D values)
+    for c in np.array_split(np.arange(cfg.rows), max(1, cfg.rows // 32)):
+        G.assert_combine_parity(out, lse, part, lse2, c)
 
 
 @pytest.mark.parametrize("S,H,D", [(1, 3, 8), (8, 5, 136), (3, 2, 520), (40, 2, 64),
@@ -261,8 +271,11 @@ def test_lse_combine_shapes_and_degenerate_cases(S, H, D):
     lse2[:, 2] = 3.5                         # equal LSEs -> mean
     lse2[0, 3] = 60.0                        # one shard dominates
     part[:, 0] = 0
-    out, lse = dsa.lse_combine(G.dev(part.view(np.int16)).view(torch.bfloat16), G.dev(lse2))
-    torch.cuda.synchronize()
+    g = G.Guards()
+    out, lse = dsa.lse_combine(G.dev(part.view(np.int16)).view(torch.bfloat16), G.dev(lse2),
+                               out=g.empty((rows, H, D), torch.bfloat16),
+                               lse_out=g.empty((rows, H), torch.float32))
+    g.check()
     G.assert_combine_parity(out, lse, part, lse2, np.arange(rows))
     o = out.float().cpu().numpy()
     assert np.all(o[0] == 0) and np.all(np.isneginf(lse.cpu().numpy()[0]))
