@@ -18,6 +18,10 @@ Modules:
               merge, index conversion with compaction
   combine     LSE combine of per-shard partial attention outputs (fp64)
   pipeline    the steps chained for one workload
+  attention   each shard's sparse MLA decode over its selected slots (fp64)
+  kv_write    the write-side slot mapping of new tokens
+  indexer_logits  the indexer's ReLU-weighted head sum of fp8 query-key dot
+              products over each shard's paged key cache (fp64)
 
 Every function is pinned by a `-m "not gpu"` test against something other than
 itself (brute force, a worked example on the pages, closed forms, invariants).

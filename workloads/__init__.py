@@ -25,7 +25,8 @@ import numpy as np
 __all__ = [
     "Config", "CONFIGS", "rng_for", "row_ranges", "global_logits",
     "iid_local_logits", "block_tables", "combine_inputs",
-    "f32_to_bf16_bits",
+    "f32_to_bf16_bits", "IDX_HEADS", "IDX_DIM", "e4m3_codes", "indexer_query",
+    "indexer_weights", "indexer_keys",
 ]
 
 
@@ -235,3 +236,35 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     rounded = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return rounded.astype(np.uint16)
 
+
+
+# Indexer-logits inputs: H_I = 64 query heads of d_I = 128 fp8 (e4m3) values per
+# query token, one fp32 weight per head, one 128-value fp8 key per cached token.
+IDX_HEADS, IDX_DIM = 64, 128
+
+
+def e4m3_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    """Random fp8 e4m3 codes (uint8): a random sign, an exponent field drawn
+    uniformly from 4..9 and three random mantissa bits, i.e. magnitudes in
+    [2^-3, 2^2 * 1.875], roughly log-uniform; no NaN code, no subnormal."""
+    sign = rng.integers(0, 2, shape, dtype=np.uint8) << np.uint8(7)
+    expo = rng.integers(4, 10, shape, dtype=np.uint8) << np.uint8(3)
+    mant = rng.integers(0, 8, shape, dtype=np.uint8)
+    return sign | expo | mant
+
+
+def indexer_query(rows: int, seed: int) -> np.ndarray:
+    """[rows, 64, 128] fp8 e4m3 codes: the query heads of each query token."""
+    return e4m3_codes(np.random.default_rng(seed), (rows, IDX_HEADS, IDX_DIM))
+
+
+def indexer_weights(rows: int, seed: int) -> np.ndarray:
+    """[rows, 64] fp32 head weights, N(0, 1/64)."""
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((rows, IDX_HEADS), dtype=np.float32) / np.float32(8.0))
+
+
+def indexer_keys(S: int, n_slots: int, seed: int) -> np.ndarray:
+    """[S, n_slots, 128] fp8 e4m3 codes: each shard's paged indexer key cache
+    by physical slot."""
+    return e4m3_codes(np.random.default_rng(seed), (S, n_slots, IDX_DIM))
