@@ -34,6 +34,8 @@ SIGNATURES = {
     "dsa_slot_mapping": ([_p, _p, _i, _i, _i, _p, _i, _i, _i, _p, _p, _p], _i),
     "dsa_sparse_mla_decode": ([_p, _p, _i64, _p, _p, _i, _i, _i, _i, ctypes.c_float, _p, _p, _p,
                                _p], _i),
+    "dsa_indexer_logits": ([_p, _p, _p, _i64, _p, _i, _i, _i, _p, _p, _p, _i, _i, _i, _p, _i64,
+                            _p, _p], _i),
     "dsa_indexer_steps_noalloc": ([_p, _i64, _i, _i, _i, _i, _p, _p, _p, _i, _i, _i, _p, _p, _p,
                                    _p, _p, _p], _i),
 }

@@ -250,3 +250,40 @@ def sparse_mla_decode(q, kv_cache, slots, counts, scale: float, out=None, lse2=N
               _ptr(counts), rows, S, H, K, float(scale), _ptr(out), _ptr(lse2), _ptr(err_flags),
               _stream(q))
     return out, lse2
+
+
+IDX_HEADS, IDX_DIM = 64, 128
+
+
+def indexer_logits(q, weights, k_cache, block_table, block_size: int, row_ends, I: int,
+                   ld: int, row_starts=None, row_to_req=None, out=None, err_flags=None):
+    """Each shard's indexer logits over its local slots.
+
+    q [rows, 64, 128] uint8 (fp8 e4m3 codes), weights [rows, 64] fp32,
+    k_cache [S, n_slots, 128] uint8 (e4m3), block_table [S, reqs, max_blocks]
+    -> logits [S, rows, ld] fp32 (only each row's local range is written)."""
+    _need(q, "q", torch.uint8, 3)
+    _need(weights, "weights", torch.float32, 2)
+    _need(k_cache, "k_cache", torch.uint8, 3)
+    _need(block_table, "block_table", torch.int32, 3)
+    _need(row_ends, "row_ends", torch.int32, 1)
+    rows = q.shape[0]
+    if tuple(q.shape[1:]) != (IDX_HEADS, IDX_DIM) or tuple(weights.shape) != (rows, IDX_HEADS):
+        raise ValueError("q must be [rows, 64, 128] and weights [rows, 64]")
+    S, n_slots, dim = k_cache.shape
+    if dim != IDX_DIM or block_table.shape[0] != S:
+        raise ValueError("k_cache must be [S, n_slots, 128] and block_table [S, reqs, max_blocks]")
+    _, reqs, max_blocks = block_table.shape
+    for name, t in (("row_starts", row_starts), ("row_to_req", row_to_req)):
+        if t is not None:
+            _need(t, name, torch.int32, 1)
+    if out is None:
+        out = torch.empty((S, rows, ld), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, 3)
+    if tuple(out.shape) != (S, rows, ld):
+        raise ValueError("out must be [S, rows, ld]")
+    _lib.call("dsa_indexer_logits", _ptr(q), _ptr(weights), _ptr(k_cache), n_slots,
+              _ptr(block_table), reqs, max_blocks, block_size, _ptr(row_to_req),
+              _ptr(row_starts), _ptr(row_ends), rows, S, I, _ptr(out), ld, _ptr(err_flags),
+              _stream(q))
+    return out

@@ -82,6 +82,10 @@ enum {
  * values in all. */
 #define DSA_MLA_DQK 576
 #define DSA_MLA_DV 512
+/* Indexer-logits shape: query heads per token and values per head / key. */
+#define DSA_IDX_HEADS 64
+#define DSA_IDX_DIM 128
+
 /* Bytes of the library-owned candidate array of dsa_indexer_steps_noalloc. */
 #define DSA_NOALLOC_SCRATCH_BYTES (64u << 20)
 
@@ -312,6 +316,47 @@ dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* kv_cache, in
                                  const int32_t* slots, const int32_t* counts, int rows, int S,
                                  int H, int K, float scale, uint16_t* out, float* lse2,
                                  uint32_t* err_flags, cudaStream_t stream);
+
+/*
+ * dsa_indexer_logits - each shard's indexer logits over its local slots.
+ * PR #46076 report, section 关键源码片段: `_assert_cutedsl_dcp_merge_supported`
+ * (fp32 indexer logits reach the DCP top-K) and the `_merge_dcp_topk_global`
+ * docstring (each rank scores its own local KV shard); PR #52046 report,
+ * "DSV3.2 PCP sharding", section 关键源码片段 (`_sparse_indexer_and_attn`: the
+ * indexer scores a request's cached keys).  The formula is not printed on the
+ * pages; the reading taken is the DeepSeek-V3.2-style indexer:
+ *
+ *   logits[s][r][l] = sum_h weights[r][h] * max(0, q[r][h] . k_s(l)),
+ *
+ * k_s(l) the key of shard s's local slot l of row r's request, at physical
+ * slot block_table[s][req][l / block_size] * block_size + l % block_size.
+ *
+ *   q           [rows][DSA_IDX_HEADS][DSA_IDX_DIM] fp8 e4m3 codes, 16-byte aligned
+ *   weights     [rows][DSA_IDX_HEADS] fp32
+ *   k_cache     [S][n_slots][DSA_IDX_DIM] fp8 e4m3 codes, 16-byte aligned:
+ *               each shard's paged key cache by physical slot
+ *   block_table [S][reqs][max_blocks] int32; row_to_req [rows] (NULL: row r
+ *               is request r); row_starts (NULL = 0) / row_ends [rows] global
+ *   logits      [S][rows][ld] fp32 out (4-byte aligned; ld % 4 == 0): entries
+ *               l in [n_s(start), n_s(end)) are written, the others untouched
+ * Products of fp8 values are exact; each head's 128 of them are summed in
+ * fp32 by the tensor cores, then ReLU, weights and the head sum in fp32.
+ *   err_flags   DSA_FLAG_BOUNDS if a range ends past ld (clipped), a request
+ *               is outside [0, reqs) or a needed table entry points outside the
+ *               cache (those keys read as zero); DSA_FLAG_TIMEOUT if a bounded
+ *               wait ran out (the CTA stops; its slots are not all written).
+ * Errors: rows < 0, ld < 4, ld % 4, n_slots < 1, reqs/max_blocks/block_size
+ *         < 1, null pointers, misalignment -> INVALID_ARG; S not in [1, 64],
+ *         I < 1, block_size not 16, 32 or a multiple of 64, sizes past the
+ *         32-bit tensor coordinates -> UNSUPPORTED; tensor-map encoding or
+ *         launch failure -> CUDA.
+ */
+dsa_status dsa_indexer_logits(const uint8_t* q, const float* weights, const uint8_t* k_cache,
+                              int64_t n_slots, const int32_t* block_table, int reqs,
+                              int max_blocks, int block_size, const int32_t* row_to_req,
+                              const int32_t* row_starts, const int32_t* row_ends, int rows,
+                              int S, int I, float* logits, int64_t ld, uint32_t* err_flags,
+                              cudaStream_t stream);
 
 /*
  * dsa_indexer_steps_noalloc - dsa_shard_topk_pack, dsa_merge_topk_stable and
