@@ -68,6 +68,10 @@ PATHS = {
     # the decode loop closed: the fused indexer, every shard's sparse MLA
     # attention over its compacted slots, and the combine of those outputs
     "attention": ("indexer_fused", "sparse_mla_decode", "lse_combine"),
+    # the indexer step from its fp8 inputs: each shard's logits over its
+    # paged key cache (tensor cores), then the step kernels on them
+    "logits": ("indexer_logits", "shard_topk_pack", "merge_topk_stable",
+               "convert_index_compact", "lse_combine"),
 }
 PATH_METRIC = {"write_slots": ("slot-mapped new tokens/s", "tokens/s"),
                "attention": ("decode rows/s (indexer, sparse MLA attention, LSE combine)",
@@ -80,7 +84,8 @@ KERNEL_SOURCES = {"shard_topk_pack": ("shard_topk.cu", "fast_select.cuh", "local
                   "indexer_fused": ("fused.cu", "local_topk.cuh", "reg_topk.cuh"),
                   "lse_combine": ("combine.cu",),
                   "slot_mapping": ("slot_mapping.cu",),
-                  "sparse_mla_decode": ("attention.cu",)}
+                  "sparse_mla_decode": ("attention.cu",),
+                  "indexer_logits": ("indexer_logits.cu",)}
 
 
 # ---------------------------------------------------------------------------
@@ -130,7 +135,8 @@ def host_inputs(cfg, replica: int, path: str = "fused"):
     the exact recipes).  Every shard of a decode row holds >= 2048 tokens, so
     no combine input is empty there."""
     starts, ends = W.row_ranges(cfg, replica)
-    logits = W.iid_local_logits(cfg, replica)
+    # the logits path computes its logits from fp8 queries and keys instead
+    logits = W.iid_local_logits(cfg, replica) if path != "logits" else None
     bt = W.block_tables(cfg, replica=replica)
     r2q = None if cfg.reqs == cfg.rows else np.zeros(cfg.rows, np.int32)
     # the token each row adds: the last position of its range
@@ -140,6 +146,9 @@ def host_inputs(cfg, replica: int, path: str = "fused"):
         d["part"], d["lse2"] = W.combine_inputs(cfg, replica=replica)
     if path == "attention":
         d["q"] = W.mla_query(cfg.rows, cfg.H, seed=1000 * replica + 7)
+    if path == "logits":
+        d["iq"] = W.indexer_query(cfg.rows, seed=1000 * replica + 9)
+        d["iw"] = W.indexer_weights(cfg.rows, seed=1000 * replica + 10)
     return d
 
 
@@ -148,16 +157,21 @@ def mla_cache_slots(cfg) -> int:
     return cfg.reqs * cfg.max_blocks * cfg.block_size
 
 
-def set_bytes(cfg) -> int:
-    b = cfg.S * cfg.rows * cfg.ld * 4
+def set_bytes(cfg, path: str = "steps") -> int:
+    """Bytes of one rotating input set: the logits (or, on the logits path,
+    the fp8 query heads and weights) and the combine's partial outputs."""
+    if path == "logits":
+        b = cfg.rows * (W.IDX_HEADS * W.IDX_DIM + 4 * W.IDX_HEADS)
+    else:
+        b = cfg.S * cfg.rows * cfg.ld * 4
     if cfg.H:
         b += cfg.S * cfg.rows * cfg.H * (cfg.D * 2 + 4)
     return b
 
 
-def replicas_for(cfg) -> int:
+def replicas_for(cfg, path: str = "steps") -> int:
     """Rotating input sets so that a set is out of L2 when it is used again."""
-    return int(min(8, max(2, -(-int(2.5 * L2_BYTES) // set_bytes(cfg)))))
+    return int(min(8, max(2, -(-int(2.5 * L2_BYTES) // set_bytes(cfg, path)))))
 
 
 def algorithmic_bytes(cfg, ends: np.ndarray) -> dict:
@@ -171,6 +185,8 @@ def algorithmic_bytes(cfg, ends: np.ndarray) -> dict:
         written, per row.
     slot_mapping: per new token its position (and request) read, one block-table
         word read, S slots written.
+    indexer_logits: per row its 64 x 128 fp8 query heads and 64 fp32 weights, the
+        keys of its request once (128 fp8 bytes a token), 4 B per logit written.
     sparse_mla_decode: per (row, shard) the query (H x 576 bf16) and its count,
         per selected slot the slot and the cache row (576 bf16) read; per (row,
         shard) H x 512 bf16 outputs and H LSEs written.  The selected slots of a
@@ -188,7 +204,25 @@ def algorithmic_bytes(cfg, ends: np.ndarray) -> dict:
         "slot_mapping": int(R * (4 + (4 if cfg.reqs != cfg.rows else 0) + 4 + 4 * S)),
         "sparse_mla_decode": int(selected(cfg, ends) * (4 + 2 * W.MLA_DQK)
                                  + R * S * (H * 2 * W.MLA_DQK + 4 + H * (2 * W.MLA_DV + 4))),
+        # the row's fp8 query heads and weights, its request's keys, the
+        # logits written (4 B per scored token)
+        "indexer_logits": int(R * (W.IDX_HEADS * W.IDX_DIM + 4 * W.IDX_HEADS)
+                              + indexer_key_bytes(cfg, ends) + logits),
     }
+
+
+def indexer_key_bytes(cfg, ends: np.ndarray) -> int:
+    """Keys the logits step must read: each request's tokens up to the longest
+    row that reads it, 128 fp8 bytes a token (one request per row, or one
+    request shared by every row)."""
+    if cfg.reqs == cfg.rows:
+        return int(W.IDX_DIM * ends.astype(np.int64).sum())
+    return int(W.IDX_DIM * int(ends.max(initial=0)))
+
+
+def indexer_flops(ends: np.ndarray) -> int:
+    """Head dot products (64 heads x 128 fp8 multiply-adds) per scored token."""
+    return int(2 * W.IDX_HEADS * W.IDX_DIM * ends.astype(np.int64).sum())
 
 
 def selected(cfg, ends: np.ndarray) -> int:
@@ -335,6 +369,23 @@ def profiled_traffic(kernel: str, workload: str = DEFAULT_WORKLOAD) -> float | N
 # the oracle as CPU baseline / reference arm
 # ---------------------------------------------------------------------------
 def oracle_rows(inp: dict, cfg, rows: np.ndarray, path: str = "fused"):
+    if path == "logits":
+        from oracle import combine as OC
+        from oracle import indexer_logits as IL
+        from oracle import pipeline as OP
+        rows = np.asarray(rows)
+        lg = IL.shard_logits(inp["iq"], inp["iw"], inp["kcache"], inp["starts"], inp["ends"],
+                             cfg.S, cfg.I, inp["bt"], cfg.block_size, row_to_req=inp["r2q"],
+                             ld=cfg.ld, rows=rows, fill=0.0)
+        # the selected rows' logits stand in rows 0.. of a batch of len(rows)
+        sub = lambda a: None if a is None else a[rows]
+        res = OP.run_rows(lg, sub(inp["starts"]), sub(inp["ends"]), cfg.S, cfg.I, cfg.K,
+                          tables=inp["bt"], row_to_req=(rows if inp["r2q"] is None
+                                                        else inp["r2q"][rows]),
+                          block_size=cfg.block_size)
+        if cfg.H:
+            OC.lse_combine(OC.bf16_to_f64(inp["part"][:, rows]), inp["lse2"][:, rows])
+        return res
     if path == "attention":
         from oracle import attention as OA
         from oracle import combine as OC
@@ -373,8 +424,8 @@ def metric_for(path: str) -> tuple[str, str]:
 def dtype_for(path: str) -> str:
     """The arithmetic the path computes in: fp32 keys and scores (the combine
     accumulates in fp32), or int32 index maps only."""
-    return {"write_slots": "i32", "attention": "f32 indexer, bf16 attention (fp32 accumulate)"}.get(
-        path, "f32")
+    return {"write_slots": "i32", "attention": "f32 indexer, bf16 attention (fp32 accumulate)",
+            "logits": "fp8 e4m3 logits (fp32 accumulate), f32 indexer"}.get(path, "f32")
 
 
 def cpu_baseline(cfg, inp: dict, budget_s: float = 10.0, path: str = "fused") -> dict:
@@ -498,6 +549,8 @@ def run_reference(args, world, rank):
     inp = host_inputs(cfg, 0, args.path)
     if args.path == "attention":
         inp["cache"] = W.mla_cache_uniform(cfg.S, mla_cache_slots(cfg), seed=4242)
+    if args.path == "logits":
+        inp["kcache"] = W.indexer_keys(cfg.S, mla_cache_slots(cfg), seed=4343)
     metric, unit = metric_for(args.path)
     t = time.perf_counter()
     oracle_rows(inp, cfg, np.array([0]), args.path)
@@ -565,13 +618,19 @@ def config_block(cfg, path: str = "fused") -> dict:
             "rows": cfg.rows, "S": cfg.S, "I": cfg.I, "K": cfg.K, "block_size": cfg.block_size,
             "H": cfg.H, "D": cfg.D,
             "path": " -> ".join(kernels_for(cfg, path)) + " (C ABI, one stream)",
-            "l2": (f"{replicas_for(cfg)} rotating input sets of {set_bytes(cfg) / 1e6:.0f} MB "
+            "l2": (f"{replicas_for(cfg, path)} rotating input sets of "
+                   f"{set_bytes(cfg, path) / 1e6:.0f} MB "
                    f"(> 2.5x L2 together); no flush" if path != "write_slots" else
                    "positions and block tables (a few MB at most) stay in L2; no flush")
                   + (f"; resident KV caches of {cfg.S * mla_cache_slots(cfg) * 2 * W.MLA_DQK / 1e9:.1f}"
                      f" GB (bf16, |v| in [0.5, 1)), softmax scale 1/sqrt(192)"
-                     if path == "attention" else ""),
-            "logits": "i.i.d. N(0,1) per shard (work-equivalent to the recipe)",
+                     if path == "attention" else "")
+                  + (f"; resident fp8 key caches of {cfg.S * mla_cache_slots(cfg) * W.IDX_DIM / 1e6:.0f}"
+                     f" MB (every block the tables address)" if path == "logits" else ""),
+            "logits": ("computed: 64 fp8 e4m3 query heads of 128 values and fp32 head weights "
+                       "per row, fp8 keys; codes with a random sign, exponent field 4..9 and "
+                       "mantissa" if path == "logits" else
+                       "i.i.d. N(0,1) per shard (work-equivalent to the recipe)"),
             "parallelism": "replicas (rows independent, no collective)"}
 
 
@@ -612,7 +671,7 @@ def main(argv=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device())
     cfg = W.CONFIGS[args.workload]
     S, R, K, H, D = cfg.S, cfg.rows, cfg.K, cfg.H, cfg.D
-    REPLICAS = replicas_for(cfg)
+    REPLICAS = replicas_for(cfg, args.path)
     if args.path in ("fused", "attention") and S > 8:
         raise SystemExit("the fused indexer takes at most 8 shards")
     if args.path == "attention" and not H:
@@ -623,8 +682,11 @@ def main(argv=None) -> int:
     d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     sets = []
     for h in host:
-        st = dict(logits=d(h["logits"]), starts=d(h["starts"]), ends=d(h["ends"]),
-                  bt=d(h["bt"]), pos=d(h["pos"]))
+        st = dict(starts=d(h["starts"]), ends=d(h["ends"]), bt=d(h["bt"]), pos=d(h["pos"]))
+        if h["logits"] is not None:
+            st["logits"] = d(h["logits"])
+        if "iq" in h:
+            st["iq"], st["iw"] = d(h["iq"]), d(h["iw"])
         if h["r2q"] is not None:
             st["r2q"] = d(h["r2q"])
         if H:
@@ -641,6 +703,13 @@ def main(argv=None) -> int:
         cache_dev = d(cache_host.view(np.int16))
         attn_out = torch.empty((S, R, H, W.MLA_DV), dtype=torch.int16, device=dev)
         attn_lse = torch.empty((S, R, H), dtype=torch.float32, device=dev)
+    if args.path == "logits":
+        # Each shard's paged fp8 key cache (every block the tables address),
+        # resident as a serving cache is; one logits buffer the steps read.
+        n_slots = mla_cache_slots(cfg)
+        kcache_host = W.indexer_keys(S, n_slots, seed=4343 + rank)
+        kcache_dev = d(kcache_host)
+        lg = torch.empty((S, R, cfg.ld), dtype=torch.float32, device=dev)
     cand = torch.empty((R, S * K, 2), dtype=torch.float32, device=dev)
     ids = torch.empty((R, K), dtype=torch.int32, device=dev)
     slots = torch.empty((S, R, K), dtype=torch.int32, device=dev)
@@ -673,6 +742,18 @@ def main(argv=None) -> int:
                                              P(attn_lse), P(err), sp)),
                 (lib.dsa_lse_combine, (P(attn_out), P(attn_lse), S, R, H, D, P(out), P(lse),
                                        P(err), sp))))
+        elif args.path == "logits":
+            calls.append((
+                (lib.dsa_indexer_logits, (P(st["iq"]), P(st["iw"]), P(kcache_dev), n_slots,
+                                          P(st["bt"]), cfg.reqs, cfg.max_blocks, cfg.block_size,
+                                          r2q, P(st["starts"]), P(st["ends"]), R, S, cfg.I,
+                                          P(lg), ld, P(err), sp)),
+                (lib.dsa_shard_topk_pack, (P(lg), ld, R, S, cfg.I, K, P(st["starts"]),
+                                           P(st["ends"]), None, P(cand), P(err), sp)),
+                (lib.dsa_merge_topk_stable, (P(cand), R, S * K, K, P(ids), None, P(err), sp)),
+                (lib.dsa_convert_index_compact, (P(ids), R, K, S, cfg.I, P(st["bt"]), cfg.reqs,
+                                                 cfg.max_blocks, cfg.block_size, r2q,
+                                                 P(slots), P(counts), P(err), sp))) + tail)
         elif args.path == "write_slots":
             calls.append(((lib.dsa_slot_mapping, (P(st["pos"]), r2q, R, S, cfg.I, P(st["bt"]),
                                                   cfg.reqs, cfg.max_blocks, cfg.block_size,
@@ -865,18 +946,44 @@ def main(argv=None) -> int:
             flops=flops, tflops=tflops, tensor_peak_tflops=tpeak,
             tensor_frac=tflops / tpeak if tpeak else None)
 
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                "bytes_per_launch": nbytes[dominant],
+                "traffic": profiled_traffic(dominant, args.workload)}
+    if "indexer_logits" in kernels:
+        # fp8 contraction: its tensor rate against the fp8 dense peak (the
+        # measured bf16 burst peak times the nominal fp8:bf16 ratio of 2), and
+        # the bound its arithmetic intensity puts it under
+        flops = float(np.mean([indexer_flops(h["ends"] - h["starts"]) for h in host]))
+        tflops = flops / (mean_ms["indexer_logits"] / 1e3) / 1e12
+        fp8_peak = 2.0 * measured_tensor_peak()
+        ridge = fp8_peak * 1e12 / (peak * 1e9)
+        intensity = flops / nbytes["indexer_logits"]
+        kernels["indexer_logits"].update(
+            flops=flops, tflops=tflops, fp8_peak_tflops=fp8_peak, tensor_frac=tflops / fp8_peak,
+            flop_per_byte=intensity, bound="tensor" if intensity > ridge else "hbm")
+        if dominant == "indexer_logits" and intensity > ridge:
+            roofline = {"bound": "tensor", "kernel": dominant, "achieved": tflops,
+                        "peak": fp8_peak, "unit": "TFLOP/s", "frac": tflops / fp8_peak,
+                        "peak_kind": "measured bf16 burst x 2 (nominal fp8:bf16 dense ratio)",
+                        "flops_per_launch": flops, "bytes_per_launch": nbytes[dominant],
+                        "traffic": profiled_traffic(dominant, args.workload)}
+
     # --- e2e through host buffers --------------------------------------------
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     hsets = []
     for h in host[:2]:
         if args.path == "write_slots":       # the new tokens and the tables they go through
             hs = dict(pos=pin(h["pos"]), bt=pin(h["bt"]))
+        elif args.path == "logits":           # fp8 queries and weights; keys stay resident
+            hs = dict(iq=pin(h["iq"]), iw=pin(h["iw"]), starts=pin(h["starts"]),
+                      ends=pin(h["ends"]), bt=pin(h["bt"]))
         else:
             hs = dict(logits=pin(h["logits"]), starts=pin(h["starts"]), ends=pin(h["ends"]),
                       bt=pin(h["bt"]))
         if h["r2q"] is not None:
             hs["r2q"] = pin(h["r2q"])
-        if H and args.path in ("fused", "steps"):
+        if H and args.path in ("fused", "steps", "logits"):
             hs["part"] = pin(h["part"].view(np.int16))
             hs["lse2"] = pin(h["lse2"])
         if "q" in h:
@@ -976,10 +1083,7 @@ def main(argv=None) -> int:
         "dtype": dtype_for(args.path), "data": "synthetic", "config": config_block(cfg, args.path),
         "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
         "hbm_frac_step": step_bytes / (ms_per_step / 1e3) / 1e9 / peak,
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                     "bytes_per_launch": nbytes[dominant],
-                     "traffic": profiled_traffic(dominant, args.workload)},
+        "roofline": roofline,
         "kernels": kernels,
         "timing": (f"K steps as CUDA-graph replays: a graph of one step on each of the {REPLICAS} "
                    "rotating input sets back to back (as a model-forward graph holds the "
@@ -1010,6 +1114,8 @@ def main(argv=None) -> int:
             base_inp = dict(host[0])
             if args.path == "attention":
                 base_inp["cache"] = cache_host
+            if args.path == "logits":
+                base_inp["kcache"] = kcache_host
             result["cpu_baseline"] = cpu_baseline(cfg, base_inp, path=args.path)
             try:
                 result["cpu_baseline_all_cores"] = cpu_baseline_all_cores(cfg, base_inp,

@@ -9,26 +9,33 @@
 // reach the DCP top-K, each rank scoring its local KV shard; the head sum is
 // the DeepSeek-V3.2-style indexer reading of that step).
 //
-// One CTA per (shard, row, chunk of 16 tiles of 128 local slots), six warps:
-//   warp 4   TMA producer: the row's 64 query heads once (8 KB), then per tile
-//            the 128 keys, one 2-D tensor copy per block of the paged cache
-//            (a 64-row box for 64-token blocks), into a 4-stage ring; the
-//            copies use the 128-byte swizzle that the MMA descriptors name.
-//            Warp 4 also allocates and frees the tensor memory.
-//   warp 5   MMA issuer (one thread): per tile, D[128 tokens][64 heads] =
-//            K_tile . Q^T as four tcgen05.mma kind::f8f6f4 (K = 32 each) into
-//            one of two 64-column fp32 accumulators in tensor memory; a commit
-//            frees the key stage, another hands the accumulator to the
-//            epilogue.
-//   warps 0-3  epilogue: warp w reads tensor-memory lanes 32w..32w+31 (one
-//            token per thread, 64 head sums), applies ReLU and the head
-//            weights, and stores the logit (a warp writes 32 consecutive
-//            slots); then it releases the accumulator.
+// Persistent CTAs walk work items (shard, group of G rows, chunk of 16 tiles
+// of 128 local slots) round-robin.  G = 4 when every row reads the same
+// request (one key tile then serves four rows), else 1.  Warp roles:
+//   producer (warp E)  TMA: per item the group's query heads (G x 8 KB) and
+//            weights into one of two slots, per tile the 128 keys, one 2-D
+//            tensor copy per block of the paged cache (a 64-row box for
+//            64-token blocks), into a 4-stage ring, 128-byte swizzle.  It also
+//            allocates and frees the tensor memory.
+//   MMA (warp E + 1, one thread)  per tile D[128 tokens][G x 64 heads] =
+//            K_tile . Q^T: four tcgen05.mma kind::f8f6f4 (N = 64 G, K = 32
+//            each) into the next accumulator in tensor memory; commits free
+//            the key stage, hand the accumulator to the epilogue and, after an
+//            item's last tile, free its query slot.
+//   epilogue (warps 0 .. E-1, E = 4 G)  warp e reads tensor-memory lanes
+//            32 (e % 4) .. + 31 (one token per thread) of row e / 4, applies
+//            ReLU and the head weights (read from shared memory) and stores
+//            one logit (a warp writes 32 consecutive slots); then it releases
+//            the accumulator.  Four accumulators when ungrouped (two CTAs per
+//            SM), two when grouped: the MMAs run ahead of the epilogue.
+// Barrier phases run on across items (a tile counter and an item counter).
 // Every wait is bounded: a wait that runs out raises DSA_FLAG_TIMEOUT, the
 // roles stop, drain their copies and MMAs (bounded) and the tensor memory is
 // freed before exit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 
@@ -38,27 +45,48 @@ namespace {
 constexpr int kHeads = DSA_IDX_HEADS;      // 64
 constexpr int kDim = DSA_IDX_DIM;          // 128 fp8 values = 128 bytes per row
 constexpr int kTile = 128;                 // tokens per tile = MMA M
-constexpr int kStages = 4;
-constexpr int kTilesPerCta = 16;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 128;        // two 64-column accumulators
+constexpr int kTilesPerItem = 16;
+// Block-table entries one item can need: 16 tiles of 128 slots in blocks of
+// at least 16 slots, plus one for a range that starts mid-block.
+constexpr int kItemBlocks = kTilesPerItem * 128 / 16 + 1;
 constexpr uint32_t kTileBytes = kTile * kDim;
-constexpr uint32_t kQBytes = kHeads * kDim;
+constexpr uint32_t kQBytes = kHeads * kDim;  // one row's query heads
 
+template <int G>
+struct LogitsCfg {
+  // Key stages: enough bytes in flight to cover the latency of the key reads
+  // at the rate the MMAs consume them (one CTA per SM when grouped).
+  static constexpr int kStages = G == 1 ? 4 : 8;
+  // One epilogue warp per (lane quarter, row): a tile's epilogue latency is
+  // one row's, and the MMAs run ahead by as many accumulators as the tensor
+  // memory holds (two CTAs per SM when ungrouped, one when grouped).
+  static constexpr int kEpiWarps = 4 * G;
+  static constexpr int kAccBufs = G == 1 ? 4 : 2;
+  static constexpr int kThreads = (kEpiWarps + 2) * 32;
+  static constexpr int kProducer = kEpiWarps, kMma = kEpiWarps + 1;
+  static constexpr uint32_t kAccCols = (uint32_t)G * kHeads;   // one accumulator
+  static constexpr uint32_t kTmemCols = kAccBufs * kAccCols;   // 256 or 512
+};
+
+template <int G>
 struct alignas(1024) LogitsSmem {
+  static constexpr int kStages = LogitsCfg<G>::kStages;
   uint8_t k[kStages][kTileBytes];          // 1024-aligned: the swizzle atom
-  uint8_t q[kQBytes];
-  float w[kHeads];
-  uint64_t full[kStages], empty[kStages], qfull, accfull[2], accempty[2], drain;
+  uint8_t q[2][G * kQBytes];               // the item's query heads, two slots
+  float w[2][G * kHeads];                  // and weights
+  int32_t pblk[kItemBlocks];               // the item's block-table entries
+  uint64_t full[kStages], empty[kStages], qfull[2], qfree[2];
+  uint64_t accfull[LogitsCfg<G>::kAccBufs], accempty[LogitsCfg<G>::kAccBufs], drain;
   uint32_t tmem;
   int abort;
 };
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1),
-// A and B e4m3 (format 0), both K-major, N = 64 (bits 17-22: N >> 3),
-// M = 128 (bits 24-28: M >> 4).
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kHeads >> 3) << 17) |
-                            ((uint32_t)(kTile >> 4) << 24);
+// A and B e4m3 (format 0), both K-major, N (bits 17-22: N >> 3), M = 128
+// (bits 24-28: M >> 4).
+constexpr uint32_t idesc_f8(int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTile >> 4) << 24);
+}
 
 // Shared-memory matrix descriptor, K-major with the 128-byte swizzle: start
 // address >> 4 (bits 0-13), leading offset (unused here, 1), stride between
@@ -79,11 +107,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accum) {
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accum) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(kIdesc), "r"(accum)
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
       : "memory");
 }
 
@@ -106,9 +135,10 @@ __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// 64 consecutive fp32 columns of this warp's 32 tensor-memory lanes (four
-// 16-column loads, then one wait).  The wait names every destination register
-// as read and written, so no use of them can be scheduled before it.
+// 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes (two
+// 16-column loads, then one wait).  The wait is followed by empty statements
+// that name every destination register as read and written, so no use of
+// them can be scheduled before it.
 #define DSA_TMEM_LD16(o)                                                                    \
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, "  \
                "%8, %9, %10, %11, %12, %13, %14, %15}, [%16];"                              \
@@ -124,26 +154,74 @@ __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
                  "+r"(r[o + 8]), "+r"(r[o + 9]), "+r"(r[o + 10]), "+r"(r[o + 11]),         \
                  "+r"(r[o + 12]), "+r"(r[o + 13]), "+r"(r[o + 14]), "+r"(r[o + 15]))
 
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   DSA_TMEM_LD16(0);
   DSA_TMEM_LD16(16);
-  DSA_TMEM_LD16(32);
-  DSA_TMEM_LD16(48);
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-  // Empty statements that read and write every destination after the wait.
   DSA_WAIT_LD16(0);
   DSA_WAIT_LD16(16);
-  DSA_WAIT_LD16(32);
-  DSA_WAIT_LD16(48);
 }
 #undef DSA_TMEM_LD16
 #undef DSA_WAIT_LD16
 
-__device__ __forceinline__ bool aborted(const LogitsSmem& sm) {
+template <int G>
+__device__ __forceinline__ bool aborted(const LogitsSmem<G>& sm) {
   return *reinterpret_cast<const volatile int*>(&sm.abort) != 0;
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+// One work item: shard s, rows r0 .. r0 + nrows - 1 (nrows <= G), the tiles
+// [t_lo, t_lo + ntiles) of local slots covering their ranges inside chunk c.
+// Every role computes it the same way from the same inputs.
+template <int G>
+struct Item {
+  int s, r0, nrows, ntiles;
+  int64_t t_lo;
+  int64_t lo[G], hi[G];
+};
+
+template <int G>
+__device__ __forceinline__ Item<G> make_item(int it, int rows, int groups, int chunks,
+                                             const int32_t* row_starts, const int32_t* row_ends,
+                                             int64_t ld, const ShardMath& sh, bool* bad) {
+  Item<G> x;
+  const int c = it % chunks;
+  const int sg = it / chunks;
+  x.s = sg / groups;
+  x.r0 = (sg - x.s * groups) * G;
+  x.nrows = min(G, rows - x.r0);
+  int64_t glo = INT64_MAX, ghi = 0;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    x.lo[g] = x.hi[g] = 0;
+    if (g < x.nrows) {
+      const int r = x.r0 + g;
+      int64_t st = row_starts ? (int64_t)row_starts[r] : 0, en = row_ends[r];
+      if (st < 0) { st = 0; *bad = true; }
+      if (en < st) { en = st; *bad = true; }
+      int64_t lo = sh.local_len((uint32_t)st, x.s), hi = sh.local_len((uint32_t)en, x.s);
+      if (hi > ld) { hi = ld; *bad = true; }
+      if (lo > hi) { lo = hi; *bad = true; }
+      x.lo[g] = lo;
+      x.hi[g] = hi;
+      if (hi > lo) {
+        glo = min(glo, lo);
+        ghi = max(ghi, hi);
+      }
+    }
+  }
+  if (ghi <= 0 || glo >= ghi) {
+    x.t_lo = 0;
+    x.ntiles = 0;
+    return x;
+  }
+  x.t_lo = max(glo / kTile, (int64_t)c * kTilesPerItem);
+  const int64_t t_hi = min((ghi + kTile - 1) / kTile, (int64_t)(c + 1) * kTilesPerItem);
+  x.ntiles = (int)max((int64_t)0, t_hi - x.t_lo);
+  return x;
+}
+
+template <int G>
+__global__ void __launch_bounds__(LogitsCfg<G>::kThreads, G == 1 ? 2 : 1)
     indexer_logits_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_q, const float* __restrict__ w,
                           const int32_t* __restrict__ block_table, int reqs, int max_blocks,
@@ -151,115 +229,147 @@ __global__ void __launch_bounds__(kThreads, 2)
                           const int32_t* __restrict__ row_to_req,
                           const int32_t* __restrict__ row_starts,
                           const int32_t* __restrict__ row_ends, int rows, int S, int64_t ld,
-                          int chunks, float* __restrict__ logits, uint32_t* flags,
-                          const ShardMath sh) {
+                          int chunks, int nitems, float* __restrict__ logits, uint32_t* flags,
+                          const ShardMath sh, const FastDiv fbs) {
+  using Cfg = LogitsCfg<G>;
+  constexpr int kStages = Cfg::kStages;
   extern __shared__ unsigned char logits_smem_raw[];
-  LogitsSmem& sm = *reinterpret_cast<LogitsSmem*>(
+  LogitsSmem<G>& sm = *reinterpret_cast<LogitsSmem<G>*>(
       (reinterpret_cast<uintptr_t>(logits_smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x % chunks;
-  const int sr = blockIdx.x / chunks;
-  const int s = sr / rows, r = sr - s * rows;
+  const int groups = (rows + G - 1) / G;
 
-  // This row's local range on shard s (clipped to ld, as the local top-K does).
-  int64_t st = row_starts ? (int64_t)row_starts[r] : 0, en = row_ends[r];
-  bool bad = false;
-  if (st < 0) { st = 0; bad = true; }
-  if (en < st) { en = st; bad = true; }
-  int64_t lo = sh.local_len((uint32_t)st, s), hi = sh.local_len((uint32_t)en, s);
-  if (hi > ld) { hi = ld; bad = true; }
-  if (lo > hi) { lo = hi; bad = true; }
-  if (bad && tid == 0 && c == 0) raise_flag(flags, DSA_FLAG_BOUNDS);
-  const int64_t t_lo = max(lo / kTile, (int64_t)c * kTilesPerCta);
-  const int64_t t_hi = min((hi + kTile - 1) / kTile, (int64_t)(c + 1) * kTilesPerCta);
-  const int ntiles = (int)max((int64_t)0, t_hi - t_lo);
-  if (ntiles == 0) return;   // same in every thread
-
-  if (warp == 4) {
+  if (warp == Cfg::kProducer) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&sm.tmem)),
-                 "r"(kTmemCols)
+                 "r"(Cfg::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (tid == 32 * 5) {
+  if (tid == 32 * Cfg::kMma) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], 1);
     }
-    mbar_init(&sm.qfull, 1);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.qfull[b], 1);
+      mbar_init(&sm.qfree[b], 1 + Cfg::kEpiWarps);   // the MMA commit + every epilogue warp
+    }
+    for (int b = 0; b < Cfg::kAccBufs; ++b) {
       mbar_init(&sm.accfull[b], 1);
-      mbar_init(&sm.accempty[b], 4);   // one arrival per epilogue warp
+      mbar_init(&sm.accempty[b], Cfg::kEpiWarps);
     }
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     mbar_init_fence();
   }
-  if (tid < kHeads) sm.w[tid] = w[(int64_t)r * kHeads + tid];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
-  const int req = row_to_req ? row_to_req[r] : r;
+  bool bad = false;
 
-  if (warp == 4) {
-    // ---- producer ---------------------------------------------------------
-    if (lane == 0) {
-      mbar_expect_tx(&sm.qfull, kQBytes);
-      tma_load_2d(sm.q, &tm_q, 0, r * kHeads, &sm.qfull);
+  if (warp == Cfg::kProducer) {
+    // ---- producer: the warp stages each item's block-table entries in shared
+    // memory (one coalesced load), lane 0 issues the copies -----------------
+    const int oob_y = (int)((int64_t)S * n_slots);   // past the cache: zero fill
+    const int boxes = box_rows == 64 ? 2 : (box_rows == 32 ? 4 : 8);   // per tile of 128 slots
+    int gt = 0, icount = 0;
+    for (int it = blockIdx.x; it < nitems && !aborted(sm); it += gridDim.x) {
+      const Item<G> x = make_item<G>(it, rows, groups, chunks, row_starts, row_ends, ld, sh, &bad);
+      if (x.ntiles == 0) continue;
+      const int req = row_to_req ? row_to_req[x.r0] : x.r0;
       const bool req_ok = req >= 0 && req < reqs;
-      if (!req_ok) raise_flag(flags, DSA_FLAG_BOUNDS);
-      const int32_t* bt = block_table + ((int64_t)s * reqs + (req_ok ? req : 0)) * max_blocks;
-      const int oob_y = (int)((int64_t)S * n_slots);   // past the cache: zero fill
-      int issued = 0;
-      for (int k = 0; k < ntiles; ++k) {
-        const int stg = k % kStages;
-        if (k >= kStages && !mbar_wait(&sm.empty[stg], (uint32_t)((k / kStages) - 1) & 1u)) {
+      if (!req_ok) bad = true;
+      const int32_t* bt = block_table + ((int64_t)x.s * reqs + (req_ok ? req : 0)) * max_blocks;
+      int64_t ghi = 0;
+#pragma unroll
+      for (int g = 0; g < G; ++g) ghi = max(ghi, x.hi[g]);
+      // Local slots are below ld < 2^31: 32-bit maps (no 64-bit division).
+      const uint32_t tok_lo = (uint32_t)(x.t_lo * kTile);
+      const uint32_t tok_end = (uint32_t)min((x.t_lo + x.ntiles) * kTile, ghi);
+      const int blk0 = (int)fdiv(tok_lo, fbs);
+      const int blk_end = min(max_blocks, (int)fdiv(tok_end + (uint32_t)block_size - 1u, fbs));
+      const int nblk = max(0, blk_end - blk0);   // <= kItemBlocks
+      __syncwarp();                      // lane 0 is done with the previous item's entries
+      for (int i = lane; i < nblk; i += 32) sm.pblk[i] = req_ok ? bt[blk0 + i] : -1;
+      __syncwarp();
+      if (lane == 0) {
+        const int qb = icount & 1;
+        if (icount >= 2 && !mbar_wait(&sm.qfree[qb], (uint32_t)((icount >> 1) - 1) & 1u)) {
           raise_flag(flags, DSA_FLAG_TIMEOUT);
           sm.abort = 1;
-          break;
-        }
-        if (aborted(sm)) break;
-        mbar_expect_tx(&sm.full[stg], kTileBytes);
-        const int64_t tok0 = (t_lo + k) * kTile;
-        for (int j = 0; j < kTile / box_rows; ++j) {
-          const int64_t l0 = tok0 + (int64_t)j * box_rows;   // first local slot of the box
-          const int64_t blk = l0 / block_size, off = l0 - blk * block_size;
-          int y = oob_y;
-          if (req_ok && l0 < hi && blk < max_blocks) {
-            const int64_t p = bt[blk];
-            if (p >= 0 && p * block_size + off + box_rows <= n_slots)
-              y = (int)((int64_t)s * n_slots + p * block_size + off);
-            else
-              raise_flag(flags, DSA_FLAG_BOUNDS);
+        } else {
+          mbar_expect_tx(&sm.qfull[qb], (uint32_t)G * kQBytes + (uint32_t)x.nrows * kHeads * 4u);
+          tma_load_2d(sm.q[qb], &tm_q, 0, x.r0 * kHeads, &sm.qfull[qb]);
+          bulk_g2s(sm.w[qb], w + (int64_t)x.r0 * kHeads, (uint32_t)x.nrows * kHeads * 4u,
+                   &sm.qfull[qb]);
+          ++icount;
+          for (int k = 0; k < x.ntiles; ++k, ++gt) {
+            const int stg = gt % kStages;
+            if (gt >= kStages &&
+                !mbar_wait(&sm.empty[stg], (uint32_t)((gt / kStages) - 1) & 1u)) {
+              raise_flag(flags, DSA_FLAG_TIMEOUT);
+              sm.abort = 1;
+              break;
+            }
+            if (aborted(sm)) break;
+            mbar_expect_tx(&sm.full[stg], kTileBytes);
+            const uint32_t tok0 = tok_lo + (uint32_t)k * kTile;
+            for (int j = 0; j < boxes; ++j) {
+              const uint32_t l0 = tok0 + (uint32_t)(j * box_rows);   // first slot of the box
+              uint32_t off;
+              const int blk = (int)fdivmod(l0, fbs, &off);
+              int y = oob_y;
+              if (blk < blk_end) {          // a block holding slots of the range
+                const int64_t p = sm.pblk[blk - blk0];
+                if (p >= 0 && p * block_size + off + box_rows <= n_slots)
+                  y = (int)((int64_t)x.s * n_slots + p * block_size + off);
+                else
+                  bad = true;
+              }
+              tma_load_2d(sm.k[stg] + (uint32_t)j * box_rows * kDim, &tm_k, 0, y, &sm.full[stg]);
+            }
           }
-          tma_load_2d(sm.k[stg] + (uint32_t)j * box_rows * kDim, &tm_k, 0, y, &sm.full[stg]);
         }
-        ++issued;
       }
-      // Drain: every issued tile's copies have landed before the CTA can exit.
-      mbar_wait(&sm.qfull, 0);
-      for (int k = max(0, issued - kStages); k < issued; ++k)
+    }
+    // Drain: every issued copy has landed before the CTA can exit.
+    if (lane == 0) {
+      for (int i = max(0, icount - 2); i < icount; ++i)
+        mbar_wait(&sm.qfull[i & 1], (uint32_t)(i >> 1) & 1u);
+      for (int k = max(0, gt - kStages); k < gt; ++k)
         mbar_wait(&sm.full[k % kStages], (uint32_t)(k / kStages) & 1u);
     }
-  } else if (warp == 5) {
+  } else if (warp == Cfg::kMma) {
     // ---- MMA issuer -------------------------------------------------------
     if (lane == 0) {
-      bool ok = mbar_wait(&sm.qfull, 0);
-      const uint64_t qdesc = sw128_desc(sm.q);
-      for (int k = 0; ok && k < ntiles; ++k) {
-        const int stg = k % kStages, b = k & 1;
-        if (k >= 2 && !mbar_wait(&sm.accempty[b], (uint32_t)((k >> 1) - 1) & 1u)) { ok = false; break; }
-        if (!mbar_wait(&sm.full[stg], (uint32_t)(k / kStages) & 1u)) { ok = false; break; }
-        if (aborted(sm)) break;
-        tc_fence_after();
-        const uint64_t kdesc = sw128_desc(sm.k[stg]);
+      constexpr uint32_t idesc = idesc_f8(G * kHeads);
+      bool ok = true;
+      int gt = 0, icount = 0;
+      for (int it = blockIdx.x; ok && it < nitems && !aborted(sm); it += gridDim.x) {
+        const Item<G> x = make_item<G>(it, rows, groups, chunks, row_starts, row_ends, ld, sh, &bad);
+        if (x.ntiles == 0) continue;
+        const int qb = icount & 1;
+        if (!mbar_wait(&sm.qfull[qb], (uint32_t)(icount >> 1) & 1u)) { ok = false; break; }
+        ++icount;
+        const uint64_t qdesc = sw128_desc(sm.q[qb]);
+        for (int k = 0; k < x.ntiles; ++k, ++gt) {
+          constexpr int NB = Cfg::kAccBufs;
+          const int stg = gt % kStages, b = gt % NB;
+          if (gt >= NB && !mbar_wait(&sm.accempty[b], (uint32_t)((gt / NB) - 1) & 1u)) { ok = false; break; }
+          if (!mbar_wait(&sm.full[stg], (uint32_t)(gt / kStages) & 1u)) { ok = false; break; }
+          if (aborted(sm)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t kdesc = sw128_desc(sm.k[stg]);
 #pragma unroll
-        for (int kk = 0; kk < kDim / 32; ++kk)   // 32 fp8 = 32 bytes = 2 descriptor units
-          mma_f8(tmem + (uint32_t)b * kHeads, kdesc + 2u * kk, qdesc + 2u * kk, kk > 0);
-        mma_commit(&sm.empty[stg]);
-        mma_commit(&sm.accfull[b]);
+          for (int kk = 0; kk < kDim / 32; ++kk)   // 32 fp8 = 32 bytes = 2 descriptor units
+            mma_f8(tmem + (uint32_t)b * Cfg::kAccCols, kdesc + 2u * kk, qdesc + 2u * kk, idesc,
+                   kk > 0);
+          mma_commit(&sm.empty[stg]);
+          mma_commit(&sm.accfull[b]);
+        }
+        mma_commit(&sm.qfree[qb]);   // the item's query slot, once its MMAs are done
       }
       if (!ok) {
         raise_flag(flags, DSA_FLAG_TIMEOUT);
@@ -270,39 +380,75 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_wait(&sm.drain, 0);
     }
   } else {
-    // ---- epilogue: warps 0-3, one token per thread --------------------------
-    float wr[kHeads];
+    // ---- epilogue: warp e reads lanes 32 (e % 4) .. + 31 for row e / 4 -----
+    const int quarter = warp & 3, g = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    int gt = 0, icount = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < nitems && !aborted(sm); it += gridDim.x) {
+      const Item<G> x = make_item<G>(it, rows, groups, chunks, row_starts, row_ends, ld, sh, &bad);
+      if (x.ntiles == 0) continue;
+      const int qb = icount & 1;
+      if (!mbar_wait(&sm.qfull[qb], (uint32_t)(icount >> 1) & 1u)) { ok = false; break; }
+      ++icount;
+      // This warp's row's range (selected with constant indices, so that the
+      // item stays in registers); empty for rows past the batch.
+      int64_t my_lo = 0, my_hi = 0;
 #pragma unroll
-    for (int h = 0; h < kHeads; ++h) wr[h] = sm.w[h];
-    float* out = logits + ((int64_t)s * rows + r) * ld;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    for (int k = 0; k < ntiles; ++k) {
-      const int b = k & 1;
-      if (!mbar_wait(&sm.accfull[b], (uint32_t)(k >> 1) & 1u)) {
-        if (lane == 0) raise_flag(flags, DSA_FLAG_TIMEOUT);
-        sm.abort = 1;
-        break;
+      for (int gg = 0; gg < G; ++gg)
+        if (gg == g && gg < x.nrows) {
+          my_lo = x.lo[gg];
+          my_hi = x.hi[gg];
+        }
+      for (int k = 0; k < x.ntiles; ++k, ++gt) {
+        constexpr int NB = Cfg::kAccBufs;
+        const int b = gt % NB;
+        if (!mbar_wait(&sm.accfull[b], (uint32_t)(gt / NB) & 1u)) { ok = false; break; }
+        if (aborted(sm)) { ok = false; break; }
+        tc_fence_after();
+        const int64_t l = (x.t_lo + k) * kTile + quarter * 32 + lane;
+        {
+          // Four partial sums (heads h mod 4), so the dependent chain is 16 deep;
+          // the 64 head sums are read 32 at a time.
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+          for (int hh = 0; hh < kHeads; hh += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + (uint32_t)b * Cfg::kAccCols + (uint32_t)(g * kHeads + hh),
+                      v);
+            const float4* wv = reinterpret_cast<const float4*>(sm.w[qb] + g * kHeads + hh);
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+              const float4 ww = wv[h4];
+              a0 = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f), a0);
+              a1 = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), a1);
+              a2 = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), a2);
+              a3 = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), a3);
+            }
+          }
+          const float acc = (a0 + a1) + (a2 + a3);
+          if (l >= my_lo && l < my_hi)
+            logits[((int64_t)x.s * rows + x.r0 + g) * ld + l] = acc;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(&sm.accempty[b]);
       }
-      if (aborted(sm)) break;
-      tc_fence_after();
-      uint32_t v[kHeads];
-      tmem_ld64(tmem + lane_base + (uint32_t)(b * kHeads), v);
-      float acc = 0.f;
-#pragma unroll
-      for (int h = 0; h < kHeads; ++h) acc = fmaf(wr[h], fmaxf(__uint_as_float(v[h]), 0.f), acc);
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive1(&sm.accempty[b]);
-      const int64_t l = (t_lo + k) * kTile + warp * 32 + lane;
-      if (l >= lo && l < hi) out[l] = acc;
+      if (lane == 0) mbar_arrive1(&sm.qfree[qb]);   // done with the item's weights
+    }
+    if (!ok) {
+      if (lane == 0) raise_flag(flags, DSA_FLAG_TIMEOUT);
+      sm.abort = 1;
     }
   }
+  if (bad) raise_flag(flags, DSA_FLAG_BOUNDS);
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == Cfg::kProducer) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
+                 "r"(Cfg::kTmemCols)
                  : "memory");
   }
 }
@@ -360,24 +506,42 @@ extern "C" dsa_status dsa_indexer_logits(const uint8_t* q, const float* weights,
     return DSA_ERR_UNSUPPORTED;
   if (rows == 0) return DSA_OK;
   if (!q || !weights || !k_cache || !block_table || !row_ends || !logits) return DSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || (reinterpret_cast<uintptr_t>(logits) & 3u))
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(weights) ||
+      (reinterpret_cast<uintptr_t>(logits) & 3u))
     return DSA_ERR_INVALID_ARG;
   const int box_rows = block_size < 64 ? block_size : 64;
+  // Four rows per MMA when every row must read the same request's keys.
+  const bool grouped = reqs == 1 && rows >= 4;
   CUtensorMap tm_k, tm_q;
   if (!encode_rows(&tm_k, k_cache, (uint64_t)S * (uint64_t)n_slots, (uint32_t)box_rows) ||
-      !encode_rows(&tm_q, q, (uint64_t)rows * kHeads, (uint32_t)kHeads))
+      !encode_rows(&tm_q, q, (uint64_t)rows * kHeads, (uint32_t)(grouped ? 4 : 1) * kHeads))
     return DSA_ERR_CUDA;
-  const int chunks = (int)((ld + (int64_t)kTile * kTilesPerCta - 1) / ((int64_t)kTile * kTilesPerCta));
-  const int64_t blocks = (int64_t)S * rows * chunks;
-  if (blocks > INT32_MAX) return DSA_ERR_UNSUPPORTED;
-  const size_t smem = sizeof(LogitsSmem) + 1024;
-  if (cudaFuncSetAttribute(indexer_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  const int chunks =
+      (int)((ld + (int64_t)kTile * kTilesPerItem - 1) / ((int64_t)kTile * kTilesPerItem));
+  const int G = grouped ? 4 : 1;
+  const int64_t nitems = (int64_t)S * ((rows + G - 1) / G) * chunks;
+  if (nitems > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return DSA_ERR_CUDA;
-  const cudaError_t e = launch_kernel(indexer_logits_kernel, dim3((unsigned)blocks),
-                                      dim3(kThreads), smem, stream, 0, tm_k, tm_q, weights,
-                                      block_table, reqs, max_blocks, block_size, box_rows,
-                                      n_slots, row_to_req, row_starts, row_ends, rows, S, ld,
-                                      chunks, logits, err_flags, ShardMath(S, I));
-  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  auto launch = [&](auto kern, int threads, int per_sm, size_t smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return DSA_ERR_CUDA;
+    // Ungrouped items (one row each, uneven lengths) go one per CTA, so the
+    // hardware's block scheduler balances them; grouped ones share one
+    // persistent CTA per SM.
+    const int grid = per_sm > 1 ? (int)nitems : (int)std::min<int64_t>(nitems, (int64_t)sms * per_sm);
+    const cudaError_t e = launch_kernel(kern, dim3((unsigned)grid), dim3(threads), smem, stream, 0,
+                                        tm_k, tm_q, weights, block_table, reqs, max_blocks,
+                                        block_size, box_rows, n_slots, row_to_req, row_starts,
+                                        row_ends, rows, S, ld, chunks, (int)nitems, logits,
+                                        err_flags, ShardMath(S, I), FastDiv((uint32_t)block_size));
+    return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  };
+  if (grouped)
+    return launch(indexer_logits_kernel<4>, LogitsCfg<4>::kThreads, 1,
+                  sizeof(LogitsSmem<4>) + 1024);
+  return launch(indexer_logits_kernel<1>, LogitsCfg<1>::kThreads, 2, sizeof(LogitsSmem<1>) + 1024);
 }

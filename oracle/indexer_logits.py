@@ -81,7 +81,7 @@ def shard_logits(q_codes, w, k_codes, starts, ends, S: int, I: int, tables, bloc
     q_codes = np.asarray(q_codes, np.uint8)
     R = q_codes.shape[0]
     rows = np.arange(R) if rows is None else np.asarray(rows)
-    keys_all = e4m3_to_f64(k_codes)                    # [S, n_slots, d]
+    k_codes = np.asarray(k_codes, np.uint8)
     if ld is None:
         ld = max(OL.local_count(int(e), s, S, I) for s in range(S) for e in ends)
     out = np.full((S, len(rows), ld), fill, np.float64)
@@ -95,7 +95,7 @@ def shard_logits(q_codes, w, k_codes, starts, ends, S: int, I: int, tables, bloc
                 continue
             l = np.arange(lo, hi)
             phys = tables[s, req, l // block_size].astype(np.int64) * block_size + l % block_size
-            out[s, j, lo:hi] = logits(q, w[r], keys_all[s, phys])
+            out[s, j, lo:hi] = logits(q, w[r], e4m3_to_f64(k_codes[s, phys]))
     return out
 
 
