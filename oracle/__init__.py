@@ -22,6 +22,8 @@ Modules:
   kv_write    the write-side slot mapping of new tokens
   indexer_logits  the indexer's ReLU-weighted head sum of fp8 query-key dot
               products over each shard's paged key cache (fp64)
+  pcp_prefill the PCP prefill cache rows: RMS norm of kv_c, interleaved
+              rotation of k_pe, the ranks' gather, the cache insert (fp64)
 
 Every function is pinned by a `-m "not gpu"` test against something other than
 itself (brute force, a worked example on the pages, closed forms, invariants).

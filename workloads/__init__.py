@@ -26,7 +26,8 @@ __all__ = [
     "Config", "CONFIGS", "rng_for", "row_ranges", "global_logits",
     "iid_local_logits", "block_tables", "combine_inputs",
     "f32_to_bf16_bits", "IDX_HEADS", "IDX_DIM", "e4m3_codes", "indexer_query",
-    "indexer_weights", "indexer_keys",
+    "indexer_weights", "indexer_keys", "PCP_DC", "PCP_DR", "pcp_token_inputs",
+    "rotation_table",
 ]
 
 
@@ -268,3 +269,27 @@ def indexer_keys(S: int, n_slots: int, seed: int) -> np.ndarray:
     """[S, n_slots, 128] fp8 e4m3 codes: each shard's paged indexer key cache
     by physical slot."""
     return e4m3_codes(np.random.default_rng(seed), (S, n_slots, IDX_DIM))
+
+
+# PCP prefill inputs: each new token's latent kv_c (512) and rope part k_pe
+# (64), bf16, the RMS-norm weight, and a per-position rotation table.
+PCP_DC, PCP_DR = 512, 64
+
+
+def pcp_token_inputs(T: int, seed: int):
+    """(kv_c bits uint16 [T, 512], k_pe bits uint16 [T, 64], weight fp32 [512]):
+    N(0,1) values rounded to bf16; weights 1 + N(0, 0.1)."""
+    rng = np.random.default_rng(seed)
+    kv = f32_to_bf16_bits(rng.standard_normal((T, PCP_DC), dtype=np.float32))
+    kpe = f32_to_bf16_bits(rng.standard_normal((T, PCP_DR), dtype=np.float32))
+    w = (1.0 + 0.1 * rng.standard_normal(PCP_DC)).astype(np.float32)
+    return kv, kpe, w
+
+
+def rotation_table(max_pos: int, seed: int) -> np.ndarray:
+    """[max_pos, 64] fp32 rotation table: for every position, the cosines then
+    the sines of 32 angles drawn uniformly from [-pi, pi) (any angles serve:
+    the path applies the table it is given)."""
+    rng = np.random.default_rng(seed)
+    ang = rng.uniform(-np.pi, np.pi, (max_pos, PCP_DR // 2))
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
