@@ -72,8 +72,13 @@ PATHS = {
     # paged key cache (tensor cores), then the step kernels on them
     "logits": ("indexer_logits", "shard_topk_pack", "merge_topk_stable",
                "convert_index_compact", "lse_combine"),
+    # the PCP prefill cache rows: each new token's kv_c normed and k_pe
+    # rotated, materialised for the ranks' gather, then inserted into the cache
+    "pcp_prefill": ("fused_norm_rope", "kv_cache_insert"),
 }
 PATH_METRIC = {"write_slots": ("slot-mapped new tokens/s", "tokens/s"),
+               "pcp_prefill": ("PCP prefill cache rows/s (norm + RoPE materialised, inserted)",
+                               "tokens/s"),
                "attention": ("decode rows/s (indexer, sparse MLA attention, LSE combine)",
                              "rows/s")}
 MLA_SCALE = 1.0 / np.sqrt(192.0)   # softmax scale of the attention path
@@ -85,7 +90,9 @@ KERNEL_SOURCES = {"shard_topk_pack": ("shard_topk.cu", "fast_select.cuh", "local
                   "lse_combine": ("combine.cu",),
                   "slot_mapping": ("slot_mapping.cu",),
                   "sparse_mla_decode": ("attention.cu",),
-                  "indexer_logits": ("indexer_logits.cu",)}
+                  "indexer_logits": ("indexer_logits.cu",),
+                  "fused_norm_rope": ("pcp_prefill.cu",),
+                  "kv_cache_insert": ("pcp_prefill.cu",)}
 
 
 # ---------------------------------------------------------------------------
@@ -149,6 +156,11 @@ def host_inputs(cfg, replica: int, path: str = "fused"):
     if path == "logits":
         d["iq"] = W.indexer_query(cfg.rows, seed=1000 * replica + 9)
         d["iw"] = W.indexer_weights(cfg.rows, seed=1000 * replica + 10)
+    if path == "pcp_prefill":
+        d["kvc"], d["kpe"], d["nw"] = W.pcp_token_inputs(cfg.rows, seed=1000 * replica + 11)
+        rng = np.random.default_rng(1000 * replica + 12)
+        d["cslots"] = rng.permutation(mla_cache_slots(cfg))[:cfg.rows].astype(np.int32)
+        d["ptable"] = W.rotation_table(cfg.max_len, seed=13)
     return d
 
 
@@ -159,7 +171,10 @@ def mla_cache_slots(cfg) -> int:
 
 def set_bytes(cfg, path: str = "steps") -> int:
     """Bytes of one rotating input set: the logits (or, on the logits path,
-    the fp8 query heads and weights) and the combine's partial outputs."""
+    the fp8 query heads and weights; on the PCP path the new tokens' rows) and
+    the combine's partial outputs."""
+    if path == "pcp_prefill":
+        return cfg.rows * (2 * W.MLA_DQK + 8)
     if path == "logits":
         b = cfg.rows * (W.IDX_HEADS * W.IDX_DIM + 4 * W.IDX_HEADS)
     else:
@@ -204,6 +219,11 @@ def algorithmic_bytes(cfg, ends: np.ndarray) -> dict:
         "slot_mapping": int(R * (4 + (4 if cfg.reqs != cfg.rows else 0) + 4 + 4 * S)),
         "sparse_mla_decode": int(selected(cfg, ends) * (4 + 2 * W.MLA_DQK)
                                  + R * S * (H * 2 * W.MLA_DQK + 4 + H * (2 * W.MLA_DV + 4))),
+        # per new token: bf16 kv_c + k_pe (1152 B), its position, its 64
+        # table entries read; the materialised row written
+        "fused_norm_rope": int(R * (2 * W.MLA_DQK + 4 + 4 * 64 + 2 * W.MLA_DQK)),
+        # per new token: the gathered row and its slot read, the cache row written
+        "kv_cache_insert": int(R * (2 * W.MLA_DQK + 4 + 2 * W.MLA_DQK)),
         # the row's fp8 query heads and weights, its request's keys, the
         # logits written (4 B per scored token)
         "indexer_logits": int(R * (W.IDX_HEADS * W.IDX_DIM + 4 * W.IDX_HEADS)
@@ -369,6 +389,16 @@ def profiled_traffic(kernel: str, workload: str = DEFAULT_WORKLOAD) -> float | N
 # the oracle as CPU baseline / reference arm
 # ---------------------------------------------------------------------------
 def oracle_rows(inp: dict, cfg, rows: np.ndarray, path: str = "fused"):
+    if path == "pcp_prefill":
+        from oracle import combine as OC
+        from oracle import pcp_prefill as PP
+        rows = np.asarray(rows)
+        kv, kpe = PP.fused_norm_rope(OC.bf16_to_f64(inp["kvc"][rows]),
+                                     OC.bf16_to_f64(inp["kpe"][rows]), inp["nw"], 1e-6,
+                                     inp["pos"][rows], inp["ptable"])
+        gathered = PP.gather_ranks([np.concatenate([kv, kpe], axis=1)])
+        return PP.cache_insert(np.zeros((len(rows), W.MLA_DQK)), gathered,
+                               np.arange(len(rows)))
     if path == "logits":
         from oracle import combine as OC
         from oracle import indexer_logits as IL
@@ -425,7 +455,8 @@ def dtype_for(path: str) -> str:
     """The arithmetic the path computes in: fp32 keys and scores (the combine
     accumulates in fp32), or int32 index maps only."""
     return {"write_slots": "i32", "attention": "f32 indexer, bf16 attention (fp32 accumulate)",
-            "logits": "fp8 e4m3 logits (fp32 accumulate), f32 indexer"}.get(path, "f32")
+            "logits": "fp8 e4m3 logits (fp32 accumulate), f32 indexer",
+            "pcp_prefill": "bf16 in/out, f32 arithmetic"}.get(path, "f32")
 
 
 def cpu_baseline(cfg, inp: dict, budget_s: float = 10.0, path: str = "fused") -> dict:
@@ -618,9 +649,12 @@ def config_block(cfg, path: str = "fused") -> dict:
             "rows": cfg.rows, "S": cfg.S, "I": cfg.I, "K": cfg.K, "block_size": cfg.block_size,
             "H": cfg.H, "D": cfg.D,
             "path": " -> ".join(kernels_for(cfg, path)) + " (C ABI, one stream)",
-            "l2": (f"{replicas_for(cfg, path)} rotating input sets of "
-                   f"{set_bytes(cfg, path) / 1e6:.0f} MB "
-                   f"(> 2.5x L2 together); no flush" if path != "write_slots" else
+            "l2": ((f"{replicas_for(cfg, path)} rotating input sets of "
+                    f"{set_bytes(cfg, path) / 1e6:.0f} MB "
+                    + ("(> 2.5x L2 together); no flush"
+                       if replicas_for(cfg, path) * set_bytes(cfg, path) > 2.5 * L2_BYTES else
+                       "(smaller than L2 together: a batch this size stays in L2); no flush"))
+                   if path != "write_slots" else
                    "positions and block tables (a few MB at most) stay in L2; no flush")
                   + (f"; resident KV caches of {cfg.S * mla_cache_slots(cfg) * 2 * W.MLA_DQK / 1e9:.1f}"
                      f" GB (bf16, |v| in [0.5, 1)), softmax scale 1/sqrt(192)"
@@ -687,6 +721,9 @@ def main(argv=None) -> int:
             st["logits"] = d(h["logits"])
         if "iq" in h:
             st["iq"], st["iw"] = d(h["iq"]), d(h["iw"])
+        if "kvc" in h:
+            st["kvc"], st["kpe"] = d(h["kvc"].view(np.int16)), d(h["kpe"].view(np.int16))
+            st["nw"], st["cslots"], st["ptable"] = d(h["nw"]), d(h["cslots"]), d(h["ptable"])
         if h["r2q"] is not None:
             st["r2q"] = d(h["r2q"])
         if H:
@@ -703,6 +740,12 @@ def main(argv=None) -> int:
         cache_dev = d(cache_host.view(np.int16))
         attn_out = torch.empty((S, R, H, W.MLA_DV), dtype=torch.int16, device=dev)
         attn_lse = torch.empty((S, R, H), dtype=torch.float32, device=dev)
+    if args.path == "pcp_prefill":
+        # the gathered (materialised) rows and the resident cache they go into
+        n_slots = mla_cache_slots(cfg)
+        kv_mat = torch.empty((R, W.MLA_DV), dtype=torch.int16, device=dev)
+        kpe_mat = torch.empty((R, W.MLA_DQK - W.MLA_DV), dtype=torch.int16, device=dev)
+        kvcache = torch.zeros((n_slots, W.MLA_DQK), dtype=torch.int16, device=dev)
     if args.path == "logits":
         # Each shard's paged fp8 key cache (every block the tables address),
         # resident as a serving cache is; one logits buffer the steps read.
@@ -742,6 +785,13 @@ def main(argv=None) -> int:
                                              P(attn_lse), P(err), sp)),
                 (lib.dsa_lse_combine, (P(attn_out), P(attn_lse), S, R, H, D, P(out), P(lse),
                                        P(err), sp))))
+        elif args.path == "pcp_prefill":
+            calls.append((
+                (lib.dsa_fused_norm_rope, (P(st["kvc"]), P(st["kpe"]), P(st["pos"]), P(st["nw"]),
+                                           1e-6, P(st["ptable"]), cfg.max_len, R, P(kv_mat),
+                                           P(kpe_mat), None, None, 0, P(err), sp)),
+                (lib.dsa_kv_cache_insert, (P(kv_mat), P(kpe_mat), P(st["cslots"]), R,
+                                           P(kvcache), n_slots, P(err), sp))))
         elif args.path == "logits":
             calls.append((
                 (lib.dsa_indexer_logits, (P(st["iq"]), P(st["iw"]), P(kcache_dev), n_slots,
@@ -975,6 +1025,9 @@ def main(argv=None) -> int:
     for h in host[:2]:
         if args.path == "write_slots":       # the new tokens and the tables they go through
             hs = dict(pos=pin(h["pos"]), bt=pin(h["bt"]))
+        elif args.path == "pcp_prefill":      # the new tokens' rows, positions and slots
+            hs = dict(kvc=pin(h["kvc"].view(np.int16)), kpe=pin(h["kpe"].view(np.int16)),
+                      pos=pin(h["pos"]), cslots=pin(h["cslots"]))
         elif args.path == "logits":           # fp8 queries and weights; keys stay resident
             hs = dict(iq=pin(h["iq"]), iw=pin(h["iw"]), starts=pin(h["starts"]),
                       ends=pin(h["ends"]), bt=pin(h["bt"]))
@@ -991,6 +1044,8 @@ def main(argv=None) -> int:
         hsets.append(hs)
     if args.path == "write_slots":
         results = [slotmap]
+    elif args.path == "pcp_prefill":
+        results = [kv_mat, kpe_mat]
     else:
         results = [slots, counts] + ([out, lse] if H else [])
     h_results = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]

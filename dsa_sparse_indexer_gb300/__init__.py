@@ -9,14 +9,16 @@ outputs.  All compute runs in hand-written CUDA kernels behind the C ABI in
 include/dsa.h (libdsa.so); this package only marshals torch tensors to it.
 """
 from . import _lib
-from .ops import (SUPPORTED_K, convert_index_compact, indexer_fused, indexer_logits,
-                  lse_combine, merge_topk_stable, new_error_flags, pack_candidates, shard_topk,
-                  shard_topk_pack, slot_mapping, sparse_mla_decode)
+from .ops import (SUPPORTED_K, convert_index_compact, fused_norm_rope, indexer_fused,
+                  indexer_logits, kv_cache_insert, lse_combine, merge_topk_stable,
+                  new_error_flags, pack_candidates, shard_topk, shard_topk_pack, slot_mapping,
+                  sparse_mla_decode)
 from ._lib import DSAError, DSA_FLAG_BOUNDS, DSA_FLAG_TIMEOUT
 
 __all__ = ["shard_topk", "pack_candidates", "shard_topk_pack", "merge_topk_stable",
            "convert_index_compact", "indexer_fused", "lse_combine", "slot_mapping",
-           "sparse_mla_decode", "indexer_logits", "new_error_flags", "DSAError",
+           "sparse_mla_decode", "indexer_logits", "fused_norm_rope", "kv_cache_insert",
+           "new_error_flags", "DSAError",
            "DSA_FLAG_BOUNDS", "DSA_FLAG_TIMEOUT", "SUPPORTED_K", "library"]
 
 

@@ -36,6 +36,9 @@ SIGNATURES = {
                                _p], _i),
     "dsa_indexer_logits": ([_p, _p, _p, _i64, _p, _i, _i, _i, _p, _p, _p, _i, _i, _i, _p, _i64,
                             _p, _p], _i),
+    "dsa_fused_norm_rope": ([_p, _p, _p, _p, ctypes.c_float, _p, _i, _i, _p, _p, _p, _p, _i64,
+                             _p, _p], _i),
+    "dsa_kv_cache_insert": ([_p, _p, _p, _i, _p, _i64, _p, _p], _i),
     "dsa_indexer_steps_noalloc": ([_p, _i64, _i, _i, _i, _i, _p, _p, _p, _i, _i, _i, _p, _p, _p,
                                    _p, _p, _p], _i),
 }

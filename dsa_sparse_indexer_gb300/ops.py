@@ -287,3 +287,55 @@ def indexer_logits(q, weights, k_cache, block_table, block_size: int, row_ends, 
               _ptr(row_starts), _ptr(row_ends), rows, S, I, _ptr(out), ld, _ptr(err_flags),
               _stream(q))
     return out
+
+
+def fused_norm_rope(kv_c, k_pe, positions, norm_weight, eps: float, cos_sin_cache,
+                    materialize: bool = True, slot_mapping=None, kv_cache=None, kv_out=None,
+                    kpe_out=None, err_flags=None):
+    """New tokens' cache rows: kv_c [T, 512] bf16 RMS-normed, k_pe [T, 64] bf16
+    rotated (interleaved pairs) by cos_sin_cache [max_pos, 64] fp32 at
+    positions [T].  Returns (kv_out, kpe_out) when materialising (else
+    (None, None)); with slot_mapping [T] and kv_cache [n_slots, 576] bf16, row
+    slot_mapping[t] of the cache is written as well."""
+    _need(kv_c, "kv_c", torch.bfloat16, 2)
+    _need(k_pe, "k_pe", torch.bfloat16, 2)
+    _need(positions, "positions", torch.int32, 1)
+    _need(norm_weight, "norm_weight", torch.float32, 1)
+    _need(cos_sin_cache, "cos_sin_cache", torch.float32, 2)
+    T = kv_c.shape[0]
+    if tuple(kv_c.shape) != (T, MLA_DV) or tuple(k_pe.shape) != (T, MLA_DQK - MLA_DV):
+        raise ValueError("kv_c must be [T, 512] and k_pe [T, 64]")
+    if cos_sin_cache.shape[1] != MLA_DQK - MLA_DV:
+        raise ValueError("cos_sin_cache must be [max_pos, 64]")
+    if materialize:
+        if kv_out is None:
+            kv_out = torch.empty((T, MLA_DV), dtype=torch.bfloat16, device=kv_c.device)
+        if kpe_out is None:
+            kpe_out = torch.empty((T, MLA_DQK - MLA_DV), dtype=torch.bfloat16, device=kv_c.device)
+        _need(kv_out, "kv_out", torch.bfloat16, 2)
+        _need(kpe_out, "kpe_out", torch.bfloat16, 2)
+    else:
+        kv_out = kpe_out = None
+    n_slots = 0
+    if slot_mapping is not None or kv_cache is not None:
+        _need(slot_mapping, "slot_mapping", torch.int32, 1)
+        _need(kv_cache, "kv_cache", torch.bfloat16, 2)
+        n_slots = kv_cache.shape[0]
+    _lib.call("dsa_fused_norm_rope", _ptr(kv_c), _ptr(k_pe), _ptr(positions), _ptr(norm_weight),
+              float(eps), _ptr(cos_sin_cache), cos_sin_cache.shape[0], T, _ptr(kv_out),
+              _ptr(kpe_out), _ptr(slot_mapping), _ptr(kv_cache), n_slots, _ptr(err_flags),
+              _stream(kv_c))
+    return kv_out, kpe_out
+
+
+def kv_cache_insert(kv_rows, kpe_rows, slot_mapping, kv_cache, err_flags=None):
+    """Gathered rows (kv_rows [T, 512], kpe_rows [T, 64] bf16) into
+    kv_cache [n_slots, 576] bf16 at slot_mapping [T] (-1: skipped)."""
+    _need(kv_rows, "kv_rows", torch.bfloat16, 2)
+    _need(kpe_rows, "kpe_rows", torch.bfloat16, 2)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    _need(kv_cache, "kv_cache", torch.bfloat16, 2)
+    T = kv_rows.shape[0]
+    _lib.call("dsa_kv_cache_insert", _ptr(kv_rows), _ptr(kpe_rows), _ptr(slot_mapping), T,
+              _ptr(kv_cache), kv_cache.shape[0], _ptr(err_flags), _stream(kv_rows))
+    return kv_cache

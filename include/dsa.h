@@ -359,6 +359,58 @@ dsa_status dsa_indexer_logits(const uint8_t* q, const float* weights, const uint
                               cudaStream_t stream);
 
 /*
+ * dsa_fused_norm_rope - the cache rows of new tokens for the PCP prefill path.
+ * PR #52046 report, "DSV3.2 PCP sharding": sections 功能与动机 (PCP shards the
+ * sequence while the KV cache is replicated, so new cache rows are gathered
+ * before they are inserted) and 实现拆解 item 1 / 关键源码片段
+ * (`_fused_norm_rope_kernel`, pid == 1: RMS norm of kv_c, interleaved RoPE of
+ * k_pe, results materialised to output buffers and/or written into the cache
+ * at the token's slot).
+ *
+ * For token t (position p = positions[t]):
+ *   kv_out[t]  = kv_c[t] / sqrt(mean(kv_c[t]^2) + eps) * norm_weight
+ *   kpe_out[t] = k_pe[t] with each pair (2i, 2i+1) rotated: (x1 c - x2 s,
+ *                x2 c + x1 s), c = cos_sin_cache[p][i], s = cos_sin_cache[p][32 + i]
+ * computed in fp32 from bf16 inputs, stored as bf16 (round to nearest even).
+ *
+ *   kv_c, kv_out   [T][DSA_MLA_DV] bf16 (uint16 bit patterns), 16-byte aligned
+ *   k_pe, kpe_out  [T][DSA_MLA_DQK - DSA_MLA_DV] bf16, 4-byte aligned
+ *   positions      [T] int32; norm_weight [DSA_MLA_DV] fp32, 16-byte aligned
+ *   cos_sin_cache  [max_pos][64] fp32: 32 cosines then 32 sines per position
+ *   kv_out/kpe_out both or neither (materialise for the PCP gather);
+ *   slot_mapping [T] int32 and kv_cache [n_slots][DSA_MLA_DQK] bf16 (16-byte
+ *   aligned) both or neither: row slot_mapping[t] of the cache receives kv_out
+ *   then kpe_out (a slot < 0 writes nothing).  At least one of the two modes.
+ *   err_flags  DSA_FLAG_BOUNDS if a position is outside [0, max_pos) (that
+ *              token's k_pe is not rotated) or a slot is >= n_slots (skipped).
+ * Errors: T < 0, max_pos < 1, eps negative or not finite, an output pair half
+ *         given, no output, null pointers, misalignment -> INVALID_ARG.
+ */
+dsa_status dsa_fused_norm_rope(const uint16_t* kv_c, const uint16_t* k_pe,
+                               const int32_t* positions, const float* norm_weight, float eps,
+                               const float* cos_sin_cache, int max_pos, int T, uint16_t* kv_out,
+                               uint16_t* kpe_out, const int32_t* slot_mapping, uint16_t* kv_cache,
+                               int64_t n_slots, uint32_t* err_flags, cudaStream_t stream);
+
+/*
+ * dsa_kv_cache_insert - gathered cache rows into the paged KV cache.
+ * PR #52046 report, "DSV3.2 PCP sharding", section 实现拆解 item 3
+ * (`maybe_gather_mla_latent_cache_inputs` gathers the PCP ranks' materialised
+ * rows, then `do_kv_cache_update` inserts them).  With the ranks' slices held
+ * in one buffer in rank order (the gather of contiguous sequence slices is
+ * their concatenation), row t goes to slot slot_mapping[t]:
+ *   kv_cache[slot][0 .. DSA_MLA_DV) = kv_rows[t], then kpe_rows[t].
+ *   kv_rows [T][DSA_MLA_DV] bf16, 16-byte aligned; kpe_rows [T][64] bf16,
+ *   4-byte aligned; kv_cache [n_slots][DSA_MLA_DQK] bf16, 16-byte aligned.
+ *   err_flags  DSA_FLAG_BOUNDS if a slot is >= n_slots (skipped); slots < 0
+ *              write nothing.
+ * Errors: T < 0, n_slots < 1, null pointers, misalignment -> INVALID_ARG.
+ */
+dsa_status dsa_kv_cache_insert(const uint16_t* kv_rows, const uint16_t* kpe_rows,
+                               const int32_t* slot_mapping, int T, uint16_t* kv_cache,
+                               int64_t n_slots, uint32_t* err_flags, cudaStream_t stream);
+
+/*
  * dsa_indexer_steps_noalloc - dsa_shard_topk_pack, dsa_merge_topk_stable and
  * dsa_convert_index_compact in turn, with the packed candidates held in a
  * static device array of this library (DSA_NOALLOC_SCRATCH_BYTES) instead of a
