@@ -52,14 +52,17 @@ constexpr int kItemBlocks = kTilesPerItem * 128 / 16 + 1;
 constexpr uint32_t kTileBytes = kTile * kDim;
 constexpr uint32_t kQBytes = kHeads * kDim;  // one row's query heads
 
-template <int G>
+template <int G, int P>
 struct LogitsCfg {
+  // G rows per MMA (N = 64 G), P passes of the MMAs over each key tile: an
+  // item holds R = G P rows, and each key tile read from memory serves all R.
+  static constexpr int R = G * P;
   // Key stages: enough bytes in flight to cover the latency of the key reads
   // at the rate the MMAs consume them (one CTA per SM when grouped).
-  static constexpr int kStages = G == 1 ? 4 : 8;
-  // One epilogue warp per (lane quarter, row): a tile's epilogue latency is
-  // one row's, and the MMAs run ahead by as many accumulators as the tensor
-  // memory holds (two CTAs per SM when ungrouped, one when grouped).
+  static constexpr int kStages = G == 1 ? 4 : 4;
+  // One epilogue warp per (lane quarter, row of a pass): a tile's epilogue
+  // latency is one row's, and the MMAs run ahead by as many accumulators as
+  // the tensor memory holds (two CTAs per SM when ungrouped, one when grouped).
   static constexpr int kEpiWarps = 4 * G;
   static constexpr int kAccBufs = G == 1 ? 4 : 2;
   static constexpr int kThreads = (kEpiWarps + 2) * 32;
@@ -68,15 +71,16 @@ struct LogitsCfg {
   static constexpr uint32_t kTmemCols = kAccBufs * kAccCols;   // 256 or 512
 };
 
-template <int G>
+template <int G, int P>
 struct alignas(1024) LogitsSmem {
-  static constexpr int kStages = LogitsCfg<G>::kStages;
+  static constexpr int kStages = LogitsCfg<G, P>::kStages;
+  static constexpr int R = G * P;
   uint8_t k[kStages][kTileBytes];          // 1024-aligned: the swizzle atom
-  uint8_t q[2][G * kQBytes];               // the item's query heads, two slots
-  float w[2][G * kHeads];                  // and weights
+  uint8_t q[2][R * kQBytes];               // the item's query heads, two slots
+  float w[2][R * kHeads];                  // and weights
   int32_t pblk[kItemBlocks];               // the item's block-table entries
   uint64_t full[kStages], empty[kStages], qfull[2], qfree[2];
-  uint64_t accfull[LogitsCfg<G>::kAccBufs], accempty[LogitsCfg<G>::kAccBufs], drain;
+  uint64_t accfull[LogitsCfg<G, P>::kAccBufs], accempty[LogitsCfg<G, P>::kAccBufs], drain;
   uint32_t tmem;
   int abort;
 };
@@ -164,34 +168,45 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 #undef DSA_TMEM_LD16
 #undef DSA_WAIT_LD16
 
-template <int G>
-__device__ __forceinline__ bool aborted(const LogitsSmem<G>& sm) {
+// Two fused multiply-adds in one instruction (fma.rn.f32x2): (a.x b.x + c.x,
+// a.y b.y + c.y), each rounded as fmaf would.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&r);
+}
+
+template <typename Smem>
+__device__ __forceinline__ bool aborted(const Smem& sm) {
   return *reinterpret_cast<const volatile int*>(&sm.abort) != 0;
 }
 
-// One work item: shard s, rows r0 .. r0 + nrows - 1 (nrows <= G), the tiles
+// One work item: shard s, rows r0 .. r0 + nrows - 1 (nrows <= R), the tiles
 // [t_lo, t_lo + ntiles) of local slots covering their ranges inside chunk c.
 // Every role computes it the same way from the same inputs.
-template <int G>
+template <int R>
 struct Item {
   int s, r0, nrows, ntiles;
   int64_t t_lo;
-  int64_t lo[G], hi[G];
+  int64_t lo[R], hi[R];
 };
 
-template <int G>
-__device__ __forceinline__ Item<G> make_item(int it, int rows, int groups, int chunks,
+template <int R>
+__device__ __forceinline__ Item<R> make_item(int it, int rows, int groups, int chunks,
                                              const int32_t* row_starts, const int32_t* row_ends,
                                              int64_t ld, const ShardMath& sh, bool* bad) {
-  Item<G> x;
+  Item<R> x;
   const int c = it % chunks;
   const int sg = it / chunks;
   x.s = sg / groups;
-  x.r0 = (sg - x.s * groups) * G;
-  x.nrows = min(G, rows - x.r0);
+  x.r0 = (sg - x.s * groups) * R;
+  x.nrows = min(R, rows - x.r0);
   int64_t glo = INT64_MAX, ghi = 0;
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
+  for (int g = 0; g < R; ++g) {
     x.lo[g] = x.hi[g] = 0;
     if (g < x.nrows) {
       const int r = x.r0 + g;
@@ -220,8 +235,8 @@ __device__ __forceinline__ Item<G> make_item(int it, int rows, int groups, int c
   return x;
 }
 
-template <int G>
-__global__ void __launch_bounds__(LogitsCfg<G>::kThreads, G == 1 ? 2 : 1)
+template <int G, int P>
+__global__ void __launch_bounds__(LogitsCfg<G, P>::kThreads, G == 1 ? 2 : 1)
     indexer_logits_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_q, const float* __restrict__ w,
                           const int32_t* __restrict__ block_table, int reqs, int max_blocks,
@@ -231,13 +246,14 @@ __global__ void __launch_bounds__(LogitsCfg<G>::kThreads, G == 1 ? 2 : 1)
                           const int32_t* __restrict__ row_ends, int rows, int S, int64_t ld,
                           int chunks, int nitems, float* __restrict__ logits, uint32_t* flags,
                           const ShardMath sh, const FastDiv fbs) {
-  using Cfg = LogitsCfg<G>;
+  using Cfg = LogitsCfg<G, P>;
   constexpr int kStages = Cfg::kStages;
+  constexpr int R = Cfg::R;
   extern __shared__ unsigned char logits_smem_raw[];
-  LogitsSmem<G>& sm = *reinterpret_cast<LogitsSmem<G>*>(
+  LogitsSmem<G, P>& sm = *reinterpret_cast<LogitsSmem<G, P>*>(
       (reinterpret_cast<uintptr_t>(logits_smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int groups = (rows + G - 1) / G;
+  const int groups = (rows + R - 1) / R;
 
   if (warp == Cfg::kProducer) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -276,7 +292,7 @@ __global__ void __launch_bounds__(LogitsCfg<G>::kThreads, G == 1 ? 2 : 1)
     const int boxes = box_rows == 64 ? 2 : (box_rows == 32 ? 4 : 8);   // per tile of 128 slots
     int gt = 0, icount = 0;
     for (int it = blockIdx.x; it < nitems && !aborted(sm); it += gridDim.x) {
-      const Item<G> x = make_item<G>(it, rows, groups, chunks, row_starts, row_ends, ld, sh, &bad);
+      const Item<R> x = make_item<R>(it, rows, groups, chunks, row_starts, row_ends, ld, sh, &bad);
       if (x.ntiles == 0) continue;
       const int req = row_to_req ? row_to_req[x.r0] : x.r0;
       const bool req_ok = req >= 0 && req < reqs;
@@ -284,7 +300,7 @@ __global__ void __launch_bounds__(LogitsCfg<G>::kThreads, G == 1 ? 2 : 1)
       const int32_t* bt = block_table + ((int64_t)x.s * reqs + (req_ok ? req : 0)) * max_blocks;
       int64_t ghi = 0;
 #pragma unroll
-      for (int g = 0; g < G; ++g) ghi = max(ghi, x.hi[g]);
+      for (int g = 0; g < R; ++g) ghi = max(ghi, x.hi[g]);
       // Local slots are below ld < 2^31: 32-bit maps (no 64-bit division).
       const uint32_t tok_lo = (uint32_t)(x.t_lo * kTile);
       const uint32_t tok_end = (uint32_t)min((x.t_lo + x.ntiles) * kTile, ghi);
@@ -300,8 +316,11 @@ __global__ void __launch_bounds__(LogitsCfg<G>::kThreads, G == 1 ? 2 : 1)
           raise_flag(flags, DSA_FLAG_TIMEOUT);
           sm.abort = 1;
         } else {
-          mbar_expect_tx(&sm.qfull[qb], (uint32_t)G * kQBytes + (uint32_t)x.nrows * kHeads * 4u);
-          tma_load_2d(sm.q[qb], &tm_q, 0, x.r0 * kHeads, &sm.qfull[qb]);
+          mbar_expect_tx(&sm.qfull[qb], (uint32_t)R * kQBytes + (uint32_t)x.nrows * kHeads * 4u);
+#pragma unroll
+          for (int pp = 0; pp < P; ++pp)    // one box of G rows' heads per pass
+            tma_load_2d(sm.q[qb] + pp * G * kQBytes, &tm_q, 0, (x.r0 + pp * G) * kHeads,
+                        &sm.qfull[qb]);
           bulk_g2s(sm.w[qb], w + (int64_t)x.r0 * kHeads, (uint32_t)x.nrows * kHeads * 4u,
                    &sm.qfull[qb]);
           ++icount;
@@ -348,26 +367,31 @@ __global__ void __launch_bounds__(LogitsCfg<G>::kThreads, G == 1 ? 2 : 1)
       bool ok = true;
       int gt = 0, icount = 0;
       for (int it = blockIdx.x; ok && it < nitems && !aborted(sm); it += gridDim.x) {
-        const Item<G> x = make_item<G>(it, rows, groups, chunks, row_starts, row_ends, ld, sh, &bad);
+        const Item<R> x = make_item<R>(it, rows, groups, chunks, row_starts, row_ends, ld, sh, &bad);
         if (x.ntiles == 0) continue;
         const int qb = icount & 1;
         if (!mbar_wait(&sm.qfull[qb], (uint32_t)(icount >> 1) & 1u)) { ok = false; break; }
         ++icount;
-        const uint64_t qdesc = sw128_desc(sm.q[qb]);
-        for (int k = 0; k < x.ntiles; ++k, ++gt) {
+        for (int kt = 0; kt < x.ntiles; ++kt, ++gt) {
           constexpr int NB = Cfg::kAccBufs;
-          const int stg = gt % kStages, b = gt % NB;
-          if (gt >= NB && !mbar_wait(&sm.accempty[b], (uint32_t)((gt / NB) - 1) & 1u)) { ok = false; break; }
+          const int stg = gt % kStages;
           if (!mbar_wait(&sm.full[stg], (uint32_t)(gt / kStages) & 1u)) { ok = false; break; }
-          if (aborted(sm)) { ok = false; break; }
-          tc_fence_after();
           const uint64_t kdesc = sw128_desc(sm.k[stg]);
+#pragma unroll 1
+          for (int pp = 0; pp < P; ++pp) {   // one accumulator per pass
+            const int u = gt * P + pp, b = u % NB;
+            if (u >= NB && !mbar_wait(&sm.accempty[b], (uint32_t)((u / NB) - 1) & 1u)) { ok = false; break; }
+            if (aborted(sm)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t qdesc = sw128_desc(sm.q[qb] + pp * G * kQBytes);
 #pragma unroll
-          for (int kk = 0; kk < kDim / 32; ++kk)   // 32 fp8 = 32 bytes = 2 descriptor units
-            mma_f8(tmem + (uint32_t)b * Cfg::kAccCols, kdesc + 2u * kk, qdesc + 2u * kk, idesc,
-                   kk > 0);
-          mma_commit(&sm.empty[stg]);
-          mma_commit(&sm.accfull[b]);
+            for (int kk = 0; kk < kDim / 32; ++kk)   // 32 fp8 = 32 bytes = 2 descriptor units
+              mma_f8(tmem + (uint32_t)b * Cfg::kAccCols, kdesc + 2u * kk, qdesc + 2u * kk, idesc,
+                     kk > 0);
+            mma_commit(&sm.accfull[b]);
+          }
+          if (!ok) break;
+          mma_commit(&sm.empty[stg]);        // after every pass over the tile
         }
         mma_commit(&sm.qfree[qb]);   // the item's query slot, once its MMAs are done
       }
@@ -386,53 +410,64 @@ __global__ void __launch_bounds__(LogitsCfg<G>::kThreads, G == 1 ? 2 : 1)
     int gt = 0, icount = 0;
     bool ok = true;
     for (int it = blockIdx.x; ok && it < nitems && !aborted(sm); it += gridDim.x) {
-      const Item<G> x = make_item<G>(it, rows, groups, chunks, row_starts, row_ends, ld, sh, &bad);
+      const Item<R> x = make_item<R>(it, rows, groups, chunks, row_starts, row_ends, ld, sh, &bad);
       if (x.ntiles == 0) continue;
       const int qb = icount & 1;
       if (!mbar_wait(&sm.qfull[qb], (uint32_t)(icount >> 1) & 1u)) { ok = false; break; }
       ++icount;
-      // This warp's row's range (selected with constant indices, so that the
-      // item stays in registers); empty for rows past the batch.
-      int64_t my_lo = 0, my_hi = 0;
+      // This warp's row of each pass and its range (selected with constant
+      // indices, so that the item stays in registers); empty past the batch.
+      int64_t my_lo[P], my_hi[P];
 #pragma unroll
-      for (int gg = 0; gg < G; ++gg)
-        if (gg == g && gg < x.nrows) {
-          my_lo = x.lo[gg];
-          my_hi = x.hi[gg];
-        }
-      for (int k = 0; k < x.ntiles; ++k, ++gt) {
-        constexpr int NB = Cfg::kAccBufs;
-        const int b = gt % NB;
-        if (!mbar_wait(&sm.accfull[b], (uint32_t)(gt / NB) & 1u)) { ok = false; break; }
-        if (aborted(sm)) { ok = false; break; }
-        tc_fence_after();
-        const int64_t l = (x.t_lo + k) * kTile + quarter * 32 + lane;
-        {
-          // Four partial sums (heads h mod 4), so the dependent chain is 16 deep;
-          // the 64 head sums are read 32 at a time.
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      for (int pp = 0; pp < P; ++pp) {
+        my_lo[pp] = my_hi[pp] = 0;
+#pragma unroll
+        for (int gg = 0; gg < R; ++gg)
+          if (gg == pp * G + g && gg < x.nrows) {
+            my_lo[pp] = x.lo[gg];
+            my_hi[pp] = x.hi[gg];
+          }
+      }
+      for (int kt = 0; kt < x.ntiles; ++kt, ++gt) {
+        const int64_t l = (x.t_lo + kt) * kTile + quarter * 32 + lane;
+#pragma unroll
+        for (int pp = 0; pp < P; ++pp) {
+          constexpr int NB = Cfg::kAccBufs;
+          const int u = gt * P + pp, b = u % NB;
+          if (!mbar_wait(&sm.accfull[b], (uint32_t)(u / NB) & 1u)) { ok = false; break; }
+          if (aborted(sm)) { ok = false; break; }
+          tc_fence_after();
+          const int row = pp * G + g;      // row of the item
+          // Four partial sums (heads h mod 4) as two packed pairs, so the
+          // dependent chain is 16 deep; the 64 head sums are read 32 at a time.
+          float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int hh = 0; hh < kHeads; hh += 32) {
             uint32_t v[32];
             tmem_ld32(tmem + lane_base + (uint32_t)b * Cfg::kAccCols + (uint32_t)(g * kHeads + hh),
                       v);
-            const float4* wv = reinterpret_cast<const float4*>(sm.w[qb] + g * kHeads + hh);
+            const float4* wv = reinterpret_cast<const float4*>(sm.w[qb] + row * kHeads + hh);
 #pragma unroll
             for (int h4 = 0; h4 < 8; ++h4) {
               const float4 ww = wv[h4];
-              a0 = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f), a0);
-              a1 = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), a1);
-              a2 = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), a2);
-              a3 = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), a3);
+              a01 = ffma2(make_float2(ww.x, ww.y),
+                          make_float2(fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.f),
+                                      fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f)),
+                          a01);
+              a23 = ffma2(make_float2(ww.z, ww.w),
+                          make_float2(fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f),
+                                      fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f)),
+                          a23);
             }
           }
-          const float acc = (a0 + a1) + (a2 + a3);
-          if (l >= my_lo && l < my_hi)
-            logits[((int64_t)x.s * rows + x.r0 + g) * ld + l] = acc;
+          const float acc = (a01.x + a01.y) + (a23.x + a23.y);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive1(&sm.accempty[b]);
+          if (l >= my_lo[pp] && l < my_hi[pp])
+            logits[((int64_t)x.s * rows + x.r0 + row) * ld + l] = acc;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive1(&sm.accempty[b]);
+        if (!ok) break;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive1(&sm.qfree[qb]);   // done with the item's weights
@@ -518,8 +553,8 @@ extern "C" dsa_status dsa_indexer_logits(const uint8_t* q, const float* weights,
     return DSA_ERR_CUDA;
   const int chunks =
       (int)((ld + (int64_t)kTile * kTilesPerItem - 1) / ((int64_t)kTile * kTilesPerItem));
-  const int G = grouped ? 4 : 1;
-  const int64_t nitems = (int64_t)S * ((rows + G - 1) / G) * chunks;
+  const int R = grouped ? 8 : 1;   // rows per item: G rows per MMA times P passes
+  const int64_t nitems = (int64_t)S * ((rows + R - 1) / R) * chunks;
   if (nitems > INT32_MAX) return DSA_ERR_UNSUPPORTED;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -541,7 +576,8 @@ extern "C" dsa_status dsa_indexer_logits(const uint8_t* q, const float* weights,
     return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
   };
   if (grouped)
-    return launch(indexer_logits_kernel<4>, LogitsCfg<4>::kThreads, 1,
-                  sizeof(LogitsSmem<4>) + 1024);
-  return launch(indexer_logits_kernel<1>, LogitsCfg<1>::kThreads, 2, sizeof(LogitsSmem<1>) + 1024);
+    return launch(indexer_logits_kernel<4, 2>, LogitsCfg<4, 2>::kThreads, 1,
+                  sizeof(LogitsSmem<4, 2>) + 1024);
+  return launch(indexer_logits_kernel<1, 1>, LogitsCfg<1, 1>::kThreads, 2,
+                sizeof(LogitsSmem<1, 1>) + 1024);
 }

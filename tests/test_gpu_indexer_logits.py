@@ -126,3 +126,22 @@ def test_decode_workload_full_size_then_the_indexer_steps():
     for k in ("local_idx", "ids", "slots", "counts"):
         np.testing.assert_array_equal(res[k], want[k])
     assert res["err"] == 0
+
+
+def test_prefill_workload_full_size_grouped_rows():
+    """The prefill batch at full size (4096 rows sharing one request, so the
+    kernel takes eight rows an item, four per MMA pass): sampled rows of every
+    shard against the oracle, including the first and last rows, rows at item
+    boundaries and the rows whose ranges end inside a chunk."""
+    cfg = W.CONFIGS["prefill"]
+    starts, ends = W.row_ranges(cfg)
+    tables = W.block_tables(cfg)
+    n_slots = cfg.reqs * cfg.max_blocks * cfg.block_size
+    c = dict(S=cfg.S, I=cfg.I, rows=cfg.rows, ld=cfg.ld, bs=cfg.block_size, starts=starts,
+             ends=ends, tables=tables, r2q=np.zeros(cfg.rows, np.int32),
+             q=W.indexer_query(cfg.rows, 41), w=W.indexer_weights(cfg.rows, 42),
+             k=W.indexer_keys(cfg.S, n_slots, 43))
+    got, err = _run(c)
+    assert err == 0
+    rows = [0, 1, 7, 8, 9, 1023, 2047, 2048, 3000, 4091, 4095]
+    assert _check(c, got, rows=rows) <= TOL_REL
