@@ -145,3 +145,24 @@ def test_prefill_workload_full_size_grouped_rows():
     assert err == 0
     rows = [0, 1, 7, 8, 9, 1023, 2047, 2048, 3000, 4091, 4095]
     assert _check(c, got, rows=rows) <= TOL_REL
+
+
+@pytest.mark.parametrize("S,I,bs,rows", [(3, 2, 64, 13), (8, 4, 32, 9), (2, 1, 16, 21),
+                                         (4, 16, 128, 4)])
+def test_grouped_rows_with_interleave_starts_and_a_partial_group(S, I, bs, rows):
+    """Rows sharing one request (the grouped kernel: eight rows an item in two
+    MMA passes of four) with interleave > 1, nonzero starts, a batch that is
+    not a multiple of eight (the last item's missing rows read zero queries
+    and write nothing), rows shorter than a tile and a row of one token."""
+    rng = np.random.default_rng(S * 7 + rows)
+    Lmax = S * I * 700 + 5
+    ends = rng.integers(Lmax // 2, Lmax + 1, rows).astype(np.int32)
+    ends[0], ends[-1] = Lmax, 1
+    starts = np.zeros(rows, np.int32)
+    starts[1::3] = rng.integers(0, 300, len(starts[1::3]))
+    starts = np.minimum(starts, ends).astype(np.int32)
+    c = _case(S, I, rows=rows, Lmax=Lmax, bs=bs, seed=S * 11 + rows, reqs=1, ends=ends,
+              starts=starts)
+    got, err = _run(c)
+    assert err == 0
+    assert _check(c, got) <= TOL_REL
