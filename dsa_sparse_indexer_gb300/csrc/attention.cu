@@ -14,20 +14,45 @@
 // sum_j 2^(s_j log2 e) with v_j the first 512 entries of row_j, and
 // lse2 = log2 sum_j exp(s_j).
 //
-// One CTA per (row, shard, group of 64 heads), tensor cores through mma.sync
-// m16n8k16 (bf16 in, fp32 accumulate), warp-specialised:
-//  * a producer warp gathers the shard's selected cache rows by slot, one row
-//    per lane and one bulk asynchronous copy (TMA, non-tensor form) per row,
-//    into two stages of 32 tokens guarded by full / empty mbarriers (invalid
-//    tokens are zeroed and masked);
-//  * eight consumer warps, a pair per 16 heads: each warp of a pair computes
-//    the scores of its 16 heads against half of the tile's tokens (all 576
-//    dimensions), the pair swaps them through shared memory under one
-//    64-thread named barrier, and each warp then runs the online softmax (exp2
-//    domain) on all 32 tokens and O += P V for its half of the 512 output
-//    dimensions (128 fp32 accumulators per thread); the softmax weights go
-//    from the score registers straight into the operand layout of P V.
-// No block-wide barrier runs inside the token loop; every wait is bounded.
+// One CTA per (row, shard, group of 128 heads, half of the 512 output
+// dimensions); the two halves are adjacent in the grid, run side by side and
+// share the gathered rows in L2.  Fifth-generation tensor cores, warp-
+// specialised, tiles of 64 selected tokens:
+//  * the group's query (128 heads x 576 bf16) stays on chip for the whole slot
+//    list: its first 320 dimensions in tensor memory (written once by the
+//    softmax warps, a head per lane), the other 256 in shared memory (four
+//    64-column blocks, 128-byte swizzle, K-major, one TMA tensor copy each);
+//  * warps 0-3 gather the selected cache rows, two warps per stage (32 rows
+//    of a tile each), tiles alternating between the stages: 16-byte
+//    asynchronous copies (cp.async, eight lanes per 128-byte row segment)
+//    placed in the 128-byte-swizzled layout, nine 64-column blocks of
+//    [64 tokens x 64 bf16]; a warp waits for its own copies, makes them
+//    visible to the tensor cores' proxy and arrives;
+//  * one thread of warp 4 issues the MMAs: S = Q K^T as 36 tcgen05.mma
+//    kind::f16 (M = 128 heads, N = 64 tokens, K = 16; bf16 in, fp32 out; A
+//    from tensor memory for the first 20 steps, from shared memory for the
+//    rest), and O += P V as four MMAs (N = 256 output dimensions, K = 16
+//    tokens; A = P from tensor memory, B = this half's four value blocks of the
+//    same gathered tile read MN-major); it polls both and issues S of tile
+//    t + 1 or P V of tile t, whichever is ready first, so the softmax of a
+//    tile overlaps the tensor work and a stage is freed as early as possible;
+//  * warps 5-8, a thread per head (its tensor-memory lane), run the softmax
+//    in the exp2 domain: scores out of tensor memory, masked tokens to -inf,
+//    weights relative to a reference maximum that moves only when a tile's
+//    maximum exceeds it by more than 8 (so O in tensor memory is rescaled
+//    rarely), bf16 weights back into tensor memory as the A operand of P V;
+//    they also write the outputs.
+// An MMA of M = 128 and K = 16 takes about 50 cycles on this GPU whatever its
+// N up to 64 (and N / 2 cycles above 128), so the scores' N is as large as
+// the on-chip memory allows: tensor memory holds O (256 columns), S (64), P
+// (32) and the query's first 320 dimensions (160); shared memory two stages of
+// 72 KB and 64 KB of the query.
+// Two row sums are kept: of the fp32 weights (the LSE) and of the bf16-rounded
+// weights that enter P V (O's normaliser).  Every wait is bounded; a wait that
+// runs out raises DSA_FLAG_TIMEOUT and stops the CTA's roles, which drain
+// their copies and MMAs in flight before the tensor memory is freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -37,335 +62,580 @@ namespace {
 
 constexpr int kDqk = DSA_MLA_DQK;            // 576: latent 512 + rope 64
 constexpr int kDv = DSA_MLA_DV;              // 512
-constexpr int kHeads = 64;                   // heads per CTA: four blocks of 16
-constexpr int kHalfDv = kDv / 2;             // output dimensions per consumer warp
-constexpr int kTile = 32;                    // tokens per stage (one per producer lane)
-constexpr int kStages = 2;
-constexpr int kConsumers = 8;                // warps 0..7; warp 8 produces
-constexpr int kAttnThreads = (kConsumers + 1) * 32;
-constexpr int kStride = kDqk + 8;            // smem row stride (elements): rows 16 B apart in banks
-constexpr int kChunks = kDqk / 8;            // 16-byte chunks per row
-constexpr uint32_t kRowBytes = kDqk * 2;     // one cache row, one bulk copy
+constexpr int kHeads = 128;                  // heads per CTA: the MMA's M
+constexpr int kHalf = kDv / 2;               // output dimensions per CTA
+constexpr int kTile = 64;                    // tokens per tile: the scores' N
+constexpr int kStages = 2;                   // one per gathering warp
+constexpr int kBlocks = kDqk / 64;           // 9 column blocks of 64 bf16 (128 bytes)
+constexpr int kQtBlocks = 5;                 // query blocks held in tensor memory
+constexpr int kQsBlocks = kBlocks - kQtBlocks;   // and in shared memory
+constexpr int kQBlock = kHeads * 128;        // bytes of one query block
+constexpr int kKvBlock = kTile * 128;        // bytes of one tile block
+constexpr int kVBlocks = kHalf / 64;         // 4 value blocks per half
+constexpr int kGatherWarps = 4;              // two per stage, 32 rows of a tile each
+constexpr int kMmaWarp = kGatherWarps;
+constexpr int kSoftmaxWarps = 4;
+constexpr int kThreads = (kGatherWarps + 1 + kSoftmaxWarps) * 32;
+// Tensor-memory columns (fp32 or packed bf16 pairs, a head per lane).
+constexpr int kOCol = 0;                     // O: 256
+constexpr int kSCol = 256;                   // S: 64
+constexpr int kPCol = 320;                   // P: 64 tokens as 32 bf16 pairs
+constexpr int kQCol = 352;                   // query dimensions 0..319: 160
+constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleGap = 8.f;           // weights stay below 2^8 before a rescale
 
-static_assert(kDqk % 32 == 0 && kHalfDv % 16 == 0, "tile shapes");
-static_assert(kTile == 32 && kStages == 2, "one token per producer lane; parity = tile & 1");
+static_assert(kGatherWarps == 2 * kStages, "two gathering warps per stage");
+static_assert(kBlocks * 64 == kDqk && kVBlocks * 64 == kHalf, "column blocks");
+static_assert(kQCol + kQtBlocks * 32 == kTmemCols && kPCol + kTile / 2 == kQCol &&
+                  kSCol + kTile == kPCol && kOCol + kHalf == kSCol,
+              "tensor-memory columns");
 
-struct AttnSmem {
-  uint64_t full[kStages];                    // a stage's rows have landed
-  uint64_t empty[kStages];                   // every consumer warp is done with a stage
-  alignas(16) __nv_bfloat16 q[kHeads * kStride];
-  alignas(16) __nv_bfloat16 kv[kStages][kTile * kStride];
-  // Score swap between the two warps of a head block: [block][token half]
-  // [tile parity][value][lane], each lane's eight scores of its half.
-  float xs[kHeads / 16][2][2][8][32];
-  uint32_t vmask[kStages];                   // bit i: token i of the stage is valid
+struct alignas(1024) MlaSmem {
+  uint8_t kv[kStages][kBlocks][kKvBlock];    // 147456: gathered tiles
+  uint8_t q[kQsBlocks][kQBlock];             // 65536: query dimensions 320..575
+  uint32_t vmask[kStages][2];                // valid tokens of a stage's tile
+  uint64_t qfull, qtm, kvfull[kStages], kvempty[kStages], sfull, sfree, pfull, pvdone, drain;
+  uint32_t tmem;
+  int abort;
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-// Named barrier over `count` threads that also returns whether any of them
-// passed pred = true.
-__device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-struct AttnArgs {
+struct MlaArgs {
   const __nv_bfloat16* q;        // [rows][H][kDqk]
   const __nv_bfloat16* cache;    // [S][n_slots][kDqk]
-  int64_t n_slots;
   const int32_t* slots;          // [S][rows][K]
   const int32_t* counts;         // [S][rows]
-  int rows, S, H, K;
+  int64_t n_slots;
+  int rows, H, K, hgroups, box_h;
   float c2;                      // scale * log2(e)
   __nv_bfloat16* out;            // [S][rows][H][kDv]
   float* lse2;                   // [S][rows][H]
   uint32_t* flags;
 };
 
-// Producer warp: tile t of 32 tokens into stage t & 1, lane i taking token i.
-__device__ __forceinline__ void produce(const AttnArgs& a, AttnSmem& sm, int count, int ntiles,
-                                        const int32_t* slot_row,
-                                        const __nv_bfloat16* shard_cache) {
-  const int lane = threadIdx.x & 31;
-  bool bad = false, ok = true;
-  int issued = 0;
+// Shared-memory matrix descriptor: start address >> 4 (bits 0-13), leading
+// byte offset >> 4 (bits 16-29), stride byte offset >> 4 (bits 32-45),
+// descriptor version 1 (bits 46-47), swizzle mode (bits 61-63: 2 = 128-byte,
+// 4 = 64-byte).  K-major swizzled operands: the stride is that of 8-row
+// groups, the leading offset unused (1).  MN-major 128-byte swizzle: the
+// leading offset steps between 64-element atoms along N, the stride between
+// 8-row groups along K.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swizzle) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)swizzle << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A
+// and B bf16 (bits 7-9, 10-12 = 1), A K-major, B K-major or MN-major (bit 16),
+// N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+constexpr uint32_t idesc_bf16(int n, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kHeads >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16_tc(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                            uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// The same MMA with A (M x 16 bf16, a row per lane as 8 columns of packed
+// pairs) in tensor memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes.  The
+// wait is followed by empty statements naming every destination register as
+// read and written, so no use of them can be scheduled before it.
+#define DSA_TMEM_LD16(o)                                                                    \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, "  \
+               "%8, %9, %10, %11, %12, %13, %14, %15}, [%16];"                              \
+               : "=r"(r[o + 0]), "=r"(r[o + 1]), "=r"(r[o + 2]), "=r"(r[o + 3]),           \
+                 "=r"(r[o + 4]), "=r"(r[o + 5]), "=r"(r[o + 6]), "=r"(r[o + 7]),           \
+                 "=r"(r[o + 8]), "=r"(r[o + 9]), "=r"(r[o + 10]), "=r"(r[o + 11]),         \
+                 "=r"(r[o + 12]), "=r"(r[o + 13]), "=r"(r[o + 14]), "=r"(r[o + 15])        \
+               : "r"(taddr + (uint32_t)(o)))
+#define DSA_WAIT_LD16(o)                                                                    \
+  asm volatile(""                                                                           \
+               : "+r"(r[o + 0]), "+r"(r[o + 1]), "+r"(r[o + 2]), "+r"(r[o + 3]),           \
+                 "+r"(r[o + 4]), "+r"(r[o + 5]), "+r"(r[o + 6]), "+r"(r[o + 7]),           \
+                 "+r"(r[o + 8]), "+r"(r[o + 9]), "+r"(r[o + 10]), "+r"(r[o + 11]),         \
+                 "+r"(r[o + 12]), "+r"(r[o + 13]), "+r"(r[o + 14]), "+r"(r[o + 15]))
+#define DSA_TMEM_ST16(o)                                                                    \
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, " \
+               "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr + (uint32_t)(o)),  \
+               "r"(r[o + 0]), "r"(r[o + 1]), "r"(r[o + 2]), "r"(r[o + 3]), "r"(r[o + 4]),   \
+               "r"(r[o + 5]), "r"(r[o + 6]), "r"(r[o + 7]), "r"(r[o + 8]), "r"(r[o + 9]),   \
+               "r"(r[o + 10]), "r"(r[o + 11]), "r"(r[o + 12]), "r"(r[o + 13]),              \
+               "r"(r[o + 14]), "r"(r[o + 15])                                               \
+               : "memory")
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  DSA_TMEM_LD16(0);
+  DSA_TMEM_LD16(16);
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  DSA_WAIT_LD16(0);
+  DSA_WAIT_LD16(16);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  DSA_TMEM_ST16(0);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  DSA_TMEM_ST16(0);
+  DSA_TMEM_ST16(16);
+}
+#undef DSA_TMEM_LD16
+#undef DSA_WAIT_LD16
+#undef DSA_TMEM_ST16
+
+__device__ __forceinline__ bool aborted(const MlaSmem& sm) {
+  return *reinterpret_cast<const volatile int*>(&sm.abort) != 0;
+}
+
+// Bounded wait that also gives up once another role of the CTA has aborted.
+__device__ __forceinline__ bool wait_or_abort(MlaSmem& sm, uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (aborted(sm)) return false;
+    if (i > 64) __nanosleep(64);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void abort_cta(MlaSmem& sm, uint32_t* flags) {
+  raise_flag(flags, DSA_FLAG_TIMEOUT);
+  *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+}
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// 2^x (ex2.approx.ftz.f32: relative error about 2^-22, results below 2^-126
+// flushed to zero; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+
+// ---- warps 0-3: the query's shared-memory blocks, then the tiles' rows -----
+// Warps w and w + 2 gather tiles w, w + 2, ... (w = 0, 1) into stage w, rows
+// 0-31 and 32-63 of each.  Lane l owns one token of those rows (slot,
+// validity); the copies go four rows at a time, eight lanes per row segment
+// of one 64-column block (128 bytes read contiguously).
+__device__ __forceinline__ void gather_tiles(const MlaArgs& a, MlaSmem& sm,
+                                             const CUtensorMap* tm_q, int r, int hg,
+                                             int64_t row_base, int count, int ntiles,
+                                             const int32_t* slot_row) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int st = warp % kStages, part = warp / kStages;   // stage, 32-row half of the tile
+  if (warp == 0 && lane == 0) {
+    mbar_expect_tx(&sm.qfull, (uint32_t)(kQsBlocks * a.box_h * 128));
+    for (int i = 0; i < kQsBlocks; ++i)
+      tma_load_3d(sm.q[i], tm_q, (kQtBlocks + i) * 64, hg * kHeads, r, &sm.qfull);
+  }
+  const uint32_t stage = smem_u32(sm.kv[st][0]) + (uint32_t)(part * 32 * 128);
+  const int cc = lane & 7, rsub = lane >> 3;
+  bool bad = false;
+  for (int t = st, k = 0; t < ntiles; t += kStages, ++k) {
+    bool ok = true;
+    if (k >= 1) ok = wait_or_abort(sm, &sm.kvempty[st], (uint32_t)(k - 1) & 1u);
+    if (!__all_sync(kFull, ok)) {
+      if (lane == 0 && !aborted(sm)) abort_cta(sm, a.flags);
+      break;
+    }
+    const int j = t * kTile + part * 32 + lane;
+    const int slot = j < count ? __ldg(slot_row + j) : -1;
+    const bool in = slot >= 0 && (int64_t)slot < a.n_slots;
+    bad |= j < count && !in;
+    const unsigned v = __ballot_sync(kFull, in);
+    // A token left out reads a row the tile already reads (its weight is 0),
+    // or the shard's first row when these 32 tokens have no valid one.
+    const int sub = v ? __shfl_sync(kFull, slot, __ffs(v) - 1) : 0;
+    const int y = in ? slot : sub;
+    if (lane == 0) sm.vmask[st][part] = v;
+#pragma unroll 2
+    for (int rq = 0; rq < 8; ++rq) {
+      const int jr = 4 * rq + rsub;                    // row among this warp's 32
+      const int yj = __shfl_sync(kFull, y, jr);
+      const char* src = reinterpret_cast<const char*>(a.cache + (row_base + yj) * kDqk) + cc * 16;
+      // Row part * 32 + jr of the tile; its swizzle phase is jr & 7.
+      const uint32_t dst = stage + (uint32_t)(jr * 128 + ((cc ^ (jr & 7)) << 4));
+#pragma unroll
+      for (int kb = 0; kb < kBlocks; ++kb) cp_async16_cg(dst + kb * kKvBlock, src + kb * 128);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // This lane's copies (generic proxy) before the MMAs read them (async proxy).
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive1(&sm.kvfull[st]);
+  }
+  if (bad) raise_flag(a.flags, DSA_FLAG_BOUNDS);
+  // The query's copies land before this warp, and so the CTA, exits.
+  if (warp == 0 && lane == 0 && !mbar_wait(&sm.qfull, 0)) abort_cta(sm, a.flags);
+}
+
+// ---- warp 4, one thread: the MMAs ------------------------------------------
+// S(t + 1) may go before P V(t): whichever is ready first is issued.
+__device__ __forceinline__ void issue_mmas(const MlaArgs& a, MlaSmem& sm, uint32_t tmem, int half,
+                                           int ntiles) {
+  constexpr uint32_t kIdS = idesc_bf16(kTile, false);
+  constexpr uint32_t kIdO = idesc_bf16(kHalf, true);
+  bool ok = wait_or_abort(sm, &sm.qfull, 0) && wait_or_abort(sm, &sm.qtm, 0);
+  tc_fence_after();
+  const uint64_t qd = smem_desc(smem_u32(sm.q[0]), 16, 1024, 2);
+  const uint32_t d_s = tmem + kSCol, d_o = tmem + kOCol, a_q = tmem + kQCol, a_p = tmem + kPCol;
+  // Descriptors advance by (bytes >> 4): 16 K-elements = 32 bytes = 2, one
+  // 64-column block = its size >> 4.
+  auto issue_s = [&](int t) {
+    const uint64_t kd = smem_desc(smem_u32(sm.kv[t & 1][0]), 16, 1024, 2);
+#pragma unroll
+    for (int ks = 0; ks < kQtBlocks * 4; ++ks)
+      mma_bf16_ts(d_s, a_q + (uint32_t)(ks * 8),
+                  kd + (uint64_t)((ks >> 2) * (kKvBlock >> 4) + (ks & 3) * 2), kIdS,
+                  ks > 0 ? 1u : 0u);
+#pragma unroll
+    for (int ks = kQtBlocks * 4; ks < kBlocks * 4; ++ks)
+      mma_bf16_tc(d_s, qd + (uint64_t)((ks / 4 - kQtBlocks) * (kQBlock >> 4) + (ks & 3) * 2),
+                  kd + (uint64_t)((ks >> 2) * (kKvBlock >> 4) + (ks & 3) * 2), kIdS, 1u);
+    mma_commit(&sm.sfull);
+  };
+  int ns = 0;                                // S issued so far
+  for (int t = 0; ok && t < ntiles; ++t) {
+    for (uint32_t polls = 0;; ++polls) {
+      // S(ns): its tile has landed and the softmax has read S(ns - 1).
+      if (ns < ntiles && ns <= t + 1 && mbar_test(&sm.kvfull[ns & 1], (uint32_t)(ns >> 1) & 1u) &&
+          (ns == 0 || mbar_test(&sm.sfree, (uint32_t)(ns - 1) & 1u))) {
+        tc_fence_after();
+        issue_s(ns++);
+        continue;
+      }
+      if (ns > t && mbar_test(&sm.pfull, (uint32_t)t & 1u)) break;
+      if (polls >= 4 * kWaitPolls || aborted(sm)) {
+        ok = false;
+        break;
+      }
+      if (polls > 64) __nanosleep(32);
+    }
+    if (!ok) break;
+    tc_fence_after();
+    // V: this half's four blocks, MN-major: 64-column atoms kKvBlock apart,
+    // 8-token groups 1024 bytes apart; 16 tokens a step = 2048 bytes.
+    const uint64_t vd = smem_desc(smem_u32(sm.kv[t & 1][half * kVBlocks]), kKvBlock, 1024, 2);
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk)
+      mma_bf16_ts(d_o, a_p + (uint32_t)(kk * 8), vd + (uint64_t)(kk * (2048 >> 4)), kIdO,
+                  (t > 0 || kk > 0) ? 1u : 0u);
+    mma_commit(&sm.kvempty[t & 1]);
+    mma_commit(&sm.pvdone);
+  }
+  if (!ok && !aborted(sm)) abort_cta(sm, a.flags);
+  // Every MMA issued completes before the tensor memory is freed.
+  mma_commit(&sm.drain);
+  if (!mbar_wait(&sm.drain, 0)) abort_cta(sm, a.flags);
+}
+
+// ---- warps 5-8: the query's tensor-memory part, softmax, the outputs -------
+__device__ __forceinline__ void softmax_and_store(const MlaArgs& a, MlaSmem& sm, uint32_t tmem,
+                                                  int r, int half, int ntiles, int64_t head0,
+                                                  int hg) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int quad = warp & 3;                 // the tensor-memory lanes this warp may access
+  const int h = quad * 32 + lane;            // this thread's head within the group
+  const int gh = hg * kHeads + h;
+  const bool active = gh < a.H;
+  const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+
+  // Query dimensions 0..319 of this head into tensor memory (zeros past H),
+  // in two batches of 20 loads in flight.
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)r * a.H + gh) * kDqk);
+#pragma unroll 1
+    for (int b = 0; b < 2; ++b) {
+      uint4 x[20];
+#pragma unroll
+      for (int i = 0; i < 20; ++i) x[i] = active ? __ldg(src + b * 20 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c = 0; c < 80; c += 16) {
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[4 * i] = x[c / 4 + i].x;
+          v[4 * i + 1] = x[c / 4 + i].y;
+          v[4 * i + 2] = x[c / 4 + i].z;
+          v[4 * i + 3] = x[c / 4 + i].w;
+        }
+        tmem_st16(trow + (uint32_t)(kQCol + b * 80 + c), v);
+      }
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive1(&sm.qtm);
+  }
+
+  float m = -INFINITY, l = 0.f, w = 0.f;
+  bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
     const int st = t & 1;
-    if (t >= kStages) ok = mbar_wait(&sm.empty[st], (uint32_t)(t / kStages - 1) & 1u);
+    ok = wait_or_abort(sm, &sm.sfull, (uint32_t)t & 1u) &&
+         wait_or_abort(sm, &sm.kvfull[st], (uint32_t)(t >> 1) & 1u);
     if (!__all_sync(kFull, ok)) {
       ok = false;
       break;
     }
-    const int idx = t * kTile + lane;
-    const int slot = idx < count ? __ldg(slot_row + idx) : -1;
-    const bool in = slot >= 0 && (int64_t)slot < a.n_slots;
-    bad |= idx < count && !in;
-    __nv_bfloat16* dst = &sm.kv[st][lane * kStride];
-    if (!in)
-      for (int c = 0; c < kChunks; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
-    const unsigned valid = __ballot_sync(kFull, in);
-    if (lane == 0) sm.vmask[st] = valid;
-    // The consumers' reads of this stage (generic proxy) before the copies.
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_after();
+    uint32_t r0[32], r1[32];
+    tmem_ld32(trow + kSCol, r0);
+    tmem_ld32(trow + kSCol + 32, r1);
+    tc_fence_before();
     __syncwarp();
-    // Arm first (zeroed rows and flags published by this arrival), then copy.
-    if (lane == 0) mbar_expect_tx(&sm.full[st], (uint32_t)__popc(valid) * kRowBytes);
-    __syncwarp();
-    if (in) bulk_g2s(dst, shard_cache + (int64_t)slot * kDqk, kRowBytes, &sm.full[st]);
-    issued = t + 1;
-  }
-  if (!ok && lane == 0) raise_flag(a.flags, DSA_FLAG_TIMEOUT);
-  if (bad) raise_flag(a.flags, DSA_FLAG_BOUNDS);
-  // Copies still in flight land before this warp, and so the block, exits.
-  for (int t = max(0, issued - kStages); t < issued; ++t)
-    mbar_wait(&sm.full[t & 1], (uint32_t)(t / kStages) & 1u);
-}
-
-__global__ void __launch_bounds__(kAttnThreads, 1) sparse_mla_decode_kernel(const AttnArgs a) {
-  extern __shared__ __align__(16) unsigned char attn_smem[];
-  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(attn_smem);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, t4 = lane & 3;
-  const int hgroups = a.H / kHeads;
-  const int hg = blockIdx.x % hgroups;
-  const int pair = blockIdx.x / hgroups;     // s * rows + r
-  const int s = pair / a.rows, r = pair - s * a.rows;
-  int count = __ldg(a.counts + pair);
-  if ((count < 0 || count > a.K) && tid == 0) raise_flag(a.flags, DSA_FLAG_BOUNDS);
-  count = min(max(count, 0), a.K);
-  const int64_t obase = (int64_t)pair * a.H + hg * kHeads;   // first head of the group
-
-  if (count == 0) {
-    // Nothing selected on this shard: O = 0, lse2 = -inf.
-    for (int i = tid; i < kHeads * kDv / 8; i += kAttnThreads)
-      *reinterpret_cast<uint4*>(a.out + (obase + i / (kDv / 8)) * kDv + (i % (kDv / 8)) * 8) =
-          make_uint4(0, 0, 0, 0);
-    if (tid < kHeads) a.lse2[obase + tid] = -INFINITY;
-    return;
-  }
-
-  // The group's query rows (cp.async by every thread) and the barriers.
-  {
-    const __nv_bfloat16* qg = a.q + ((int64_t)r * a.H + hg * kHeads) * kDqk;
-    for (int c = tid; c < kHeads * kChunks; c += kAttnThreads) {
-      const int h = c / kChunks, j = c - h * kChunks;
-      cp_async16(&sm.q[h * kStride + j * 8], qg + (int64_t)h * kDqk + j * 8);
+    if (lane == 0) mbar_arrive1(&sm.sfree);
+    const uint32_t vm0 = sm.vmask[st][0], vm1 = sm.vmask[st][1];
+    float x[kTile];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      x[j] = ((vm0 >> j) & 1u) ? __uint_as_float(r0[j]) * a.c2 : -INFINITY;
+      x[32 + j] = ((vm1 >> j) & 1u) ? __uint_as_float(r1[j]) * a.c2 : -INFINITY;
+      mx = fmaxf(mx, fmaxf(x[j], x[32 + j]));
     }
-    cp_async_commit();
-  }
-  if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) {
-      mbar_init(&sm.full[st], 1);
-      mbar_init(&sm.empty[st], kConsumers);
+    const float mn = mx > m + kRescaleGap ? mx : m;   // m = -inf takes any finite max
+    const float alpha = m == -INFINITY ? 1.f : fast_exp2(m - mn);
+    const float ref = mn == -INFINITY ? 0.f : mn;
+    uint32_t pk[kTile / 2];
+    float s = 0.f, sb = 0.f;
+#pragma unroll
+    for (int j = 0; j < kTile / 2; ++j) {
+      const float e0 = fast_exp2(x[2 * j] - ref), e1 = fast_exp2(x[2 * j + 1] - ref);
+      pk[j] = pack_bf16(e0, e1);
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[j]));
+      s += e0 + e1;
+      sb += f.x + f.y;
     }
-    mbar_init_fence();
-  }
-  cp_async_wait_all();
-  __syncthreads();
-  const int ntiles = (count + kTile - 1) / kTile;
-
-  if (warp == kConsumers) {
-    produce(a, sm, count, ntiles, a.slots + (int64_t)pair * a.K,
-            a.cache + (int64_t)s * a.n_slots * kDqk);
-    return;
-  }
-
-  // ---- consumer warps: head block hb (16 heads), half dh -------------------
-  const int hb = warp >> 1, dh = warp & 1;
-  const uint32_t qa = smem_u32(&sm.q[(hb * 16 + (lane & 15)) * kStride + (lane >> 4) * 8]);
-  float acc[kHalfDv / 8][4];                 // 32 n-tiles of 8 dims x (rows g, g + 8)
-#pragma unroll
-  for (int j = 0; j < kHalfDv / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-  // Running max and two row sums: of the fp32 weights (for the LSE) and of
-  // the bf16-rounded weights that enter P V (to normalise O, which is then an
-  // exact convex mix of what was multiplied).
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, w0 = 0.f, w1 = 0.f;
-  bool ok = true;
-
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t & 1;
-    const bool landed = mbar_wait(&sm.full[st], (uint32_t)(t / kStages) & 1u);
-
-    // Scores of the 16 heads against tokens dh*16 .. dh*16+15 (two n-tiles),
-    // even and odd k-steps in separate accumulators.
-    float c[2][2][4];
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) c[n][e][0] = c[n][e][1] = c[n][e][2] = c[n][e][3] = 0.f;
-    const uint32_t kb = smem_u32(&sm.kv[st][(dh * 16 + (lane & 7) + ((lane >> 4) & 1) * 8) *
-                                                kStride + ((lane >> 3) & 1) * 8]);
-#pragma unroll 3
-    for (int ks = 0; ks < kDqk / 16; ks += 2) {
-      uint32_t af[4], bf[4], ag[4], bg[4];
-      ldsm_x4(qa + ks * 32, af);
-      ldsm_x4(kb + ks * 32, bf);
-      ldsm_x4(qa + ks * 32 + 32, ag);
-      ldsm_x4(kb + ks * 32 + 32, bg);
-      mma_bf16(c[0][0], af, bf[0], bf[1]);
-      mma_bf16(c[1][0], af, bf[2], bf[3]);
-      mma_bf16(c[0][1], ag, bg[0], bg[1]);
-      mma_bf16(c[1][1], ag, bg[2], bg[3]);
-    }
-    // x[kk][v]: k-step kk (tokens kk*16 ..); v in A-fragment order: rows g
-    // (v = 0, 1, 4, 5) and g + 8 (v = 2, 3, 6, 7) at tokens 2t, 2t+1, 2t+8, 2t+9.
-    float own[8], oth[8];
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int u = 0; u < 4; ++u) own[4 * n + u] = (c[n][0][u] + c[n][1][u]) * a.c2;
-    float* mine = &sm.xs[hb][dh][st][0][lane];
-#pragma unroll
-    for (int v = 0; v < 8; ++v) mine[v * 32] = own[v];
-    if (bar_any(1 + hb, 64, !landed)) {      // both warps of the block see the same answer
+    l = l * alpha + s;
+    w = w * alpha + sb;
+    m = mn;
+    // P V of the previous tile is done: the weights' columns are free and O
+    // holds every earlier tile.
+    if (t > 0) ok = wait_or_abort(sm, &sm.pvdone, (uint32_t)(t - 1) & 1u);
+    if (!__all_sync(kFull, ok)) {
       ok = false;
       break;
     }
-    const float* other = &sm.xs[hb][dh ^ 1][st][0][lane];
+    tc_fence_after();
+    if (__any_sync(kFull, alpha != 1.f)) {     // the reference moved: rescale O
+#pragma unroll 1
+      for (int c = 0; c < kHalf; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(trow + (uint32_t)(kOCol + c), o);
 #pragma unroll
-    for (int v = 0; v < 8; ++v) oth[v] = other[v * 32];
-    float x[2][8];                           // by k-step, selected without indexing by dh
-#pragma unroll
-    for (int v = 0; v < 8; ++v) {
-      x[0][v] = dh ? oth[v] : own[v];
-      x[1][v] = dh ? own[v] : oth[v];
-    }
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-    const uint32_t vm = sm.vmask[st] >> (2 * t4);
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const int tok = kk * 16 + (v & 1) + ((v >> 2) << 3);   // + 2 t4, folded into vm
-        if (!((vm >> tok) & 1u)) x[kk][v] = -INFINITY;
-        if ((v >> 1) & 1) mx1 = fmaxf(mx1, x[kk][v]);
-        else mx0 = fmaxf(mx0, x[kk][v]);
-      }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
-    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-    // Rows with nothing valid yet keep m = -inf: use 0 as the reference.
-    const float ref0 = n0 == -INFINITY ? 0.f : n0, ref1 = n1 == -INFINITY ? 0.f : n1;
-    const float al0 = exp2f(m0 - ref0), al1 = exp2f(m1 - ref1);
-    m0 = n0;
-    m1 = n1;
-    uint32_t pa[2][4];
-    float s0 = 0.f, s1 = 0.f, r0 = 0.f, r1 = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      float e[8];
-#pragma unroll
-      for (int v = 0; v < 8; ++v) e[v] = exp2f(x[kk][v] - (((v >> 1) & 1) ? ref1 : ref0));
-#pragma unroll
-      for (int q2 = 0; q2 < 4; ++q2) {
-        pa[kk][q2] = pack_bf16(e[2 * q2], e[2 * q2 + 1]);
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa[kk][q2]));
-        if (q2 & 1) {
-          s1 += e[2 * q2] + e[2 * q2 + 1];
-          r1 += f.x + f.y;
-        } else {
-          s0 += e[2 * q2] + e[2 * q2 + 1];
-          r0 += f.x + f.y;
-        }
+        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+        tmem_st32(trow + (uint32_t)(kOCol + c), o);
       }
     }
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      s0 += __shfl_xor_sync(kFull, s0, o);
-      s1 += __shfl_xor_sync(kFull, s1, o);
-      r0 += __shfl_xor_sync(kFull, r0, o);
-      r1 += __shfl_xor_sync(kFull, r1, o);
-    }
-    l0 = l0 * al0 + s0;
-    l1 = l1 * al1 + s1;
-    w0 = w0 * al0 + r0;
-    w1 = w1 * al1 + r1;
-    if (__any_sync(kFull, al0 != 1.f || al1 != 1.f)) {   // the max moved: rescale O
-#pragma unroll
-      for (int j = 0; j < kHalfDv / 8; ++j) {
-        acc[j][0] *= al0;
-        acc[j][1] *= al0;
-        acc[j][2] *= al1;
-        acc[j][3] *= al1;
-      }
-    }
-    // O += P V over this warp's 256 output dimensions.
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const uint32_t vb = smem_u32(&sm.kv[st][(kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) *
-                                                  kStride + dh * kHalfDv + (lane >> 4) * 8]);
-#pragma unroll
-      for (int j = 0; j < kHalfDv / 16; ++j) {
-        uint32_t bf[4];
-        ldsm_x4_t(vb + j * 32, bf);
-        mma_bf16(acc[2 * j], pa[kk], bf[0], bf[1]);
-        mma_bf16(acc[2 * j + 1], pa[kk], bf[2], bf[3]);
-      }
-    }
+    tmem_st32(trow + kPCol, pk);
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[st]);   // this warp is done with the stage
+    if (lane == 0) mbar_arrive1(&sm.pfull);
   }
-  if (!ok && lane == 0) raise_flag(a.flags, DSA_FLAG_TIMEOUT);
-
-  // ---- O / w in bf16, lse2 = m + log2 l ----------------------------------------
-  const float inv0 = w0 > 0.f ? 1.f / w0 : 0.f, inv1 = w1 > 0.f ? 1.f / w1 : 0.f;
-  const int64_t h0 = obase + hb * 16 + g;
-  __nv_bfloat16* o0 = a.out + h0 * kDv + dh * kHalfDv + 2 * t4;
-  __nv_bfloat16* o1 = o0 + 8 * kDv;
+  if (ok && ntiles > 0) ok = wait_or_abort(sm, &sm.pvdone, (uint32_t)(ntiles - 1) & 1u);
+  if (!__all_sync(kFull, ok)) {
+    if (lane == 0 && !aborted(sm)) abort_cta(sm, a.flags);
+    return;
+  }
+  tc_fence_after();
+  // O / w in bf16 (this CTA's 256 dimensions); lse2 = m + log2 l.
+  const float inv = w > 0.f ? 1.f / w : 0.f;
+  __nv_bfloat16* orow = a.out + (head0 + h) * kDv + half * kHalf;
+#pragma unroll 1
+  for (int c = 0; c < kHalf; c += 32) {
+    uint32_t o[32];
+    tmem_ld32(trow + (uint32_t)(kOCol + c), o);
+    if (active) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
-  for (int j = 0; j < kHalfDv / 8; ++j) {
-    *reinterpret_cast<uint32_t*>(o0 + j * 8) = pack_bf16(acc[j][0] * inv0, acc[j][1] * inv0);
-    *reinterpret_cast<uint32_t*>(o1 + j * 8) = pack_bf16(acc[j][2] * inv1, acc[j][3] * inv1);
+      for (int v = 0; v < 4; ++v) {
+        uint32_t b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          b[i] = pack_bf16(__uint_as_float(o[8 * v + 2 * i]) * inv,
+                           __uint_as_float(o[8 * v + 2 * i + 1]) * inv);
+        dst[v] = make_uint4(b[0], b[1], b[2], b[3]);
+      }
+    }
   }
-  if (dh == 0 && t4 == 0) {
-    a.lse2[h0] = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
-    a.lse2[h0 + 8] = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
+  if (active && half == 0) a.lse2[head0 + h] = l > 0.f ? m + log2f(l) : -INFINITY;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const MlaArgs a) {
+  extern __shared__ unsigned char mla_smem_raw[];
+  MlaSmem& sm = *reinterpret_cast<MlaSmem*>(
+      (reinterpret_cast<uintptr_t>(mla_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int half = blockIdx.x & 1;
+  const int x = blockIdx.x >> 1;
+  const int hg = x % a.hgroups;
+  const int pair = x / a.hgroups;            // s * rows + r
+  const int s = pair / a.rows, r = pair - s * a.rows;
+  int count = __ldg(a.counts + pair);
+  if ((count < 0 || count > a.K) && tid == 0 && half == 0) raise_flag(a.flags, DSA_FLAG_BOUNDS);
+  count = min(max(count, 0), a.K);
+  const int ntiles = (count + kTile - 1) / kTile;
+  const int64_t head0 = (int64_t)pair * a.H + hg * kHeads;   // first head of the group
+  const int nheads = min(kHeads, a.H - hg * kHeads);
+
+  if (count == 0) {
+    // Nothing selected on this shard: O = 0, lse2 = -inf.
+    for (int i = tid; i < nheads * (kHalf / 8); i += kThreads)
+      *reinterpret_cast<uint4*>(a.out + (head0 + i / (kHalf / 8)) * kDv + half * kHalf +
+                                (i % (kHalf / 8)) * 8) = make_uint4(0, 0, 0, 0);
+    if (half == 0 && tid < nheads) a.lse2[head0 + tid] = -INFINITY;
+    return;
+  }
+
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sm.tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    mbar_init(&sm.qfull, 1);
+    mbar_init(&sm.qtm, kSoftmaxWarps);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sm.kvfull[i], 32 * kGatherWarps / kStages);   // every gathering lane
+      mbar_init(&sm.kvempty[i], 1);
+    }
+    mbar_init(&sm.sfull, 1);
+    mbar_init(&sm.sfree, kSoftmaxWarps);
+    mbar_init(&sm.pfull, kSoftmaxWarps);
+    mbar_init(&sm.pvdone, 1);
+    mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    mbar_init_fence();
+  }
+  if (a.box_h < kHeads && warp > kMmaWarp) {
+    // Fewer heads than a box: the shared-memory query rows past them are zeros.
+    const int per_block = (kHeads - a.box_h) * 8;   // 16-byte chunks
+    for (int i = tid - (kMmaWarp + 1) * 32; i < kQsBlocks * per_block; i += kSoftmaxWarps * 32)
+      *reinterpret_cast<uint4*>(sm.q[i / per_block] + a.box_h * 128 + (i % per_block) * 16) =
+          make_uint4(0, 0, 0, 0);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+
+  if (warp < kGatherWarps) {
+    gather_tiles(a, sm, &tm_q, r, hg, (int64_t)s * a.n_slots, count, ntiles,
+                 a.slots + (int64_t)pair * a.K);
+  } else if (warp == kMmaWarp) {
+    if ((tid & 31) == 0) issue_mmas(a, sm, tmem, half, ntiles);
+    __syncwarp();
+  } else {
+    softmax_and_store(a, sm, tmem, r, half, ntiles, head0, hg);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
   }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// The queries as [rows][H] rows of kDqk bf16: boxes of 64 columns (128 bytes,
+// 128-byte swizzle) by box_h heads of one row.
+bool encode_queries(CUtensorMap* map, const void* q, int rows, int H, int box_h) {
+  const auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kDqk, (cuuint64_t)H, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)kDqk * 2, (cuuint64_t)kDqk * 2 * (cuuint64_t)H};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_h, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
 
 }  // namespace
 }  // namespace dsa
@@ -379,31 +649,36 @@ extern "C" dsa_status dsa_sparse_mla_decode(const uint16_t* q, const uint16_t* k
                                             uint32_t* err_flags, cudaStream_t stream) {
   if (rows < 0 || K < 1 || n_slots < 1 || !(scale == scale) || isinf(scale))
     return DSA_ERR_INVALID_ARG;
-  if (S < 1 || S > DSA_MAX_SHARDS || H < kHeads || H % kHeads) return DSA_ERR_UNSUPPORTED;
+  if (S < 1 || S > DSA_MAX_SHARDS || H < 64 || H % 64) return DSA_ERR_UNSUPPORTED;
   if (rows == 0) return DSA_OK;
   if (!q || !kv_cache || !slots || !counts || !out || !lse2) return DSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
   if (n_slots > (int64_t)INT32_MAX + 1) return DSA_ERR_UNSUPPORTED;
-  const int64_t blocks = (int64_t)rows * S * (H / kHeads);
+  const int hgroups = (H + kHeads - 1) / kHeads;
+  const int64_t blocks = (int64_t)rows * S * hgroups * 2;
   if (blocks > INT32_MAX) return DSA_ERR_UNSUPPORTED;
-  const int smem = (int)sizeof(AttnSmem);
+  const int box_h = H < kHeads ? H : kHeads;
+  CUtensorMap tm_q;
+  if (!encode_queries(&tm_q, q, rows, H, box_h)) return DSA_ERR_CUDA;
+  const int smem = (int)sizeof(MlaSmem) + 1024;
   if (cudaFuncSetAttribute(sparse_mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return DSA_ERR_CUDA;
-  const AttnArgs a{reinterpret_cast<const __nv_bfloat16*>(q),
-                   reinterpret_cast<const __nv_bfloat16*>(kv_cache),
-                   n_slots,
-                   slots,
-                   counts,
-                   rows,
-                   S,
-                   H,
-                   K,
-                   scale * kLog2e,
-                   reinterpret_cast<__nv_bfloat16*>(out),
-                   lse2,
-                   err_flags};
+  const MlaArgs a{reinterpret_cast<const __nv_bfloat16*>(q),
+                  reinterpret_cast<const __nv_bfloat16*>(kv_cache),
+                  slots,
+                  counts,
+                  n_slots,
+                  rows,
+                  H,
+                  K,
+                  hgroups,
+                  box_h,
+                  scale * kLog2e,
+                  reinterpret_cast<__nv_bfloat16*>(out),
+                  lse2,
+                  err_flags};
   const cudaError_t e = launch_kernel(sparse_mla_decode_kernel, dim3((unsigned)blocks),
-                                      dim3(kAttnThreads), (size_t)smem, stream, 0, a);
+                                      dim3(kThreads), (size_t)smem, stream, 0, tm_q, a);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
