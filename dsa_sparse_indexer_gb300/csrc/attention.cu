@@ -73,6 +73,7 @@ constexpr int kQBlock = kHeads * 128;        // bytes of one query block
 constexpr int kKvBlock = kTile * 128;        // bytes of one tile block
 constexpr int kVBlocks = kHalf / 64;         // 4 value blocks per half
 constexpr int kGatherWarps = 4;              // two per stage, 32 rows of a tile each
+constexpr int kABlocks = kBlocks - kVBlocks; // 5 blocks only the scores read
 constexpr int kMmaWarp = kGatherWarps;
 constexpr int kSoftmaxWarps = 4;
 constexpr int kThreads = (kGatherWarps + 1 + kSoftmaxWarps) * 32;
@@ -94,8 +95,11 @@ static_assert(kQCol + kQtBlocks * 32 == kTmemCols && kPCol + kTile / 2 == kQCol 
 struct alignas(1024) MlaSmem {
   uint8_t kv[kStages][kBlocks][kKvBlock];    // 147456: gathered tiles
   uint8_t q[kQsBlocks][kQBlock];             // 65536: query dimensions 320..575
-  uint32_t vmask[kStages][2];                // valid tokens of a stage's tile
-  uint64_t qfull, qtm, kvfull[kStages], kvempty[kStages], sfull, sfree, pfull, pvdone, drain;
+  uint32_t vmask[4][2];                      // valid tokens of tile t, at t & 3
+  // A stage in two parts: the five blocks only the scores read (A) and this
+  // half's four value blocks (B), filled and freed separately.
+  uint64_t qfull, qtm, fullA[kStages], fullB[kStages], emptyA[kStages], emptyB[kStages];
+  uint64_t sfull, sfree, pfull, pvdone, drain;
   uint32_t tmem;
   int abort;
 };
@@ -112,6 +116,14 @@ struct MlaArgs {
   float* lse2;                   // [S][rows][H]
   uint32_t* flags;
 };
+
+// Column block of step i of part A (the blocks only the scores read) and of
+// part B (this half's value blocks): half 0 reads values from blocks 0-3, so
+// its part A is 4-8; half 1 reads 4-7, so its part A is 0-3 and 8.
+__host__ __device__ constexpr int block_a(int half, int i) {
+  return half == 0 ? kVBlocks + i : (i < kVBlocks ? i : kBlocks - 1);
+}
+__host__ __device__ constexpr int block_b(int half, int i) { return half * kVBlocks + i; }
 
 // Shared-memory matrix descriptor: start address >> 4 (bits 0-13), leading
 // byte offset >> 4 (bits 16-29), stride byte offset >> 4 (bits 32-45),
@@ -269,6 +281,24 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Two fused multiply-adds in one instruction (fma.rn.f32x2) and two additions
+// (add.rn.f32x2), each rounded as the scalar operation would be.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&r);
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&r);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -279,9 +309,42 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // Warps w and w + 2 gather tiles w, w + 2, ... (w = 0, 1) into stage w, rows
 // 0-31 and 32-63 of each.  Lane l owns one token of those rows (slot,
 // validity); the copies go four rows at a time, eight lanes per row segment
-// of one 64-column block (128 bytes read contiguously).
+// of one 64-column block (128 bytes read contiguously).  Part A of a tile
+// goes as soon as the scores of the stage's previous tile are done, part B
+// once its P V is.
+__device__ __forceinline__ void copy_part(const MlaArgs& a, uint32_t stage, int64_t row_base,
+                                          int y, int half, bool part_a) {
+  const int lane = threadIdx.x & 31;
+  const int cc = lane & 7, rsub = lane >> 3;
+#pragma unroll 2
+  for (int rq = 0; rq < 8; ++rq) {
+    const int jr = 4 * rq + rsub;                      // row among this warp's 32
+    const int yj = __shfl_sync(kFull, y, jr);
+    const char* src = reinterpret_cast<const char*>(a.cache + (row_base + yj) * kDqk) + cc * 16;
+    // The row's swizzle phase within its 8-row group is jr & 7.
+    const uint32_t dst = stage + (uint32_t)(jr * 128 + ((cc ^ (jr & 7)) << 4));
+    if (part_a) {
+#pragma unroll
+      for (int i = 0; i < kABlocks; ++i) {
+        const int kb = block_a(half, i);
+        cp_async16_cg(dst + kb * kKvBlock, src + kb * 128);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kVBlocks; ++i) {
+        const int kb = block_b(half, i);
+        cp_async16_cg(dst + kb * kKvBlock, src + kb * 128);
+      }
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  // This lane's copies (generic proxy) before the MMAs read them (async proxy).
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void gather_tiles(const MlaArgs& a, MlaSmem& sm,
-                                             const CUtensorMap* tm_q, int r, int hg,
+                                             const CUtensorMap* tm_q, int r, int hg, int half,
                                              int64_t row_base, int count, int ntiles,
                                              const int32_t* slot_row) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -292,15 +355,10 @@ __device__ __forceinline__ void gather_tiles(const MlaArgs& a, MlaSmem& sm,
       tma_load_3d(sm.q[i], tm_q, (kQtBlocks + i) * 64, hg * kHeads, r, &sm.qfull);
   }
   const uint32_t stage = smem_u32(sm.kv[st][0]) + (uint32_t)(part * 32 * 128);
-  const int cc = lane & 7, rsub = lane >> 3;
-  bool bad = false;
+  bool bad = false, ok = true;
   for (int t = st, k = 0; t < ntiles; t += kStages, ++k) {
-    bool ok = true;
-    if (k >= 1) ok = wait_or_abort(sm, &sm.kvempty[st], (uint32_t)(k - 1) & 1u);
-    if (!__all_sync(kFull, ok)) {
-      if (lane == 0 && !aborted(sm)) abort_cta(sm, a.flags);
-      break;
-    }
+    if (k >= 1) ok = wait_or_abort(sm, &sm.emptyA[st], (uint32_t)(k - 1) & 1u);
+    if (!__all_sync(kFull, ok)) break;
     const int j = t * kTile + part * 32 + lane;
     const int slot = j < count ? __ldg(slot_row + j) : -1;
     const bool in = slot >= 0 && (int64_t)slot < a.n_slots;
@@ -310,31 +368,27 @@ __device__ __forceinline__ void gather_tiles(const MlaArgs& a, MlaSmem& sm,
     // or the shard's first row when these 32 tokens have no valid one.
     const int sub = v ? __shfl_sync(kFull, slot, __ffs(v) - 1) : 0;
     const int y = in ? slot : sub;
-    if (lane == 0) sm.vmask[st][part] = v;
-#pragma unroll 2
-    for (int rq = 0; rq < 8; ++rq) {
-      const int jr = 4 * rq + rsub;                    // row among this warp's 32
-      const int yj = __shfl_sync(kFull, y, jr);
-      const char* src = reinterpret_cast<const char*>(a.cache + (row_base + yj) * kDqk) + cc * 16;
-      // Row part * 32 + jr of the tile; its swizzle phase is jr & 7.
-      const uint32_t dst = stage + (uint32_t)(jr * 128 + ((cc ^ (jr & 7)) << 4));
-#pragma unroll
-      for (int kb = 0; kb < kBlocks; ++kb) cp_async16_cg(dst + kb * kKvBlock, src + kb * 128);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    // This lane's copies (generic proxy) before the MMAs read them (async proxy).
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive1(&sm.kvfull[st]);
+    if (lane == 0) sm.vmask[t & 3][part] = v;   // published by this lane's arrivals
+    copy_part(a, stage, row_base, y, half, true);
+    mbar_arrive1(&sm.fullA[st]);
+    if (k >= 1) ok = wait_or_abort(sm, &sm.emptyB[st], (uint32_t)(k - 1) & 1u);
+    if (!__all_sync(kFull, ok)) break;
+    copy_part(a, stage, row_base, y, half, false);
+    mbar_arrive1(&sm.fullB[st]);
   }
+  if (!__all_sync(kFull, ok) && lane == 0 && !aborted(sm)) abort_cta(sm, a.flags);
   if (bad) raise_flag(a.flags, DSA_FLAG_BOUNDS);
   // The query's copies land before this warp, and so the CTA, exits.
   if (warp == 0 && lane == 0 && !mbar_wait(&sm.qfull, 0)) abort_cta(sm, a.flags);
 }
 
 // ---- warp 4, one thread: the MMAs ------------------------------------------
-// S(t + 1) may go before P V(t): whichever is ready first is issued.
-__device__ __forceinline__ void issue_mmas(const MlaArgs& a, MlaSmem& sm, uint32_t tmem, int half,
+// Scores in two parts following the stage's (part A's five blocks, then part
+// B's four), P V, each issued as soon as its operands are ready: P V of tile
+// t first (it frees part B of the stage), then part B of S, then part A of
+// the next S once the softmax has read the previous scores.
+template <int HALF>
+__device__ __forceinline__ void issue_mmas(const MlaArgs& a, MlaSmem& sm, uint32_t tmem,
                                            int ntiles) {
   constexpr uint32_t kIdS = idesc_bf16(kTile, false);
   constexpr uint32_t kIdO = idesc_bf16(kHalf, true);
@@ -342,49 +396,66 @@ __device__ __forceinline__ void issue_mmas(const MlaArgs& a, MlaSmem& sm, uint32
   tc_fence_after();
   const uint64_t qd = smem_desc(smem_u32(sm.q[0]), 16, 1024, 2);
   const uint32_t d_s = tmem + kSCol, d_o = tmem + kOCol, a_q = tmem + kQCol, a_p = tmem + kPCol;
-  // Descriptors advance by (bytes >> 4): 16 K-elements = 32 bytes = 2, one
-  // 64-column block = its size >> 4.
-  auto issue_s = [&](int t) {
-    const uint64_t kd = smem_desc(smem_u32(sm.kv[t & 1][0]), 16, 1024, 2);
+  // The four K-steps of one 64-column block kb (descriptors advance by bytes
+  // >> 4: 16 K-elements = 32 bytes = 2, one block = its size >> 4); A is the
+  // query block, in tensor memory for kb < kQtBlocks.
+  auto block_steps = [&](uint64_t kd, int kb, bool first) {
 #pragma unroll
-    for (int ks = 0; ks < kQtBlocks * 4; ++ks)
-      mma_bf16_ts(d_s, a_q + (uint32_t)(ks * 8),
-                  kd + (uint64_t)((ks >> 2) * (kKvBlock >> 4) + (ks & 3) * 2), kIdS,
-                  ks > 0 ? 1u : 0u);
-#pragma unroll
-    for (int ks = kQtBlocks * 4; ks < kBlocks * 4; ++ks)
-      mma_bf16_tc(d_s, qd + (uint64_t)((ks / 4 - kQtBlocks) * (kQBlock >> 4) + (ks & 3) * 2),
-                  kd + (uint64_t)((ks >> 2) * (kKvBlock >> 4) + (ks & 3) * 2), kIdS, 1u);
-    mma_commit(&sm.sfull);
-  };
-  int ns = 0;                                // S issued so far
-  for (int t = 0; ok && t < ntiles; ++t) {
-    for (uint32_t polls = 0;; ++polls) {
-      // S(ns): its tile has landed and the softmax has read S(ns - 1).
-      if (ns < ntiles && ns <= t + 1 && mbar_test(&sm.kvfull[ns & 1], (uint32_t)(ns >> 1) & 1u) &&
-          (ns == 0 || mbar_test(&sm.sfree, (uint32_t)(ns - 1) & 1u))) {
-        tc_fence_after();
-        issue_s(ns++);
-        continue;
-      }
-      if (ns > t && mbar_test(&sm.pfull, (uint32_t)t & 1u)) break;
-      if (polls >= 4 * kWaitPolls || aborted(sm)) {
-        ok = false;
-        break;
-      }
-      if (polls > 64) __nanosleep(32);
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const uint64_t db = kd + (uint64_t)(kb * (kKvBlock >> 4) + k4 * 2);
+      const uint32_t acc = (first && k4 == 0) ? 0u : 1u;
+      if (kb < kQtBlocks)
+        mma_bf16_ts(d_s, a_q + (uint32_t)(kb * 32 + k4 * 8), db, kIdS, acc);
+      else
+        mma_bf16_tc(d_s, qd + (uint64_t)((kb - kQtBlocks) * (kQBlock >> 4) + k4 * 2), db, kIdS,
+                    acc);
     }
-    if (!ok) break;
-    tc_fence_after();
-    // V: this half's four blocks, MN-major: 64-column atoms kKvBlock apart,
-    // 8-token groups 1024 bytes apart; 16 tokens a step = 2048 bytes.
-    const uint64_t vd = smem_desc(smem_u32(sm.kv[t & 1][half * kVBlocks]), kKvBlock, 1024, 2);
+  };
+  int na = 0, nb = 0;                        // S parts A and B issued so far
+  uint32_t idle = 0;                         // polls since the last issue
+  for (int t = 0; ok && t < ntiles;) {
+    if (nb > t && mbar_test(&sm.pfull, (uint32_t)t & 1u)) {
+      tc_fence_after();
+      // V: this half's four blocks, MN-major: 64-column atoms kKvBlock apart,
+      // 8-token groups 1024 bytes apart; 16 tokens a step = 2048 bytes.
+      const uint64_t vd = smem_desc(smem_u32(sm.kv[t & 1][HALF * kVBlocks]), kKvBlock, 1024, 2);
 #pragma unroll
-    for (int kk = 0; kk < kTile / 16; ++kk)
-      mma_bf16_ts(d_o, a_p + (uint32_t)(kk * 8), vd + (uint64_t)(kk * (2048 >> 4)), kIdO,
-                  (t > 0 || kk > 0) ? 1u : 0u);
-    mma_commit(&sm.kvempty[t & 1]);
-    mma_commit(&sm.pvdone);
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_bf16_ts(d_o, a_p + (uint32_t)(kk * 8), vd + (uint64_t)(kk * (2048 >> 4)), kIdO,
+                    (t > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(&sm.emptyB[t & 1]);
+      mma_commit(&sm.pvdone);
+      ++t;
+      idle = 0;
+      continue;
+    }
+    if (na > nb && mbar_test(&sm.fullB[nb & 1], (uint32_t)(nb >> 1) & 1u)) {
+      tc_fence_after();
+      const uint64_t kd = smem_desc(smem_u32(sm.kv[nb & 1][0]), 16, 1024, 2);
+#pragma unroll
+      for (int i = 0; i < kVBlocks; ++i) block_steps(kd, block_b(HALF, i), false);
+      mma_commit(&sm.sfull);
+      mma_commit(&sm.emptyA[nb & 1]);
+      ++nb;
+      idle = 0;
+      continue;
+    }
+    if (na == nb && na < ntiles && mbar_test(&sm.fullA[na & 1], (uint32_t)(na >> 1) & 1u) &&
+        (na == 0 || mbar_test(&sm.sfree, (uint32_t)(na - 1) & 1u))) {
+      tc_fence_after();
+      const uint64_t kd = smem_desc(smem_u32(sm.kv[na & 1][0]), 16, 1024, 2);
+#pragma unroll
+      for (int i = 0; i < kABlocks; ++i) block_steps(kd, block_a(HALF, i), i == 0);
+      ++na;
+      idle = 0;
+      continue;
+    }
+    // Nothing ready: poll again (bounded, as every wait).
+    if (++idle >= 4 * kWaitPolls || aborted(sm)) {
+      ok = false;
+      break;
+    }
+    if (idle > 64) __nanosleep(32);
   }
   if (!ok && !aborted(sm)) abort_cta(sm, a.flags);
   // Every MMA issued completes before the tensor memory is freed.
@@ -435,8 +506,9 @@ __device__ __forceinline__ void softmax_and_store(const MlaArgs& a, MlaSmem& sm,
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
     const int st = t & 1;
+    // Part B of the tile has landed: its validity masks are visible.
     ok = wait_or_abort(sm, &sm.sfull, (uint32_t)t & 1u) &&
-         wait_or_abort(sm, &sm.kvfull[st], (uint32_t)(t >> 1) & 1u);
+         wait_or_abort(sm, &sm.fullB[st], (uint32_t)(t >> 1) & 1u);
     if (!__all_sync(kFull, ok)) {
       ok = false;
       break;
@@ -448,28 +520,53 @@ __device__ __forceinline__ void softmax_and_store(const MlaArgs& a, MlaSmem& sm,
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive1(&sm.sfree);
-    const uint32_t vm0 = sm.vmask[st][0], vm1 = sm.vmask[st][1];
-    float x[kTile];
-    float mx = -INFINITY;
+    const uint32_t vm0 = sm.vmask[t & 3][0], vm1 = sm.vmask[t & 3][1];
+    // Every token valid and a positive scale (the usual case, the same for the
+    // whole CTA): the maximum of the raw scores, scaled once, in four
+    // independent chains; otherwise masked tokens are -inf.
+    const bool full = (vm0 & vm1) == kFull && a.c2 > 0.f;
+    float mx;
+    if (full) {
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      x[j] = ((vm0 >> j) & 1u) ? __uint_as_float(r0[j]) * a.c2 : -INFINITY;
-      x[32 + j] = ((vm1 >> j) & 1u) ? __uint_as_float(r1[j]) * a.c2 : -INFINITY;
-      mx = fmaxf(mx, fmaxf(x[j], x[32 + j]));
+      for (int j = 0; j < 32; ++j)
+        m4[j & 3] = fmaxf(m4[j & 3], fmaxf(__uint_as_float(r0[j]), __uint_as_float(r1[j])));
+      mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.c2;
+    } else {
+      mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if ((vm0 >> j) & 1u) mx = fmaxf(mx, __uint_as_float(r0[j]) * a.c2);
+        if ((vm1 >> j) & 1u) mx = fmaxf(mx, __uint_as_float(r1[j]) * a.c2);
+      }
     }
     const float mn = mx > m + kRescaleGap ? mx : m;   // m = -inf takes any finite max
     const float alpha = m == -INFINITY ? 1.f : fast_exp2(m - mn);
     const float ref = mn == -INFINITY ? 0.f : mn;
+    // Weights 2^(s c2 - ref) two at a time (one fused multiply-add pair), packed
+    // to bf16; the fp32 and the bf16-rounded sums in two-wide accumulators.
     uint32_t pk[kTile / 2];
-    float s = 0.f, sb = 0.f;
+    float2 as[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 ab[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    const float2 c2v = make_float2(a.c2, a.c2), nref = make_float2(-ref, -ref);
 #pragma unroll
     for (int j = 0; j < kTile / 2; ++j) {
-      const float e0 = fast_exp2(x[2 * j] - ref), e1 = fast_exp2(x[2 * j + 1] - ref);
+      const uint32_t* rr = j < 16 ? r0 : r1;
+      const int i = 2 * (j & 15);
+      float2 xv = ffma2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])), c2v, nref);
+      if (!full) {
+        const uint32_t vm = j < 16 ? vm0 : vm1;
+        if (!((vm >> i) & 1u)) xv.x = -INFINITY;
+        if (!((vm >> (i + 1)) & 1u)) xv.y = -INFINITY;
+      }
+      const float e0 = fast_exp2(xv.x), e1 = fast_exp2(xv.y);
       pk[j] = pack_bf16(e0, e1);
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[j]));
-      s += e0 + e1;
-      sb += f.x + f.y;
+      as[j & 1] = fadd2(as[j & 1], make_float2(e0, e1));
+      ab[j & 1] = fadd2(ab[j & 1], make_float2(__uint_as_float(pk[j] << 16),
+                                               __uint_as_float(pk[j] & 0xFFFF0000u)));
     }
+    const float s = (as[0].x + as[0].y) + (as[1].x + as[1].y);
+    const float sb = (ab[0].x + ab[0].y) + (ab[1].x + ab[1].y);
     l = l * alpha + s;
     w = w * alpha + sb;
     m = mn;
@@ -564,8 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.qfull, 1);
     mbar_init(&sm.qtm, kSoftmaxWarps);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm.kvfull[i], 32 * kGatherWarps / kStages);   // every gathering lane
-      mbar_init(&sm.kvempty[i], 1);
+      mbar_init(&sm.fullA[i], 32 * kGatherWarps / kStages);   // every gathering lane
+      mbar_init(&sm.fullB[i], 32 * kGatherWarps / kStages);
+      mbar_init(&sm.emptyA[i], 1);
+      mbar_init(&sm.emptyB[i], 1);
     }
     mbar_init(&sm.sfull, 1);
     mbar_init(&sm.sfree, kSoftmaxWarps);
@@ -589,10 +688,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem;
 
   if (warp < kGatherWarps) {
-    gather_tiles(a, sm, &tm_q, r, hg, (int64_t)s * a.n_slots, count, ntiles,
+    gather_tiles(a, sm, &tm_q, r, hg, half, (int64_t)s * a.n_slots, count, ntiles,
                  a.slots + (int64_t)pair * a.K);
   } else if (warp == kMmaWarp) {
-    if ((tid & 31) == 0) issue_mmas(a, sm, tmem, half, ntiles);
+    if ((tid & 31) == 0) {
+      if (half == 0) issue_mmas<0>(a, sm, tmem, ntiles);
+      else issue_mmas<1>(a, sm, tmem, ntiles);
+    }
     __syncwarp();
   } else {
     softmax_and_store(a, sm, tmem, r, half, ntiles, head0, hg);
