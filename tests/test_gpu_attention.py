@@ -1,8 +1,9 @@
 """GPU parity of the sparse MLA decode attention (dsa_sparse_mla_decode) with
 the oracle (oracle/attention.py): first on random slot sets over a seeded
-cache (counts from 0 to K, tile tails, H = 64 / 128 / 192), then through the
-whole decode path, the indexer's compacted slots into the attention and its
-outputs into the LSE combine, against the oracle pipeline.
+cache (counts from 0 to K, tile tails, H = 64 / 128 / 192), at the decode
+batch's full shape in the benchmark's launch configuration (sampled pairs),
+then through the whole decode path, the indexer's compacted slots into the
+attention and its outputs into the LSE combine, against the oracle pipeline.
 
 Tolerance (derived from the arithmetic): scores are exact bf16 products summed
 in fp32, so lse2 is within 1e-5 * max(1, |ref|); the softmax weights enter the
@@ -135,3 +136,32 @@ def test_decode_loop_with_ties_and_tails():
     assert np.array_equal(np.isneginf(lse), np.isneginf(want_lse))
     fin = np.isfinite(want_lse)
     assert (np.abs(lse[fin] - want_lse[fin]) <= 1e-5 * np.maximum(1.0, np.abs(want_lse[fin]))).all()
+
+
+def test_decode_batch_size_in_the_benchmarks_launch_configuration():
+    """The decode batch's shape as the benchmark launches it (64 rows, S = 4,
+    H = 128: 512 CTAs over the SMs, 400-640 selected slots per (row, shard),
+    so every CTA runs seven to ten 64-token tiles and some a partial last
+    one), caches of 300 K slots per shard (1.4 GB, larger than L2) with the
+    benchmark's value distribution; a dozen (row, shard) pairs, the longest
+    among them, checked against the oracle."""
+    S, R, H, K, n_slots = 4, 64, 128, 2048, 300_000
+    rng = np.random.default_rng(77)
+    q = W.mla_query(R, H, seed=78)
+    cache = W.mla_cache_uniform(S, n_slots, seed=79)
+    counts = rng.integers(400, 641, (S, R))
+    slots = np.full((S, R, K), -1, np.int64)
+    for s in range(S):
+        for r in range(R):
+            slots[s, r, :counts[s, r]] = rng.integers(0, n_slots, counts[s, r])
+    out, lse2, err = _attend(q, cache, slots, counts)
+    assert err == 0
+    flat = np.argsort(counts, axis=None)
+    pairs = [np.unravel_index(i, counts.shape) for i in
+             list(flat[-2:]) + list(rng.choice(flat[:-2], 10, replace=False))]
+    for s, r in pairs:
+        c = counts[s, r]
+        want_o, want_l = OA.sparse_mla_decode(OC.bf16_to_f64(q[r]),
+                                              OC.bf16_to_f64(cache[s, slots[s, r, :c]]), SCALE,
+                                              W.MLA_DV)
+        _assert_close(out[s, r], lse2[s, r], want_o, want_l)
