@@ -87,14 +87,15 @@ STALLED_COPY_TEST_LIB = os.path.join(BUILD, "libdsa_stalled_copy_test.so")
 
 
 def build_stalled_copy_test(force: bool = False) -> str:
-    """A test-only library, separate from libdsa.so: the local top-K entry
-    points (shard_topk.cu alone) built with DSA_TEST_STALLED_COPY, whose
-    staging wait also waits on an mbarrier that no copy completes, with a
-    short poll bound.  Every real copy still lands; the bounded wait runs out
-    and the kernel returns with DSA_FLAG_TIMEOUT set.  Used by the tests of
-    that flag only."""
-    src = os.path.join(CSRC, "shard_topk.cu")
-    deps = [src, os.path.abspath(__file__), os.path.join(INCLUDE, "dsa.h")] + \
+    """A test-only library, separate from libdsa.so: the local top-K and the
+    sparse MLA decode entry points (shard_topk.cu, attention.cu) built with
+    DSA_TEST_STALLED_COPY, where the top-K's staging wait also waits on an
+    mbarrier that no copy completes and the attention's stage barriers expect
+    one arrival that nothing makes, with a short poll bound.  Every real copy
+    still lands; the bounded waits run out and the kernels return with
+    DSA_FLAG_TIMEOUT set.  Used by the tests of that flag only."""
+    srcs = [os.path.join(CSRC, "shard_topk.cu"), os.path.join(CSRC, "attention.cu")]
+    deps = srcs + [os.path.abspath(__file__), os.path.join(INCLUDE, "dsa.h")] + \
         [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     if (not force and os.path.exists(STALLED_COPY_TEST_LIB) and
             all(os.path.getmtime(f) <= os.path.getmtime(STALLED_COPY_TEST_LIB) for f in deps)):
@@ -102,7 +103,7 @@ def build_stalled_copy_test(force: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     tmp = STALLED_COPY_TEST_LIB + ".tmp"
     cmd = [nvcc(), *ARCH, *FLAGS, "-DDSA_TEST_STALLED_COPY", "-shared", "-cudart", "shared",
-           src, "-o", tmp]
+           *srcs, "-o", tmp]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed on the stalled-copy test build:\n{res.stdout}\n{res.stderr}")

@@ -85,6 +85,14 @@ constexpr int kQCol = 352;                   // query dimensions 0..319: 160
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleGap = 8.f;           // weights stay below 2^8 before a rescale
+#ifdef DSA_TEST_STALLED_COPY
+// The test-only build (never libdsa.so): every stage's part-A barrier expects
+// one arrival that nothing makes, so the first scores' wait runs out (every
+// copy still lands) and the kernel returns with DSA_FLAG_TIMEOUT.
+constexpr uint32_t kStalledArrivals = 1;
+#else
+constexpr uint32_t kStalledArrivals = 0;
+#endif
 
 static_assert(kGatherWarps == 2 * kStages, "two gathering warps per stage");
 static_assert(kBlocks * 64 == kDqk && kVBlocks * 64 == kHalf, "column blocks");
@@ -661,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.qfull, 1);
     mbar_init(&sm.qtm, kSoftmaxWarps);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm.fullA[i], 32 * kGatherWarps / kStages);   // every gathering lane
+      mbar_init(&sm.fullA[i], 32 * kGatherWarps / kStages + kStalledArrivals);   // every gathering lane
       mbar_init(&sm.fullB[i], 32 * kGatherWarps / kStages);
       mbar_init(&sm.emptyA[i], 1);
       mbar_init(&sm.emptyB[i], 1);

@@ -1,10 +1,11 @@
 """DSA_FLAG_TIMEOUT: a bounded mbarrier wait that runs out, on the GPU, with
 no fault and no hang.
 
-A separate test-only library (`build_stalled_copy_test`: shard_topk.cu built
-with DSA_TEST_STALLED_COPY, never libdsa.so) adds one mbarrier to the staging
-wait of the local top-K, armed for 16 bytes that no copy delivers, and cuts
-the poll bound to 4096.  Every real bulk copy still lands (its own barrier
+A separate test-only library (`build_stalled_copy_test`: shard_topk.cu and
+attention.cu built with DSA_TEST_STALLED_COPY, never libdsa.so) adds one
+mbarrier to the staging wait of the local top-K, armed for 16 bytes that no
+copy delivers, makes the attention's stage barriers expect one arrival that
+nothing makes, and cuts the poll bound to 4096.  Every real bulk copy still lands (its own barrier
 completes); the extra wait runs out, the kernel raises DSA_FLAG_TIMEOUT in the
 caller's error word, drains its copies and returns without writing its
 outputs.  The same context then runs the production library to full parity.
@@ -73,3 +74,56 @@ def test_a_stalled_copy_sets_the_timeout_flag_and_the_device_stays_usable(stalle
     got = G.run_gpu(case)
     assert got["err"] == 0
     G.assert_indexer_parity(case, got, np.arange(cfg.rows))
+
+
+def test_a_stalled_attention_stage_sets_the_timeout_flag_and_the_device_stays_usable(stalled_lib):
+    """The tcgen05 sparse MLA decode in the test build: the first tile's stage
+    barrier waits for one arrival that never comes.  Every gathered row and the
+    query still land; the MMA thread's bounded polling runs out, every role of
+    the CTA stops at its next bounded wait, nothing is written, and the tensor
+    memory is freed.  The production library then attends the same slots to
+    parity."""
+    import torch
+
+    import dsa_sparse_indexer_gb300 as dsa
+    from oracle import attention as OA
+    from oracle import combine as OC
+    p, i, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    stalled_lib.dsa_sparse_mla_decode.argtypes = [p, p, i64, p, p, i, i, i, i, ctypes.c_float,
+                                                  p, p, p, p]
+    stalled_lib.dsa_sparse_mla_decode.restype = i
+    S, R, H, K, n_slots = 2, 3, 128, 512, 5000
+    rng = np.random.default_rng(31)
+    q = W.mla_query(R, H, seed=32)
+    cache = W.mla_cache(S, n_slots, seed=33)
+    counts = np.array([[200, 64, 1], [129, 512, 70]])
+    slots = rng.integers(0, n_slots, (S, R, K)).astype(np.int32)
+    dq = G.dev(q.view(np.int16)).view(torch.bfloat16)
+    dc = G.dev(cache.view(np.int16)).view(torch.bfloat16)
+    ds, dn = G.dev(slots), G.dev(counts.astype(np.int32))
+    out = torch.full((S, R, H, W.MLA_DV), 7, dtype=torch.int16, device="cuda")
+    lse2 = torch.full((S, R, H), 7.0, dtype=torch.float32, device="cuda")
+    err = dsa.new_error_flags("cuda")
+    scale = 1.0 / np.sqrt(192.0)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for _ in range(2):          # the second call starts from a clean barrier too
+        err.zero_()
+        st = stalled_lib.dsa_sparse_mla_decode(dq.data_ptr(), dc.data_ptr(), n_slots,
+                                               ds.data_ptr(), dn.data_ptr(), R, S, H, K, scale,
+                                               out.data_ptr(), lse2.data_ptr(), err.data_ptr(),
+                                               stream)
+        assert st == 0
+        torch.cuda.synchronize()             # returns: no hang, no fault
+        assert int(err.item()) & FLAG_TIMEOUT
+        assert not int(err.item()) & FLAG_BOUNDS
+        assert (out == 7).all() and (lse2 == 7.0).all()   # a timed-out CTA writes nothing
+
+    # The context is intact: the production library attends the same slots.
+    o, l2 = dsa.sparse_mla_decode(dq, dc, ds, dn, scale, err_flags=err.zero_())
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = OC.bf16_to_f64(o.view(torch.int16).cpu().numpy().view(np.uint16))
+    want_o, want_l = OA.shard_attention(OC.bf16_to_f64(q), OC.bf16_to_f64(cache), slots, counts,
+                                        scale, W.MLA_DV)
+    assert (np.abs(got - want_o) <= G.combine_tolerance(want_o)).all()
+    assert (np.abs(l2.cpu().numpy() - want_l) <= 1e-5 * np.maximum(1.0, np.abs(want_l))).all()
