@@ -65,7 +65,7 @@ constexpr int kDv = DSA_MLA_DV;              // 512
 constexpr int kHeads = 128;                  // heads per CTA: the MMA's M
 constexpr int kHalf = kDv / 2;               // output dimensions per CTA
 constexpr int kTile = 64;                    // tokens per tile: the scores' N
-constexpr int kStages = 2;                   // one per gathering warp
+constexpr int kStages = 2;                   // tiles in flight
 constexpr int kBlocks = kDqk / 64;           // 9 column blocks of 64 bf16 (128 bytes)
 constexpr int kQtBlocks = 5;                 // query blocks held in tensor memory
 constexpr int kQsBlocks = kBlocks - kQtBlocks;   // and in shared memory
@@ -136,7 +136,7 @@ __host__ __device__ constexpr int block_b(int half, int i) { return half * kVBlo
 // Shared-memory matrix descriptor: start address >> 4 (bits 0-13), leading
 // byte offset >> 4 (bits 16-29), stride byte offset >> 4 (bits 32-45),
 // descriptor version 1 (bits 46-47), swizzle mode (bits 61-63: 2 = 128-byte,
-// 4 = 64-byte).  K-major swizzled operands: the stride is that of 8-row
+// the layout TMA and the gathers write).  K-major operands: the stride is that of 8-row
 // groups, the leading offset unused (1).  MN-major 128-byte swizzle: the
 // leading offset steps between 64-element atoms along N, the stride between
 // 8-row groups along K.
