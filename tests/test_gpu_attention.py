@@ -165,3 +165,23 @@ def test_decode_batch_size_in_the_benchmarks_launch_configuration():
                                               OC.bf16_to_f64(cache[s, slots[s, r, :c]]), SCALE,
                                               W.MLA_DV)
         _assert_close(out[s, r], lse2[s, r], want_o, want_l)
+
+
+@pytest.mark.parametrize("scale", [-1.0 / np.sqrt(192.0), 0.0])
+def test_negative_and_zero_scales(scale):
+    """The softmax's general path with every token valid: a negative scale
+    (the maximum is the most negative dot product) and a zero one (every
+    weight 1: O is the plain mean of the selected values, lse2 = log2 n)."""
+    S, R, H, K, n_slots = 2, 3, 128, 512, 4000
+    rng = np.random.default_rng(41)
+    q = W.mla_query(R, H, seed=42)
+    cache = W.mla_cache(S, n_slots, seed=43)
+    counts = np.array([[64, 300, 1], [512, 65, 128]])
+    slots = rng.integers(0, n_slots, (S, R, K))
+    out, lse2, err = _attend(q, cache, slots, counts, scale=scale)
+    assert err == 0
+    want_out, want_lse2 = OA.shard_attention(OC.bf16_to_f64(q), OC.bf16_to_f64(cache), slots,
+                                             counts, scale, W.MLA_DV)
+    _assert_close(out, lse2, want_out, want_lse2)
+    if scale == 0.0:
+        np.testing.assert_allclose(lse2, np.log2(counts)[:, :, None] * np.ones(H), rtol=1e-6)
