@@ -87,14 +87,15 @@ STALLED_COPY_TEST_LIB = os.path.join(BUILD, "libdsa_stalled_copy_test.so")
 
 
 def build_stalled_copy_test(force: bool = False) -> str:
-    """A test-only library, separate from libdsa.so: the local top-K and the
-    sparse MLA decode entry points (shard_topk.cu, attention.cu) built with
-    DSA_TEST_STALLED_COPY, where the top-K's staging wait also waits on an
+    """A test-only library, separate from libdsa.so: the local top-K, the
+    sparse MLA decode and the indexer logits entry points (shard_topk.cu,
+    attention.cu, indexer_logits.cu) built with DSA_TEST_STALLED_COPY, where
+    the top-K's staging wait and the logits' first MMA also wait on an
     mbarrier that no copy completes and the attention's stage barriers expect
     one arrival that nothing makes, with a short poll bound.  Every real copy
     still lands; the bounded waits run out and the kernels return with
     DSA_FLAG_TIMEOUT set.  Used by the tests of that flag only."""
-    srcs = [os.path.join(CSRC, "shard_topk.cu"), os.path.join(CSRC, "attention.cu")]
+    srcs = [os.path.join(CSRC, f) for f in ("shard_topk.cu", "attention.cu", "indexer_logits.cu")]
     deps = srcs + [os.path.abspath(__file__), os.path.join(INCLUDE, "dsa.h")] + \
         [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     if (not force and os.path.exists(STALLED_COPY_TEST_LIB) and

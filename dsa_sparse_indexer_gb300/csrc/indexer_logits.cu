@@ -81,6 +81,7 @@ struct alignas(1024) LogitsSmem {
   int32_t pblk[kItemBlocks];               // the item's block-table entries
   uint64_t full[kStages], empty[kStages], qfull[2], qfree[2];
   uint64_t accfull[LogitsCfg<G, P>::kAccBufs], accempty[LogitsCfg<G, P>::kAccBufs], drain;
+  uint64_t stall;                          // the test-only build's wait that runs out
   uint32_t tmem;
   int abort;
 };
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(LogitsCfg<G, P>::kThreads, G == 1 ? 2 : 1)
       mbar_init(&sm.accempty[b], Cfg::kEpiWarps);
     }
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.stall, 1);
     sm.abort = 0;
     mbar_init_fence();
   }
@@ -372,6 +374,15 @@ __global__ void __launch_bounds__(LogitsCfg<G, P>::kThreads, G == 1 ? 2 : 1)
         const int qb = icount & 1;
         if (!mbar_wait(&sm.qfull[qb], (uint32_t)(icount >> 1) & 1u)) { ok = false; break; }
         ++icount;
+#ifdef DSA_TEST_STALLED_COPY
+        // The test-only build (never libdsa.so): before its first MMA the
+        // thread waits on an mbarrier armed for 16 bytes that no copy delivers;
+        // every real copy still lands on its own barrier, this wait runs out.
+        if (icount == 1) {
+          mbar_expect_tx(&sm.stall, 16u);
+          if (!mbar_wait(&sm.stall, 0)) { ok = false; break; }
+        }
+#endif
         for (int kt = 0; kt < x.ntiles; ++kt, ++gt) {
           constexpr int NB = Cfg::kAccBufs;
           const int stg = gt % kStages;

@@ -1,11 +1,12 @@
 """DSA_FLAG_TIMEOUT: a bounded mbarrier wait that runs out, on the GPU, with
 no fault and no hang.
 
-A separate test-only library (`build_stalled_copy_test`: shard_topk.cu and
-attention.cu built with DSA_TEST_STALLED_COPY, never libdsa.so) adds one
-mbarrier to the staging wait of the local top-K, armed for 16 bytes that no
-copy delivers, makes the attention's stage barriers expect one arrival that
-nothing makes, and cuts the poll bound to 4096.  Every real bulk copy still lands (its own barrier
+A separate test-only library (`build_stalled_copy_test`: shard_topk.cu,
+attention.cu and indexer_logits.cu built with DSA_TEST_STALLED_COPY, never
+libdsa.so) adds one mbarrier, armed for 16 bytes that no copy delivers, to the
+staging wait of the local top-K and before the logits' first MMA, makes the
+attention's stage barriers expect one arrival that nothing makes, and cuts the
+poll bound to 4096.  Every real bulk copy still lands (its own barrier
 completes); the extra wait runs out, the kernel raises DSA_FLAG_TIMEOUT in the
 caller's error word, drains its copies and returns without writing its
 outputs.  The same context then runs the production library to full parity.
@@ -127,3 +128,44 @@ def test_a_stalled_attention_stage_sets_the_timeout_flag_and_the_device_stays_us
                                         scale, W.MLA_DV)
     assert (np.abs(got - want_o) <= G.combine_tolerance(want_o)).all()
     assert (np.abs(l2.cpu().numpy() - want_l) <= 1e-5 * np.maximum(1.0, np.abs(want_l))).all()
+
+
+def test_a_stalled_logits_mma_sets_the_timeout_flag_and_the_device_stays_usable(stalled_lib):
+    """The tcgen05 indexer logits in the test build: before its first MMA the
+    issuing thread waits on an mbarrier armed for 16 bytes that no copy
+    delivers.  The query and key copies land on their own barriers; the wait
+    runs out, the roles stop at their bounded waits, nothing is written, and
+    the production library then computes the same logits to parity."""
+    import torch
+
+    import dsa_sparse_indexer_gb300 as dsa
+    from tests import test_gpu_indexer_logits as TL
+    p, i, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    stalled_lib.dsa_indexer_logits.argtypes = [p, p, p, i64, p, i, i, i, p, p, p, i, i, i, p, i64,
+                                               p, p]
+    stalled_lib.dsa_indexer_logits.restype = i
+    c = TL._case(2, 1, rows=5, Lmax=2 * 1500 + 11, bs=64, seed=51)
+    reqs, max_blocks = c["tables"].shape[1], c["tables"].shape[2]
+    n_slots = c["k"].shape[1]
+    dq, dw, dk = G.dev(c["q"]), G.dev(c["w"]), G.dev(c["k"])
+    dt, de, ds0 = G.dev(c["tables"]), G.dev(c["ends"]), G.dev(c["starts"])
+    out = torch.full((c["S"], c["rows"], c["ld"]), 7.0, dtype=torch.float32, device="cuda")
+    err = dsa.new_error_flags("cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for _ in range(2):          # the second call starts from a clean barrier too
+        err.zero_()
+        st = stalled_lib.dsa_indexer_logits(dq.data_ptr(), dw.data_ptr(), dk.data_ptr(), n_slots,
+                                            dt.data_ptr(), reqs, max_blocks, c["bs"], None,
+                                            ds0.data_ptr(), de.data_ptr(), c["rows"], c["S"],
+                                            c["I"], out.data_ptr(), c["ld"], err.data_ptr(),
+                                            stream)
+        assert st == 0
+        torch.cuda.synchronize()             # returns: no hang, no fault
+        assert int(err.item()) & FLAG_TIMEOUT
+        assert not int(err.item()) & FLAG_BOUNDS
+        assert (out == 7.0).all()            # nothing written
+
+    # The context is intact: the production library computes the same logits.
+    got, e = TL._run(c)
+    assert e == 0
+    TL._check(c, got)
