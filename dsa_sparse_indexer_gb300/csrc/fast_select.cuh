@@ -43,7 +43,7 @@ struct FastSelectSmem {
   uint32_t bst_s[kFsRankCap];   // and slot
   int scan[33];
   int nb, bstar, above, bcnt, eq;
-  uint32_t kmin, kmax;
+  uint32_t wmin[32], wmax[32];   // each warp's smallest and largest score key
   unsigned long long thr64;
 };
 
@@ -71,24 +71,24 @@ template <int NT, int V, typename SlotOf>
 __device__ bool fast_select(const float (&f)[V][4], int K, float fmn, float fmx, SlotOf slot_of,
                             FastSelectSmem& sm, FastSelectResult* out) {
   using ull = unsigned long long;
-  const int tid = threadIdx.x, lane = tid & 31;
+  constexpr int W = NT / 32;
+  static_assert(W <= 32, "one lane per warp in the reductions");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int b = tid; b < kFsBins; b += NT) sm.bins[b] = 0u;
-  if (tid == 0) {
-    sm.nb = 0;
-    sm.kmin = 0xffffffffu;
-    sm.kmax = 0u;
-  }
+  if (tid == 0) sm.nb = 0;
   {
     const uint32_t mn = __reduce_min_sync(kFull, score_key(fmn));
     const uint32_t mx = __reduce_max_sync(kFull, score_key(fmx));
-    __syncthreads();
     if (lane == 0) {
-      atomicMin(&sm.kmin, mn);
-      atomicMax(&sm.kmax, mx);
+      sm.wmin[warp] = mn;
+      sm.wmax[warp] = mx;
     }
   }
   __syncthreads();
-  const float fmin = key_score(sm.kmin), fmax = key_score(sm.kmax);
+  // Every warp reduces the warps' keys itself (no second barrier).
+  const uint32_t kmin = __reduce_min_sync(kFull, lane < W ? sm.wmin[lane] : 0xffffffffu);
+  const uint32_t kmax = __reduce_max_sync(kFull, lane < W ? sm.wmax[lane] : 0u);
+  const float fmin = key_score(kmin), fmax = key_score(kmax);
   constexpr float kTwo23 = 8388608.0f;
   const float scale = __fdividef(2045.0f, fmax - fmin);
   const LinearBins bin_of{scale, (kTwo23 + 1.0f) - fmin * scale};
@@ -111,8 +111,14 @@ __device__ bool fast_select(const float (&f)[V][4], int K, float fmn, float fmx,
       cnt[j] = (int)sm.bins[g + per - 1 - j];
       local += cnt[j];
     }
-    int total;
-    int run = block_exclusive_scan(local, sm.scan, &total);
+    // Exclusive prefix over the block with one barrier: a warp scan, the
+    // warps' totals, and every warp adding up the totals of the warps before.
+    const int incl = warp_inclusive_scan(local);
+    if (lane == 31) sm.scan[warp] = incl;
+    __syncthreads();
+    const int ws = lane < W ? sm.scan[lane] : 0;
+    const int wincl = warp_inclusive_scan(ws);
+    int run = __shfl_sync(kFull, wincl - ws, warp) + incl - local;
 #pragma unroll
     for (int j = 0; j < per; ++j) {
       if (run < K && run + cnt[j] >= K) {
