@@ -203,22 +203,25 @@ __global__ void __launch_bounds__(NT)
         blk_c[c] = __ldg(bt + ((int64_t)o * reqs + req) * max_blocks + col);
     }
   }
-  // Positions among the warp's ids of the same shard, in id order.
+  // Positions among the warp's ids of the same shard, in id order: the lanes
+  // whose ids share this lane's shard (one match) give its rank in the
+  // chunk, and one-hot 8-bit fields summed over the warp give every shard's
+  // count in the chunk (at most 32 each; shards 4-7 in a second sum).
   int run = 0;   // lane s < S: this warp's ids of shard s so far
 #pragma unroll
   for (int c = 0; c < kCvMaxChunks; ++c) {
     if (c < nch) {
       const int o = own_c[c];
-      unsigned mybal = 0u;
-      int add = 0;
-      for (int s = 0; s < S; ++s) {
-        const unsigned b = __ballot_sync(kFull, o == s);
-        if (o == s) mybal = b;
-        if (lane == s) add = __popc(b);
+      const unsigned same = __match_any_sync(kFull, o);
+      const uint32_t one = o < 0 ? 0u : 1u << (8 * (o & 3));
+      uint32_t cnt = __reduce_add_sync(kFull, o < 4 ? one : 0u);
+      if (S > 4) {
+        const uint32_t hi = __reduce_add_sync(kFull, o >= 4 ? one : 0u);
+        if (lane >= 4) cnt = hi;
       }
       const int base = __shfl_sync(kFull, run, o < 0 ? 0 : o);
-      own_c[c] = o < 0 ? -1 : (o | ((base + __popc(mybal & lt)) << 8));
-      run += add;
+      own_c[c] = o < 0 ? -1 : (o | ((base + __popc(same & lt)) << 8));
+      if (lane < S) run += (int)((cnt >> (8 * (lane & 3))) & 0xffu);
     }
   }
   if (lane < S) wbase[warp][lane] = run;
