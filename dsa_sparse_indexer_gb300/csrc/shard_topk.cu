@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
   constexpr int kCap = 4 * V * NT;
   __shared__ TopkFastSmem<NT, V> sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int s = blockIdx.x / rows, r = blockIdx.x - s * rows;
+  const int r = blockIdx.x, s = blockIdx.y;
   const float* row = logits + ((int64_t)s * rows + r) * ld;
 
   // Global range -> this shard's local range (ld <= INT32_MAX: slots fit int).
@@ -397,7 +397,7 @@ dsa_status launch_topk(const float* logits, int64_t ld, int rows, int S, int I, 
   const ShardMath shm(S, I);
   if (ld <= 32 * 512) {
     auto launch_fast = [&](auto kern, int nt) {
-      const cudaError_t e = launch_kernel(kern, dim3((unsigned)(rows * S)), dim3((unsigned)nt), 0,
+      const cudaError_t e = launch_kernel(kern, dim3((unsigned)rows, (unsigned)S), dim3((unsigned)nt), 0,
                                           stream, 0, logits, ld, rows, S, I, K, row_starts,
                                           row_ends, local_idx, cand, err_flags, shm);
       return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
