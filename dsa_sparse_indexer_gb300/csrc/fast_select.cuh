@@ -67,9 +67,9 @@ struct LinearBins {
 // More than K real scores.  fmn / fmx: this thread's smallest and largest real
 // score (+inf / -inf if it holds none).  Every thread calls it.  On true it
 // ends with a barrier; on false the caller must synchronise before reusing sm.
-template <int NT, int V, typename SlotOf>
+template <int NT, int V, typename SlotOf, typename ScoreAt>
 __device__ bool fast_select(const float (&f)[V][4], int K, float fmn, float fmx, SlotOf slot_of,
-                            FastSelectSmem& sm, FastSelectResult* out) {
+                            ScoreAt score_at, FastSelectSmem& sm, FastSelectResult* out) {
   using ull = unsigned long long;
   constexpr int W = NT / 32;
   static_assert(W <= 32, "one lane per warp in the reductions");
@@ -148,15 +148,17 @@ __device__ bool fast_select(const float (&f)[V][4], int K, float fmn, float fmx,
     int b0 = 0;
     if (lane == 31) b0 = atomicAdd(&sm.nb, incl);
     int q = __shfl_sync(kFull, b0, 31) + incl - mine;
-#pragma unroll
-    for (int j = 0; j < V; ++j)
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (bm >> (4 * j + c) & 1u) {
-          sm.bst_k[q] = score_key(f[j][c]);
-          sm.bst_s[q] = slot_of(j, c);
-          ++q;
-        }
+    // Most lanes hold no member: walk the set bits, each member's score read
+    // back by its slot (the value loaded into f; a register array cannot be
+    // indexed by a run-time bit).
+    while (bm != 0u) {
+      const int k = __ffs((int)bm) - 1;
+      bm &= bm - 1u;
+      const uint32_t sl = slot_of(k >> 2, k & 3);
+      sm.bst_k[q] = score_key(score_at(sl));
+      sm.bst_s[q] = sl;
+      ++q;
+    }
   }
   __syncthreads();
   // Rank on (score key, ~slot): the member with take - 1 above it.  It also

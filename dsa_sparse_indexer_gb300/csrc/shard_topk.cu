@@ -220,20 +220,25 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
   if (bad && tid == 0) raise_flag(flags, DSA_FLAG_BOUNDS);
   const int lo = (int)lo64, hi = (int)hi64, n = hi - lo;
 
-  int32_t* out_idx = local_idx ? local_idx + ((int64_t)s * rows + r) * K : nullptr;
-  float2* out_cand = kPack ? reinterpret_cast<float2*>(cand) + ((int64_t)r * S + s) * K : nullptr;
-  const TopkEmitter<kPack> emit{row, out_idx, out_cand, K, s, sh};
+  // Built where used (cheap functions of the arguments), so that nothing of
+  // it is held in registers across the selection.
+  auto make_emit = [&]() {
+    return TopkEmitter<kPack>{
+        row, local_idx ? local_idx + ((int64_t)s * rows + r) * K : nullptr,
+        kPack ? reinterpret_cast<float2*>(cand) + ((int64_t)r * S + s) * K : nullptr, K, s, sh};
+  };
 
   if (n <= K) {  // every slot is selected: slots lo..hi-1 in order, then padding
+    const TopkEmitter<kPack> emit = make_emit();
     for (int j = tid; j < K; j += NT) {
       if (j < n) emit(j, (uint32_t)(lo + j), __ldg(row + lo + j));
-      else write_pad(out_idx, out_cand, j);
+      else write_pad(emit.out_idx, emit.out_cand, j);
     }
     return;
   }
   const int base = lo & ~3;
   if (hi - base > kCap) {   // only for an unaligned start right at the limit
-    topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, emit);
+    topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, make_emit());
     return;
   }
 
@@ -275,9 +280,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
   auto slot = [&](int j, int c) { return (uint32_t)(base + (j * NT + tid) * 4 + c); };
 
   FastSelectResult fs;
-  if (!fast_select<NT, V>(f, K, fmn, fmx, slot, sm.f.sel, &fs)) {
+  auto score_at = [&](uint32_t l) { return __ldg(row + l); };
+  if (!fast_select<NT, V>(f, K, fmn, fmx, slot, score_at, sm.f.sel, &fs)) {
     __syncthreads();   // the fallback's shared memory overlaps the selection's
-    topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, emit);
+    topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, make_emit());
     return;
   }
 
@@ -338,6 +344,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
       }
   }
   __syncthreads();
+  const TopkEmitter<kPack> emit = make_emit();
   for (int p = tid; p < K; p += NT) emit(p, sm.f.stage_s[p], sm.f.stage_v[p]);
 }
 
