@@ -113,8 +113,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 }
 
 // ---------------------------------------------------------------------------
-// Throughput path for local ranges of up to 4 V NT slots (V = 4 float4 rows
-// per thread; NT = 512 or 1024 threads).  Each thread keeps V float4 of the
+// Throughput path for local ranges of up to 4 V NT slots (NT = 256 threads
+// with V = 8 float4 rows each up to 8192 slots, three CTAs per SM; 1024 with
+// V = 4 up to 16384).  Each thread keeps V float4 of the
 // range as scores in registers (slot e = base + 4 (j NT + tid) + c; -inf
 // outside the range).  The exact threshold (score, slot) comes from
 // fast_select (fast_select.cuh: a histogram of the scores linear in the score
@@ -141,7 +142,7 @@ struct TopkFastSmem {
       // stores made the compiler move the register scores to local memory).
       float stage_v[kTMaxK];
       uint32_t stage_s[kTMaxK];
-      uint32_t wt[NT / 32];        // packed per-row winner counts of each warp
+      uint32_t wt[V / 4][NT / 32]; // packed per-row winner counts of each warp
       int off[V][NT / 32];         // output offset of each (float4 row, warp)
     } f;
     struct {                       // fallback: radix select over the registers
@@ -194,13 +195,19 @@ __device__ __noinline__ void topk_fallback(const float* __restrict__ row, int lo
   });
 }
 
+// Four float4 rows a thread fill 64 registers (two or one CTAs of 512 or 1024
+// threads per SM); eight take up to 80 (three CTAs of 256 threads).
+template <int NT, int V>
+constexpr int topk_fast_min_blocks() { return V == 4 ? 1024 / NT : 768 / NT; }
+
 template <int NT, int V, bool kPack>
-__global__ void __launch_bounds__(NT, 1024 / NT)
+__global__ void __launch_bounds__(NT, (topk_fast_min_blocks<NT, V>()))
     topk_fast_kernel(const float* __restrict__ logits, int64_t ld, int rows, int S, int I, int K,
                      const int32_t* __restrict__ row_starts, const int32_t* __restrict__ row_ends,
                      int32_t* __restrict__ local_idx, float* __restrict__ cand, uint32_t* flags,
                      const ShardMath sh) {
-  static_assert(V == 4, "per-row winner counts are packed four to a word");
+  static_assert(V % 4 == 0 && V <= 8, "per-row winner counts are packed four to a word");
+  constexpr int NW = V / 4;
   constexpr int W = NT / 32;
   constexpr int kCap = 4 * V * NT;
   __shared__ TopkFastSmem<NT, V> sm;
@@ -305,25 +312,36 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
         wmask |= (uint32_t)(f[j][c] > thr || (f[j][c] == thr && slot(j, c) <= last))
                  << (4 * j + c);
   }
-  uint32_t pk = 0u;   // winners per float4 row j, 8 bits each
+  uint32_t pk[NW], inc[NW];   // winners per float4 row j: word j / 4, 8 bits each
 #pragma unroll
-  for (int j = 0; j < V; ++j) pk |= (uint32_t)__popc((wmask >> (4 * j)) & 0xfu) << (8 * j);
-  uint32_t inc = pk;   // fields stay below 256: at most 128 a warp
+  for (int w = 0; w < NW; ++w) {
+    pk[w] = 0u;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+      pk[w] |= (uint32_t)__popc((wmask >> (4 * (4 * w + jj))) & 0xfu) << (8 * jj);
+    inc[w] = pk[w];   // fields stay below 256: at most 128 a warp
+  }
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, inc, o);
-    if (lane >= o) inc += y;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const uint32_t y = __shfl_up_sync(kFull, inc[w], o);
+      if (lane >= o) inc[w] += y;
+    }
   }
-  if (lane == 31) sm.f.wt[warp] = inc;
+  if (lane == 31) {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) sm.f.wt[w][warp] = inc[w];
+  }
   __syncthreads();
   if (warp == 0) {
     // Lane w < W: exclusive prefix over warps of each row's count, then the
     // rows' totals in order.
-    const uint32_t wt = lane < W ? sm.f.wt[lane] : 0u;
     int row_base = 0;
 #pragma unroll
     for (int j = 0; j < V; ++j) {
-      const int c = (int)((wt >> (8 * j)) & 0xffu);
+      const uint32_t wt = lane < W ? sm.f.wt[j / 4][lane] : 0u;
+      const int c = (int)((wt >> (8 * (j % 4))) & 0xffu);
       const int incl = warp_inclusive_scan(c);
       if (lane < W) sm.f.off[j][lane] = row_base + incl - c;
       row_base += __shfl_sync(kFull, incl, 31);
@@ -332,7 +350,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
   __syncthreads();
 #pragma unroll
   for (int j = 0; j < V; ++j) {
-    int p = sm.f.off[j][warp] + (int)(((inc - pk) >> (8 * j)) & 0xffu);
+    int p = sm.f.off[j][warp] + (int)(((inc[j / 4] - pk[j / 4]) >> (8 * (j % 4))) & 0xffu);
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       if (wmask >> (4 * j + c) & 1u) {
@@ -409,7 +427,7 @@ dsa_status launch_topk(const float* logits, int64_t ld, int rows, int S, int I, 
                                           row_ends, local_idx, cand, err_flags, shm);
       return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
     };
-    if (ld <= 16 * 512) return launch_fast(topk_fast_kernel<512, 4, kPack>, 512);
+    if (ld <= 32 * 256) return launch_fast(topk_fast_kernel<256, 8, kPack>, 256);
     return launch_fast(topk_fast_kernel<1024, 4, kPack>, 1024);
   }
   // Rows that fit the register path need no staging area.
