@@ -35,7 +35,7 @@ namespace dsa {
 constexpr int kFsBins = 2048;
 constexpr int kFsRankCap = 256;
 
-struct FastSelectSmem {
+struct alignas(16) FastSelectSmem {
   uint32_t bins[kFsBins];
   // Stores are 32-bit: 64-bit stores of (key, slot) pairs made the compiler
   // move the callers' register scores to local memory.
@@ -103,13 +103,13 @@ __device__ bool fast_select(const float (&f)[V][4], int K, float fmn, float fmx,
   __syncthreads();
   {
     constexpr int per = kFsBins / NT;
+    static_assert(per % 2 == 0, "bins read in pairs");
     const int g = kFsBins - per * (tid + 1);
-    int cnt[per];
     int local = 0;
 #pragma unroll
-    for (int j = 0; j < per; ++j) {
-      cnt[j] = (int)sm.bins[g + per - 1 - j];
-      local += cnt[j];
+    for (int j = 0; j < per; j += 2) {
+      const uint2 c = *reinterpret_cast<const uint2*>(&sm.bins[g + j]);
+      local += (int)(c.x + c.y);
     }
     // Exclusive prefix over the block with one barrier: a warp scan, the
     // warps' totals, and every warp adding up the totals of the warps before.
@@ -119,14 +119,19 @@ __device__ bool fast_select(const float (&f)[V][4], int K, float fmn, float fmx,
     const int ws = lane < W ? sm.scan[lane] : 0;
     const int wincl = warp_inclusive_scan(ws);
     int run = __shfl_sync(kFull, wincl - ws, warp) + incl - local;
-#pragma unroll
-    for (int j = 0; j < per; ++j) {
-      if (run < K && run + cnt[j] >= K) {
-        sm.bstar = g + per - 1 - j;
-        sm.above = run;
-        sm.bcnt = cnt[j];
+    // One thread's bins hold the K-th position: it finds b* among them (the
+    // counts read again rather than held in registers beside the scores).
+    if (run < K && run + local >= K) {
+      for (int j = 0; j < per; ++j) {
+        const int b = g + per - 1 - j, c = (int)sm.bins[b];
+        if (run + c >= K) {
+          sm.bstar = b;
+          sm.above = run;
+          sm.bcnt = c;
+          break;
+        }
+        run += c;
       }
-      run += cnt[j];
     }
   }
   __syncthreads();
