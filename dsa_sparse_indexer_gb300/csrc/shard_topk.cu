@@ -138,10 +138,7 @@ struct TopkFastSmem {
   union {
     struct {
       FastSelectSmem sel;
-      // Winners by output position, as separate 32-bit words (64-bit pair
-      // stores made the compiler move the register scores to local memory).
-      float stage_v[kTMaxK];
-      uint32_t stage_s[kTMaxK];
+      float2 stage[kTMaxK];        // winners by output position: (score, slot bits)
       uint32_t wt[V / 4][NT / 32]; // packed per-row winner counts of each warp
       int off[V][NT / 32];         // output offset of each (float4 row, warp)
     } f;
@@ -354,16 +351,16 @@ __global__ void __launch_bounds__(NT, (topk_fast_min_blocks<NT, V>()))
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       if (wmask >> (4 * j + c) & 1u) {
-        if (p < K) {
-          sm.f.stage_v[p] = f[j][c];
-          sm.f.stage_s[p] = slot(j, c);
-        }
+        if (p < K) sm.f.stage[p] = make_float2(f[j][c], __uint_as_float(slot(j, c)));
         ++p;
       }
   }
   __syncthreads();
   const TopkEmitter<kPack> emit = make_emit();
-  for (int p = tid; p < K; p += NT) emit(p, sm.f.stage_s[p], sm.f.stage_v[p]);
+  for (int p = tid; p < K; p += NT) {
+    const float2 w = sm.f.stage[p];
+    emit(p, __float_as_uint(w.y), w.x);
+  }
 }
 
 // Standalone pack: cand[r][s*K + j] from local_idx[s][r][j].  Each thread
