@@ -26,6 +26,31 @@
 namespace dsa {
 namespace {
 
+// Block-wide exclusive prefix sum with one __syncthreads(): every warp scans
+// the warp totals itself instead of waiting for one warp to publish them.
+// The caller puts a barrier between this call and the next write to
+// `scratch` (at least blockDim.x / 32 ints).
+__device__ __forceinline__ int block_exclusive_scan_1bar(int v, int* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  const int w = lane < nwarps ? scratch[lane] : 0;
+  int incl = w;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  return __shfl_sync(kFull, incl - w, warp) + x - v;
+}
+
 constexpr int kMergeThreads = 1024;
 constexpr int kMaxK = 2048;
 
@@ -494,8 +519,7 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
       const int target = min(nsv, (int)((float)K * (float)nslots * 1.125f / (float)C) + 16);
       // Thread t < kSampBins takes bin kSampBins - 1 - t (bins from the top).
       const int local = tid < kSampBins ? (int)sm.w.scnt[kSampBins - 1 - tid] : 0;
-      int tot;
-      const int run = block_exclusive_scan(local, sm.scan, &tot);
+      const int run = block_exclusive_scan_1bar(local, sm.scan);
       if (tid < kSampBins && run < target && run + local >= target) {
         // Bin b holds scores from about smin + (b - 1) / scale; one bin lower
         // for the rounding of the map.
@@ -561,8 +585,7 @@ __global__ void __launch_bounds__(NT, merge_fast_min_blocks<NT>())
         cnt[j] = (int)sm.h.end[g + per - 1 - j];
         local += cnt[j];
       }
-      int tot;
-      int run = block_exclusive_scan(local, sm.scan, &tot);
+      int run = block_exclusive_scan_1bar(local, sm.scan);
       int mx = 0;
 #pragma unroll
       for (int j = 0; j < per; ++j) {
@@ -752,8 +775,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
           cnt[j] = (int)sm.h.end[g + per - 1 - j];
           local += cnt[j];
         }
-        int tot;
-        int run = block_exclusive_scan(local, sm.scan, &tot);
+        int run = block_exclusive_scan_1bar(local, sm.scan);
         int mx = 0;
 #pragma unroll
         for (int j = 0; j < per; ++j) {
