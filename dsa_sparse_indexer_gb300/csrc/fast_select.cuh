@@ -1,8 +1,9 @@
-// The K-th largest of register-resident scores, exactly, without a radix pass
-// over all of them (sm_103a).
+// The K-th largest of a CTA's scores, exactly, without a radix pass over all
+// of them (sm_103a).
 //
-// Each of the NT threads holds V float4 rows of scores, f[j][c] at a slot
-// given by the caller (slots order ties: the smaller slot ranks first); -inf
+// Each of the NT threads owns V float4 rows of scores, read through get4(j)
+// (registers or shared memory), element c of row j at a slot given by the
+// caller (slots order ties: the smaller slot ranks first); -inf
 // marks an empty slot (the fast path runs only when every real score is
 // finite).  Steps:
 //   1. a 2048-bin histogram of every score, the bins linear in the score
@@ -67,8 +68,12 @@ struct LinearBins {
 // More than K real scores.  fmn / fmx: this thread's smallest and largest real
 // score (+inf / -inf if it holds none).  Every thread calls it.  On true it
 // ends with a barrier; on false the caller must synchronise before reusing sm.
-template <int NT, int V, typename SlotOf, typename ScoreAt>
-__device__ bool fast_select(const float (&f)[V][4], int K, float fmn, float fmx, SlotOf slot_of,
+__device__ __forceinline__ float f4at(const float4& v, int c) {
+  return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
+}
+
+template <int NT, int V, typename Get4, typename SlotOf, typename ScoreAt>
+__device__ bool fast_select(Get4 get4, int K, float fmn, float fmx, SlotOf slot_of,
                             ScoreAt score_at, FastSelectSmem& sm, FastSelectResult* out) {
   using ull = unsigned long long;
   constexpr int W = NT / 32;
@@ -97,9 +102,11 @@ __device__ bool fast_select(const float (&f)[V][4], int K, float fmn, float fmx,
       !(bin_of.v(fmin) >= kTwo23) || !(bin_of.v(fmax) <= kTwo23 + (float)(kFsBins - 1)))
     return false;
 #pragma unroll
-  for (int j = 0; j < V; ++j)
+  for (int j = 0; j < V; ++j) {
+    const float4 v = get4(j);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) atomicAdd(&sm.bins[bin_of(f[j][c])], 1u);
+    for (int c = 0; c < 4; ++c) atomicAdd(&sm.bins[bin_of(f4at(v, c))], 1u);
+  }
   __syncthreads();
   {
     constexpr int per = kFsBins / NT;
@@ -144,9 +151,12 @@ __device__ bool fast_select(const float (&f)[V][4], int K, float fmn, float fmx,
   const float vstar = kTwo23 + (float)sm.bstar;
   uint32_t bm = 0u;   // bit 4 j + c: slot (j, c) is in b*
 #pragma unroll
-  for (int j = 0; j < V; ++j)
+  for (int j = 0; j < V; ++j) {
+    const float4 v = get4(j);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) bm |= (uint32_t)(bin_of.v(f[j][c]) == vstar) << (4 * j + c);
+    for (int c = 0; c < 4; ++c)
+      bm |= (uint32_t)(bin_of.v(f4at(v, c)) == vstar) << (4 * j + c);
+  }
   if (__any_sync(kFull, bm != 0u)) {   // most warps hold no member
     const int mine = __popc(bm);
     const int incl = warp_inclusive_scan(mine);

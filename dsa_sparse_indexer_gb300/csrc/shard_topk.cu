@@ -8,10 +8,10 @@
 // One CTA per (shard, row); the winners are written in ascending slot order
 // (ties on the score go to the smaller slot, i.e. the smaller global id).
 // Local ranges of up to 16384 slots take the throughput kernel below
-// (topk_fast_kernel): scores in registers, the exact threshold from one
-// histogram linear in the score (bins read off the bits of one FFMA) and a
-// ranking of its threshold bin (fast_select.cuh), slot-ordered placement
-// through shared memory.
+// (topk_smem_kernel): the range copied into shared memory by TMA, the exact
+// threshold from one histogram linear in the score (bins read off the bits
+// of one FFMA) and a ranking of its threshold bin (fast_select.cuh),
+// slot-ordered placement through shared memory.
 // Longer ranges are staged in shared memory with bulk async copies (TMA) or
 // read from global memory, and a radix select with an ordered ballot sweep
 // picks the winners (shard_topk_kernel, local_topk.cuh).  The standalone pack
@@ -114,41 +114,28 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 
 // ---------------------------------------------------------------------------
 // Throughput path for local ranges of up to 4 V NT slots (NT = 256 threads
-// with V = 8 float4 rows each up to 8192 slots, three CTAs per SM; 1024 with
-// V = 4 up to 16384).  Each thread keeps V float4 of the
-// range as scores in registers (slot e = base + 4 (j NT + tid) + c; -inf
-// outside the range).  The exact threshold (score, slot) comes from
-// fast_select (fast_select.cuh: a histogram of the scores linear in the score
-// over their range, a ranking of the threshold bin): a slot wins if its score
-// is above the threshold score, or equal to it at a slot no later than the
-// threshold slot (scores compare as floats: -0.0 ties +0.0, as their keys do,
-// and each keeps its own sign in the candidate).  The winners are then
-// placed in slot order: per-thread counts for each of the V float4 rows,
-// packed into one word, take one warp scan, and a small table gives each
-// (row, warp) its output offset; each thread drops its winners' (score, slot)
-// at their output positions in shared memory, and all threads then write the
-// outputs with coalesced stores.  Rows with an infinite score or a crowded
-// threshold bin fall back to the radix select over the registers.
+// with V = 8 float4 rows each up to 8192 slots, four CTAs per SM; 512 up to
+// 16384, two CTAs per SM).  One bulk copy (TMA) brings the row's range into
+// shared memory, completing on an mbarrier; thread tid owns float4 rows
+// j NT + tid (slot e = base + 4 (j NT + tid) + c) and reads them from shared
+// memory in every pass, the first of which writes -inf over its slots outside
+// [lo, hi).  No score is held in registers between passes, which leaves room
+// for four CTAs of 256 threads an SM.  The exact threshold (score, slot)
+// comes from fast_select (fast_select.cuh: a histogram of the scores linear
+// in the score over their range, a ranking of the threshold bin): a slot
+// wins if its score is above the threshold score, or equal to it at a slot
+// no later than the threshold slot (scores compare as floats: -0.0 ties
+// +0.0, as their keys do, and each keeps its own sign in the candidate).
+// The winners are then placed in slot order: per-thread counts for each of
+// the V float4 rows, packed four to a word, take one warp scan a word, and a
+// small table gives each (row, warp) its output offset; each thread drops
+// its winners' slots at their output positions in shared memory, and all
+// threads then write the outputs with coalesced stores, the scores read back
+// from the copy.  Rows with an infinite score or a crowded threshold bin
+// rank the copy with the radix select (local_topk.cuh).
 // ---------------------------------------------------------------------------
 using ull = unsigned long long;
 constexpr int kTMaxK = 2048;     // largest K
-
-template <int NT, int V>
-struct TopkFastSmem {
-  union {
-    struct {
-      FastSelectSmem sel;
-      float2 stage[kTMaxK];        // winners by output position: (score, slot bits)
-      uint32_t wt[V / 4][NT / 32]; // packed per-row winner counts of each warp
-      int off[V][NT / 32];         // output offset of each (float4 row, warp)
-    } f;
-    struct {                       // fallback: radix select over the registers
-      LocalTopkSmem loc;
-      RegEmitSmem<NT, V> es;
-      uint32_t list[kListCap];
-    } g;
-  };
-};
 
 // Writes winner p of a (shard, row): local slot l and the packed candidate.
 template <bool kPack>
@@ -170,44 +157,38 @@ struct TopkEmitter {
   }
 };
 
-// Fallback of the throughput path: the radix select over the keys, re-read
-// from the row (in L2) into registers, or over the row in global memory when
-// the range does not fit the registers.
-template <int NT, int V, bool kPack>
-__device__ __noinline__ void topk_fallback(const float* __restrict__ row, int lo, int hi, int K,
-                                           TopkFastSmem<NT, V>& sm,
-                                           const TopkEmitter<kPack> emit) {
-  const int base = lo & ~3;
-  if (hi - base > 4 * V * NT) {
-    local_topk_emit<NT>(row + lo, hi - lo, K, sm.g.loc,
-                        [&](int p, int i, float v) { emit(p, (uint32_t)(lo + i), v); });
-    return;
-  }
-  uint32_t key[V][4];
-  load_keys<NT, V>(row, lo, hi, key);
-  int eq;
-  const SelectResult res = select_regs<NT, V>(key, K, sm.g.loc.sel, sm.g.list, sm.g.es, &eq);
-  emit_winners<NT, V>(key, res.thr, res.take_eq, sm.g.es, [&](int p, int e, uint32_t k) {
-    emit.from_key(p, (uint32_t)(base + e), k);
-  });
-}
-
-// Four float4 rows a thread fill 64 registers (two or one CTAs of 512 or 1024
-// threads per SM); eight take up to 80 (three CTAs of 256 threads).
 template <int NT, int V>
-constexpr int topk_fast_min_blocks() { return V == 4 ? 1024 / NT : 768 / NT; }
+struct TopkSmemLayout {
+  float4 sc[V * NT];               // slots [base, base + 4 V NT) of the row
+  union {
+    struct {
+      FastSelectSmem sel;
+      uint32_t stage[kTMaxK];      // winners' slots by output position
+      uint32_t wt[V / 4][NT / 32]; // packed per-row winner counts of each warp
+      int off[V][NT / 32];         // output offset of each (float4 row, warp)
+    } f;
+    LocalTopkSmem loc;             // fallback: radix select over the copy
+  };
+  uint64_t bar;
+#ifdef DSA_TEST_STALLED_COPY
+  uint64_t stall;                  // test build: armed for bytes no copy delivers
+#endif
+};
+
+static_assert(sizeof(TopkSmemLayout<256, 8>) <= 56 * 1024, "four CTAs of 256 threads an SM");
+static_assert(sizeof(TopkSmemLayout<512, 8>) <= 113 * 1024, "two CTAs of 512 threads an SM");
 
 template <int NT, int V, bool kPack>
-__global__ void __launch_bounds__(NT, (topk_fast_min_blocks<NT, V>()))
-    topk_fast_kernel(const float* __restrict__ logits, int64_t ld, int rows, int S, int I, int K,
+__global__ void __launch_bounds__(NT, 1024 / NT)
+    topk_smem_kernel(const float* __restrict__ logits, int64_t ld, int rows, int S, int I, int K,
                      const int32_t* __restrict__ row_starts, const int32_t* __restrict__ row_ends,
                      int32_t* __restrict__ local_idx, float* __restrict__ cand, uint32_t* flags,
                      const ShardMath sh) {
   static_assert(V % 4 == 0 && V <= 8, "per-row winner counts are packed four to a word");
   constexpr int NW = V / 4;
   constexpr int W = NT / 32;
-  constexpr int kCap = 4 * V * NT;
-  __shared__ TopkFastSmem<NT, V> sm;
+  extern __shared__ __align__(16) unsigned char topk_smem_raw[];
+  TopkSmemLayout<NT, V>& sm = *reinterpret_cast<TopkSmemLayout<NT, V>*>(topk_smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.x, s = blockIdx.y;
   const float* row = logits + ((int64_t)s * rows + r) * ld;
@@ -217,21 +198,17 @@ __global__ void __launch_bounds__(NT, (topk_fast_min_blocks<NT, V>()))
   bool bad = false;
   if (st < 0) { st = 0; bad = true; }
   if (en < st) { en = st; bad = true; }
-  // st and en are int32 row bounds clamped to >= 0: the 32-bit map applies.
   int64_t lo64 = sh.local_len((uint32_t)st, s), hi64 = sh.local_len((uint32_t)en, s);
   if (hi64 > ld) { hi64 = ld; bad = true; }
   if (lo64 > hi64) { lo64 = hi64; bad = true; }
   if (bad && tid == 0) raise_flag(flags, DSA_FLAG_BOUNDS);
   const int lo = (int)lo64, hi = (int)hi64, n = hi - lo;
 
-  // Built where used (cheap functions of the arguments), so that nothing of
-  // it is held in registers across the selection.
   auto make_emit = [&]() {
     return TopkEmitter<kPack>{
         row, local_idx ? local_idx + ((int64_t)s * rows + r) * K : nullptr,
         kPack ? reinterpret_cast<float2*>(cand) + ((int64_t)r * S + s) * K : nullptr, K, s, sh};
   };
-
   if (n <= K) {  // every slot is selected: slots lo..hi-1 in order, then padding
     const TopkEmitter<kPack> emit = make_emit();
     for (int j = tid; j < K; j += NT) {
@@ -240,74 +217,87 @@ __global__ void __launch_bounds__(NT, (topk_fast_min_blocks<NT, V>()))
     }
     return;
   }
-  const int base = lo & ~3;
-  if (hi - base > kCap) {   // only for an unaligned start right at the limit
-    topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, make_emit());
+  // The copy: [base, hi rounded up to 4) (inside the row: ld % 4 == 0; at
+  // most 4 V NT slots, which the launch guarantees with ld <= 4 V NT).
+  const int base = lo & ~3, top = (hi + 3) & ~3;
+  const uint32_t bytes = (uint32_t)(top - base) * 4u;
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+#ifdef DSA_TEST_STALLED_COPY
+    mbar_init(&sm.stall, 1);
+#endif
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0) {   // in pieces of at most 16 KB, all completing on one barrier
+    mbar_expect_tx(&sm.bar, bytes);
+    for (uint32_t off = 0; off < bytes; off += 16384u)
+      bulk_g2s(reinterpret_cast<unsigned char*>(sm.sc) + off,
+               reinterpret_cast<const unsigned char*>(row + base) + off, min(16384u, bytes - off),
+               &sm.bar);
+  }
+#ifdef DSA_TEST_STALLED_COPY
+  if (tid == 0) mbar_expect_tx(&sm.stall, 16u);
+#endif
+  bool good = mbar_wait(&sm.bar, 0);
+#ifdef DSA_TEST_STALLED_COPY
+  good &= mbar_wait(&sm.stall, 0);
+#endif
+  if (__syncthreads_or(!good)) {
+    if (tid == 0) raise_flag(flags, DSA_FLAG_TIMEOUT);
+    mbar_wait(&sm.bar, 0);   // the copy must land before the CTA's memory goes
     return;
   }
 
-  // Scores of the range (-inf outside it) and their range.
-  float f[V][4];
+  // Range pass: each thread's float4 rows, -inf written over its slots
+  // outside [lo, hi) (it is the only reader of them until the next barrier).
   float fmn = INFINITY, fmx = -INFINITY;
-  {
-    float4 v[V];
 #pragma unroll
-    for (int j = 0; j < V; ++j) {
-      const int e0 = base + (j * NT + tid) * 4;
-      v[j] = e0 < hi ? __ldg(reinterpret_cast<const float4*>(row + e0))
-                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    }
+  for (int j = 0; j < V; ++j) {
+    const int q = j * NT + tid, e0 = base + 4 * q;
+    if (e0 >= lo && e0 + 4 <= hi) {
+      const float4 v = sm.sc[q];
+      fmn = fminf(fminf(fminf(fminf(fmn, v.x), v.y), v.z), v.w);
+      fmx = fmaxf(fmaxf(fmaxf(fmaxf(fmx, v.x), v.y), v.z), v.w);
+    } else {
+      float4 v = e0 < top ? sm.sc[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+      float* e = reinterpret_cast<float*>(&v);
 #pragma unroll
-    for (int j = 0; j < V; ++j) {
-      const int e0 = base + (j * NT + tid) * 4;
-      f[j][0] = v[j].x;
-      f[j][1] = v[j].y;
-      f[j][2] = v[j].z;
-      f[j][3] = v[j].w;
-      if (e0 >= lo && e0 + 4 <= hi) {   // the whole float4 is inside the range
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          fmn = fminf(fmn, f[j][c]);
-          fmx = fmaxf(fmx, f[j][c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const bool in = e0 + c >= lo && e0 + c < hi;
-          f[j][c] = in ? f[j][c] : -INFINITY;
-          fmn = in ? fminf(fmn, f[j][c]) : fmn;
-          fmx = in ? fmaxf(fmx, f[j][c]) : fmx;
-        }
+      for (int c = 0; c < 4; ++c) {
+        const bool in = e0 + c >= lo && e0 + c < hi;
+        e[c] = in ? e[c] : -INFINITY;
+        fmn = in ? fminf(fmn, e[c]) : fmn;
+        fmx = in ? fmaxf(fmx, e[c]) : fmx;
       }
+      sm.sc[q] = v;
     }
   }
+  const float* scf = reinterpret_cast<const float*>(sm.sc);
   auto slot = [&](int j, int c) { return (uint32_t)(base + (j * NT + tid) * 4 + c); };
+  auto get4 = [&](int j) { return sm.sc[j * NT + tid]; };
+  auto score_at = [&](uint32_t l) { return scf[l - (uint32_t)base]; };
 
   FastSelectResult fs;
-  auto score_at = [&](uint32_t l) { return __ldg(row + l); };
-  if (!fast_select<NT, V>(f, K, fmn, fmx, slot, score_at, sm.f.sel, &fs)) {
+  if (!fast_select<NT, V>(get4, K, fmn, fmx, slot, score_at, sm.f.sel, &fs)) {
     __syncthreads();   // the fallback's shared memory overlaps the selection's
-    topk_fallback<NT, V, kPack>(row, lo, hi, K, sm, make_emit());
+    const TopkEmitter<kPack> emit = make_emit();
+    local_topk_emit<NT>(scf + (lo - base), n, K, sm.loc,
+                        [&](int p, int i, float v) { emit(p, (uint32_t)(lo + i), v); });
     return;
   }
 
-  // Slot-ordered placement of the winners.  With one score at the threshold
-  // (the threshold's own) every score at or above it wins.
   const float thr = fs.thr;
   const uint32_t last = fs.last;
   uint32_t wmask = 0u;   // bit 4 j + c: slot (j, c) wins
-  if (fs.eq == 1) {
 #pragma unroll
-    for (int j = 0; j < V; ++j)
+  for (int j = 0; j < V; ++j) {
+    const float4 v = get4(j);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) wmask |= (uint32_t)(f[j][c] >= thr) << (4 * j + c);
-  } else {
-#pragma unroll
-    for (int j = 0; j < V; ++j)
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        wmask |= (uint32_t)(f[j][c] > thr || (f[j][c] == thr && slot(j, c) <= last))
-                 << (4 * j + c);
+    for (int c = 0; c < 4; ++c) {
+      const float x = f4at(v, c);
+      wmask |= (uint32_t)(fs.eq == 1 ? x >= thr : (x > thr || (x == thr && slot(j, c) <= last)))
+               << (4 * j + c);
+    }
   }
   uint32_t pk[NW], inc[NW];   // winners per float4 row j: word j / 4, 8 bits each
 #pragma unroll
@@ -316,7 +306,7 @@ __global__ void __launch_bounds__(NT, (topk_fast_min_blocks<NT, V>()))
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj)
       pk[w] |= (uint32_t)__popc((wmask >> (4 * (4 * w + jj))) & 0xfu) << (8 * jj);
-    inc[w] = pk[w];   // fields stay below 256: at most 128 a warp
+    inc[w] = pk[w];
   }
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -332,8 +322,6 @@ __global__ void __launch_bounds__(NT, (topk_fast_min_blocks<NT, V>()))
   }
   __syncthreads();
   if (warp == 0) {
-    // Lane w < W: exclusive prefix over warps of each row's count, then the
-    // rows' totals in order.
     int row_base = 0;
 #pragma unroll
     for (int j = 0; j < V; ++j) {
@@ -351,15 +339,15 @@ __global__ void __launch_bounds__(NT, (topk_fast_min_blocks<NT, V>()))
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       if (wmask >> (4 * j + c) & 1u) {
-        if (p < K) sm.f.stage[p] = make_float2(f[j][c], __uint_as_float(slot(j, c)));
+        if (p < K) sm.f.stage[p] = slot(j, c);
         ++p;
       }
   }
   __syncthreads();
   const TopkEmitter<kPack> emit = make_emit();
   for (int p = tid; p < K; p += NT) {
-    const float2 w = sm.f.stage[p];
-    emit(p, __float_as_uint(w.y), w.x);
+    const uint32_t l = sm.f.stage[p];
+    emit(p, l, scf[l - (uint32_t)base]);
   }
 }
 
@@ -424,8 +412,19 @@ dsa_status launch_topk(const float* logits, int64_t ld, int rows, int S, int I, 
                                           row_ends, local_idx, cand, err_flags, shm);
       return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
     };
-    if (ld <= 32 * 256) return launch_fast(topk_fast_kernel<256, 8, kPack>, 256);
-    return launch_fast(topk_fast_kernel<1024, 4, kPack>, 1024);
+    auto launch_smem = [&](auto kern, int nt, size_t smem) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+        return DSA_ERR_CUDA;
+      const cudaError_t e = launch_kernel(kern, dim3((unsigned)rows, (unsigned)S),
+                                          dim3((unsigned)nt), smem, stream, 0, logits, ld, rows,
+                                          S, I, K, row_starts, row_ends, local_idx, cand,
+                                          err_flags, shm);
+      return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    };
+    if (ld <= 32 * 256)
+      return launch_smem(topk_smem_kernel<256, 8, kPack>, 256, sizeof(TopkSmemLayout<256, 8>));
+    return launch_smem(topk_smem_kernel<512, 8, kPack>, 512, sizeof(TopkSmemLayout<512, 8>));
   }
   // Rows that fit the register path need no staging area.
   const int stage_cap = ld <= RT::kCap ? 0 : (ld < kStageCapElems ? (int)ld : kStageCapElems);

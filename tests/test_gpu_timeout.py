@@ -4,7 +4,9 @@ no fault and no hang.
 A separate test-only library (`build_stalled_copy_test`: shard_topk.cu,
 attention.cu and indexer_logits.cu built with DSA_TEST_STALLED_COPY, never
 libdsa.so) adds one mbarrier, armed for 16 bytes that no copy delivers, to the
-staging wait of the local top-K and before the logits' first MMA, makes the
+staging waits of the local top-K (the staged kernel for long rows and the
+shared-memory kernel for rows up to 16384 slots) and before the logits' first
+MMA, makes the
 attention's stage barriers expect one arrival that nothing makes, and cuts the
 poll bound to 4096.  Every real bulk copy still lands (its own barrier
 completes); the extra wait runs out, the kernel raises DSA_FLAG_TIMEOUT in the
@@ -72,6 +74,47 @@ def test_a_stalled_copy_sets_the_timeout_flag_and_the_device_stays_usable(stalle
         assert (out == 7).all()              # a timed-out CTA writes nothing
 
     # The context is intact: the production library runs the same rows to parity.
+    got = G.run_gpu(case)
+    assert got["err"] == 0
+    G.assert_indexer_parity(case, got, np.arange(cfg.rows))
+
+
+def _smem_case():
+    """Local rows of 6-8 K slots: the throughput kernel copies each range into
+    shared memory with one bulk copy."""
+    rng = np.random.default_rng(22)
+    rows, S, I, K, ld = 2, 1, 1, 2048, 8000
+    x = rng.standard_normal((rows, ld)).astype(np.float32)
+    ends = np.array([ld, ld - 1999], np.int32)
+    cfg = W.Config("adhoc", 9, rows=rows, S=S, I=I, K=K, block_size=64, max_len=ld, ld=ld,
+                   reqs=rows, max_blocks=(ld + 63) // 64)
+    local = OL.shard_rows(x, ends, S, I, ld)
+    bt = np.stack([rng.permutation(rows * cfg.max_blocks).astype(np.int32).reshape(rows, -1)])
+    return dict(cfg=cfg, x=x, local=local, starts=np.zeros(rows, np.int32), ends=ends, bt=bt,
+                r2q=None)
+
+
+def test_a_stalled_copy_in_the_shared_memory_top_k(stalled_lib):
+    import torch
+
+    import dsa_sparse_indexer_gb300 as dsa
+    case = _smem_case()
+    cfg = case["cfg"]
+    logits, ends = G.dev(case["local"]), G.dev(case["ends"])
+    out = torch.full((cfg.S, cfg.rows, cfg.K), 7, dtype=torch.int32, device="cuda")
+    err = dsa.new_error_flags("cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for _ in range(2):
+        err.zero_()
+        st = stalled_lib.dsa_shard_topk(logits.data_ptr(), cfg.ld, cfg.rows, cfg.S, cfg.I, cfg.K,
+                                        None, ends.data_ptr(), out.data_ptr(), err.data_ptr(),
+                                        stream)
+        assert st == 0
+        torch.cuda.synchronize()
+        assert int(err.item()) & FLAG_TIMEOUT
+        assert not int(err.item()) & FLAG_BOUNDS
+        assert (out == 7).all()
+
     got = G.run_gpu(case)
     assert got["err"] == 0
     G.assert_indexer_parity(case, got, np.arange(cfg.rows))
