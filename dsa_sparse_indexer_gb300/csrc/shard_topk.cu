@@ -114,13 +114,13 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 
 // ---------------------------------------------------------------------------
 // Throughput path for local ranges of up to 4 V NT slots (NT = 256 threads
-// with V = 8 float4 rows each up to 8192 slots, four CTAs per SM; 512 up to
+// with V = 8 float4 rows each up to 8192 slots, five CTAs per SM; 512 up to
 // 16384, two CTAs per SM).  One bulk copy (TMA) brings the row's range into
 // shared memory, completing on an mbarrier; thread tid owns float4 rows
 // j NT + tid (slot e = base + 4 (j NT + tid) + c) and reads them from shared
 // memory in every pass, the first of which writes -inf over its slots outside
 // [lo, hi).  No score is held in registers between passes, which leaves room
-// for four CTAs of 256 threads an SM.  The exact threshold (score, slot)
+// for five CTAs of 256 threads an SM.  The exact threshold (score, slot)
 // comes from fast_select (fast_select.cuh: a histogram of the scores linear
 // in the score over their range, a ranking of the threshold bin): a slot
 // wins if its score is above the threshold score, or equal to it at a slot
@@ -162,8 +162,9 @@ struct TopkSmemLayout {
   float4 sc[V * NT];               // slots [base, base + 4 V NT) of the row
   union {
     struct {
+      // The selection's bins are dead once the threshold is known: the
+      // winners' slots are staged by output position in their place.
       FastSelectSmem sel;
-      uint32_t stage[kTMaxK];      // winners' slots by output position
       uint32_t wt[V / 4][NT / 32]; // packed per-row winner counts of each warp
       int off[V][NT / 32];         // output offset of each (float4 row, warp)
     } f;
@@ -175,11 +176,16 @@ struct TopkSmemLayout {
 #endif
 };
 
-static_assert(sizeof(TopkSmemLayout<256, 8>) <= 56 * 1024, "four CTAs of 256 threads an SM");
+static_assert(kFsBins >= kTMaxK, "the staged winners fit the bins");
+static_assert(sizeof(TopkSmemLayout<256, 8>) <= 44 * 1024, "five CTAs of 256 threads an SM");
 static_assert(sizeof(TopkSmemLayout<512, 8>) <= 113 * 1024, "two CTAs of 512 threads an SM");
 
+// CTAs an SM: five of 256 threads (44 KB of shared memory each), two of 512.
+template <int NT>
+constexpr int topk_smem_min_blocks() { return NT == 256 ? 5 : 1024 / NT; }
+
 template <int NT, int V, bool kPack>
-__global__ void __launch_bounds__(NT, 1024 / NT)
+__global__ void __launch_bounds__(NT, topk_smem_min_blocks<NT>())
     topk_smem_kernel(const float* __restrict__ logits, int64_t ld, int rows, int S, int I, int K,
                      const int32_t* __restrict__ row_starts, const int32_t* __restrict__ row_ends,
                      int32_t* __restrict__ local_idx, float* __restrict__ cand, uint32_t* flags,
@@ -339,14 +345,14 @@ __global__ void __launch_bounds__(NT, 1024 / NT)
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       if (wmask >> (4 * j + c) & 1u) {
-        if (p < K) sm.f.stage[p] = slot(j, c);
+        if (p < K) sm.f.sel.bins[p] = slot(j, c);
         ++p;
       }
   }
   __syncthreads();
   const TopkEmitter<kPack> emit = make_emit();
   for (int p = tid; p < K; p += NT) {
-    const uint32_t l = sm.f.stage[p];
+    const uint32_t l = sm.f.sel.bins[p];
     emit(p, l, scf[l - (uint32_t)base]);
   }
 }
