@@ -1,9 +1,9 @@
 // The K-th largest of a CTA's scores, exactly, without a radix pass over all
 // of them (sm_103a).
 //
-// Each of the NT threads owns V float4 rows of scores, read through get4(j)
-// (registers or shared memory), element c of row j at a slot given by the
-// caller (slots order ties: the smaller slot ranks first); -inf
+// Each of the NT threads owns V float4 rows of scores, read through get4h(j)
+// for the histogram and get4(j) afterwards (registers or shared memory),
+// element c of row j at a slot given by the caller (slots order ties: the smaller slot ranks first); -inf
 // marks an empty slot (the fast path runs only when every real score is
 // finite).  Steps:
 //   1. a 2048-bin histogram of every score, the bins linear in the score
@@ -72,8 +72,8 @@ __device__ __forceinline__ float f4at(const float4& v, int c) {
   return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
 }
 
-template <int NT, int V, typename Get4, typename SlotOf, typename ScoreAt>
-__device__ bool fast_select(Get4 get4, int K, float fmn, float fmx, SlotOf slot_of,
+template <int NT, int V, typename Get4H, typename Get4, typename SlotOf, typename ScoreAt>
+__device__ bool fast_select(Get4H get4h, Get4 get4, int K, float fmn, float fmx, SlotOf slot_of,
                             ScoreAt score_at, FastSelectSmem& sm, FastSelectResult* out) {
   using ull = unsigned long long;
   constexpr int W = NT / 32;
@@ -103,7 +103,7 @@ __device__ bool fast_select(Get4 get4, int K, float fmn, float fmx, SlotOf slot_
     return false;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
-    const float4 v = get4(j);
+    const float4 v = get4h(j);
 #pragma unroll
     for (int c = 0; c < 4; ++c) atomicAdd(&sm.bins[bin_of(f4at(v, c))], 1u);
   }

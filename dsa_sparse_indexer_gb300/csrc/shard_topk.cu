@@ -256,15 +256,17 @@ __global__ void __launch_bounds__(NT, topk_smem_min_blocks<NT>())
   }
 
   // Range pass: each thread's float4 rows, -inf written over its slots
-  // outside [lo, hi) (it is the only reader of them until the next barrier).
+  // outside [lo, hi) (it is the only reader of them until the next barrier);
+  // the rows stay in registers for the histogram, the next pass.
   float fmn = INFINITY, fmx = -INFINITY;
+  float4 rv[V];
 #pragma unroll
   for (int j = 0; j < V; ++j) {
     const int q = j * NT + tid, e0 = base + 4 * q;
     if (e0 >= lo && e0 + 4 <= hi) {
-      const float4 v = sm.sc[q];
-      fmn = fminf(fminf(fminf(fminf(fmn, v.x), v.y), v.z), v.w);
-      fmx = fmaxf(fmaxf(fmaxf(fmaxf(fmx, v.x), v.y), v.z), v.w);
+      rv[j] = sm.sc[q];
+      fmn = fminf(fminf(fminf(fminf(fmn, rv[j].x), rv[j].y), rv[j].z), rv[j].w);
+      fmx = fmaxf(fmaxf(fmaxf(fmaxf(fmx, rv[j].x), rv[j].y), rv[j].z), rv[j].w);
     } else {
       float4 v = e0 < top ? sm.sc[q] : make_float4(0.f, 0.f, 0.f, 0.f);
       float* e = reinterpret_cast<float*>(&v);
@@ -276,6 +278,7 @@ __global__ void __launch_bounds__(NT, topk_smem_min_blocks<NT>())
         fmx = in ? fmaxf(fmx, e[c]) : fmx;
       }
       sm.sc[q] = v;
+      rv[j] = v;
     }
   }
   const float* scf = reinterpret_cast<const float*>(sm.sc);
@@ -284,7 +287,8 @@ __global__ void __launch_bounds__(NT, topk_smem_min_blocks<NT>())
   auto score_at = [&](uint32_t l) { return scf[l - (uint32_t)base]; };
 
   FastSelectResult fs;
-  if (!fast_select<NT, V>(get4, K, fmn, fmx, slot, score_at, sm.f.sel, &fs)) {
+  auto get4h = [&](int j) { return rv[j]; };
+  if (!fast_select<NT, V>(get4h, get4, K, fmn, fmx, slot, score_at, sm.f.sel, &fs)) {
     __syncthreads();   // the fallback's shared memory overlaps the selection's
     const TopkEmitter<kPack> emit = make_emit();
     local_topk_emit<NT>(scf + (lo - base), n, K, sm.loc,
