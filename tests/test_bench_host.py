@@ -82,6 +82,31 @@ def test_committed_profiles_name_their_sources():
         assert "source_sha256_16:" in text and "dram_bytes_per_launch:" in text, name
 
 
+def test_committed_profiles_match_the_current_sources():
+    """Every committed summary was captured on the kernel sources as they stand:
+    a kernel summary's source hash, and each (kernel, hash) pair a launch list
+    cites, equal what bench.py computes now, so a kernel change without a new
+    capture fails here."""
+    import glob
+    import os
+    import re
+    now = {k: bench.kernel_source_hash(k) for k in bench.KERNEL_SOURCES}
+    for path in glob.glob(os.path.join(bench.ROOT, "profiles", "*.md")):
+        name = os.path.basename(path)[:-3]
+        text = open(path, encoding="utf-8").read()
+        if name.startswith("launches_"):
+            cited = re.findall(r"(\w+) ([0-9a-f]{16})\b", text)
+            assert cited, name
+            for kernel, h in cited:
+                if kernel in now:
+                    assert now[kernel] == h, (name, kernel)
+        else:
+            kernel = [k for k in now if name.startswith(k)]
+            assert len(kernel) == 1, name
+            h = re.search(r"source_sha256_16: ([0-9a-f]{16})", text).group(1)
+            assert now[kernel[0]] == h, name
+
+
 def test_oracle_over_all_cores_counts_rows_of_every_process():
     """The all-cores CPU baseline: spawned processes read the batch from shared
     memory, run whole rows and report how many they finished."""
