@@ -108,7 +108,10 @@ int dsa_version(void);
  *               [n_s(start), n_s(end)), ascending; -1 after the first
  *               min(K, n_s(end) - n_s(start)).  Absolute local slots.
  *   err_flags   DSA_FLAG_BOUNDS if a local range ends past ld (the range is
- *               clipped to ld) or starts after it ends (treated as empty).
+ *               clipped to ld) or starts after it ends (treated as empty);
+ *               DSA_FLAG_TIMEOUT if the bounded wait for a row's copy into
+ *               shared memory runs out (that (shard, row)'s outputs are then
+ *               not written).
  * Errors: S not in [1, 64], I < 1, K not in {512, 1024, 2048} -> UNSUPPORTED;
  *         null pointers, rows < 0, ld < 4, ld % 4, misaligned logits -> INVALID_ARG.
  */
@@ -138,8 +141,8 @@ dsa_status dsa_pack_candidates(const float* logits, int64_t ld, const int32_t* l
 /*
  * dsa_shard_topk_pack - dsa_shard_topk and dsa_pack_candidates in one kernel:
  * the winning logits are packed while still in shared memory, so the pack
- * step's gather from the logits is not repeated.  Same arguments and results;
- * local_idx may be NULL when only the candidates are wanted.
+ * step's gather from the logits is not repeated.  Same arguments, results and
+ * error flags; local_idx may be NULL when only the candidates are wanted.
  */
 dsa_status dsa_shard_topk_pack(const float* logits, int64_t ld, int rows, int S, int I,
                                int K, const int32_t* row_starts, const int32_t* row_ends,
