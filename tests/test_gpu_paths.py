@@ -223,3 +223,29 @@ def test_local_topk_signed_zeros_at_the_threshold_keep_their_sign():
     got = cand.cpu().numpy()[0, :, 0]
     np.testing.assert_array_equal(got.view(np.uint32), row[li].view(np.uint32))
     assert np.array_equal(np.intersect1d(li, zeros), zeros[:8])
+
+
+@pytest.mark.parametrize("ld,K", [(8192, 2048), (8196, 2048), (16384, 2048), (8196, 512)])
+def test_local_topk_at_the_kernel_size_boundaries(ld, K):
+    """Rows whose allocated length sits at or just past a kernel variant's
+    capacity (256 threads x 32 scores up to 8192 slots, 512 x 32 up to
+    16384): ranges ending at ld, ranges just above K with an unaligned start
+    (the copy starts at the float4 holding it), a range one slot short of ld.
+    Bit-exact against the oracle (S = 1, I = 1: local slots are the row's)."""
+    import torch
+
+    import dsa_sparse_indexer_gb300 as dsa
+    rng = np.random.default_rng(ld + K)
+    ranges = [(0, ld), (3, K + 4), (7, ld - 1)]
+    rows = len(ranges)
+    x = rng.standard_normal((1, rows, ld)).astype(np.float32)
+    starts = torch.tensor([a for a, _ in ranges], dtype=torch.int32, device="cuda")
+    ends = torch.tensor([b for _, b in ranges], dtype=torch.int32, device="cuda")
+    err = dsa.new_error_flags("cuda")
+    local_idx = dsa.shard_topk(torch.from_numpy(x).cuda(), ends, K, 1, row_starts=starts,
+                               err_flags=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = local_idx.cpu().numpy()[0]
+    for r, (lo, hi) in enumerate(ranges):
+        np.testing.assert_array_equal(got[r], OX.shard_topk(x[0, r], lo, hi, K))
