@@ -65,9 +65,9 @@ struct LinearBins {
   }
 };
 
-// More than K real scores.  fmn / fmx: this thread's smallest and largest real
-// score (+inf / -inf if it holds none).  Every thread calls it.  On true it
-// ends with a barrier; on false the caller must synchronise before reusing sm.
+// f4at: element c of a float4.  fast_select: more than K real scores; fmn / fmx
+// this thread's smallest and largest real score (+inf / -inf if none); every
+// thread calls it; true ends with a barrier, false needs one before sm is reused.
 __device__ __forceinline__ float f4at(const float4& v, int c) {
   return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
 }
