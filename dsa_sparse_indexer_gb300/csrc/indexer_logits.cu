@@ -45,7 +45,7 @@ namespace {
 constexpr int kHeads = DSA_IDX_HEADS;      // 64
 constexpr int kDim = DSA_IDX_DIM;          // 128 fp8 values = 128 bytes per row
 constexpr int kTile = 128;                 // tokens per tile = MMA M
-constexpr int kTilesPerItem = 16;
+constexpr int kTilesPerItem = 32;
 // Block-table entries one item can need: 16 tiles of 128 slots in blocks of
 // at least 16 slots, plus one for a range that starts mid-block.
 constexpr int kItemBlocks = kTilesPerItem * 128 / 16 + 1;
