@@ -134,7 +134,6 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 // from the copy.  Rows with an infinite score or a crowded threshold bin
 // rank the copy with the radix select (local_topk.cuh).
 // ---------------------------------------------------------------------------
-using ull = unsigned long long;
 constexpr int kTMaxK = 2048;     // largest K
 
 // Writes winner p of a (shard, row): local slot l and the packed candidate.
@@ -149,11 +148,6 @@ struct TopkEmitter {
     if (p >= K) return;
     if (out_idx) out_idx[p] = (int32_t)l;
     if (kPack) out_cand[p] = make_float2(v, __int_as_float((int)sh.global_id(s, l)));
-  }
-  // The candidate's score from its key: exact except that both zeros share a
-  // key, so a zero is read back from the row to keep its sign bit.
-  __device__ __forceinline__ void from_key(int p, uint32_t l, uint32_t k) const {
-    (*this)(p, l, k == 0x80000000u ? __ldg(row + l) : key_score(k));
   }
 };
 
